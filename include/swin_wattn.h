@@ -1,0 +1,144 @@
+/*
+ * swin_wattn: fused Swin window / shifted-window multi-head attention (W-MSA / SW-MSA)
+ * on one NVIDIA GB300 GPU (sm_103a). C ABI; every call is asynchronous on the stream
+ * it is given and reports failure only through its return code.
+ *
+ * What is computed (sources cited by page and section):
+ *  - NVIDIA "visual large-model training and inference optimisation" talk, full
+ *    transcript (uticex.com, article 1598), section 1: attention among the tokens of each
+ *    non-overlapping M x M window, a cyclic window shift that bridges window borders, and
+ *    a learned relative position bias added to the attention logits.
+ *  - same transcript, section 2: shift, window partition and window reverse are index
+ *    mappings only; the mask and the bias reach the fused attention as tensors.
+ *  - same transcript, section 3: the relative-position bias lookup runs once, as
+ *    preprocessing, producing a dense per-head bias; batch GEMM + softmax + batch GEMM
+ *    run as one fused kernel whose loads and stores absorb the layout transposes.
+ *  - Baidu AIAK-Training talk (jxzklqfsx.com, article 743345), section 2, the fused
+ *    WindowAttention case: one kernel staging HBM -> shared memory -> registers, tensor
+ *    cores for both products, and a backward that recomputes instead of reloading.
+ *
+ * For an activation qkv of shape [B, H, W, 3C] (channel t*C + h*hd + d, t in {q,k,v},
+ * head h < nH, hd = C/nH = 32), window size M and shift s (0 <= s < M):
+ *   rolled token (y, x) reads original token ((y+s) mod H, (x+s) mod W);
+ *   windows are row-major over (H/M, W/M), tokens row-major inside a window;
+ *   logit(i,j) = hd^-0.5 * q_i.k_j + table[idx(i,j), h] + mask_w(i,j), with
+ *   idx(i,j) = (yi-yj+M-1)*(2M-1) + (xi-xj+M-1) for local window positions,
+ *   mask_w(i,j) = -100 when the two tokens carry different shift-region labels
+ *   (per axis of length L on the rolled grid: [0,L-M), [L-M,L-s), [L-s,L); label =
+ *   3*region_y + region_x), else 0; no mask when s = 0;
+ *   P = row softmax of the logits, O = P V, written to channel h*hd + d of the same
+ *   token position it was read from: out has shape [B, H, W, C].
+ *
+ * Conventions for every entry point:
+ *  - Tensor pointers are device pointers (cudaMalloc, or torch CUDA tensors), contiguous
+ *    in the layouts above, 16-byte aligned, owned by the caller. A host pointer is
+ *    rejected with SWIN_WATTN_ERR_INVALID_ARG before any launch.
+ *  - Activation dtype is fixed per plan: SWIN_WATTN_BF16 (bf16 in and out) or
+ *    SWIN_WATTN_FP32 (fp32 in and out; values are rounded to bf16, round-to-nearest-
+ *    even, on load). Arithmetic: bf16 tensor-core products with fp32 accumulation,
+ *    fp32 softmax.
+ *  - The bias table is fp32 [(2M-1)^2, nH], row-major; its gradient likewise.
+ *  - Errors come back as status codes; nothing aborts, traps or throws across the ABI.
+ *    After SWIN_WATTN_ERR_CUDA, swin_wattn_last_error() holds the CUDA error text of the
+ *    calling thread.
+ */
+#ifndef SWIN_WATTN_H
+#define SWIN_WATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st; /* cudaStream_t */
+
+typedef struct swin_wattn_plan_s* swin_wattn_plan_t;
+
+enum swin_wattn_status {
+  SWIN_WATTN_OK = 0,
+  SWIN_WATTN_ERR_INVALID_ARG = 1,  /* null/host pointer, bad dtype, s out of range, ... */
+  SWIN_WATTN_ERR_UNSUPPORTED = 2,  /* M not in {4,7,12}, head width != 32, H%M or W%M != 0 */
+  SWIN_WATTN_ERR_MISALIGNED = 3,   /* tensor pointer not 16-byte aligned (table: 4-byte) */
+  SWIN_WATTN_ERR_BAD_PLAN = 4,     /* null, destroyed or foreign plan handle */
+  SWIN_WATTN_ERR_CUDA = 5,         /* a CUDA runtime call failed; see swin_wattn_last_error */
+  SWIN_WATTN_ERR_TIMEOUT = 6       /* reserved: a bounded device-side wait gave up */
+};
+
+enum swin_wattn_dtype { SWIN_WATTN_BF16 = 0, SWIN_WATTN_FP32 = 1 };
+
+/*
+ * Create a plan for one layer shape and run the preprocessing on `stream`:
+ * the dense bias [nH, M^2, M^2] is expanded from `bias_table` (the lookup done once, as
+ * in section 3 of the NVIDIA transcript) and, for s > 0, the shift mask [nW, M^2, M^2]
+ * (nW = (H/M)(W/M), values 0 / -100) is built.
+ *   out         receives the plan handle (set to NULL on failure).
+ *   B           batch (B = 0 is allowed: every call on the plan is then a no-op,
+ *               except that swin_wattn_bwd still zeroes dtable).
+ *   H, W        token grid; multiples of M.
+ *   C           channels per q/k/v; C = 32 * num_heads.
+ *   window      M in {4, 7, 12}.  shift: s in [0, M).
+ *   dtype       SWIN_WATTN_BF16 or SWIN_WATTN_FP32 activation I/O.
+ *   bias_table  device fp32 [(2M-1)^2, num_heads]; read during this call's launch only.
+ * The plan owns its dense bias, its mask and the backward's reduction scratch (device
+ * memory allocated here, freed by swin_wattn_destroy). A plan is used by one stream at a
+ * time; swin_wattn_fwd and swin_wattn_bwd allocate nothing.
+ */
+int swin_wattn_plan(swin_wattn_plan_t* out, int B, int H, int W, int C, int num_heads,
+                    int window, int shift, int dtype, const float* bias_table,
+                    struct CUstream_st* stream);
+
+/* Re-expand the dense bias from an updated table (training). Same table layout. */
+int swin_wattn_set_bias(swin_wattn_plan_t plan, const float* bias_table,
+                        struct CUstream_st* stream);
+
+/*
+ * Forward: qkv [B,H,W,3C] -> out [B,H,W,C] (plan dtype). One kernel launch: the roll and
+ * window partition are folded into the load addressing and the reverse and un-roll into
+ * the store; logits, bias, mask and softmax stay on chip. `out` must not overlap `qkv`.
+ */
+int swin_wattn_fwd(swin_wattn_plan_t plan, const void* qkv, void* out,
+                   struct CUstream_st* stream);
+
+/*
+ * Backward for an upstream gradient dout [B,H,W,C] (plan dtype):
+ *   dqkv   [B,H,W,3C] plan dtype, fully overwritten (dq, dk, dv at the channels the
+ *          forward read q, k, v from);
+ *   dtable [(2M-1)^2, nH] fp32, overwritten (not accumulated) with the bias-table
+ *          gradient summed over every batch, window and (i, j) pair.
+ * The forward's probabilities are recomputed, not stored (AIAK-Training talk,
+ * section 2). Deterministic: the same inputs give bit-identical outputs.
+ */
+int swin_wattn_bwd(swin_wattn_plan_t plan, const void* qkv, const void* dout, void* dqkv,
+                   float* dtable, struct CUstream_st* stream);
+
+/*
+ * Debug dumps of the plan's index maps and preprocessed tensors (device pointers, any
+ * may be NULL to skip):
+ *   gather     int32 [nW, M^2]: original token index y*W + x that window w, slot i
+ *              reads (and writes), computed by the same addressing as the kernels;
+ *   relidx     int32 [M^2, M^2]: relative position index idx(i, j);
+ *   mask       fp32 [nW, M^2, M^2]: the plan's shift mask (all zeros when s = 0);
+ *   dense_bias fp32 [nH, M^2, M^2]: the plan's expanded bias.
+ */
+int swin_wattn_debug_maps(swin_wattn_plan_t plan, int32_t* gather, int32_t* relidx,
+                          float* mask, float* dense_bias, struct CUstream_st* stream);
+
+/* Free the plan's device memory (synchronises the device first). NULL is a no-op. */
+int swin_wattn_destroy(swin_wattn_plan_t plan);
+
+/* Static text for a status code. */
+const char* swin_wattn_status_string(int status);
+
+/* CUDA error text behind the calling thread's last SWIN_WATTN_ERR_CUDA ("" if none). */
+const char* swin_wattn_last_error(void);
+
+/* Kernel launches issued by the calling thread since the last reset (for accounting). */
+uint64_t swin_wattn_launch_count(int reset);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SWIN_WATTN_H */

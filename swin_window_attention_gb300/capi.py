@@ -1,0 +1,190 @@
+"""ctypes binding of libswin_wattn.so (declared in include/swin_wattn.h).
+
+Argument marshalling only: every function forwards to the C entry point of the same
+name and returns its status code; ``WindowAttention`` wraps a plan for torch CUDA
+tensors. Every step of the computation runs in the library's CUDA kernels. If the
+library has not been built (``python -m swin_window_attention_gb300.build``), ``load()``
+raises instead of falling back to anything else.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libswin_wattn.so")
+
+OK = 0
+ERR_INVALID_ARG = 1
+ERR_UNSUPPORTED = 2
+ERR_MISALIGNED = 3
+ERR_BAD_PLAN = 4
+ERR_CUDA = 5
+ERR_TIMEOUT = 6
+BF16 = 0
+FP32 = 1
+
+# Every symbol include/swin_wattn.h declares, with (argtypes, restype).
+_vp, _i, _cp = ctypes.c_void_p, ctypes.c_int, ctypes.c_char_p
+SIGNATURES = {
+    "swin_wattn_plan": ([ctypes.POINTER(_vp), _i, _i, _i, _i, _i, _i, _i, _i, _vp, _vp], _i),
+    "swin_wattn_set_bias": ([_vp, _vp, _vp], _i),
+    "swin_wattn_fwd": ([_vp, _vp, _vp, _vp], _i),
+    "swin_wattn_bwd": ([_vp, _vp, _vp, _vp, _vp, _vp], _i),
+    "swin_wattn_debug_maps": ([_vp, _vp, _vp, _vp, _vp, _vp], _i),
+    "swin_wattn_destroy": ([_vp], _i),
+    "swin_wattn_status_string": ([_i], _cp),
+    "swin_wattn_last_error": ([], _cp),
+    "swin_wattn_launch_count": ([_i], ctypes.c_uint64),
+}
+
+_lib = None
+
+
+class SwinWAttnError(RuntimeError):
+    def __init__(self, where: str, status: int):
+        lib = load()
+        msg = lib.swin_wattn_status_string(status).decode()
+        if status == ERR_CUDA:
+            msg += ": " + lib.swin_wattn_last_error().decode()
+        super().__init__(f"{where}: {msg} (status {status})")
+        self.status = status
+
+
+def load() -> ctypes.CDLL:
+    """Load the library (once). Raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build it with `python -m swin_window_attention_gb300.build`")
+        lib = ctypes.CDLL(LIB_PATH)
+        for name, (args, res) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = lib
+    return _lib
+
+
+# ---- same names as the C entry points --------------------------------------------------
+
+def swin_wattn_plan(B, H, W, C, num_heads, window, shift, dtype, bias_table_ptr, stream):
+    """Returns (status, plan handle or None)."""
+    h = _vp()
+    rc = load().swin_wattn_plan(ctypes.byref(h), B, H, W, C, num_heads, window, shift, dtype,
+                                bias_table_ptr, stream)
+    return rc, (h.value if rc == OK else None)
+
+
+def swin_wattn_set_bias(plan, bias_table_ptr, stream):
+    return load().swin_wattn_set_bias(plan, bias_table_ptr, stream)
+
+
+def swin_wattn_fwd(plan, qkv_ptr, out_ptr, stream):
+    return load().swin_wattn_fwd(plan, qkv_ptr, out_ptr, stream)
+
+
+def swin_wattn_bwd(plan, qkv_ptr, dout_ptr, dqkv_ptr, dtable_ptr, stream):
+    return load().swin_wattn_bwd(plan, qkv_ptr, dout_ptr, dqkv_ptr, dtable_ptr, stream)
+
+
+def swin_wattn_debug_maps(plan, gather_ptr, relidx_ptr, mask_ptr, dense_bias_ptr, stream):
+    return load().swin_wattn_debug_maps(plan, gather_ptr, relidx_ptr, mask_ptr, dense_bias_ptr,
+                                        stream)
+
+
+def swin_wattn_destroy(plan):
+    return load().swin_wattn_destroy(plan)
+
+
+def swin_wattn_status_string(status):
+    return load().swin_wattn_status_string(status).decode()
+
+
+def swin_wattn_last_error():
+    return load().swin_wattn_last_error().decode()
+
+
+def swin_wattn_launch_count(reset=False):
+    return int(load().swin_wattn_launch_count(1 if reset else 0))
+
+
+# ---- torch convenience wrapper ---------------------------------------------------------
+
+def _stream_handle(stream):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+class WindowAttention:
+    """A plan for one layer shape, driven with torch CUDA tensors.
+
+    ``table`` is the fp32 [(2M-1)^2, nH] bias table on the GPU. Activations are bf16 or
+    fp32 [B,H,W,3C] tensors (contiguous); outputs are allocated by the caller or here.
+    """
+
+    def __init__(self, B, H, W, C, num_heads, window, shift, table, dtype="bf16", stream=None):
+        import torch
+        self.B, self.H, self.W, self.C = B, H, W, C
+        self.nH, self.M, self.s = num_heads, window, shift
+        self.dtype = torch.bfloat16 if dtype == "bf16" else torch.float32
+        code = BF16 if dtype == "bf16" else FP32
+        rc, h = swin_wattn_plan(B, H, W, C, num_heads, window, shift, code, table.data_ptr(),
+                                _stream_handle(stream))
+        if rc != OK:
+            raise SwinWAttnError("swin_wattn_plan", rc)
+        self.handle = h
+
+    def set_bias(self, table, stream=None):
+        rc = swin_wattn_set_bias(self.handle, table.data_ptr(), _stream_handle(stream))
+        if rc != OK:
+            raise SwinWAttnError("swin_wattn_set_bias", rc)
+
+    def fwd(self, qkv, out=None, stream=None):
+        import torch
+        if out is None:
+            out = torch.empty(self.B, self.H, self.W, self.C, dtype=self.dtype, device=qkv.device)
+        rc = swin_wattn_fwd(self.handle, qkv.data_ptr(), out.data_ptr(), _stream_handle(stream))
+        if rc != OK:
+            raise SwinWAttnError("swin_wattn_fwd", rc)
+        return out
+
+    def bwd(self, qkv, dout, dqkv=None, dtable=None, stream=None):
+        import torch
+        if dqkv is None:
+            dqkv = torch.empty_like(qkv)
+        if dtable is None:
+            dtable = torch.empty((2 * self.M - 1) ** 2, self.nH, dtype=torch.float32,
+                                 device=qkv.device)
+        rc = swin_wattn_bwd(self.handle, qkv.data_ptr(), dout.data_ptr(), dqkv.data_ptr(),
+                            dtable.data_ptr(), _stream_handle(stream))
+        if rc != OK:
+            raise SwinWAttnError("swin_wattn_bwd", rc)
+        return dqkv, dtable
+
+    def debug_maps(self, stream=None):
+        import torch
+        dev = torch.device("cuda")
+        N, nW = self.M * self.M, (self.H // self.M) * (self.W // self.M)
+        gather = torch.empty(nW, N, dtype=torch.int32, device=dev)
+        relidx = torch.empty(N, N, dtype=torch.int32, device=dev)
+        mask = torch.empty(nW, N, N, dtype=torch.float32, device=dev)
+        dense = torch.empty(self.nH, N, N, dtype=torch.float32, device=dev)
+        rc = swin_wattn_debug_maps(self.handle, gather.data_ptr(), relidx.data_ptr(),
+                                   mask.data_ptr(), dense.data_ptr(), _stream_handle(stream))
+        if rc != OK:
+            raise SwinWAttnError("swin_wattn_debug_maps", rc)
+        return gather, relidx, mask, dense
+
+    def close(self):
+        if getattr(self, "handle", None):
+            swin_wattn_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

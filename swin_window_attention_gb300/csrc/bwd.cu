@@ -1,0 +1,520 @@
+// Fused (shifted-)window attention backward for sm_103a, with the bias-table gradient.
+//
+// The backward recomputes the forward's logits and probabilities from q and k instead
+// of reloading stored ones (Baidu AIAK-Training talk, jxzklqfsx.com article 743345,
+// section 2, fused WindowAttention case): a whole window row fits one tile, so nothing
+// but q, k, v and the upstream gradient is read. The shift, partition, reverse and
+// un-roll are again pure addressing (NVIDIA Swin talk transcript, uticex.com article
+// 1598, section 2), so dq, dk and dv land at exactly the channels q, k and v came from.
+//
+// Per window and head (P row-stochastic, dO upstream gradient of O):
+//   dP = dO V^T,  D_i = sum_j P_ij dP_ij,  dS = P o (dP - D),
+//   dQ = scale dS K,  dK = scale dS^T Q,  dV = P^T dO,
+//   dtable[idx(i,j), h] += dS_ij   (fp32 dS, never bf16-rounded).
+// Warp w owns query rows [16w, 16w+16) for S, P, dP, dS and dQ, then key rows
+// [16w, 16w+16) for dK and dV, reading every warp's P and dS from shared memory. The
+// per-(i,j) dS sums stay in registers across the CTA's windows; at the end one thread
+// per table row folds them in a fixed order into a per-CTA partial, and a second
+// kernel sums the partials in a fixed order: the result is deterministic.
+#include "common.cuh"
+
+namespace swin {
+
+template <int M>
+struct BGeo {
+  using G = Geo<M>;
+  static constexpr int PS_STRIDE = G::NPAD * 2 + 16;  // bytes per row of the P / dS tiles
+  static constexpr int PS_BYTES = G::NPAD * PS_STRIDE;
+  static constexpr int STAGE_BYTES = 4 * G::TILE_BYTES;  // q, k, v, dO
+  static constexpr int CHUNKS = 4 * G::N * 4;
+  static constexpr int CH_ITERS = (CHUNKS + G::THREADS - 1) / G::THREADS;
+  static constexpr int STG_BYTES = G::WARPS * 16 * 64;  // per-warp bf16 output staging
+  static constexpr int R = (2 * M - 1) * (2 * M - 1);
+};
+
+struct BwdParams {
+  const void* qkv;
+  const void* dout;
+  void* dqkv;
+  const float* dense_bias;
+  const float* mask;
+  float* partial;  // [grid, R]
+  int H, W, C, nH, s, nWy, nWx, nW;
+  int64_t total_windows;
+  int chunks;
+  float qk_scale_log2;
+  float scale;
+};
+
+template <int M, int STAGES>
+constexpr int bwd_smem_bytes() {
+  return Geo<M>::BIAS_BYTES + Geo<M>::MASK_BYTES + 2 * BGeo<M>::PS_BYTES + BGeo<M>::STG_BYTES +
+         STAGES * BGeo<M>::STAGE_BYTES;
+}
+
+// Store a warp's 16 rows x 32 channels (fp32 fragments of m16n8 tiles nd = 0..3) scaled
+// by `mul` to slice `slice` (0: q, 1: k, 2: v) of the gradient tensor at the tokens of
+// window rows 16*warp + r.
+template <int M, typename TIO>
+__device__ __forceinline__ void store_rows(float (&acc)[4][4], float mul, unsigned char* stg,
+                                           TIO* dqkv, int slice, int warp, int lane, int b,
+                                           int wy, int wx, int s, int H, int W, int C, int h) {
+  constexpr int N = M * M;
+  const int g = lane >> 2, t = lane & 3;
+  if constexpr (sizeof(TIO) == 2) {
+#pragma unroll
+    for (int nd = 0; nd < 4; ++nd) {
+      *reinterpret_cast<uint32_t*>(stg + tile_off(g, nd) + 4 * t) =
+          pack_bf16(acc[nd][0] * mul, acc[nd][1] * mul);
+      *reinterpret_cast<uint32_t*>(stg + tile_off(g + 8, nd) + 4 * t) =
+          pack_bf16(acc[nd][2] * mul, acc[nd][3] * mul);
+    }
+    __syncwarp();
+#pragma unroll
+    for (int e = lane; e < 64; e += 32) {
+      const int r = e >> 2, c = e & 3, i = warp * 16 + r;
+      if (i < N) {
+        const int64_t tok = gather_token(b, wy, wx, i, M, s, H, W);
+        *reinterpret_cast<uint4*>(dqkv + tok * 3 * C + slice * C + h * kHeadDim + c * 8) =
+            *reinterpret_cast<const uint4*>(stg + tile_off(r, c));
+      }
+    }
+    __syncwarp();
+  } else {
+    const int i0 = warp * 16 + g, i1 = i0 + 8;
+    if (i0 < N) {
+      float* dst = dqkv + gather_token(b, wy, wx, i0, M, s, H, W) * 3 * C + slice * C + h * kHeadDim + 2 * t;
+#pragma unroll
+      for (int nd = 0; nd < 4; ++nd)
+        *reinterpret_cast<float2*>(dst + nd * 8) = make_float2(acc[nd][0] * mul, acc[nd][1] * mul);
+    }
+    if (i1 < N) {
+      float* dst = dqkv + gather_token(b, wy, wx, i1, M, s, H, W) * 3 * C + slice * C + h * kHeadDim + 2 * t;
+#pragma unroll
+      for (int nd = 0; nd < 4; ++nd)
+        *reinterpret_cast<float2*>(dst + nd * 8) = make_float2(acc[nd][2] * mul, acc[nd][3] * mul);
+    }
+  }
+}
+
+template <int M, typename TIO, int STAGES>
+__global__ void __launch_bounds__(Geo<M>::THREADS) bwd_kernel(const BwdParams p) {
+  using G = Geo<M>;
+  using BG = BGeo<M>;
+  constexpr int N = G::N, NT = G::NT, KT = G::KT, MW = G::MW, THREADS = G::THREADS;
+  constexpr int PS = BG::PS_STRIDE;
+  extern __shared__ __align__(128) unsigned char smem[];
+  float4* sbias = reinterpret_cast<float4*>(smem);
+  uint32_t* smask = reinterpret_cast<uint32_t*>(smem + G::BIAS_BYTES);
+  unsigned char* sP = smem + G::BIAS_BYTES + G::MASK_BYTES;
+  unsigned char* sdS = sP + BG::PS_BYTES;
+  unsigned char* sstg = sdS + BG::PS_BYTES;
+  unsigned char* stiles = sstg + BG::STG_BYTES;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, t = lane & 3;
+  const int h = blockIdx.x % p.nH;
+  const int chunk = blockIdx.x / p.nH;
+  const int64_t w_begin = p.total_windows * chunk / p.chunks;
+  const int nwin = (int)(p.total_windows * (chunk + 1) / p.chunks - w_begin);
+  const int C = p.C, H = p.H, W = p.W, s = p.s;
+  unsigned char* stg = sstg + warp * 16 * 64;
+
+  auto issue = [&](int64_t widx, int stage) {
+    const int b = (int)(widx / p.nW), w = (int)(widx % p.nW);
+    const int wy = w / p.nWx, wx = w % p.nWx;
+    unsigned char* base = stiles + stage * BG::STAGE_BYTES;
+#pragma unroll
+    for (int k = 0; k < BG::CH_ITERS; ++k) {
+      const int id = tid + k * THREADS;
+      if (id < BG::CHUNKS) {
+        const int c = id & 3, rest = id >> 2;
+        const int i = rest % N, tt = rest / N;
+        const int64_t tok = gather_token(b, wy, wx, i, M, s, H, W);
+        const TIO* src = tt < 3
+            ? reinterpret_cast<const TIO*>(p.qkv) + tok * 3 * C + tt * C + h * kHeadDim + c * 8
+            : reinterpret_cast<const TIO*>(p.dout) + tok * C + h * kHeadDim + c * 8;
+        load_chunk<TIO>(smem_u32(base + tt * G::TILE_BYTES + tile_off(i, c)), src);
+      }
+    }
+  };
+
+#pragma unroll
+  for (int st = 0; st < STAGES - 1; ++st) {
+    if (st < nwin) issue(w_begin + st, st);
+    cp_async_commit();
+  }
+
+  if constexpr (G::NPAD > N) {
+    constexpr int PADROWS = G::NPAD - N;
+    for (int e = tid; e < STAGES * 4 * PADROWS * 4; e += THREADS) {
+      const int c = e & 3, r = (e >> 2) % PADROWS, tile = (e >> 2) / PADROWS;
+      *reinterpret_cast<uint4*>(stiles + tile * G::TILE_BYTES + tile_off(N + r, c)) =
+          make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+  // P and dS tiles start zeroed: columns NT*8..NPAD-1 are never written.
+  for (int e = tid; e < 2 * BG::PS_BYTES / 16; e += THREADS)
+    reinterpret_cast<uint4*>(sP)[e] = make_uint4(0u, 0u, 0u, 0u);
+  {
+    const float* db = p.dense_bias + (int64_t)h * N * N;
+    for (int e = tid; e < G::WARPS * NT * 32; e += THREADS) {
+      const int ln = e & 31, nt = (e >> 5) % NT, wp = (e >> 5) / NT;
+      const int r0 = wp * 16 + (ln >> 2), c0 = nt * 8 + 2 * (ln & 3);
+      float v[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int r = r0 + 8 * (q >> 1), c = c0 + (q & 1);
+        v[q] = c >= N ? -INFINITY : (r >= N ? 0.0f : db[r * N + c] * kLog2e);
+      }
+      sbias[e] = make_float4(v[0], v[1], v[2], v[3]);
+    }
+  }
+  if (p.mask != nullptr) {
+    for (int cls = 1; cls < 4; ++cls) {
+      const int wy = (cls & 2) ? p.nWy - 1 : 0, wx = (cls & 1) ? p.nWx - 1 : 0;
+      const float* mw = p.mask + (int64_t)(wy * p.nWx + wx) * N * N;
+      uint32_t bits[MW];
+#pragma unroll
+      for (int m = 0; m < MW; ++m) bits[m] = 0u;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int r = warp * 16 + g + 8 * (q >> 1), c = nt * 8 + 2 * t + (q & 1);
+          if (r < N && c < N && mw[r * N + c] != 0.0f) bits[(nt * 4 + q) >> 5] |= 1u << ((nt * 4 + q) & 31);
+        }
+#pragma unroll
+      for (int m = 0; m < MW; ++m) smask[(cls * MW + m) * THREADS + tid] = bits[m];
+    }
+  }
+
+  const float mask_l2 = kMaskValue * kLog2e;
+  const float4* bfrag = sbias + warp * NT * 32 + lane;
+  const int r0 = warp * 16 + g, r1 = r0 + 8;
+  float dtacc[NT][4];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) dtacc[nt][0] = dtacc[nt][1] = dtacc[nt][2] = dtacc[nt][3] = 0.0f;
+
+  for (int it = 0; it < nwin; ++it) {
+    cp_async_wait<STAGES - 2>();
+    __syncthreads();
+    {
+      const int nx = it + STAGES - 1;
+      if (nx < nwin) issue(w_begin + nx, nx % STAGES);
+      cp_async_commit();
+    }
+    const int64_t widx = w_begin + it;
+    const int b = (int)(widx / p.nW), w = (int)(widx % p.nW);
+    const int wy = w / p.nWx, wx = w % p.nWx;
+    const uint32_t qb = smem_u32(stiles + (it % STAGES) * BG::STAGE_BYTES);
+    const uint32_t kb = qb + G::TILE_BYTES, vb = kb + G::TILE_BYTES, ob = vb + G::TILE_BYTES;
+
+    // ---- recompute S and P ---------------------------------------------------------
+    float pr[NT][4];
+    {
+      uint32_t qa[2][4];
+      const int mi = lane >> 3, row = warp * 16 + (lane & 7) + ((mi & 1) << 3);
+#pragma unroll
+      for (int kk = 0; kk < 2; ++kk)
+        ldsm_x4(qb + tile_off(row, 2 * kk + (mi >> 1)), qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        pr[nt][0] = pr[nt][1] = pr[nt][2] = pr[nt][3] = 0.0f;
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(kb + tile_off(nt * 8 + (lane & 7), lane >> 3), b0, b1, b2, b3);
+        mma_bf16(pr[nt], qa[0][0], qa[0][1], qa[0][2], qa[0][3], b0, b1);
+        mma_bf16(pr[nt], qa[1][0], qa[1][1], qa[1][2], qa[1][3], b2, b3);
+      }
+    }
+    int cls = 0;
+    if (p.mask != nullptr) cls = (wy == p.nWy - 1 ? 2 : 0) | (wx == p.nWx - 1 ? 1 : 0);
+    uint32_t mb[MW];
+#pragma unroll
+    for (int m = 0; m < MW; ++m) mb[m] = cls ? smask[(cls * MW + m) * THREADS + tid] : 0u;
+    float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const float4 bb = bfrag[nt * 32];
+      float z0 = fmaf(pr[nt][0], p.qk_scale_log2, bb.x);
+      float z1 = fmaf(pr[nt][1], p.qk_scale_log2, bb.y);
+      float z2 = fmaf(pr[nt][2], p.qk_scale_log2, bb.z);
+      float z3 = fmaf(pr[nt][3], p.qk_scale_log2, bb.w);
+      if (cls) {
+        const uint32_t word = mb[(nt * 4) >> 5], sh = (nt * 4) & 31;
+        if ((word >> sh) & 1u) z0 += mask_l2;
+        if ((word >> (sh + 1)) & 1u) z1 += mask_l2;
+        if ((word >> (sh + 2)) & 1u) z2 += mask_l2;
+        if ((word >> (sh + 3)) & 1u) z3 += mask_l2;
+      }
+      pr[nt][0] = z0;
+      pr[nt][1] = z1;
+      pr[nt][2] = z2;
+      pr[nt][3] = z3;
+      mx0 = fmaxf(mx0, fmaxf(z0, z1));
+      mx1 = fmaxf(mx1, fmaxf(z2, z3));
+    }
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+    float l0 = 0.0f, l1 = 0.0f;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      pr[nt][0] = fast_exp2(pr[nt][0] - mx0);
+      pr[nt][1] = fast_exp2(pr[nt][1] - mx0);
+      pr[nt][2] = fast_exp2(pr[nt][2] - mx1);
+      pr[nt][3] = fast_exp2(pr[nt][3] - mx1);
+      l0 += pr[nt][0] + pr[nt][1];
+      l1 += pr[nt][2] + pr[nt][3];
+    }
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+    // Normalised probabilities; padded query rows are zeroed so they add nothing below.
+    const float inv0 = r0 < N ? 1.0f / l0 : 0.0f, inv1 = r1 < N ? 1.0f / l1 : 0.0f;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      pr[nt][0] *= inv0;
+      pr[nt][1] *= inv0;
+      pr[nt][2] *= inv1;
+      pr[nt][3] *= inv1;
+    }
+
+    // ---- dP = dO V^T ---------------------------------------------------------------
+    float ds[NT][4];
+    {
+      uint32_t da[2][4];
+      const int mi = lane >> 3, row = warp * 16 + (lane & 7) + ((mi & 1) << 3);
+#pragma unroll
+      for (int kk = 0; kk < 2; ++kk)
+        ldsm_x4(ob + tile_off(row, 2 * kk + (mi >> 1)), da[kk][0], da[kk][1], da[kk][2], da[kk][3]);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        ds[nt][0] = ds[nt][1] = ds[nt][2] = ds[nt][3] = 0.0f;
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(vb + tile_off(nt * 8 + (lane & 7), lane >> 3), b0, b1, b2, b3);
+        mma_bf16(ds[nt], da[0][0], da[0][1], da[0][2], da[0][3], b0, b1);
+        mma_bf16(ds[nt], da[1][0], da[1][1], da[1][2], da[1][3], b2, b3);
+      }
+    }
+    // ---- D = rowsum(P o dP), dS = P o (dP - D) ---------------------------------------
+    float D0 = 0.0f, D1 = 0.0f;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      D0 = fmaf(pr[nt][0], ds[nt][0], fmaf(pr[nt][1], ds[nt][1], D0));
+      D1 = fmaf(pr[nt][2], ds[nt][2], fmaf(pr[nt][3], ds[nt][3], D1));
+    }
+    D0 += __shfl_xor_sync(0xffffffffu, D0, 1);
+    D0 += __shfl_xor_sync(0xffffffffu, D0, 2);
+    D1 += __shfl_xor_sync(0xffffffffu, D1, 1);
+    D1 += __shfl_xor_sync(0xffffffffu, D1, 2);
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      ds[nt][0] = pr[nt][0] * (ds[nt][0] - D0);
+      ds[nt][1] = pr[nt][1] * (ds[nt][1] - D0);
+      ds[nt][2] = pr[nt][2] * (ds[nt][2] - D1);
+      ds[nt][3] = pr[nt][3] * (ds[nt][3] - D1);
+      dtacc[nt][0] += ds[nt][0];
+      dtacc[nt][1] += ds[nt][1];
+      dtacc[nt][2] += ds[nt][2];
+      dtacc[nt][3] += ds[nt][3];
+      const int col2 = (nt * 8 + 2 * t) * 2;
+      *reinterpret_cast<uint32_t*>(sP + r0 * PS + col2) = pack_bf16(pr[nt][0], pr[nt][1]);
+      *reinterpret_cast<uint32_t*>(sP + r1 * PS + col2) = pack_bf16(pr[nt][2], pr[nt][3]);
+      *reinterpret_cast<uint32_t*>(sdS + r0 * PS + col2) = pack_bf16(ds[nt][0], ds[nt][1]);
+      *reinterpret_cast<uint32_t*>(sdS + r1 * PS + col2) = pack_bf16(ds[nt][2], ds[nt][3]);
+    }
+
+    // ---- dQ = scale dS K --------------------------------------------------------------
+    {
+      float dq[4][4];
+#pragma unroll
+      for (int nd = 0; nd < 4; ++nd) dq[nd][0] = dq[nd][1] = dq[nd][2] = dq[nd][3] = 0.0f;
+#pragma unroll
+      for (int kk = 0; kk < KT; ++kk) {
+        const uint32_t a0 = pack_bf16(ds[2 * kk][0], ds[2 * kk][1]);
+        const uint32_t a1 = pack_bf16(ds[2 * kk][2], ds[2 * kk][3]);
+        uint32_t a2 = 0u, a3 = 0u;
+        if (2 * kk + 1 < NT) {
+          a2 = pack_bf16(ds[2 * kk + 1][0], ds[2 * kk + 1][1]);
+          a3 = pack_bf16(ds[2 * kk + 1][2], ds[2 * kk + 1][3]);
+        }
+        const int mi = lane >> 3, row = kk * 16 + (lane & 7) + ((mi & 1) << 3);
+#pragma unroll
+        for (int pp = 0; pp < 2; ++pp) {
+          uint32_t v0, v1, v2, v3;
+          ldsm_x4_t(kb + tile_off(row, 2 * pp + (mi >> 1)), v0, v1, v2, v3);
+          mma_bf16(dq[2 * pp], a0, a1, a2, a3, v0, v1);
+          mma_bf16(dq[2 * pp + 1], a0, a1, a2, a3, v2, v3);
+        }
+      }
+      store_rows<M, TIO>(dq, p.scale, stg, reinterpret_cast<TIO*>(p.dqkv), 0, warp, lane, b, wy, wx,
+                         s, H, W, C, h);
+    }
+    __syncthreads();  // every warp's P and dS rows are in shared memory
+
+    // ---- dK = scale dS^T Q and dV = P^T dO for key rows [16w, 16w+16) -----------------
+    {
+      float dk[4][4], dv[4][4];
+#pragma unroll
+      for (int nd = 0; nd < 4; ++nd) {
+        dk[nd][0] = dk[nd][1] = dk[nd][2] = dk[nd][3] = 0.0f;
+        dv[nd][0] = dv[nd][1] = dv[nd][2] = dv[nd][3] = 0.0f;
+      }
+      const int mi = lane >> 3;
+#pragma unroll
+      for (int kk = 0; kk < KT; ++kk) {
+        const int rowA = kk * 16 + (lane & 7) + 8 * (mi >> 1), chA = 2 * warp + (mi & 1);
+        uint32_t a0, a1, a2, a3, p0, p1, p2, p3;
+        ldsm_x4_t(smem_u32(sdS + rowA * PS + chA * 16), a0, a1, a2, a3);
+        ldsm_x4_t(smem_u32(sP + rowA * PS + chA * 16), p0, p1, p2, p3);
+        const int rowB = kk * 16 + (lane & 7) + ((mi & 1) << 3);
+#pragma unroll
+        for (int pp = 0; pp < 2; ++pp) {
+          uint32_t q0, q1, q2, q3, d0, d1, d2, d3;
+          ldsm_x4_t(qb + tile_off(rowB, 2 * pp + (mi >> 1)), q0, q1, q2, q3);
+          mma_bf16(dk[2 * pp], a0, a1, a2, a3, q0, q1);
+          mma_bf16(dk[2 * pp + 1], a0, a1, a2, a3, q2, q3);
+          ldsm_x4_t(ob + tile_off(rowB, 2 * pp + (mi >> 1)), d0, d1, d2, d3);
+          mma_bf16(dv[2 * pp], p0, p1, p2, p3, d0, d1);
+          mma_bf16(dv[2 * pp + 1], p0, p1, p2, p3, d2, d3);
+        }
+      }
+      store_rows<M, TIO>(dk, p.scale, stg, reinterpret_cast<TIO*>(p.dqkv), 1, warp, lane, b, wy, wx,
+                         s, H, W, C, h);
+      store_rows<M, TIO>(dv, 1.0f, stg, reinterpret_cast<TIO*>(p.dqkv), 2, warp, lane, b, wy, wx,
+                         s, H, W, C, h);
+    }
+  }
+  cp_async_wait<0>();
+  __syncthreads();
+
+  // ---- fold the per-(i,j) dS sums into this CTA's table-gradient partial -------------
+  float* sdt = reinterpret_cast<float*>(stiles);  // N*N floats fit the tile buffers
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int r = r0 + 8 * (q >> 1), c = nt * 8 + 2 * t + (q & 1);
+      if (r < N && c < N) sdt[r * N + c] = dtacc[nt][q];
+    }
+  __syncthreads();
+  for (int rr = tid; rr < BG::R; rr += THREADS) {
+    const int dy = rr / (2 * M - 1) - (M - 1), dx = rr % (2 * M - 1) - (M - 1);
+    float acc = 0.0f;
+    for (int yi = 0; yi < M; ++yi) {
+      const int yj = yi - dy;
+      if (yj < 0 || yj >= M) continue;
+      for (int xi = 0; xi < M; ++xi) {
+        const int xj = xi - dx;
+        if (xj < 0 || xj >= M) continue;
+        acc += sdt[(yi * M + xi) * N + (yj * M + xj)];
+      }
+    }
+    p.partial[(int64_t)blockIdx.x * BG::R + rr] = acc;
+  }
+}
+
+// dtable[r, h] = sum over chunks c (in order) of partial[c*nH + h, r].
+__global__ void dtable_reduce_kernel(const float* __restrict__ partial, int R, int nH, int chunks,
+                                     float* __restrict__ dtable) {
+  const int e = blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= R * nH) return;
+  const int r = e / nH, h = e % nH;
+  float acc = 0.0f;
+  for (int c = 0; c < chunks; ++c) acc += partial[(int64_t)(c * nH + h) * R + r];
+  dtable[e] = acc;
+}
+
+// ---- host side ---------------------------------------------------------------------
+
+template <int M> struct BwdStages { static constexpr int value = 2; };
+
+template <int M, typename TIO, int STAGES>
+static cudaError_t bconfig_t(const Plan& pl, BwdLaunch* L) {
+  using G = Geo<M>;
+  constexpr int smem = bwd_smem_bytes<M, STAGES>();
+  static_assert(G::NPAD * G::NPAD * 4 <= STAGES * BGeo<M>::STAGE_BYTES, "dS sums must fit the tiles");
+  auto kern = bwd_kernel<M, TIO, STAGES>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  int occ = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, G::THREADS, smem);
+  if (e != cudaSuccess) return e;
+  if (occ < 1) return cudaErrorInvalidConfiguration;
+  const int64_t total = (int64_t)pl.B * pl.nW;
+  int64_t chunks = ((int64_t)pl.num_sms * occ) / pl.nH;
+  if (chunks < 1) chunks = 1;
+  if (total > 0 && chunks > total) chunks = total;
+  L->chunks = (int)chunks;
+  L->grid = (int)(chunks * pl.nH);
+  L->threads = G::THREADS;
+  L->smem = smem;
+  L->partial_rows = L->grid;
+  return cudaSuccess;
+}
+
+template <int M, typename TIO, int STAGES>
+static cudaError_t blaunch_t(const Plan& pl, const BwdLaunch& L, const void* qkv, const void* dout,
+                             void* dqkv, float* dtable, cudaStream_t st) {
+  BwdParams p;
+  p.qkv = qkv;
+  p.dout = dout;
+  p.dqkv = dqkv;
+  p.dense_bias = pl.dense_bias;
+  p.mask = pl.s > 0 ? pl.mask : nullptr;
+  p.partial = pl.dt_partial;
+  p.H = pl.H;
+  p.W = pl.W;
+  p.C = pl.C;
+  p.nH = pl.nH;
+  p.s = pl.s;
+  p.nWy = pl.nWy;
+  p.nWx = pl.nWx;
+  p.nW = pl.nW;
+  p.total_windows = (int64_t)pl.B * pl.nW;
+  p.chunks = L.chunks;
+  p.scale = 1.0f / sqrtf((float)kHeadDim);
+  p.qk_scale_log2 = p.scale * kLog2e;
+  bwd_kernel<M, TIO, STAGES><<<L.grid, L.threads, L.smem, st>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int R = BGeo<M>::R;
+  dtable_reduce_kernel<<<(R * pl.nH + 255) / 256, 256, 0, st>>>(pl.dt_partial, R, pl.nH, L.chunks,
+                                                                dtable);
+  return cudaGetLastError();
+}
+
+cudaError_t bwd_config(const Plan& pl, BwdLaunch* L) {
+  const bool f32 = pl.dtype == SWIN_WATTN_FP32;
+  switch (pl.M) {
+    case 4:
+      return f32 ? bconfig_t<4, float, BwdStages<4>::value>(pl, L)
+                 : bconfig_t<4, __nv_bfloat16, BwdStages<4>::value>(pl, L);
+    case 7:
+      return f32 ? bconfig_t<7, float, BwdStages<7>::value>(pl, L)
+                 : bconfig_t<7, __nv_bfloat16, BwdStages<7>::value>(pl, L);
+    default:  // no backward for this window size: the plan still serves the forward
+      *L = BwdLaunch();
+      return cudaSuccess;
+  }
+}
+
+cudaError_t bwd_launch(const Plan& pl, const BwdLaunch& L, const void* qkv, const void* dout,
+                       void* dqkv, float* dtable, cudaStream_t st) {
+  const bool f32 = pl.dtype == SWIN_WATTN_FP32;
+  switch (pl.M) {
+    case 4:
+      return f32 ? blaunch_t<4, float, BwdStages<4>::value>(pl, L, qkv, dout, dqkv, dtable, st)
+                 : blaunch_t<4, __nv_bfloat16, BwdStages<4>::value>(pl, L, qkv, dout, dqkv, dtable, st);
+    case 7:
+      return f32 ? blaunch_t<7, float, BwdStages<7>::value>(pl, L, qkv, dout, dqkv, dtable, st)
+                 : blaunch_t<7, __nv_bfloat16, BwdStages<7>::value>(pl, L, qkv, dout, dqkv, dtable, st);
+    default:
+      return cudaErrorNotSupported;
+  }
+}
+
+}  // namespace swin

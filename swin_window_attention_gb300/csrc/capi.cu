@@ -1,0 +1,266 @@
+// C ABI of the swin_wattn library: argument validation, plan ownership, launches and
+// error surfacing. No exception, abort or trap crosses this boundary.
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <unordered_set>
+
+#include "common.cuh"
+
+namespace swin {
+cudaError_t launch_expand_bias(const float* table, int nH, int M, float* dense, cudaStream_t st);
+cudaError_t launch_build_mask(int H, int W, int M, int s, float* mask, cudaStream_t st);
+cudaError_t launch_gather_map(int H, int W, int M, int s, int32_t* out, cudaStream_t st);
+cudaError_t launch_relidx(int M, int32_t* out, cudaStream_t st);
+cudaError_t fwd_config(const Plan& pl, FwdLaunch* L);
+cudaError_t fwd_launch(const Plan& pl, const FwdLaunch& L, const void* qkv, void* out,
+                       cudaStream_t st);
+cudaError_t bwd_config(const Plan& pl, BwdLaunch* L);
+cudaError_t bwd_launch(const Plan& pl, const BwdLaunch& L, const void* qkv, const void* dout,
+                       void* dqkv, float* dtable, cudaStream_t st);
+}  // namespace swin
+
+struct swin_wattn_plan_s {
+  swin::Plan p;
+  swin::FwdLaunch fwd;
+  swin::BwdLaunch bwd;
+};
+
+namespace {
+
+thread_local char g_last_error[256] = "";
+thread_local uint64_t g_launches = 0;
+
+int cuda_fail(cudaError_t e, const char* where) {
+  std::snprintf(g_last_error, sizeof(g_last_error), "%s: %s (%s)", where, cudaGetErrorName(e),
+                cudaGetErrorString(e));
+  return SWIN_WATTN_ERR_CUDA;
+}
+
+// A pointer the GPU can dereference: device or managed memory, or host memory mapped
+// into the device address space.
+int check_device_ptr(const void* ptr, size_t align) {
+  if (ptr == nullptr) return SWIN_WATTN_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(ptr) % align != 0) return SWIN_WATTN_ERR_MISALIGNED;
+  cudaPointerAttributes a;
+  cudaError_t e = cudaPointerGetAttributes(&a, ptr);
+  if (e != cudaSuccess) {
+    cudaGetLastError();  // clear the sticky-free error state of this query
+    return SWIN_WATTN_ERR_INVALID_ARG;
+  }
+  if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) return SWIN_WATTN_OK;
+  if (a.type == cudaMemoryTypeHost && a.devicePointer == ptr) return SWIN_WATTN_OK;
+  return SWIN_WATTN_ERR_INVALID_ARG;
+}
+
+// Live plans. A handle is checked against this set before it is dereferenced, so a
+// destroyed or foreign handle is reported instead of read.
+std::mutex g_plans_mu;
+std::unordered_set<const swin_wattn_plan_s*> g_plans;
+
+int check_plan(const swin_wattn_plan_s* pl) {
+  if (pl == nullptr) return SWIN_WATTN_ERR_BAD_PLAN;
+  {
+    std::lock_guard<std::mutex> lk(g_plans_mu);
+    if (g_plans.find(pl) == g_plans.end()) return SWIN_WATTN_ERR_BAD_PLAN;
+  }
+  if (pl->p.magic != swin::kPlanMagic) return SWIN_WATTN_ERR_BAD_PLAN;
+  return SWIN_WATTN_OK;
+}
+
+void free_plan_buffers(swin::Plan& p) {
+  if (p.dense_bias) cudaFree(p.dense_bias);
+  if (p.mask) cudaFree(p.mask);
+  if (p.dt_partial) cudaFree(p.dt_partial);
+  p.dense_bias = p.mask = p.dt_partial = nullptr;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* swin_wattn_status_string(int status) {
+  switch (status) {
+    case SWIN_WATTN_OK: return "ok";
+    case SWIN_WATTN_ERR_INVALID_ARG: return "invalid argument";
+    case SWIN_WATTN_ERR_UNSUPPORTED: return "unsupported shape";
+    case SWIN_WATTN_ERR_MISALIGNED: return "misaligned pointer";
+    case SWIN_WATTN_ERR_BAD_PLAN: return "bad plan handle";
+    case SWIN_WATTN_ERR_CUDA: return "CUDA error";
+    case SWIN_WATTN_ERR_TIMEOUT: return "device wait timed out";
+    default: return "unknown status";
+  }
+}
+
+const char* swin_wattn_last_error(void) { return g_last_error; }
+
+uint64_t swin_wattn_launch_count(int reset) {
+  const uint64_t n = g_launches;
+  if (reset) g_launches = 0;
+  return n;
+}
+
+int swin_wattn_plan(swin_wattn_plan_t* out, int B, int H, int W, int C, int num_heads,
+                    int window, int shift, int dtype, const float* bias_table,
+                    struct CUstream_st* stream) {
+  if (out == nullptr) return SWIN_WATTN_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (B < 0 || H <= 0 || W <= 0 || C <= 0 || num_heads <= 0) return SWIN_WATTN_ERR_INVALID_ARG;
+  if (dtype != SWIN_WATTN_BF16 && dtype != SWIN_WATTN_FP32) return SWIN_WATTN_ERR_INVALID_ARG;
+  if (window != 4 && window != 7 && window != 12) return SWIN_WATTN_ERR_UNSUPPORTED;
+  if (shift < 0 || shift >= window) return SWIN_WATTN_ERR_INVALID_ARG;
+  if (H % window != 0 || W % window != 0) return SWIN_WATTN_ERR_UNSUPPORTED;
+  if (C % num_heads != 0 || C / num_heads != swin::kHeadDim) return SWIN_WATTN_ERR_UNSUPPORTED;
+  if ((int64_t)B * H * W * 3 * C >= ((int64_t)1 << 40)) return SWIN_WATTN_ERR_UNSUPPORTED;
+  int rc = check_device_ptr(bias_table, 4);
+  if (rc != SWIN_WATTN_OK) return rc;
+
+  swin_wattn_plan_s* pl = new (std::nothrow) swin_wattn_plan_s();
+  if (pl == nullptr) return SWIN_WATTN_ERR_INVALID_ARG;
+  swin::Plan& p = pl->p;
+  std::memset(&p, 0, sizeof(p));
+  p.B = B;
+  p.H = H;
+  p.W = W;
+  p.C = C;
+  p.nH = num_heads;
+  p.M = window;
+  p.s = shift;
+  p.dtype = dtype;
+  p.N = window * window;
+  p.nWy = H / window;
+  p.nWx = W / window;
+  p.nW = p.nWy * p.nWx;
+
+  cudaError_t e = cudaGetDevice(&p.device);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&p.num_sms, cudaDevAttrMultiProcessorCount, p.device);
+  const size_t nn = (size_t)p.N * p.N;
+  if (e == cudaSuccess) e = cudaMalloc(&p.dense_bias, sizeof(float) * nn * p.nH);
+  // The mask tensor always exists (all zeros for s = 0) so that it can be dumped.
+  if (e == cudaSuccess) e = cudaMalloc(&p.mask, sizeof(float) * nn * p.nW);
+  if (e == cudaSuccess) e = swin::fwd_config(p, &pl->fwd);
+  if (e == cudaSuccess) e = swin::bwd_config(p, &pl->bwd);
+  if (e == cudaSuccess && pl->bwd.partial_rows > 0) {
+    p.dt_partial_rows = pl->bwd.partial_rows;
+    e = cudaMalloc(&p.dt_partial, sizeof(float) * (size_t)p.dt_partial_rows * (2 * p.M - 1) *
+                                      (2 * p.M - 1));
+  }
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (e == cudaSuccess) {
+    e = swin::launch_expand_bias(bias_table, p.nH, p.M, p.dense_bias, st);
+    ++g_launches;
+  }
+  if (e == cudaSuccess) {
+    e = swin::launch_build_mask(p.H, p.W, p.M, p.s, p.mask, st);
+    ++g_launches;
+  }
+  if (e != cudaSuccess) {
+    rc = cuda_fail(e, "swin_wattn_plan");
+    free_plan_buffers(p);
+    delete pl;
+    return rc;
+  }
+  p.magic = swin::kPlanMagic;
+  {
+    std::lock_guard<std::mutex> lk(g_plans_mu);
+    g_plans.insert(pl);
+  }
+  *out = pl;
+  return SWIN_WATTN_OK;
+}
+
+int swin_wattn_set_bias(swin_wattn_plan_t plan, const float* bias_table,
+                        struct CUstream_st* stream) {
+  int rc = check_plan(plan);
+  if (rc != SWIN_WATTN_OK) return rc;
+  rc = check_device_ptr(bias_table, 4);
+  if (rc != SWIN_WATTN_OK) return rc;
+  const swin::Plan& p = plan->p;
+  cudaError_t e = swin::launch_expand_bias(bias_table, p.nH, p.M, p.dense_bias,
+                                           reinterpret_cast<cudaStream_t>(stream));
+  ++g_launches;
+  return e == cudaSuccess ? SWIN_WATTN_OK : cuda_fail(e, "swin_wattn_set_bias");
+}
+
+int swin_wattn_fwd(swin_wattn_plan_t plan, const void* qkv, void* out,
+                   struct CUstream_st* stream) {
+  int rc = check_plan(plan);
+  if (rc != SWIN_WATTN_OK) return rc;
+  const swin::Plan& p = plan->p;
+  if (p.B == 0) return SWIN_WATTN_OK;
+  if ((rc = check_device_ptr(qkv, 16)) != SWIN_WATTN_OK) return rc;
+  if ((rc = check_device_ptr(out, 16)) != SWIN_WATTN_OK) return rc;
+  cudaError_t e = swin::fwd_launch(p, plan->fwd, qkv, out, reinterpret_cast<cudaStream_t>(stream));
+  ++g_launches;
+  return e == cudaSuccess ? SWIN_WATTN_OK : cuda_fail(e, "swin_wattn_fwd");
+}
+
+int swin_wattn_bwd(swin_wattn_plan_t plan, const void* qkv, const void* dout, void* dqkv,
+                   float* dtable, struct CUstream_st* stream) {
+  int rc = check_plan(plan);
+  if (rc != SWIN_WATTN_OK) return rc;
+  const swin::Plan& p = plan->p;
+  if (plan->bwd.grid == 0 && p.B > 0) return SWIN_WATTN_ERR_UNSUPPORTED;
+  if ((rc = check_device_ptr(dtable, 4)) != SWIN_WATTN_OK) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const size_t tbytes = sizeof(float) * (size_t)(2 * p.M - 1) * (2 * p.M - 1) * p.nH;
+  if (p.B == 0) {
+    cudaError_t e = cudaMemsetAsync(dtable, 0, tbytes, st);
+    return e == cudaSuccess ? SWIN_WATTN_OK : cuda_fail(e, "swin_wattn_bwd");
+  }
+  if ((rc = check_device_ptr(qkv, 16)) != SWIN_WATTN_OK) return rc;
+  if ((rc = check_device_ptr(dout, 16)) != SWIN_WATTN_OK) return rc;
+  if ((rc = check_device_ptr(dqkv, 16)) != SWIN_WATTN_OK) return rc;
+  cudaError_t e = swin::bwd_launch(p, plan->bwd, qkv, dout, dqkv, dtable, st);
+  g_launches += 2;
+  return e == cudaSuccess ? SWIN_WATTN_OK : cuda_fail(e, "swin_wattn_bwd");
+}
+
+int swin_wattn_debug_maps(swin_wattn_plan_t plan, int32_t* gather, int32_t* relidx,
+                          float* mask, float* dense_bias, struct CUstream_st* stream) {
+  int rc = check_plan(plan);
+  if (rc != SWIN_WATTN_OK) return rc;
+  const swin::Plan& p = plan->p;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const size_t nn = (size_t)p.N * p.N;
+  cudaError_t e = cudaSuccess;
+  if (gather) {
+    if ((rc = check_device_ptr(gather, 4)) != SWIN_WATTN_OK) return rc;
+    e = swin::launch_gather_map(p.H, p.W, p.M, p.s, gather, st);
+    ++g_launches;
+  }
+  if (e == cudaSuccess && relidx) {
+    if ((rc = check_device_ptr(relidx, 4)) != SWIN_WATTN_OK) return rc;
+    e = swin::launch_relidx(p.M, relidx, st);
+    ++g_launches;
+  }
+  if (e == cudaSuccess && mask) {
+    if ((rc = check_device_ptr(mask, 4)) != SWIN_WATTN_OK) return rc;
+    e = cudaMemcpyAsync(mask, p.mask, sizeof(float) * nn * p.nW, cudaMemcpyDeviceToDevice, st);
+  }
+  if (e == cudaSuccess && dense_bias) {
+    if ((rc = check_device_ptr(dense_bias, 4)) != SWIN_WATTN_OK) return rc;
+    e = cudaMemcpyAsync(dense_bias, p.dense_bias, sizeof(float) * nn * p.nH,
+                        cudaMemcpyDeviceToDevice, st);
+  }
+  return e == cudaSuccess ? SWIN_WATTN_OK : cuda_fail(e, "swin_wattn_debug_maps");
+}
+
+int swin_wattn_destroy(swin_wattn_plan_t plan) {
+  if (plan == nullptr) return SWIN_WATTN_OK;
+  int rc = check_plan(plan);
+  if (rc != SWIN_WATTN_OK) return rc;
+  {
+    std::lock_guard<std::mutex> lk(g_plans_mu);
+    g_plans.erase(plan);
+  }
+  cudaError_t e = cudaDeviceSynchronize();
+  plan->p.magic = 0;
+  free_plan_buffers(plan->p);
+  delete plan;
+  return e == cudaSuccess ? SWIN_WATTN_OK : cuda_fail(e, "swin_wattn_destroy");
+}
+
+}  // extern "C"

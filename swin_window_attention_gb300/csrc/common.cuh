@@ -1,0 +1,166 @@
+// Shared device helpers and the plan structure of the swin_wattn library (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/swin_wattn.h"
+
+namespace swin {
+
+constexpr uint32_t kPlanMagic = 0x5357414eu;  // "SWAN"
+constexpr int kHeadDim = 32;
+constexpr float kMaskValue = -100.0f;
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct Plan {
+  uint32_t magic;
+  int B, H, W, C, nH, M, s, dtype;
+  int N, nWy, nWx, nW;
+  int device;
+  int num_sms;
+  float* dense_bias;  // [nH, N, N], owned
+  float* mask;        // [nW, N, N], owned; null when s == 0
+  float* dt_partial;  // backward reduction scratch, owned
+  int dt_partial_rows;
+};
+
+// ---- geometry shared by every kernel that touches a window -----------------------
+
+// Original-grid token index (b*H + y)*W + x read by slot i of window w in batch b.
+// Rolled (y, x) = (wy*M + i/M, wx*M + i%M) reads original ((y+s) mod H, (x+s) mod W).
+__device__ __forceinline__ int64_t gather_token(int b, int wy, int wx, int i, int M, int s,
+                                                int H, int W) {
+  int y = wy * M + i / M + s;
+  int x = wx * M + i % M + s;
+  if (y >= H) y -= H;
+  if (x >= W) x -= W;
+  return ((int64_t)b * H + y) * W + x;
+}
+
+// Relative position index of local positions i, j in an M x M window.
+__device__ __forceinline__ int rel_index(int i, int j, int M) {
+  return (i / M - j / M + M - 1) * (2 * M - 1) + (i % M - j % M + M - 1);
+}
+
+// Shift-region label of a rolled coordinate pair (per axis [0,L-M), [L-M,L-s), [L-s,L)).
+__device__ __forceinline__ int region_1d(int c, int L, int M, int s) {
+  return c < L - M ? 0 : (c < L - s ? 1 : 2);
+}
+__device__ __forceinline__ int region_label(int ry, int rx, int H, int W, int M, int s) {
+  return 3 * region_1d(ry, H, M, s) + region_1d(rx, W, M, s);
+}
+
+// ---- PTX wrappers ----------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;\n" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                          uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+// D += A(16x16, row) * B(16x8, col), bf16 inputs, fp32 accumulate.
+__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Two fp32 -> packed bf16x2 (round to nearest even); `lo` lands in the low half.
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;\n" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Byte offset of 16-byte chunk c (0..3) of row r in a [rows][32 x bf16] shared tile,
+// XOR-swizzled so that 8 consecutive rows of one chunk column hit distinct banks.
+__device__ __forceinline__ uint32_t tile_off(int r, int c) {
+  return (uint32_t)(r * 64 + ((c ^ ((r >> 1) & 3)) << 4));
+}
+
+// ---- window tiles -------------------------------------------------------------------
+
+// Compile-time geometry of one window-head tile for window size M (hd = 32).
+template <int M_>
+struct Geo {
+  static constexpr int M = M_;
+  static constexpr int N = M * M;
+  static constexpr int MT = (N + 15) / 16;  // query row tiles = warps per CTA
+  static constexpr int NT = (N + 7) / 8;    // key n8 tiles of S
+  static constexpr int KT = MT;             // k16 steps of P.V
+  static constexpr int NPAD = MT * 16;      // rows of the shared q/k/v tiles
+  static constexpr int WARPS = MT;
+  static constexpr int THREADS = WARPS * 32;
+  static constexpr int MW = (NT * 4 + 31) / 32;  // mask words per thread per class
+  static constexpr int CHUNKS = 3 * N * 4;       // 16-byte bf16 chunks per window-head
+  static constexpr int CH_ITERS = (CHUNKS + THREADS - 1) / THREADS;
+  static constexpr int TILE_BYTES = NPAD * 64;
+  static constexpr int STAGE_BYTES = 3 * TILE_BYTES;
+  static constexpr int BIAS_BYTES = WARPS * NT * 32 * 16;
+  static constexpr int MASK_BYTES = 4 * MW * THREADS * 4;
+  static_assert(NT * 8 <= NPAD, "key tiles must fit the padded tile");
+};
+
+// One 16-byte bf16 chunk (8 channels) of a token's head slice into shared memory: a
+// cp.async for bf16 sources; fp32 sources are read, rounded to bf16 (nearest even) and
+// stored.
+template <typename TIO>
+__device__ __forceinline__ void load_chunk(uint32_t dst, const TIO* src);
+
+template <>
+__device__ __forceinline__ void load_chunk<__nv_bfloat16>(uint32_t dst, const __nv_bfloat16* src) {
+  cp_async_16(dst, src);
+}
+
+template <>
+__device__ __forceinline__ void load_chunk<float>(uint32_t dst, const float* src) {
+  const float4 a = __ldg(reinterpret_cast<const float4*>(src));
+  const float4 b = __ldg(reinterpret_cast<const float4*>(src) + 1);
+  const uint32_t w0 = pack_bf16(a.x, a.y), w1 = pack_bf16(a.z, a.w);
+  const uint32_t w2 = pack_bf16(b.x, b.y), w3 = pack_bf16(b.z, b.w);
+  asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(dst), "r"(w0), "r"(w1), "r"(w2),
+               "r"(w3)
+               : "memory");
+}
+
+struct FwdLaunch {
+  int grid = 0, threads = 0, smem = 0, chunks = 0;
+};
+struct BwdLaunch {
+  int grid = 0, threads = 0, smem = 0, chunks = 0, partial_rows = 0;
+};
+
+}  // namespace swin

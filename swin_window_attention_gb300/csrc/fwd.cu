@@ -1,0 +1,357 @@
+// Fused (shifted-)window attention forward for sm_103a.
+//
+// One kernel replaces the roll, window partition, batch GEMM, bias add, mask add,
+// softmax, batch GEMM, window reverse and un-roll chain (NVIDIA Swin talk transcript,
+// uticex.com article 1598, section 2 "training optimisation" for the window ops and
+// the fused attention, section 3 for the transposes folded into the fused kernel's
+// loads and stores; Baidu AIAK-Training talk, jxzklqfsx.com article 743345, section 2,
+// for the single fused WindowAttention kernel staging HBM -> shared -> registers).
+//
+// Work decomposition. A CTA owns one head h and a contiguous range of windows (across
+// the batch). Its dense bias (already log2(e)-scaled, in mma-fragment order) and the
+// shift-mask bit patterns of the four window classes (interior, last column, last row,
+// corner: the only patterns the region labels can form) are staged in shared memory
+// once. Each window's q/k/v head slices (64 bytes per token each) are gathered with
+// 16-byte cp.async straight from the rolled positions into a swizzled shared tile,
+// STAGES deep, so several windows are in flight per CTA. Warp w owns query rows
+// [16w, 16w+16): S = Q K^T on bf16 tensor cores (m16n8k16, fp32 accumulate), fused
+// scale + bias + mask, a register softmax with quad shuffles, P (bf16) V, and the
+// normalised rows go back to the token positions they were read from.
+#include "common.cuh"
+
+namespace swin {
+
+struct FwdParams {
+  const void* qkv;
+  void* out;
+  const float* dense_bias;  // [nH, N, N]
+  const float* mask;        // [nW, N, N] or null
+  int H, W, C, nH, s, nWy, nWx, nW;
+  int64_t total_windows;  // B * nW
+  int chunks;             // window ranges per head
+  float qk_scale_log2;    // hd^-0.5 * log2(e)
+};
+
+template <int M, typename TIO, int STAGES>
+constexpr int fwd_smem_bytes() {
+  return Geo<M>::BIAS_BYTES + Geo<M>::MASK_BYTES + STAGES * Geo<M>::STAGE_BYTES;
+}
+
+template <int M, typename TIO, int STAGES>
+__global__ void __launch_bounds__(Geo<M>::THREADS) fwd_kernel(const FwdParams p) {
+  using G = Geo<M>;
+  constexpr int N = G::N, NT = G::NT, KT = G::KT, MW = G::MW, THREADS = G::THREADS;
+  extern __shared__ __align__(128) unsigned char smem[];
+  float4* sbias = reinterpret_cast<float4*>(smem);
+  uint32_t* smask = reinterpret_cast<uint32_t*>(smem + G::BIAS_BYTES);
+  unsigned char* stiles = smem + G::BIAS_BYTES + G::MASK_BYTES;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, t = lane & 3;
+  const int h = blockIdx.x % p.nH;
+  const int chunk = blockIdx.x / p.nH;
+  const int64_t w_begin = p.total_windows * chunk / p.chunks;
+  const int nwin = (int)(p.total_windows * (chunk + 1) / p.chunks - w_begin);
+  const int C = p.C, H = p.H, W = p.W, s = p.s;
+
+  auto issue = [&](int64_t widx, int stage) {
+    const int b = (int)(widx / p.nW), w = (int)(widx % p.nW);
+    const int wy = w / p.nWx, wx = w % p.nWx;
+    unsigned char* base = stiles + stage * G::STAGE_BYTES;
+#pragma unroll
+    for (int k = 0; k < G::CH_ITERS; ++k) {
+      const int id = tid + k * THREADS;
+      if (id < G::CHUNKS) {
+        const int c = id & 3, rest = id >> 2;
+        const int i = rest % N, tt = rest / N;
+        const int64_t tok = gather_token(b, wy, wx, i, M, s, H, W);
+        const TIO* src = reinterpret_cast<const TIO*>(p.qkv) + tok * 3 * C + tt * C + h * kHeadDim + c * 8;
+        load_chunk<TIO>(smem_u32(base + tt * G::TILE_BYTES + tile_off(i, c)), src);
+      }
+    }
+  };
+
+  // Start the first windows' loads before the one-off staging below.
+#pragma unroll
+  for (int st = 0; st < STAGES - 1; ++st) {
+    if (st < nwin) issue(w_begin + st, st);
+    cp_async_commit();
+  }
+
+  // Padded rows N..NPAD-1 of every q/k/v tile are zero (loads never touch them).
+  if constexpr (G::NPAD > N) {
+    constexpr int PADROWS = G::NPAD - N;
+    for (int e = tid; e < STAGES * 3 * PADROWS * 4; e += THREADS) {
+      const int c = e & 3, r = (e >> 2) % PADROWS, tile = (e >> 2) / PADROWS;
+      *reinterpret_cast<uint4*>(stiles + tile * G::TILE_BYTES + tile_off(N + r, c)) =
+          make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+  // Bias fragments: lane (g,t) of warp wp, key tile nt holds rows 16wp+g, +8 and
+  // columns 8nt+2t, +1. Padded key columns get -inf, padded query rows 0.
+  {
+    const float* db = p.dense_bias + (int64_t)h * N * N;
+    for (int e = tid; e < G::WARPS * NT * 32; e += THREADS) {
+      const int ln = e & 31, nt = (e >> 5) % NT, wp = (e >> 5) / NT;
+      const int r0 = wp * 16 + (ln >> 2), c0 = nt * 8 + 2 * (ln & 3);
+      float v[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int r = r0 + 8 * (q >> 1), c = c0 + (q & 1);
+        v[q] = c >= N ? -INFINITY : (r >= N ? 0.0f : db[r * N + c] * kLog2e);
+      }
+      sbias[e] = make_float4(v[0], v[1], v[2], v[3]);
+    }
+  }
+  // Mask bit patterns of the window classes 1..3 (bit 1: last window row, bit 0: last
+  // window column), read from the plan's mask tensor at one window of each class.
+  if (p.mask != nullptr) {
+    for (int cls = 1; cls < 4; ++cls) {
+      const int wy = (cls & 2) ? p.nWy - 1 : 0, wx = (cls & 1) ? p.nWx - 1 : 0;
+      const float* mw = p.mask + (int64_t)(wy * p.nWx + wx) * N * N;
+      uint32_t bits[MW];
+#pragma unroll
+      for (int m = 0; m < MW; ++m) bits[m] = 0u;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int r = warp * 16 + g + 8 * (q >> 1), c = nt * 8 + 2 * t + (q & 1);
+          if (r < N && c < N && mw[r * N + c] != 0.0f) bits[(nt * 4 + q) >> 5] |= 1u << ((nt * 4 + q) & 31);
+        }
+#pragma unroll
+      for (int m = 0; m < MW; ++m) smask[(cls * MW + m) * THREADS + tid] = bits[m];
+    }
+  }
+
+  const float mask_l2 = kMaskValue * kLog2e;
+  const float4* bfrag = sbias + warp * NT * 32 + lane;
+
+  for (int it = 0; it < nwin; ++it) {
+    cp_async_wait<STAGES - 2>();
+    __syncthreads();
+    {
+      const int nx = it + STAGES - 1;
+      if (nx < nwin) issue(w_begin + nx, nx % STAGES);
+      cp_async_commit();
+    }
+    const int64_t widx = w_begin + it;
+    const int b = (int)(widx / p.nW), w = (int)(widx % p.nW);
+    const int wy = w / p.nWx, wx = w % p.nWx;
+    unsigned char* tq = stiles + (it % STAGES) * G::STAGE_BYTES;
+    const uint32_t qb = smem_u32(tq), kb = qb + G::TILE_BYTES, vb = kb + G::TILE_BYTES;
+
+    // ---- S = Q K^T -------------------------------------------------------------
+    uint32_t qa[2][4];
+    {
+      const int mi = lane >> 3, row = warp * 16 + (lane & 7) + ((mi & 1) << 3);
+#pragma unroll
+      for (int kk = 0; kk < 2; ++kk)
+        ldsm_x4(qb + tile_off(row, 2 * kk + (mi >> 1)), qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
+    }
+    float sacc[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.0f;
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4(kb + tile_off(nt * 8 + (lane & 7), lane >> 3), b0, b1, b2, b3);
+      mma_bf16(sacc[nt], qa[0][0], qa[0][1], qa[0][2], qa[0][3], b0, b1);
+      mma_bf16(sacc[nt], qa[1][0], qa[1][1], qa[1][2], qa[1][3], b2, b3);
+    }
+
+    // ---- logits (log2 domain): scale, bias, mask; row max ----------------------
+    int cls = 0;
+    if (p.mask != nullptr) cls = (wy == p.nWy - 1 ? 2 : 0) | (wx == p.nWx - 1 ? 1 : 0);
+    uint32_t mb[MW];
+#pragma unroll
+    for (int m = 0; m < MW; ++m) mb[m] = cls ? smask[(cls * MW + m) * THREADS + tid] : 0u;
+    float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const float4 bb = bfrag[nt * 32];
+      float z0 = fmaf(sacc[nt][0], p.qk_scale_log2, bb.x);
+      float z1 = fmaf(sacc[nt][1], p.qk_scale_log2, bb.y);
+      float z2 = fmaf(sacc[nt][2], p.qk_scale_log2, bb.z);
+      float z3 = fmaf(sacc[nt][3], p.qk_scale_log2, bb.w);
+      if (cls) {
+        const uint32_t word = mb[(nt * 4) >> 5], sh = (nt * 4) & 31;
+        if ((word >> sh) & 1u) z0 += mask_l2;
+        if ((word >> (sh + 1)) & 1u) z1 += mask_l2;
+        if ((word >> (sh + 2)) & 1u) z2 += mask_l2;
+        if ((word >> (sh + 3)) & 1u) z3 += mask_l2;
+      }
+      sacc[nt][0] = z0;
+      sacc[nt][1] = z1;
+      sacc[nt][2] = z2;
+      sacc[nt][3] = z3;
+      mx0 = fmaxf(mx0, fmaxf(z0, z1));
+      mx1 = fmaxf(mx1, fmaxf(z2, z3));
+    }
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+
+    // ---- softmax numerators and row sums -----------------------------------------
+    float l0 = 0.0f, l1 = 0.0f;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      sacc[nt][0] = fast_exp2(sacc[nt][0] - mx0);
+      sacc[nt][1] = fast_exp2(sacc[nt][1] - mx0);
+      sacc[nt][2] = fast_exp2(sacc[nt][2] - mx1);
+      sacc[nt][3] = fast_exp2(sacc[nt][3] - mx1);
+      l0 += sacc[nt][0] + sacc[nt][1];
+      l1 += sacc[nt][2] + sacc[nt][3];
+    }
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+
+    // ---- O = P V ------------------------------------------------------------------
+    float o[4][4];
+#pragma unroll
+    for (int nd = 0; nd < 4; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.0f;
+#pragma unroll
+    for (int kk = 0; kk < KT; ++kk) {
+      const uint32_t a0 = pack_bf16(sacc[2 * kk][0], sacc[2 * kk][1]);
+      const uint32_t a1 = pack_bf16(sacc[2 * kk][2], sacc[2 * kk][3]);
+      uint32_t a2 = 0u, a3 = 0u;
+      if (2 * kk + 1 < NT) {
+        a2 = pack_bf16(sacc[2 * kk + 1][0], sacc[2 * kk + 1][1]);
+        a3 = pack_bf16(sacc[2 * kk + 1][2], sacc[2 * kk + 1][3]);
+      }
+      const int mi = lane >> 3, row = kk * 16 + (lane & 7) + ((mi & 1) << 3);
+#pragma unroll
+      for (int pr = 0; pr < 2; ++pr) {
+        uint32_t v0, v1, v2, v3;
+        ldsm_x4_t(vb + tile_off(row, 2 * pr + (mi >> 1)), v0, v1, v2, v3);
+        mma_bf16(o[2 * pr], a0, a1, a2, a3, v0, v1);
+        mma_bf16(o[2 * pr + 1], a0, a1, a2, a3, v2, v3);
+      }
+    }
+
+    // ---- normalise and store at the gathered token positions ----------------------
+    const float inv0 = 1.0f / l0, inv1 = 1.0f / l1;
+    if constexpr (sizeof(TIO) == 2) {
+      // Stage the warp's 16 x 32 bf16 rows in its own Q rows (only this warp reads
+      // them, and they are consumed), then write 64 contiguous bytes per token.
+      const int r0 = warp * 16 + g, r1 = r0 + 8;
+#pragma unroll
+      for (int nd = 0; nd < 4; ++nd) {  // columns 8nd..8nd+7 = 16-byte chunk nd
+        if (r0 < N)
+          *reinterpret_cast<uint32_t*>(tq + tile_off(r0, nd) + 4 * t) =
+              pack_bf16(o[nd][0] * inv0, o[nd][1] * inv0);
+        if (r1 < N)
+          *reinterpret_cast<uint32_t*>(tq + tile_off(r1, nd) + 4 * t) =
+              pack_bf16(o[nd][2] * inv1, o[nd][3] * inv1);
+      }
+      __syncwarp();
+#pragma unroll
+      for (int e = lane; e < 64; e += 32) {
+        const int r = e >> 2, c = e & 3, i = warp * 16 + r;
+        if (i < N) {
+          const int64_t tok = gather_token(b, wy, wx, i, M, s, H, W);
+          const uint4 val = *reinterpret_cast<const uint4*>(tq + tile_off(i, c));
+          *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + tok * C + h * kHeadDim + c * 8) = val;
+        }
+      }
+    } else {
+      const int i0 = warp * 16 + g, i1 = i0 + 8;
+      float* outp = reinterpret_cast<float*>(p.out);
+      if (i0 < N) {
+        float* dst = outp + gather_token(b, wy, wx, i0, M, s, H, W) * C + h * kHeadDim + 2 * t;
+#pragma unroll
+        for (int nd = 0; nd < 4; ++nd)
+          *reinterpret_cast<float2*>(dst + nd * 8) = make_float2(o[nd][0] * inv0, o[nd][1] * inv0);
+      }
+      if (i1 < N) {
+        float* dst = outp + gather_token(b, wy, wx, i1, M, s, H, W) * C + h * kHeadDim + 2 * t;
+#pragma unroll
+        for (int nd = 0; nd < 4; ++nd)
+          *reinterpret_cast<float2*>(dst + nd * 8) = make_float2(o[nd][2] * inv1, o[nd][3] * inv1);
+      }
+    }
+  }
+  cp_async_wait<0>();
+}
+
+// ---- host side ---------------------------------------------------------------------
+
+template <int M, typename TIO, int STAGES>
+static cudaError_t config_t(const Plan& pl, FwdLaunch* L) {
+  using G = Geo<M>;
+  constexpr int smem = fwd_smem_bytes<M, TIO, STAGES>();
+  auto kern = fwd_kernel<M, TIO, STAGES>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  int occ = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, G::THREADS, smem);
+  if (e != cudaSuccess) return e;
+  if (occ < 1) return cudaErrorInvalidConfiguration;
+  const int64_t total = (int64_t)pl.B * pl.nW;
+  int64_t target = (int64_t)pl.num_sms * occ;
+  int64_t chunks = target / pl.nH;
+  if (chunks < 1) chunks = 1;
+  if (chunks > total) chunks = total;
+  L->chunks = (int)chunks;
+  L->grid = (int)(chunks * pl.nH);
+  L->threads = G::THREADS;
+  L->smem = smem;
+  return cudaSuccess;
+}
+
+template <int M, typename TIO, int STAGES>
+static cudaError_t launch_t(const Plan& pl, const FwdLaunch& L, const void* qkv, void* out,
+                            cudaStream_t st) {
+  FwdParams p;
+  p.qkv = qkv;
+  p.out = out;
+  p.dense_bias = pl.dense_bias;
+  p.mask = pl.s > 0 ? pl.mask : nullptr;
+  p.H = pl.H;
+  p.W = pl.W;
+  p.C = pl.C;
+  p.nH = pl.nH;
+  p.s = pl.s;
+  p.nWy = pl.nWy;
+  p.nWx = pl.nWx;
+  p.nW = pl.nW;
+  p.total_windows = (int64_t)pl.B * pl.nW;
+  p.chunks = L.chunks;
+  p.qk_scale_log2 = kLog2e / sqrtf((float)kHeadDim);
+  fwd_kernel<M, TIO, STAGES><<<L.grid, L.threads, L.smem, st>>>(p);
+  return cudaGetLastError();
+}
+
+// Pipeline depth per window size: enough windows in flight per SM while keeping the
+// shared-memory footprint within the residency target.
+template <int M> struct FwdStages { static constexpr int value = 3; };
+template <> struct FwdStages<12> { static constexpr int value = 2; };
+
+#define SWIN_FWD_DISPATCH(FN, ...)                                                       \
+  do {                                                                                  \
+    const bool f32 = pl.dtype == SWIN_WATTN_FP32;                                       \
+    switch (pl.M) {                                                                     \
+      case 4:                                                                           \
+        return f32 ? FN<4, float, FwdStages<4>::value>(__VA_ARGS__)                      \
+                   : FN<4, __nv_bfloat16, FwdStages<4>::value>(__VA_ARGS__);             \
+      case 7:                                                                           \
+        return f32 ? FN<7, float, FwdStages<7>::value>(__VA_ARGS__)                      \
+                   : FN<7, __nv_bfloat16, FwdStages<7>::value>(__VA_ARGS__);             \
+      case 12:                                                                          \
+        return f32 ? FN<12, float, FwdStages<12>::value>(__VA_ARGS__)                    \
+                   : FN<12, __nv_bfloat16, FwdStages<12>::value>(__VA_ARGS__);           \
+      default:                                                                          \
+        return cudaErrorInvalidValue;                                                   \
+    }                                                                                   \
+  } while (0)
+
+cudaError_t fwd_config(const Plan& pl, FwdLaunch* L) { SWIN_FWD_DISPATCH(config_t, pl, L); }
+
+cudaError_t fwd_launch(const Plan& pl, const FwdLaunch& L, const void* qkv, void* out,
+                       cudaStream_t st) {
+  SWIN_FWD_DISPATCH(launch_t, pl, L, qkv, out, st);
+}
+
+}  // namespace swin

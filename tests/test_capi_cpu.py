@@ -1,0 +1,73 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, exports every
+entry point include/swin_wattn.h declares, and rejects bad arguments before any CUDA
+call is made."""
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from swin_window_attention_gb300 import build, capi
+    build.build()
+    return capi
+
+
+def _declared():
+    txt = open(os.path.join(ROOT, "include", "swin_wattn.h")).read()
+    txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+    return sorted(set(re.findall(r"\b(swin_wattn_[a-z_]+)\s*\(", txt)))
+
+
+def test_header_declares_the_documented_entry_points():
+    names = _declared()
+    for n in ("swin_wattn_plan", "swin_wattn_fwd", "swin_wattn_bwd", "swin_wattn_set_bias",
+              "swin_wattn_debug_maps", "swin_wattn_destroy", "swin_wattn_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    so = lib.load()
+    for n in _declared():
+        assert hasattr(so, n), n
+    assert set(_declared()) == set(lib.SIGNATURES)
+
+
+def test_status_strings(lib):
+    for code in range(7):
+        assert lib.swin_wattn_status_string(code)
+    assert lib.swin_wattn_status_string(99) == "unknown status"
+
+
+@pytest.mark.parametrize("args,status", [
+    # (B, H, W, C, nH, M, s, dtype)
+    ((1, 8, 8, 64, 2, 5, 0, 0), 2),     # window size not supported
+    ((1, 8, 8, 64, 2, 4, 4, 0), 1),     # shift >= M
+    ((1, 8, 8, 64, 2, 4, -1, 0), 1),    # negative shift
+    ((1, 10, 8, 64, 2, 4, 0, 0), 2),    # H not a multiple of M
+    ((1, 8, 8, 96, 2, 4, 0, 0), 2),     # head width 48
+    ((1, 8, 8, 64, 3, 4, 0, 0), 2),     # C not divisible by nH
+    ((1, 8, 8, 64, 2, 4, 0, 7), 1),     # bad dtype code
+    ((-1, 8, 8, 64, 2, 4, 0, 0), 1),    # negative batch
+    ((1, 0, 8, 64, 2, 4, 0, 0), 1),     # empty grid
+])
+def test_plan_rejects_bad_shapes_before_touching_cuda(lib, args, status):
+    rc, h = lib.swin_wattn_plan(*args, None, None)
+    assert rc == status and h is None
+
+
+def test_null_and_foreign_plan_handles(lib):
+    assert lib.swin_wattn_fwd(None, None, None, None) == lib.ERR_BAD_PLAN
+    assert lib.swin_wattn_bwd(12345678, None, None, None, None, None) == lib.ERR_BAD_PLAN
+    assert lib.swin_wattn_set_bias(None, None, None) == lib.ERR_BAD_PLAN
+    assert lib.swin_wattn_debug_maps(None, None, None, None, None, None) == lib.ERR_BAD_PLAN
+    assert lib.swin_wattn_destroy(None) == lib.OK
+    assert lib.swin_wattn_destroy(987654) == lib.ERR_BAD_PLAN
+
+
+def test_null_out_handle(lib):
+    so = lib.load()
+    assert so.swin_wattn_plan(None, 1, 8, 8, 64, 2, 4, 0, 0, None, None) == lib.ERR_INVALID_ARG
