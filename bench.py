@@ -1,0 +1,506 @@
+"""Benchmark of the fused shifted-window attention on GB300.
+
+A step is one pass of the hot path over the Swin-L 224 stage sweep at batch 64: the
+fused forward of each of the four stages (56x56 C=192 nH=6 s=3; 28x28 C=384 nH=12 s=3;
+14x14 C=768 nH=24 s=3; 7x7 C=1536 nH=48 s=0; window 7, bf16), with the dense bias and
+shift mask built once per plan. The line also reports the Swin-B 224 training step (bias
+re-expansion + forward + backward of its four stages) as `train_step`.
+
+Prints one JSON line (rank 0). `value` is tokens/s over the whole job with inputs
+resident in HBM; `e2e` is the same metric through the host-buffer entry point, with the
+host<->device copies inside the timed region. `--impl reference` times the fp64 CPU
+oracle on a bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from swin_window_attention_gb300 import inputs  # noqa: E402
+
+METRIC = "fused SW-MSA fwd/bwd tokens/s on 1 GB300; achieved HBM GB/s as % of roofline"
+SWEEP = ["swin_l224_s1", "swin_l224_s2", "swin_l224_s3", "swin_l224_s4"]
+TRAIN = ["swin_b224_s1", "swin_b224_s2", "swin_b224_s3", "swin_b224_s4"]
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ---- algorithmic work per launch --------------------------------------------------------
+
+def fwd_bytes(wl) -> int:
+    """qkv read + output write + dense bias + shift mask (s > 0)."""
+    esz = 2 if wl.dtype == "bf16" else 4
+    nn = wl.N * wl.N
+    return (wl.tokens * 4 * wl.C * esz + wl.nH * nn * 4 + (wl.nW * nn * 4 if wl.s > 0 else 0))
+
+
+def bwd_bytes(wl) -> int:
+    """qkv + dO read, dqkv write, dense bias, mask, table gradient write."""
+    esz = 2 if wl.dtype == "bf16" else 4
+    nn = wl.N * wl.N
+    return (wl.tokens * 10 * wl.C * esz + wl.nH * nn * 4 + (wl.nW * nn * 4 if wl.s > 0 else 0)
+            + (2 * wl.M - 1) ** 2 * wl.nH * 4)
+
+
+def fwd_flops(wl) -> int:
+    return 4 * wl.N * wl.N * wl.hd * wl.window_heads
+
+
+def bwd_flops(wl) -> int:
+    return 10 * wl.N * wl.N * wl.hd * wl.window_heads
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "swin_window_attention_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel_hash: str):
+    """Per-launch DRAM bytes of the forward kernel on the first sweep stage, from the
+    committed ncu summary, if it was captured on the current kernel sources."""
+    path = os.path.join(ROOT, "profiles", "fwd_swin_l224_s1_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if d.get("kernel_source_hash") != kernel_hash:
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+# ---- clocks -----------------------------------------------------------------------------
+
+class ClockSampler:
+    """nvidia-smi sampled every 100 ms in the background; only samples taken while the
+    timed region ran (by wall clock) count."""
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.gpu = gpu_index
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def mark(self, begin: bool):
+        if begin:
+            self.t0 = time.time()
+        else:
+            self.t1 = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        import datetime
+        rows = []
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                ts = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(f[1]), float(f[2]), f[5:9]))
+            except ValueError:
+                continue
+        inside = [r for r in rows if self.t0 is not None and self.t0 - 0.1 <= r[0] <= self.t1 + 0.1]
+        if not inside and rows and self.t0 is not None:
+            inside = [min(rows, key=lambda r: abs(r[0] - self.t0))]
+        reasons = set()
+        for r in inside:
+            for n, v in zip(self.NAMES, r[3]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(r[1] for r in inside) if inside else None,
+                "sm_max_mhz": inside[0][2] if inside else None, "reasons": sorted(reasons),
+                "samples": len(inside), "timed_region_s": round((self.t1 or 0) - (self.t0 or 0), 3)}
+
+
+# ---- GPU arm ----------------------------------------------------------------------------
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, ws: int) -> float:
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def cpu_baseline(wls, target_s: float = 12.0):
+    """The fp64 oracle, as it stands, on host cores: images of the sweep one at a time,
+    round-robin over the stages, until about `target_s` seconds have been spent."""
+    import oracle
+    oracle.build()
+    cores = oracle.max_threads()
+    data = []
+    for wl in wls:
+        one = wl.with_batch(1)
+        q = inputs.act_f64(inputs.make_qkv(one))
+        t = inputs.make_table(wl).double().numpy()
+        data.append((wl, q, t))
+    tokens, images, t0 = 0, 0, time.perf_counter()
+    while True:
+        for wl, q, t in data:
+            oracle.fwd(q, t, wl.nH, wl.M, wl.s)
+            tokens += wl.H * wl.W
+            images += 1
+        el = time.perf_counter() - t0
+        if el >= target_s:
+            break
+    return {"value": tokens / el, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{images} images ({images // len(data)} per stage) of the sweep, "
+                      f"batch 1 each, {el:.1f} s wall"}
+
+
+def run_gpu(args):
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from swin_window_attention_gb300 import build, capi
+    if rank == 0 or ws == 1:
+        build.build()
+    barrier(ws)
+    lib = capi.load()
+    stream = torch.cuda.Stream(device=dev)
+    sh = stream.cuda_stream
+
+    # ---- inference sweep: plans and resident inputs ------------------------------------
+    sweep = [inputs.BY_NAME[n] for n in (args.workload or SWEEP)]
+    plans, qkvs, outs, hosts = [], [], [], []
+    with torch.cuda.stream(stream):
+        for wl in sweep:
+            q = inputs.make_qkv(wl)
+            tab = inputs.make_table(wl).to(dev)
+            rc, h = capi.swin_wattn_plan(wl.B, wl.H, wl.W, wl.C, wl.nH, wl.M, wl.s, capi.BF16,
+                                         tab.data_ptr(), sh)
+            if rc != capi.OK:
+                raise capi.SwinWAttnError("swin_wattn_plan", rc)
+            plans.append(h)
+            qkvs.append(q.to(dev))
+            outs.append(torch.empty(wl.B, wl.H, wl.W, wl.C, dtype=torch.bfloat16, device=dev))
+            hosts.append((q.pin_memory(),
+                          torch.empty(wl.B, wl.H, wl.W, wl.C, dtype=torch.bfloat16).pin_memory()))
+    torch.cuda.synchronize()
+
+    def step(events=None):
+        for k, (h, q, o) in enumerate(zip(plans, qkvs, outs)):
+            if events is not None:
+                events[k][0].record(stream)
+            rc = lib.swin_wattn_fwd(h, q.data_ptr(), o.data_ptr(), sh)
+            if events is not None:
+                events[k][1].record(stream)
+            if rc != capi.OK:
+                raise capi.SwinWAttnError("swin_wattn_fwd", rc)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in sweep]
+          for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    capi.swin_wattn_launch_count(reset=True)
+    barrier(ws)
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    clocks.mark(True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(ev[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    clocks.mark(False)
+    barrier(ws)
+    launches = capi.swin_wattn_launch_count()
+    clk = clocks.stop()
+    total_ms = t_start.elapsed_time(t_end)
+    total_ms = max_over_ranks(total_ms, ws)
+    per_stage_ms = [statistics.mean(ev[i][k][0].elapsed_time(ev[i][k][1])
+                                    for i in range(args.steps)) for k in range(len(sweep))]
+
+    tokens_step = sum(wl.tokens for wl in sweep)
+    value = ws * tokens_step * args.steps / (total_ms / 1e3)
+    peaks, peak_src = load_peaks()
+    hbm = float(peaks["hbm_gbs"])
+
+    stages = []
+    for wl, ms in zip(sweep, per_stage_ms):
+        gbs = fwd_bytes(wl) / (ms / 1e3) / 1e9
+        stages.append({"workload": wl.name, "us": round(ms * 1e3, 2),
+                       "tokens_per_s": wl.tokens / (ms / 1e3), "GBps": round(gbs, 1),
+                       "frac_of_measured_hbm": round(gbs / hbm, 4),
+                       "tflops": round(fwd_flops(wl) / (ms / 1e3) / 1e12, 1)})
+    sweep_bytes = sum(fwd_bytes(wl) for wl in sweep)
+    sweep_ms = sum(per_stage_ms)
+
+    # dominant kernel: the largest share of the step
+    kdom = max(range(len(sweep)), key=lambda k: per_stage_ms[k])
+    wdom = sweep[kdom]
+    ach = fwd_bytes(wdom) / (per_stage_ms[kdom] / 1e3) / 1e9
+    khash = kernel_source_hash()
+    roofline = {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(ach / hbm, 4), "traffic": ncu_traffic(khash) if kdom == 0 else None,
+                "kernel": f"fwd_kernel<7,bf16> on {wdom.name}",
+                "bytes_per_launch": fwd_bytes(wdom), "peak_source": peak_src + " hbm_gbs",
+                "kernel_source_hash": khash}
+
+    # ---- end to end through the host-buffer entry point --------------------------------
+    e2e_steps = max(3, min(args.steps, 20))
+    h2d = sum(q.numel() * q.element_size() for q, _ in hosts)
+    d2h = sum(o.numel() * o.element_size() for _, o in hosts)
+
+    def e2e_step():
+        for h, q, o, (qh, oh) in zip(plans, qkvs, outs, hosts):
+            rc = lib.swin_wattn_fwd_host(h, qh.data_ptr(), oh.data_ptr(), q.data_ptr(),
+                                         o.data_ptr(), sh)
+            if rc != capi.OK:
+                raise capi.SwinWAttnError("swin_wattn_fwd_host", rc)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(ws)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), ws)
+    e2e = {"value": ws * tokens_step * e2e_steps / (e2e_ms / 1e3), "unit": "tokens/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+           "entry_point": "swin_wattn_fwd_host (pinned host buffers)", "steps": e2e_steps}
+
+    for h in plans:
+        capi.swin_wattn_destroy(h)
+    del qkvs, outs, hosts
+    torch.cuda.empty_cache()
+
+    train = run_train_step(args, dev, stream, lib, capi, hbm, ws) if not args.skip_train else None
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic (seeded N(0,1) qkv, trunc-normal table)",
+            "config": {"workload": "swin_l224_sweep_fwd", "batch_per_gpu": 64, "window": 7,
+                       "stages": [f"{w.H}x{w.W} C={w.C} nH={w.nH} s={w.s}" for w in sweep],
+                       "tokens_per_step_per_gpu": tokens_step,
+                       "algorithmic_bytes_per_step": sweep_bytes,
+                       "l2": f"step working set {sweep_bytes / 1e6:.0f} MB > 129 MB L2 "
+                             "(stages run in turn; each stage's inputs are evicted by the "
+                             "others' before they are read again); no flush",
+                       "parallelism": f"dp{ws} (independent batch shards, no collective)"},
+            "roofline": roofline,
+            "sweep": {"us": round(sweep_ms * 1e3, 2),
+                      "GBps": round(sweep_bytes / (sweep_ms / 1e3) / 1e9, 1),
+                      "frac_of_measured_hbm": round(sweep_bytes / (sweep_ms / 1e3) / 1e9 / hbm, 4),
+                      "stages": stages},
+            "e2e": e2e,
+            "gpu_launches": int(launches),
+            "clocks": clk,
+            "train_step": train,
+        }
+        if ws == 1 and not args.skip_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(sweep)
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_train_step(args, dev, stream, lib, capi, hbm, ws):
+    """Swin-B 224 training step of the path: per stage, bias re-expansion from the
+    (updated) table, forward, and backward with the table gradient."""
+    sh = stream.cuda_stream
+    wls = [inputs.BY_NAME[n] for n in TRAIN]
+    st = []
+    with torch.cuda.stream(stream):
+        for wl in wls:
+            tab = inputs.make_table(wl).to(dev)
+            rc, h = capi.swin_wattn_plan(wl.B, wl.H, wl.W, wl.C, wl.nH, wl.M, wl.s, capi.BF16,
+                                         tab.data_ptr(), sh)
+            if rc != capi.OK:
+                raise capi.SwinWAttnError("swin_wattn_plan", rc)
+            q = inputs.make_qkv(wl).to(dev)
+            d = inputs.make_dout(wl).to(dev)
+            st.append(dict(wl=wl, h=h, tab=tab, q=q, d=d, o=torch.empty_like(d),
+                           dq=torch.empty_like(q), dt=torch.empty_like(tab)))
+    torch.cuda.synchronize()
+    steps = max(3, min(args.steps, 50))
+
+    def one(events=None):
+        for k, x in enumerate(st):
+            if events is not None:
+                events[k][0].record(stream)
+            ok = lib.swin_wattn_set_bias(x["h"], x["tab"].data_ptr(), sh) == capi.OK
+            if events is not None:
+                events[k][1].record(stream)
+            ok &= lib.swin_wattn_fwd(x["h"], x["q"].data_ptr(), x["o"].data_ptr(), sh) == capi.OK
+            if events is not None:
+                events[k][2].record(stream)
+            ok &= lib.swin_wattn_bwd(x["h"], x["q"].data_ptr(), x["d"].data_ptr(),
+                                     x["dq"].data_ptr(), x["dt"].data_ptr(), sh) == capi.OK
+            if events is not None:
+                events[k][3].record(stream)
+            if not ok:
+                raise RuntimeError("training step call failed")
+
+    for _ in range(max(3, args.warmup)):
+        one()
+    torch.cuda.synchronize()
+    ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in st] for _ in range(steps)]
+    barrier(ws)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for i in range(steps):
+        one(ev[i])
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(a.elapsed_time(b), ws) / steps
+    tokens = sum(x["wl"].tokens for x in st)
+    stages = []
+    for k, x in enumerate(st):
+        wl = x["wl"]
+        f_ms = statistics.mean(ev[i][k][1].elapsed_time(ev[i][k][2]) for i in range(steps))
+        b_ms = statistics.mean(ev[i][k][2].elapsed_time(ev[i][k][3]) for i in range(steps))
+        s_ms = statistics.mean(ev[i][k][0].elapsed_time(ev[i][k][1]) for i in range(steps))
+        stages.append({"workload": wl.name, "set_bias_us": round(s_ms * 1e3, 2),
+                       "fwd_us": round(f_ms * 1e3, 2), "bwd_us": round(b_ms * 1e3, 2),
+                       "fwd_frac_of_measured_hbm": round(fwd_bytes(wl) / (f_ms / 1e3) / 1e9 / hbm, 4),
+                       "bwd_frac_of_measured_hbm": round(bwd_bytes(wl) / (b_ms / 1e3) / 1e9 / hbm, 4),
+                       "bwd_tflops": round(bwd_flops(wl) / (b_ms / 1e3) / 1e12, 1)})
+    for x in st:
+        capi.swin_wattn_destroy(x["h"])
+    return {"workload": "swin_b224_train_step (B=128, 4 stages: set_bias + fwd + bwd)",
+            "steps": steps, "ms_per_step": ms, "tokens_per_s": ws * tokens / (ms / 1e3),
+            "stages": stages}
+
+
+# ---- reference arm: the oracle --------------------------------------------------------
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if ws > 1 and rank != 0:
+        return
+    import oracle
+    oracle.build()
+    sweep = [inputs.BY_NAME[n] for n in SWEEP]
+    data = []
+    for wl in sweep:
+        one = wl.with_batch(1)
+        data.append((wl, inputs.act_f64(inputs.make_qkv(one)), inputs.make_table(wl).double().numpy()))
+
+    def step():
+        for wl, q, t in data:
+            oracle.fwd(q, t, wl.nH, wl.M, wl.s)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    el = time.perf_counter() - t0
+    tokens = sum(wl.H * wl.W for wl in sweep)
+    value = tokens * args.steps / el
+    cores = oracle.max_threads()
+    sample = "one image per stage of the Swin-L 224 sweep per step (batch 1 of 64)"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": el * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "swin_l224_sweep_fwd", "batch_per_step": 1, "window": 7},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=8000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", action="append", choices=sorted(inputs.BY_NAME),
+                    help="time only these forward workloads instead of the Swin-L 224 sweep "
+                         "(profiling runs)")
+    ap.add_argument("--skip-train", action="store_true")
+    ap.add_argument("--skip-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

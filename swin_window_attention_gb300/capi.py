@@ -30,6 +30,7 @@ SIGNATURES = {
     "swin_wattn_plan": ([ctypes.POINTER(_vp), _i, _i, _i, _i, _i, _i, _i, _i, _vp, _vp], _i),
     "swin_wattn_set_bias": ([_vp, _vp, _vp], _i),
     "swin_wattn_fwd": ([_vp, _vp, _vp, _vp], _i),
+    "swin_wattn_fwd_host": ([_vp, _vp, _vp, _vp, _vp, _vp], _i),
     "swin_wattn_bwd": ([_vp, _vp, _vp, _vp, _vp, _vp], _i),
     "swin_wattn_debug_maps": ([_vp, _vp, _vp, _vp, _vp, _vp], _i),
     "swin_wattn_destroy": ([_vp], _i),
@@ -83,6 +84,11 @@ def swin_wattn_set_bias(plan, bias_table_ptr, stream):
 
 def swin_wattn_fwd(plan, qkv_ptr, out_ptr, stream):
     return load().swin_wattn_fwd(plan, qkv_ptr, out_ptr, stream)
+
+
+def swin_wattn_fwd_host(plan, qkv_host_ptr, out_host_ptr, dev_qkv_ptr, dev_out_ptr, stream):
+    return load().swin_wattn_fwd_host(plan, qkv_host_ptr, out_host_ptr, dev_qkv_ptr,
+                                      dev_out_ptr, stream)
 
 
 def swin_wattn_bwd(plan, qkv_ptr, dout_ptr, dqkv_ptr, dtable_ptr, stream):
@@ -150,6 +156,15 @@ class WindowAttention:
         if rc != OK:
             raise SwinWAttnError("swin_wattn_fwd", rc)
         return out
+
+    def fwd_host(self, qkv_host, out_host, dev_qkv, dev_out, stream=None):
+        """Host-resident qkv -> host-resident out through the library's host entry point
+        (copies and kernel in order on the stream; synchronise before reading out_host)."""
+        rc = swin_wattn_fwd_host(self.handle, qkv_host.data_ptr(), out_host.data_ptr(),
+                                 dev_qkv.data_ptr(), dev_out.data_ptr(), _stream_handle(stream))
+        if rc != OK:
+            raise SwinWAttnError("swin_wattn_fwd_host", rc)
+        return out_host
 
     def bwd(self, qkv, dout, dqkv=None, dtable=None, stream=None):
         import torch

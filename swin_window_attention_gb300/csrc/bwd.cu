@@ -12,7 +12,9 @@
 //   dQ = scale dS K,  dK = scale dS^T Q,  dV = P^T dO,
 //   dtable[idx(i,j), h] += dS_ij   (fp32 dS, never bf16-rounded).
 // Warp w owns query rows [16w, 16w+16) for S, P, dP, dS and dQ, then key rows
-// [16w, 16w+16) for dK and dV, reading every warp's P and dS from shared memory. The
+// [16w, 16w+16) for dK and dV, reading every warp's P and dS from shared memory. P
+// enters dV as a bf16 hi/lo pair: a single bf16 P alone costs up to 2^-9 relative per
+// term, which for peaked rows reaches the same size as the bf16 rounding of dV itself. The
 // per-(i,j) dS sums stay in registers across the CTA's windows; at the end one thread
 // per table row folds them in a fixed order into a per-CTA partial, and a second
 // kernel sums the partials in a fixed order: the result is deterministic.
@@ -48,7 +50,7 @@ struct BwdParams {
 
 template <int M, int STAGES>
 constexpr int bwd_smem_bytes() {
-  return Geo<M>::BIAS_BYTES + Geo<M>::MASK_BYTES + 2 * BGeo<M>::PS_BYTES + BGeo<M>::STG_BYTES +
+  return Geo<M>::BIAS_BYTES + Geo<M>::MASK_BYTES + 3 * BGeo<M>::PS_BYTES + BGeo<M>::STG_BYTES +
          STAGES * BGeo<M>::STAGE_BYTES;
 }
 
@@ -107,7 +109,8 @@ __global__ void __launch_bounds__(Geo<M>::THREADS) bwd_kernel(const BwdParams p)
   float4* sbias = reinterpret_cast<float4*>(smem);
   uint32_t* smask = reinterpret_cast<uint32_t*>(smem + G::BIAS_BYTES);
   unsigned char* sP = smem + G::BIAS_BYTES + G::MASK_BYTES;
-  unsigned char* sdS = sP + BG::PS_BYTES;
+  unsigned char* sPlo = sP + BG::PS_BYTES;
+  unsigned char* sdS = sPlo + BG::PS_BYTES;
   unsigned char* sstg = sdS + BG::PS_BYTES;
   unsigned char* stiles = sstg + BG::STG_BYTES;
 
@@ -153,8 +156,8 @@ __global__ void __launch_bounds__(Geo<M>::THREADS) bwd_kernel(const BwdParams p)
           make_uint4(0u, 0u, 0u, 0u);
     }
   }
-  // P and dS tiles start zeroed: columns NT*8..NPAD-1 are never written.
-  for (int e = tid; e < 2 * BG::PS_BYTES / 16; e += THREADS)
+  // P, P_lo and dS tiles start zeroed: columns NT*8..NPAD-1 are never written.
+  for (int e = tid; e < 3 * BG::PS_BYTES / 16; e += THREADS)
     reinterpret_cast<uint4*>(sP)[e] = make_uint4(0u, 0u, 0u, 0u);
   {
     const float* db = p.dense_bias + (int64_t)h * N * N;
@@ -320,9 +323,16 @@ __global__ void __launch_bounds__(Geo<M>::THREADS) bwd_kernel(const BwdParams p)
       dtacc[nt][1] += ds[nt][1];
       dtacc[nt][2] += ds[nt][2];
       dtacc[nt][3] += ds[nt][3];
+      // P goes to shared memory as a bf16 pair P = P_hi + P_lo (the second term is the
+      // rounding residual of the first), so dV = P^T dO keeps ~16 mantissa bits of P.
       const int col2 = (nt * 8 + 2 * t) * 2;
-      *reinterpret_cast<uint32_t*>(sP + r0 * PS + col2) = pack_bf16(pr[nt][0], pr[nt][1]);
-      *reinterpret_cast<uint32_t*>(sP + r1 * PS + col2) = pack_bf16(pr[nt][2], pr[nt][3]);
+      const uint32_t h0 = pack_bf16(pr[nt][0], pr[nt][1]), h1 = pack_bf16(pr[nt][2], pr[nt][3]);
+      *reinterpret_cast<uint32_t*>(sP + r0 * PS + col2) = h0;
+      *reinterpret_cast<uint32_t*>(sP + r1 * PS + col2) = h1;
+      *reinterpret_cast<uint32_t*>(sPlo + r0 * PS + col2) =
+          pack_bf16(pr[nt][0] - __uint_as_float(h0 << 16), pr[nt][1] - __uint_as_float(h0 & 0xffff0000u));
+      *reinterpret_cast<uint32_t*>(sPlo + r1 * PS + col2) =
+          pack_bf16(pr[nt][2] - __uint_as_float(h1 << 16), pr[nt][3] - __uint_as_float(h1 & 0xffff0000u));
       *reinterpret_cast<uint32_t*>(sdS + r0 * PS + col2) = pack_bf16(ds[nt][0], ds[nt][1]);
       *reinterpret_cast<uint32_t*>(sdS + r1 * PS + col2) = pack_bf16(ds[nt][2], ds[nt][3]);
     }
@@ -367,9 +377,10 @@ __global__ void __launch_bounds__(Geo<M>::THREADS) bwd_kernel(const BwdParams p)
 #pragma unroll
       for (int kk = 0; kk < KT; ++kk) {
         const int rowA = kk * 16 + (lane & 7) + 8 * (mi >> 1), chA = 2 * warp + (mi & 1);
-        uint32_t a0, a1, a2, a3, p0, p1, p2, p3;
+        uint32_t a0, a1, a2, a3, p0, p1, p2, p3, e0, e1, e2, e3;
         ldsm_x4_t(smem_u32(sdS + rowA * PS + chA * 16), a0, a1, a2, a3);
         ldsm_x4_t(smem_u32(sP + rowA * PS + chA * 16), p0, p1, p2, p3);
+        ldsm_x4_t(smem_u32(sPlo + rowA * PS + chA * 16), e0, e1, e2, e3);
         const int rowB = kk * 16 + (lane & 7) + ((mi & 1) << 3);
 #pragma unroll
         for (int pp = 0; pp < 2; ++pp) {
@@ -380,6 +391,8 @@ __global__ void __launch_bounds__(Geo<M>::THREADS) bwd_kernel(const BwdParams p)
           ldsm_x4_t(ob + tile_off(rowB, 2 * pp + (mi >> 1)), d0, d1, d2, d3);
           mma_bf16(dv[2 * pp], p0, p1, p2, p3, d0, d1);
           mma_bf16(dv[2 * pp + 1], p0, p1, p2, p3, d2, d3);
+          mma_bf16(dv[2 * pp], e0, e1, e2, e3, d0, d1);
+          mma_bf16(dv[2 * pp + 1], e0, e1, e2, e3, d2, d3);
         }
       }
       store_rows<M, TIO>(dk, p.scale, stg, reinterpret_cast<TIO*>(p.dqkv), 1, warp, lane, b, wy, wx,

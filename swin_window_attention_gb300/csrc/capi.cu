@@ -197,6 +197,28 @@ int swin_wattn_fwd(swin_wattn_plan_t plan, const void* qkv, void* out,
   return e == cudaSuccess ? SWIN_WATTN_OK : cuda_fail(e, "swin_wattn_fwd");
 }
 
+int swin_wattn_fwd_host(swin_wattn_plan_t plan, const void* qkv_host, void* out_host,
+                        void* dev_qkv, void* dev_out, struct CUstream_st* stream) {
+  int rc = check_plan(plan);
+  if (rc != SWIN_WATTN_OK) return rc;
+  const swin::Plan& p = plan->p;
+  if (p.B == 0) return SWIN_WATTN_OK;
+  if (qkv_host == nullptr || out_host == nullptr) return SWIN_WATTN_ERR_INVALID_ARG;
+  if ((rc = check_device_ptr(dev_qkv, 16)) != SWIN_WATTN_OK) return rc;
+  if ((rc = check_device_ptr(dev_out, 16)) != SWIN_WATTN_OK) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const size_t esz = p.dtype == SWIN_WATTN_FP32 ? 4 : 2;
+  const size_t tokens = (size_t)p.B * p.H * p.W;
+  cudaError_t e = cudaMemcpyAsync(dev_qkv, qkv_host, tokens * 3 * p.C * esz, cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess) {
+    e = swin::fwd_launch(p, plan->fwd, dev_qkv, dev_out, st);
+    ++g_launches;
+  }
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(out_host, dev_out, tokens * p.C * esz, cudaMemcpyDeviceToHost, st);
+  return e == cudaSuccess ? SWIN_WATTN_OK : cuda_fail(e, "swin_wattn_fwd_host");
+}
+
 int swin_wattn_bwd(swin_wattn_plan_t plan, const void* qkv, const void* dout, void* dqkv,
                    float* dtable, struct CUstream_st* stream) {
   int rc = check_plan(plan);

@@ -1,5 +1,8 @@
 """Helpers for the GPU parity tests: run the library through its C ABI on seeded inputs
 and compare with the fp64 oracle on the same bf16-rounded values."""
+import json
+import os
+
 import numpy as np
 import torch
 
@@ -24,6 +27,11 @@ def errors(got, ref):
 
 def assert_close(name, got, ref):
     ma, rl = errors(got, ref)
+    log = os.environ.get("SWIN_PARITY_LOG")
+    if log:
+        with open(log, "a") as f:
+            f.write(json.dumps({"case": os.environ.get("PYTEST_CURRENT_TEST", "").split(" ")[0],
+                                "tensor": name, "max_abs": ma, "rel_l2": rl}) + "\n")
     assert ma <= TOL_ABS and rl <= TOL_REL, f"{name}: max-abs {ma:.3g}, rel-L2 {rl:.3g}"
     return ma, rl
 
