@@ -12,9 +12,10 @@
 //   dQ = scale dS K,  dK = scale dS^T Q,  dV = P^T dO,
 //   dtable[idx(i,j), h] += dS_ij   (fp32 dS, never bf16-rounded).
 // Warp w owns query rows [16w, 16w+16) for S, P, dP, dS and dQ, then key rows
-// [16w, 16w+16) for dK and dV, reading every warp's P and dS from shared memory. P
-// enters dV as a bf16 hi/lo pair: a single bf16 P alone costs up to 2^-9 relative per
-// term, which for peaked rows reaches the same size as the bf16 rounding of dV itself. The
+// [16w, 16w+16) for dK and dV, reading every warp's P and dS from shared memory. P and
+// dS enter the dV, dQ and dK products as bf16 hi/lo pairs: a single bf16 operand costs
+// up to 2^-9 relative per term, which over a 49-term sum reaches the size of the bf16
+// rounding of the result itself and breaks a 1e-2 absolute bound on its own. The
 // per-(i,j) dS sums stay in registers across the CTA's windows; at the end one thread
 // per table row folds them in a fixed order into a per-CTA partial, and a second
 // kernel sums the partials in a fixed order: the result is deterministic.
@@ -50,7 +51,7 @@ struct BwdParams {
 
 template <int M, int STAGES>
 constexpr int bwd_smem_bytes() {
-  return Geo<M>::BIAS_BYTES + Geo<M>::MASK_BYTES + 3 * BGeo<M>::PS_BYTES + BGeo<M>::STG_BYTES +
+  return Geo<M>::BIAS_BYTES + Geo<M>::MASK_BYTES + 4 * BGeo<M>::PS_BYTES + BGeo<M>::STG_BYTES +
          STAGES * BGeo<M>::STAGE_BYTES;
 }
 
@@ -111,7 +112,8 @@ __global__ void __launch_bounds__(Geo<M>::THREADS) bwd_kernel(const BwdParams p)
   unsigned char* sP = smem + G::BIAS_BYTES + G::MASK_BYTES;
   unsigned char* sPlo = sP + BG::PS_BYTES;
   unsigned char* sdS = sPlo + BG::PS_BYTES;
-  unsigned char* sstg = sdS + BG::PS_BYTES;
+  unsigned char* sdSlo = sdS + BG::PS_BYTES;
+  unsigned char* sstg = sdSlo + BG::PS_BYTES;
   unsigned char* stiles = sstg + BG::STG_BYTES;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -156,8 +158,8 @@ __global__ void __launch_bounds__(Geo<M>::THREADS) bwd_kernel(const BwdParams p)
           make_uint4(0u, 0u, 0u, 0u);
     }
   }
-  // P, P_lo and dS tiles start zeroed: columns NT*8..NPAD-1 are never written.
-  for (int e = tid; e < 3 * BG::PS_BYTES / 16; e += THREADS)
+  // P and dS tiles (hi and lo) start zeroed: columns NT*8..NPAD-1 are never written.
+  for (int e = tid; e < 4 * BG::PS_BYTES / 16; e += THREADS)
     reinterpret_cast<uint4*>(sP)[e] = make_uint4(0u, 0u, 0u, 0u);
   {
     const float* db = p.dense_bias + (int64_t)h * N * N;
@@ -323,18 +325,22 @@ __global__ void __launch_bounds__(Geo<M>::THREADS) bwd_kernel(const BwdParams p)
       dtacc[nt][1] += ds[nt][1];
       dtacc[nt][2] += ds[nt][2];
       dtacc[nt][3] += ds[nt][3];
-      // P goes to shared memory as a bf16 pair P = P_hi + P_lo (the second term is the
-      // rounding residual of the first), so dV = P^T dO keeps ~16 mantissa bits of P.
+      // P and dS go to shared memory as bf16 hi/lo pairs (the lo term is the rounding
+      // residual of the hi term), so the MMAs that read them keep ~16 bits of each.
       const int col2 = (nt * 8 + 2 * t) * 2;
-      const uint32_t h0 = pack_bf16(pr[nt][0], pr[nt][1]), h1 = pack_bf16(pr[nt][2], pr[nt][3]);
-      *reinterpret_cast<uint32_t*>(sP + r0 * PS + col2) = h0;
-      *reinterpret_cast<uint32_t*>(sP + r1 * PS + col2) = h1;
-      *reinterpret_cast<uint32_t*>(sPlo + r0 * PS + col2) =
-          pack_bf16(pr[nt][0] - __uint_as_float(h0 << 16), pr[nt][1] - __uint_as_float(h0 & 0xffff0000u));
-      *reinterpret_cast<uint32_t*>(sPlo + r1 * PS + col2) =
-          pack_bf16(pr[nt][2] - __uint_as_float(h1 << 16), pr[nt][3] - __uint_as_float(h1 & 0xffff0000u));
-      *reinterpret_cast<uint32_t*>(sdS + r0 * PS + col2) = pack_bf16(ds[nt][0], ds[nt][1]);
-      *reinterpret_cast<uint32_t*>(sdS + r1 * PS + col2) = pack_bf16(ds[nt][2], ds[nt][3]);
+      uint32_t hi, lo;
+      split_bf16(pr[nt][0], pr[nt][1], hi, lo);
+      *reinterpret_cast<uint32_t*>(sP + r0 * PS + col2) = hi;
+      *reinterpret_cast<uint32_t*>(sPlo + r0 * PS + col2) = lo;
+      split_bf16(pr[nt][2], pr[nt][3], hi, lo);
+      *reinterpret_cast<uint32_t*>(sP + r1 * PS + col2) = hi;
+      *reinterpret_cast<uint32_t*>(sPlo + r1 * PS + col2) = lo;
+      split_bf16(ds[nt][0], ds[nt][1], hi, lo);
+      *reinterpret_cast<uint32_t*>(sdS + r0 * PS + col2) = hi;
+      *reinterpret_cast<uint32_t*>(sdSlo + r0 * PS + col2) = lo;
+      split_bf16(ds[nt][2], ds[nt][3], hi, lo);
+      *reinterpret_cast<uint32_t*>(sdS + r1 * PS + col2) = hi;
+      *reinterpret_cast<uint32_t*>(sdSlo + r1 * PS + col2) = lo;
     }
 
     // ---- dQ = scale dS K --------------------------------------------------------------
@@ -344,12 +350,12 @@ __global__ void __launch_bounds__(Geo<M>::THREADS) bwd_kernel(const BwdParams p)
       for (int nd = 0; nd < 4; ++nd) dq[nd][0] = dq[nd][1] = dq[nd][2] = dq[nd][3] = 0.0f;
 #pragma unroll
       for (int kk = 0; kk < KT; ++kk) {
-        const uint32_t a0 = pack_bf16(ds[2 * kk][0], ds[2 * kk][1]);
-        const uint32_t a1 = pack_bf16(ds[2 * kk][2], ds[2 * kk][3]);
-        uint32_t a2 = 0u, a3 = 0u;
+        uint32_t a0, a1, a2 = 0u, a3 = 0u, l0, l1, l2 = 0u, l3 = 0u;
+        split_bf16(ds[2 * kk][0], ds[2 * kk][1], a0, l0);
+        split_bf16(ds[2 * kk][2], ds[2 * kk][3], a1, l1);
         if (2 * kk + 1 < NT) {
-          a2 = pack_bf16(ds[2 * kk + 1][0], ds[2 * kk + 1][1]);
-          a3 = pack_bf16(ds[2 * kk + 1][2], ds[2 * kk + 1][3]);
+          split_bf16(ds[2 * kk + 1][0], ds[2 * kk + 1][1], a2, l2);
+          split_bf16(ds[2 * kk + 1][2], ds[2 * kk + 1][3], a3, l3);
         }
         const int mi = lane >> 3, row = kk * 16 + (lane & 7) + ((mi & 1) << 3);
 #pragma unroll
@@ -358,6 +364,8 @@ __global__ void __launch_bounds__(Geo<M>::THREADS) bwd_kernel(const BwdParams p)
           ldsm_x4_t(kb + tile_off(row, 2 * pp + (mi >> 1)), v0, v1, v2, v3);
           mma_bf16(dq[2 * pp], a0, a1, a2, a3, v0, v1);
           mma_bf16(dq[2 * pp + 1], a0, a1, a2, a3, v2, v3);
+          mma_bf16(dq[2 * pp], l0, l1, l2, l3, v0, v1);
+          mma_bf16(dq[2 * pp + 1], l0, l1, l2, l3, v2, v3);
         }
       }
       store_rows<M, TIO>(dq, p.scale, stg, reinterpret_cast<TIO*>(p.dqkv), 0, warp, lane, b, wy, wx,
@@ -377,8 +385,9 @@ __global__ void __launch_bounds__(Geo<M>::THREADS) bwd_kernel(const BwdParams p)
 #pragma unroll
       for (int kk = 0; kk < KT; ++kk) {
         const int rowA = kk * 16 + (lane & 7) + 8 * (mi >> 1), chA = 2 * warp + (mi & 1);
-        uint32_t a0, a1, a2, a3, p0, p1, p2, p3, e0, e1, e2, e3;
+        uint32_t a0, a1, a2, a3, f0, f1, f2, f3, p0, p1, p2, p3, e0, e1, e2, e3;
         ldsm_x4_t(smem_u32(sdS + rowA * PS + chA * 16), a0, a1, a2, a3);
+        ldsm_x4_t(smem_u32(sdSlo + rowA * PS + chA * 16), f0, f1, f2, f3);
         ldsm_x4_t(smem_u32(sP + rowA * PS + chA * 16), p0, p1, p2, p3);
         ldsm_x4_t(smem_u32(sPlo + rowA * PS + chA * 16), e0, e1, e2, e3);
         const int rowB = kk * 16 + (lane & 7) + ((mi & 1) << 3);
@@ -388,6 +397,8 @@ __global__ void __launch_bounds__(Geo<M>::THREADS) bwd_kernel(const BwdParams p)
           ldsm_x4_t(qb + tile_off(rowB, 2 * pp + (mi >> 1)), q0, q1, q2, q3);
           mma_bf16(dk[2 * pp], a0, a1, a2, a3, q0, q1);
           mma_bf16(dk[2 * pp + 1], a0, a1, a2, a3, q2, q3);
+          mma_bf16(dk[2 * pp], f0, f1, f2, f3, q0, q1);
+          mma_bf16(dk[2 * pp + 1], f0, f1, f2, f3, q2, q3);
           ldsm_x4_t(ob + tile_off(rowB, 2 * pp + (mi >> 1)), d0, d1, d2, d3);
           mma_bf16(dv[2 * pp], p0, p1, p2, p3, d0, d1);
           mma_bf16(dv[2 * pp + 1], p0, p1, p2, p3, d2, d3);
