@@ -47,10 +47,10 @@ def fwd_bytes(wl) -> int:
 
 
 def bwd_bytes(wl) -> int:
-    """qkv + dO read, dqkv write, dense bias, mask, table gradient write."""
+    """qkv (3C) + dO (C) read, dqkv (3C) write, dense bias, mask, table gradient write."""
     esz = 2 if wl.dtype == "bf16" else 4
     nn = wl.N * wl.N
-    return (wl.tokens * 10 * wl.C * esz + wl.nH * nn * 4 + (wl.nW * nn * 4 if wl.s > 0 else 0)
+    return (wl.tokens * 7 * wl.C * esz + wl.nH * nn * 4 + (wl.nW * nn * 4 if wl.s > 0 else 0)
             + (2 * wl.M - 1) ** 2 * wl.nH * 4)
 
 
