@@ -125,28 +125,57 @@ __global__ void __launch_bounds__(Geo<M>::THREADS) bwd_kernel(const BwdParams p)
   const int C = p.C, H = p.H, W = p.W, s = p.s;
   unsigned char* stg = sstg + warp * 16 * 64;
 
-  auto issue = [&](int64_t widx, int stage) {
-    const int b = (int)(widx / p.nW), w = (int)(widx % p.nW);
-    const int wy = w / p.nWx, wx = w % p.nWx;
+  // Per-thread gather descriptors, packed: shared offset (bits 0-15), window row (16-19),
+  // window column (20-23), slice q/k/v/dO (24-25), 16-byte chunk (26-27).
+  uint32_t ld_desc[BG::CH_ITERS];
+#pragma unroll
+  for (int k = 0; k < BG::CH_ITERS; ++k) {
+    const int id = tid + k * THREADS;
+    const int c = id & 3, rest = id >> 2;
+    const int i = rest % N, tt = (rest / N) & 3;
+    ld_desc[k] = (uint32_t)(tt * G::TILE_BYTES + tile_off(i, c)) | ((uint32_t)(i / M) << 16) |
+                 ((uint32_t)(i % M) << 20) | ((uint32_t)tt << 24) | ((uint32_t)c << 26);
+  }
+  int lb, lwy, lwx;
+  {
+    lb = (int)(w_begin / p.nW);
+    const int w = (int)(w_begin - (int64_t)lb * p.nW);
+    lwy = w / p.nWx;
+    lwx = w - lwy * p.nWx;
+  }
+  int cb = lb, cwy = lwy, cwx = lwx;
+
+  auto issue = [&](int stage) {
     unsigned char* base = stiles + stage * BG::STAGE_BYTES;
+    const int64_t img = (int64_t)lb * H * W;
+    const int y0 = lwy * M + s, x0 = lwx * M + s;
 #pragma unroll
     for (int k = 0; k < BG::CH_ITERS; ++k) {
-      const int id = tid + k * THREADS;
-      if (id < BG::CHUNKS) {
-        const int c = id & 3, rest = id >> 2;
-        const int i = rest % N, tt = rest / N;
-        const int64_t tok = gather_token(b, wy, wx, i, M, s, H, W);
+      if (k < BG::CH_ITERS - 1 || tid + k * THREADS < BG::CHUNKS) {
+        const uint32_t d = ld_desc[k];
+        const int tt = (d >> 24) & 3, c = (d >> 26) & 3;
+        int y = y0 + (int)((d >> 16) & 15), x = x0 + (int)((d >> 20) & 15);
+        y = y >= H ? y - H : y;
+        x = x >= W ? x - W : x;
+        const int64_t tok = img + y * W + x;
         const TIO* src = tt < 3
             ? reinterpret_cast<const TIO*>(p.qkv) + tok * 3 * C + tt * C + h * kHeadDim + c * 8
             : reinterpret_cast<const TIO*>(p.dout) + tok * C + h * kHeadDim + c * 8;
-        load_chunk<TIO>(smem_u32(base + tt * G::TILE_BYTES + tile_off(i, c)), src);
+        load_chunk<TIO>(smem_u32(base + (d & 0xffffu)), src);
+      }
+    }
+    if (++lwx == p.nWx) {
+      lwx = 0;
+      if (++lwy == p.nWy) {
+        lwy = 0;
+        ++lb;
       }
     }
   };
 
 #pragma unroll
   for (int st = 0; st < STAGES - 1; ++st) {
-    if (st < nwin) issue(w_begin + st, st);
+    if (st < nwin) issue(st);
     cp_async_commit();
   }
 
@@ -206,12 +235,17 @@ __global__ void __launch_bounds__(Geo<M>::THREADS) bwd_kernel(const BwdParams p)
     __syncthreads();
     {
       const int nx = it + STAGES - 1;
-      if (nx < nwin) issue(w_begin + nx, nx % STAGES);
+      if (nx < nwin) issue(nx % STAGES);
       cp_async_commit();
     }
-    const int64_t widx = w_begin + it;
-    const int b = (int)(widx / p.nW), w = (int)(widx % p.nW);
-    const int wy = w / p.nWx, wx = w % p.nWx;
+    const int b = cb, wy = cwy, wx = cwx;
+    if (++cwx == p.nWx) {
+      cwx = 0;
+      if (++cwy == p.nWy) {
+        cwy = 0;
+        ++cb;
+      }
+    }
     const uint32_t qb = smem_u32(stiles + (it % STAGES) * BG::STAGE_BYTES);
     const uint32_t kb = qb + G::TILE_BYTES, vb = kb + G::TILE_BYTES, ob = vb + G::TILE_BYTES;
 

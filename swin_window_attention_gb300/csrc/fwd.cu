@@ -41,6 +41,7 @@ template <int M, typename TIO, int STAGES>
 __global__ void __launch_bounds__(Geo<M>::THREADS) fwd_kernel(const FwdParams p) {
   using G = Geo<M>;
   constexpr int N = G::N, NT = G::NT, KT = G::KT, MW = G::MW, THREADS = G::THREADS;
+  constexpr int CH_ITERS = G::CH_ITERS;
   extern __shared__ __align__(128) unsigned char smem[];
   float4* sbias = reinterpret_cast<float4*>(smem);
   uint32_t* smask = reinterpret_cast<uint32_t*>(smem + G::BIAS_BYTES);
@@ -52,21 +53,52 @@ __global__ void __launch_bounds__(Geo<M>::THREADS) fwd_kernel(const FwdParams p)
   const int chunk = blockIdx.x / p.nH;
   const int64_t w_begin = p.total_windows * chunk / p.chunks;
   const int nwin = (int)(p.total_windows * (chunk + 1) / p.chunks - w_begin);
-  const int C = p.C, H = p.H, W = p.W, s = p.s;
+  const int C3 = 3 * p.C, H = p.H, W = p.W, s = p.s;
+  const TIO* __restrict__ qkv = reinterpret_cast<const TIO*>(p.qkv);
 
-  auto issue = [&](int64_t widx, int stage) {
-    const int b = (int)(widx / p.nW), w = (int)(widx % p.nW);
-    const int wy = w / p.nWx, wx = w % p.nWx;
-    unsigned char* base = stiles + stage * G::STAGE_BYTES;
+  // Per-thread gather descriptors, fixed for every window: chunk k of this thread is
+  // 16-byte chunk c of slice tt (q, k or v) of window slot i.
+  uint32_t ld_soff[CH_ITERS];
+  int ld_chan[CH_ITERS], ld_ly[CH_ITERS], ld_lx[CH_ITERS];
 #pragma unroll
-    for (int k = 0; k < G::CH_ITERS; ++k) {
-      const int id = tid + k * THREADS;
-      if (id < G::CHUNKS) {
-        const int c = id & 3, rest = id >> 2;
-        const int i = rest % N, tt = rest / N;
-        const int64_t tok = gather_token(b, wy, wx, i, M, s, H, W);
-        const TIO* src = reinterpret_cast<const TIO*>(p.qkv) + tok * 3 * C + tt * C + h * kHeadDim + c * 8;
-        load_chunk<TIO>(smem_u32(base + tt * G::TILE_BYTES + tile_off(i, c)), src);
+  for (int k = 0; k < CH_ITERS; ++k) {
+    const int id = tid + k * THREADS;
+    const int c = id & 3, rest = id >> 2;
+    const int i = rest % N, tt = rest / N;
+    ld_soff[k] = tt * G::TILE_BYTES + tile_off(i, c);
+    ld_chan[k] = tt * p.C + h * kHeadDim + c * 8;
+    ld_ly[k] = i / M;
+    ld_lx[k] = i % M;
+  }
+  // Window cursor of the next window to load: (b, wy, wx) advanced one window at a time.
+  int lb, lwy, lwx;
+  {
+    const int64_t w0 = w_begin;
+    lb = (int)(w0 / p.nW);
+    const int w = (int)(w0 - (int64_t)lb * p.nW);
+    lwy = w / p.nWx;
+    lwx = w - lwy * p.nWx;
+  }
+  int cb = lb, cwy = lwy, cwx = lwx;  // cursor of the window being computed
+
+  auto issue = [&](int stage) {
+    unsigned char* base = stiles + stage * G::STAGE_BYTES;
+    const TIO* img = qkv + (int64_t)lb * H * W * C3;
+    const int y0 = lwy * M + s, x0 = lwx * M + s;
+#pragma unroll
+    for (int k = 0; k < CH_ITERS; ++k) {
+      if (k < CH_ITERS - 1 || tid + k * THREADS < G::CHUNKS) {
+        int y = y0 + ld_ly[k], x = x0 + ld_lx[k];
+        y = y >= H ? y - H : y;
+        x = x >= W ? x - W : x;
+        load_chunk<TIO>(smem_u32(base + ld_soff[k]), img + (int64_t)(y * W + x) * C3 + ld_chan[k]);
+      }
+    }
+    if (++lwx == p.nWx) {
+      lwx = 0;
+      if (++lwy == p.nWy) {
+        lwy = 0;
+        ++lb;
       }
     }
   };
@@ -74,7 +106,7 @@ __global__ void __launch_bounds__(Geo<M>::THREADS) fwd_kernel(const FwdParams p)
   // Start the first windows' loads before the one-off staging below.
 #pragma unroll
   for (int st = 0; st < STAGES - 1; ++st) {
-    if (st < nwin) issue(w_begin + st, st);
+    if (st < nwin) issue(st);
     cp_async_commit();
   }
 
@@ -126,18 +158,29 @@ __global__ void __launch_bounds__(Geo<M>::THREADS) fwd_kernel(const FwdParams p)
 
   const float mask_l2 = kMaskValue * kLog2e;
   const float4* bfrag = sbias + warp * NT * 32 + lane;
+  // Output slots of this lane: rows warp*16 + g + {0, 8}, 16-byte chunk t.
+  const int os0 = warp * 16 + g, os1 = os0 + 8;
+  const int oly0 = os0 / M, olx0 = os0 % M, oly1 = os1 / M, olx1 = os1 % M;
+  // B operand of all ones: one extra m16n8 tile of P V yields the row sums of the very
+  // bf16 P values that weight V.
+  const uint32_t ones = 0x3F803F80u;
 
   for (int it = 0; it < nwin; ++it) {
     cp_async_wait<STAGES - 2>();
     __syncthreads();
     {
       const int nx = it + STAGES - 1;
-      if (nx < nwin) issue(w_begin + nx, nx % STAGES);
+      if (nx < nwin) issue(nx % STAGES);
       cp_async_commit();
     }
-    const int64_t widx = w_begin + it;
-    const int b = (int)(widx / p.nW), w = (int)(widx % p.nW);
-    const int wy = w / p.nWx, wx = w % p.nWx;
+    const int b = cb, wy = cwy, wx = cwx;
+    if (++cwx == p.nWx) {
+      cwx = 0;
+      if (++cwy == p.nWy) {
+        cwy = 0;
+        ++cb;
+      }
+    }
     unsigned char* tq = stiles + (it % STAGES) * G::STAGE_BYTES;
     const uint32_t qb = smem_u32(tq), kb = qb + G::TILE_BYTES, vb = kb + G::TILE_BYTES;
 
@@ -162,54 +205,46 @@ __global__ void __launch_bounds__(Geo<M>::THREADS) fwd_kernel(const FwdParams p)
     // ---- logits (log2 domain): scale, bias, mask; row max ----------------------
     int cls = 0;
     if (p.mask != nullptr) cls = (wy == p.nWy - 1 ? 2 : 0) | (wx == p.nWx - 1 ? 1 : 0);
-    uint32_t mb[MW];
-#pragma unroll
-    for (int m = 0; m < MW; ++m) mb[m] = cls ? smask[(cls * MW + m) * THREADS + tid] : 0u;
     float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       const float4 bb = bfrag[nt * 32];
-      float z0 = fmaf(sacc[nt][0], p.qk_scale_log2, bb.x);
-      float z1 = fmaf(sacc[nt][1], p.qk_scale_log2, bb.y);
-      float z2 = fmaf(sacc[nt][2], p.qk_scale_log2, bb.z);
-      float z3 = fmaf(sacc[nt][3], p.qk_scale_log2, bb.w);
-      if (cls) {
-        const uint32_t word = mb[(nt * 4) >> 5], sh = (nt * 4) & 31;
-        if ((word >> sh) & 1u) z0 += mask_l2;
-        if ((word >> (sh + 1)) & 1u) z1 += mask_l2;
-        if ((word >> (sh + 2)) & 1u) z2 += mask_l2;
-        if ((word >> (sh + 3)) & 1u) z3 += mask_l2;
-      }
-      sacc[nt][0] = z0;
-      sacc[nt][1] = z1;
-      sacc[nt][2] = z2;
-      sacc[nt][3] = z3;
-      mx0 = fmaxf(mx0, fmaxf(z0, z1));
-      mx1 = fmaxf(mx1, fmaxf(z2, z3));
+      sacc[nt][0] = fmaf(sacc[nt][0], p.qk_scale_log2, bb.x);
+      sacc[nt][1] = fmaf(sacc[nt][1], p.qk_scale_log2, bb.y);
+      sacc[nt][2] = fmaf(sacc[nt][2], p.qk_scale_log2, bb.z);
+      sacc[nt][3] = fmaf(sacc[nt][3], p.qk_scale_log2, bb.w);
+    }
+    if (cls) {  // boundary windows only: add the mask from the class bit pattern
+      uint32_t mb[MW];
+#pragma unroll
+      for (int m = 0; m < MW; ++m) mb[m] = smask[(cls * MW + m) * THREADS + tid];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if ((mb[(nt * 4 + q) >> 5] >> ((nt * 4 + q) & 31)) & 1u) sacc[nt][q] += mask_l2;
+    }
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      mx0 = fmaxf(mx0, fmaxf(sacc[nt][0], sacc[nt][1]));
+      mx1 = fmaxf(mx1, fmaxf(sacc[nt][2], sacc[nt][3]));
     }
     mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
     mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
     mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
     mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
 
-    // ---- softmax numerators and row sums -----------------------------------------
-    float l0 = 0.0f, l1 = 0.0f;
+    // ---- softmax numerators -------------------------------------------------------
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       sacc[nt][0] = fast_exp2(sacc[nt][0] - mx0);
       sacc[nt][1] = fast_exp2(sacc[nt][1] - mx0);
       sacc[nt][2] = fast_exp2(sacc[nt][2] - mx1);
       sacc[nt][3] = fast_exp2(sacc[nt][3] - mx1);
-      l0 += sacc[nt][0] + sacc[nt][1];
-      l1 += sacc[nt][2] + sacc[nt][3];
     }
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
 
-    // ---- O = P V ------------------------------------------------------------------
-    float o[4][4];
+    // ---- O = P V, row sums from the ones tile ---------------------------------------
+    float o[4][4], lsum[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
     for (int nd = 0; nd < 4; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.0f;
 #pragma unroll
@@ -229,44 +264,49 @@ __global__ void __launch_bounds__(Geo<M>::THREADS) fwd_kernel(const FwdParams p)
         mma_bf16(o[2 * pr], a0, a1, a2, a3, v0, v1);
         mma_bf16(o[2 * pr + 1], a0, a1, a2, a3, v2, v3);
       }
+      mma_bf16(lsum, a0, a1, a2, a3, ones, ones);
     }
 
     // ---- normalise and store at the gathered token positions ----------------------
-    const float inv0 = 1.0f / l0, inv1 = 1.0f / l1;
+    const float inv0 = 1.0f / lsum[0], inv1 = 1.0f / lsum[2];
+    const int y0 = wy * M + s, x0 = wx * M + s;
+    int ya = y0 + oly0, xa = x0 + olx0, yb = y0 + oly1, xb = x0 + olx1;
+    ya = ya >= H ? ya - H : ya;
+    xa = xa >= W ? xa - W : xa;
+    yb = yb >= H ? yb - H : yb;
+    xb = xb >= W ? xb - W : xb;
+    const int64_t img = (int64_t)b * H * W;
+    const int64_t tok0 = img + ya * W + xa, tok1 = img + yb * W + xb;
     if constexpr (sizeof(TIO) == 2) {
       // Stage the warp's 16 x 32 bf16 rows in its own Q rows (only this warp reads
       // them, and they are consumed), then write 64 contiguous bytes per token.
-      const int r0 = warp * 16 + g, r1 = r0 + 8;
 #pragma unroll
       for (int nd = 0; nd < 4; ++nd) {  // columns 8nd..8nd+7 = 16-byte chunk nd
-        if (r0 < N)
-          *reinterpret_cast<uint32_t*>(tq + tile_off(r0, nd) + 4 * t) =
+        if (os0 < N)
+          *reinterpret_cast<uint32_t*>(tq + tile_off(os0, nd) + 4 * t) =
               pack_bf16(o[nd][0] * inv0, o[nd][1] * inv0);
-        if (r1 < N)
-          *reinterpret_cast<uint32_t*>(tq + tile_off(r1, nd) + 4 * t) =
+        if (os1 < N)
+          *reinterpret_cast<uint32_t*>(tq + tile_off(os1, nd) + 4 * t) =
               pack_bf16(o[nd][2] * inv1, o[nd][3] * inv1);
       }
       __syncwarp();
-#pragma unroll
-      for (int e = lane; e < 64; e += 32) {
-        const int r = e >> 2, c = e & 3, i = warp * 16 + r;
-        if (i < N) {
-          const int64_t tok = gather_token(b, wy, wx, i, M, s, H, W);
-          const uint4 val = *reinterpret_cast<const uint4*>(tq + tile_off(i, c));
-          *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + tok * C + h * kHeadDim + c * 8) = val;
-        }
-      }
+      __nv_bfloat16* outp = reinterpret_cast<__nv_bfloat16*>(p.out) + h * kHeadDim + t * 8;
+      if (os0 < N)
+        *reinterpret_cast<uint4*>(outp + tok0 * p.C) = *reinterpret_cast<const uint4*>(tq + tile_off(os0, t));
+      if (os1 < N)
+        *reinterpret_cast<uint4*>(outp + tok1 * p.C) = *reinterpret_cast<const uint4*>(tq + tile_off(os1, t));
     } else {
-      const int i0 = warp * 16 + g, i1 = i0 + 8;
-      float* outp = reinterpret_cast<float*>(p.out);
-      if (i0 < N) {
-        float* dst = outp + gather_token(b, wy, wx, i0, M, s, H, W) * C + h * kHeadDim + 2 * t;
+      // fp32 output: each lane writes its own fragment pairs (rows g and g+8).
+      float* outp = reinterpret_cast<float*>(p.out) + h * kHeadDim + 2 * t;
+      // rows g / g+8 of this warp are slots os0 / os1 (same as the staging slots)
+      if (os0 < N) {
+        float* dst = outp + tok0 * p.C;
 #pragma unroll
         for (int nd = 0; nd < 4; ++nd)
           *reinterpret_cast<float2*>(dst + nd * 8) = make_float2(o[nd][0] * inv0, o[nd][1] * inv0);
       }
-      if (i1 < N) {
-        float* dst = outp + gather_token(b, wy, wx, i1, M, s, H, W) * C + h * kHeadDim + 2 * t;
+      if (os1 < N) {
+        float* dst = outp + tok1 * p.C;
 #pragma unroll
         for (int nd = 0; nd < 4; ++nd)
           *reinterpret_cast<float2*>(dst + nd * 8) = make_float2(o[nd][2] * inv1, o[nd][3] * inv1);
