@@ -39,8 +39,8 @@ struct BwdParams {
   const void* qkv;
   const void* dout;
   void* dqkv;
-  const float* dense_bias;
-  const float* mask;
+  const float4* bias_frag;
+  const uint32_t* mask_frag;
   float* partial;  // [grid, R]
   int H, W, C, nH, s, nWy, nWx, nW;
   int64_t total_windows;
@@ -173,6 +173,17 @@ __global__ void __launch_bounds__(Geo<M>::THREADS) bwd_kernel(const BwdParams p)
     }
   };
 
+  // This head's bias fragments and the class mask bits (built by the plan in this
+  // kernel's fragment order) travel in the first copy group, with window 0.
+  {
+    const unsigned char* bsrc = reinterpret_cast<const unsigned char*>(p.bias_frag) + (size_t)h * G::BIAS_BYTES;
+    for (int e = tid; e < G::BIAS_BYTES / 16; e += THREADS) cp_async_16(smem_u32(smem + e * 16), bsrc + e * 16);
+    if (p.mask_frag != nullptr) {
+      const unsigned char* msrc = reinterpret_cast<const unsigned char*>(p.mask_frag);
+      for (int e = tid; e < G::MASK_BYTES / 16; e += THREADS)
+        cp_async_16(smem_u32(smem + G::BIAS_BYTES + e * 16), msrc + e * 16);
+    }
+  }
 #pragma unroll
   for (int st = 0; st < STAGES - 1; ++st) {
     if (st < nwin) issue(st);
@@ -190,39 +201,6 @@ __global__ void __launch_bounds__(Geo<M>::THREADS) bwd_kernel(const BwdParams p)
   // P and dS tiles (hi and lo) start zeroed: columns NT*8..NPAD-1 are never written.
   for (int e = tid; e < 4 * BG::PS_BYTES / 16; e += THREADS)
     reinterpret_cast<uint4*>(sP)[e] = make_uint4(0u, 0u, 0u, 0u);
-  {
-    const float* db = p.dense_bias + (int64_t)h * N * N;
-    for (int e = tid; e < G::WARPS * NT * 32; e += THREADS) {
-      const int ln = e & 31, nt = (e >> 5) % NT, wp = (e >> 5) / NT;
-      const int r0 = wp * 16 + (ln >> 2), c0 = nt * 8 + 2 * (ln & 3);
-      float v[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int r = r0 + 8 * (q >> 1), c = c0 + (q & 1);
-        v[q] = c >= N ? -INFINITY : (r >= N ? 0.0f : db[r * N + c] * kLog2e);
-      }
-      sbias[e] = make_float4(v[0], v[1], v[2], v[3]);
-    }
-  }
-  if (p.mask != nullptr) {
-    for (int cls = 1; cls < 4; ++cls) {
-      const int wy = (cls & 2) ? p.nWy - 1 : 0, wx = (cls & 1) ? p.nWx - 1 : 0;
-      const float* mw = p.mask + (int64_t)(wy * p.nWx + wx) * N * N;
-      uint32_t bits[MW];
-#pragma unroll
-      for (int m = 0; m < MW; ++m) bits[m] = 0u;
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int r = warp * 16 + g + 8 * (q >> 1), c = nt * 8 + 2 * t + (q & 1);
-          if (r < N && c < N && mw[r * N + c] != 0.0f) bits[(nt * 4 + q) >> 5] |= 1u << ((nt * 4 + q) & 31);
-        }
-#pragma unroll
-      for (int m = 0; m < MW; ++m) smask[(cls * MW + m) * THREADS + tid] = bits[m];
-    }
-  }
-
   const float mask_l2 = kMaskValue * kLog2e;
   const float4* bfrag = sbias + warp * NT * 32 + lane;
   const int r0 = warp * 16 + g, r1 = r0 + 8;
@@ -267,7 +245,7 @@ __global__ void __launch_bounds__(Geo<M>::THREADS) bwd_kernel(const BwdParams p)
       }
     }
     int cls = 0;
-    if (p.mask != nullptr) cls = (wy == p.nWy - 1 ? 2 : 0) | (wx == p.nWx - 1 ? 1 : 0);
+    if (p.mask_frag != nullptr) cls = (wy == p.nWy - 1 ? 2 : 0) | (wx == p.nWx - 1 ? 1 : 0);
     uint32_t mb[MW];
 #pragma unroll
     for (int m = 0; m < MW; ++m) mb[m] = cls ? smask[(cls * MW + m) * THREADS + tid] : 0u;
@@ -521,8 +499,8 @@ static cudaError_t blaunch_t(const Plan& pl, const BwdLaunch& L, const void* qkv
   p.qkv = qkv;
   p.dout = dout;
   p.dqkv = dqkv;
-  p.dense_bias = pl.dense_bias;
-  p.mask = pl.s > 0 ? pl.mask : nullptr;
+  p.bias_frag = pl.bias_frag;
+  p.mask_frag = pl.s > 0 ? pl.mask_frag : nullptr;
   p.partial = pl.dt_partial;
   p.H = pl.H;
   p.W = pl.W;

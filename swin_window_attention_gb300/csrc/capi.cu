@@ -14,6 +14,9 @@ cudaError_t launch_expand_bias(const float* table, int nH, int M, float* dense, 
 cudaError_t launch_build_mask(int H, int W, int M, int s, float* mask, cudaStream_t st);
 cudaError_t launch_gather_map(int H, int W, int M, int s, int32_t* out, cudaStream_t st);
 cudaError_t launch_relidx(int M, int32_t* out, cudaStream_t st);
+cudaError_t launch_fragments(const Plan& p, cudaStream_t st);
+size_t bias_frag_bytes(int M, int nH);
+size_t mask_frag_bytes(int M);
 cudaError_t fwd_config(const Plan& pl, FwdLaunch* L);
 cudaError_t fwd_launch(const Plan& pl, const FwdLaunch& L, const void* qkv, void* out,
                        cudaStream_t st);
@@ -74,7 +77,11 @@ void free_plan_buffers(swin::Plan& p) {
   if (p.dense_bias) cudaFree(p.dense_bias);
   if (p.mask) cudaFree(p.mask);
   if (p.dt_partial) cudaFree(p.dt_partial);
+  if (p.bias_frag) cudaFree(p.bias_frag);
+  if (p.mask_frag) cudaFree(p.mask_frag);
   p.dense_bias = p.mask = p.dt_partial = nullptr;
+  p.bias_frag = nullptr;
+  p.mask_frag = nullptr;
 }
 
 }  // namespace
@@ -140,6 +147,8 @@ int swin_wattn_plan(swin_wattn_plan_t* out, int B, int H, int W, int C, int num_
   if (e == cudaSuccess) e = cudaMalloc(&p.dense_bias, sizeof(float) * nn * p.nH);
   // The mask tensor always exists (all zeros for s = 0) so that it can be dumped.
   if (e == cudaSuccess) e = cudaMalloc(&p.mask, sizeof(float) * nn * p.nW);
+  if (e == cudaSuccess) e = cudaMalloc(&p.bias_frag, swin::bias_frag_bytes(p.M, p.nH));
+  if (e == cudaSuccess && p.s > 0) e = cudaMalloc(&p.mask_frag, swin::mask_frag_bytes(p.M));
   if (e == cudaSuccess) e = swin::fwd_config(p, &pl->fwd);
   if (e == cudaSuccess) e = swin::bwd_config(p, &pl->bwd);
   if (e == cudaSuccess && pl->bwd.partial_rows > 0) {
@@ -154,6 +163,10 @@ int swin_wattn_plan(swin_wattn_plan_t* out, int B, int H, int W, int C, int num_
   }
   if (e == cudaSuccess) {
     e = swin::launch_build_mask(p.H, p.W, p.M, p.s, p.mask, st);
+    ++g_launches;
+  }
+  if (e == cudaSuccess) {
+    e = swin::launch_fragments(p, st);
     ++g_launches;
   }
   if (e != cudaSuccess) {
@@ -178,9 +191,13 @@ int swin_wattn_set_bias(swin_wattn_plan_t plan, const float* bias_table,
   rc = check_device_ptr(bias_table, 4);
   if (rc != SWIN_WATTN_OK) return rc;
   const swin::Plan& p = plan->p;
-  cudaError_t e = swin::launch_expand_bias(bias_table, p.nH, p.M, p.dense_bias,
-                                           reinterpret_cast<cudaStream_t>(stream));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = swin::launch_expand_bias(bias_table, p.nH, p.M, p.dense_bias, st);
   ++g_launches;
+  if (e == cudaSuccess) {
+    e = swin::launch_fragments(p, st);
+    ++g_launches;
+  }
   return e == cudaSuccess ? SWIN_WATTN_OK : cuda_fail(e, "swin_wattn_set_bias");
 }
 

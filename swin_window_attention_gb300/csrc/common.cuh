@@ -24,6 +24,12 @@ struct Plan {
   float* mask;        // [nW, N, N], owned; null when s == 0
   float* dt_partial;  // backward reduction scratch, owned
   int dt_partial_rows;
+  // Per-head dense bias in the kernels' mma-fragment order, log2(e)-scaled, -inf in
+  // padded key columns: [nH][WARPS][NT][32 lanes] float4. Owned.
+  float4* bias_frag;
+  // Shift-mask bit patterns of the four window classes in fragment order:
+  // [4 classes][MW][THREADS] uint32 (class 0 all clear). Owned; null when s == 0.
+  uint32_t* mask_frag;
 };
 
 // ---- geometry shared by every kernel that touches a window -----------------------

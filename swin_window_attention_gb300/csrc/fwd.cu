@@ -24,8 +24,8 @@ namespace swin {
 struct FwdParams {
   const void* qkv;
   void* out;
-  const float* dense_bias;  // [nH, N, N]
-  const float* mask;        // [nW, N, N] or null
+  const float4* bias_frag;    // plan fragments [nH][WARPS][NT][32]
+  const uint32_t* mask_frag;  // plan class bit patterns [4][MW][THREADS] or null
   int H, W, C, nH, s, nWy, nWx, nW;
   int64_t total_windows;  // B * nW
   int chunks;             // window ranges per head
@@ -104,6 +104,17 @@ __global__ void __launch_bounds__(Geo<M>::THREADS) fwd_kernel(const FwdParams p)
   };
 
   // Start the first windows' loads before the one-off staging below.
+  // This head's bias fragments and the class mask bits (built by the plan in this
+  // kernel's fragment order) travel in the first copy group, with window 0.
+  {
+    const unsigned char* bsrc = reinterpret_cast<const unsigned char*>(p.bias_frag) + (size_t)h * G::BIAS_BYTES;
+    for (int e = tid; e < G::BIAS_BYTES / 16; e += THREADS) cp_async_16(smem_u32(smem + e * 16), bsrc + e * 16);
+    if (p.mask_frag != nullptr) {
+      const unsigned char* msrc = reinterpret_cast<const unsigned char*>(p.mask_frag);
+      for (int e = tid; e < G::MASK_BYTES / 16; e += THREADS)
+        cp_async_16(smem_u32(smem + G::BIAS_BYTES + e * 16), msrc + e * 16);
+    }
+  }
 #pragma unroll
   for (int st = 0; st < STAGES - 1; ++st) {
     if (st < nwin) issue(st);
@@ -119,43 +130,6 @@ __global__ void __launch_bounds__(Geo<M>::THREADS) fwd_kernel(const FwdParams p)
           make_uint4(0u, 0u, 0u, 0u);
     }
   }
-  // Bias fragments: lane (g,t) of warp wp, key tile nt holds rows 16wp+g, +8 and
-  // columns 8nt+2t, +1. Padded key columns get -inf, padded query rows 0.
-  {
-    const float* db = p.dense_bias + (int64_t)h * N * N;
-    for (int e = tid; e < G::WARPS * NT * 32; e += THREADS) {
-      const int ln = e & 31, nt = (e >> 5) % NT, wp = (e >> 5) / NT;
-      const int r0 = wp * 16 + (ln >> 2), c0 = nt * 8 + 2 * (ln & 3);
-      float v[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int r = r0 + 8 * (q >> 1), c = c0 + (q & 1);
-        v[q] = c >= N ? -INFINITY : (r >= N ? 0.0f : db[r * N + c] * kLog2e);
-      }
-      sbias[e] = make_float4(v[0], v[1], v[2], v[3]);
-    }
-  }
-  // Mask bit patterns of the window classes 1..3 (bit 1: last window row, bit 0: last
-  // window column), read from the plan's mask tensor at one window of each class.
-  if (p.mask != nullptr) {
-    for (int cls = 1; cls < 4; ++cls) {
-      const int wy = (cls & 2) ? p.nWy - 1 : 0, wx = (cls & 1) ? p.nWx - 1 : 0;
-      const float* mw = p.mask + (int64_t)(wy * p.nWx + wx) * N * N;
-      uint32_t bits[MW];
-#pragma unroll
-      for (int m = 0; m < MW; ++m) bits[m] = 0u;
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int r = warp * 16 + g + 8 * (q >> 1), c = nt * 8 + 2 * t + (q & 1);
-          if (r < N && c < N && mw[r * N + c] != 0.0f) bits[(nt * 4 + q) >> 5] |= 1u << ((nt * 4 + q) & 31);
-        }
-#pragma unroll
-      for (int m = 0; m < MW; ++m) smask[(cls * MW + m) * THREADS + tid] = bits[m];
-    }
-  }
-
   const float mask_l2 = kMaskValue * kLog2e;
   const float4* bfrag = sbias + warp * NT * 32 + lane;
   // Output slots of this lane: rows warp*16 + g + {0, 8}, 16-byte chunk t.
@@ -204,7 +178,7 @@ __global__ void __launch_bounds__(Geo<M>::THREADS) fwd_kernel(const FwdParams p)
 
     // ---- logits (log2 domain): scale, bias, mask; row max ----------------------
     int cls = 0;
-    if (p.mask != nullptr) cls = (wy == p.nWy - 1 ? 2 : 0) | (wx == p.nWx - 1 ? 1 : 0);
+    if (p.mask_frag != nullptr) cls = (wy == p.nWy - 1 ? 2 : 0) | (wx == p.nWx - 1 ? 1 : 0);
     float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
@@ -347,8 +321,8 @@ static cudaError_t launch_t(const Plan& pl, const FwdLaunch& L, const void* qkv,
   FwdParams p;
   p.qkv = qkv;
   p.out = out;
-  p.dense_bias = pl.dense_bias;
-  p.mask = pl.s > 0 ? pl.mask : nullptr;
+  p.bias_frag = pl.bias_frag;
+  p.mask_frag = pl.s > 0 ? pl.mask_frag : nullptr;
   p.H = pl.H;
   p.W = pl.W;
   p.C = pl.C;
