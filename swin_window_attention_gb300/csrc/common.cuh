@@ -13,6 +13,9 @@ constexpr uint32_t kPlanMagic = 0x5357414eu;  // "SWAN"
 constexpr int kHeadDim = 32;
 constexpr float kMaskValue = -100.0f;
 constexpr float kLog2e = 1.4426950408889634f;
+// 1 / scale = sqrt(hd) for hd = 32: the kernels accumulate z = q.k + (bias + mask) / scale
+// in the MMA, so that the logit is scale * z.
+constexpr float kInvScale = 5.6568542494923802f;
 
 struct Plan {
   uint32_t magic;

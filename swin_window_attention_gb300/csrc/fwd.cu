@@ -57,18 +57,21 @@ __global__ void __launch_bounds__(Geo<M>::THREADS) fwd_kernel(const FwdParams p)
   const TIO* __restrict__ qkv = reinterpret_cast<const TIO*>(p.qkv);
 
   // Per-thread gather descriptors, fixed for every window: chunk k of this thread is
-  // 16-byte chunk c of slice tt (q, k or v) of window slot i.
-  uint32_t ld_soff[CH_ITERS];
-  int ld_chan[CH_ITERS], ld_ly[CH_ITERS], ld_lx[CH_ITERS];
+  // 16-byte chunk c of slice tt (q, k or v) of window slot i = (ly, lx). ld_loff is the
+  // element offset of that chunk from the window's first token when the window does not
+  // wrap around the grid edge.
+  // Packed: shared offset (bits 0-15), window row (16-19), window column (20-23), slice
+  // (24-25), chunk (26-27).
+  uint32_t ld_desc[CH_ITERS];
+  int ld_loff[CH_ITERS];
 #pragma unroll
   for (int k = 0; k < CH_ITERS; ++k) {
     const int id = tid + k * THREADS;
     const int c = id & 3, rest = id >> 2;
-    const int i = rest % N, tt = rest / N;
-    ld_soff[k] = tt * G::TILE_BYTES + tile_off(i, c);
-    ld_chan[k] = tt * p.C + h * kHeadDim + c * 8;
-    ld_ly[k] = i / M;
-    ld_lx[k] = i % M;
+    const int i = rest % N, tt = (rest / N) & 3;
+    ld_desc[k] = (uint32_t)(tt * G::TILE_BYTES + tile_off(i, c)) | ((uint32_t)(i / M) << 16) |
+                 ((uint32_t)(i % M) << 20) | ((uint32_t)tt << 24) | ((uint32_t)c << 26);
+    ld_loff[k] = ((i / M) * W + i % M) * C3 + tt * p.C + h * kHeadDim + c * 8;
   }
   // Window cursor of the next window to load: (b, wy, wx) advanced one window at a time.
   int lb, lwy, lwx;
@@ -80,18 +83,29 @@ __global__ void __launch_bounds__(Geo<M>::THREADS) fwd_kernel(const FwdParams p)
     lwx = w - lwy * p.nWx;
   }
   int cb = lb, cwy = lwy, cwx = lwx;  // cursor of the window being computed
+  const uint32_t tiles_u32 = smem_u32(stiles);
 
-  auto issue = [&](int stage) {
-    unsigned char* base = stiles + stage * G::STAGE_BYTES;
-    const TIO* img = qkv + (int64_t)lb * H * W * C3;
+  auto issue = [&](uint32_t stage_off) {
+    const uint32_t base = tiles_u32 + stage_off;
     const int y0 = lwy * M + s, x0 = lwx * M + s;
+    if (y0 + M <= H && x0 + M <= W) {  // no wrap: one base plus fixed offsets
+      const TIO* wbase = qkv + ((int64_t)lb * H * W + (int64_t)y0 * W + x0) * C3;
 #pragma unroll
-    for (int k = 0; k < CH_ITERS; ++k) {
-      if (k < CH_ITERS - 1 || tid + k * THREADS < G::CHUNKS) {
-        int y = y0 + ld_ly[k], x = x0 + ld_lx[k];
-        y = y >= H ? y - H : y;
-        x = x >= W ? x - W : x;
-        load_chunk<TIO>(smem_u32(base + ld_soff[k]), img + (int64_t)(y * W + x) * C3 + ld_chan[k]);
+      for (int k = 0; k < CH_ITERS; ++k)
+        if (k < CH_ITERS - 1 || tid + k * THREADS < G::CHUNKS)
+          load_chunk<TIO>(base + (ld_desc[k] & 0xffffu), wbase + ld_loff[k]);
+    } else {
+      const TIO* img = qkv + (int64_t)lb * H * W * C3;
+#pragma unroll
+      for (int k = 0; k < CH_ITERS; ++k) {
+        if (k < CH_ITERS - 1 || tid + k * THREADS < G::CHUNKS) {
+          const uint32_t d = ld_desc[k];
+          int y = y0 + (int)((d >> 16) & 15), x = x0 + (int)((d >> 20) & 15);
+          y = y >= H ? y - H : y;
+          x = x >= W ? x - W : x;
+          const int chan = (int)((d >> 24) & 3) * p.C + h * kHeadDim + (int)((d >> 26) & 3) * 8;
+          load_chunk<TIO>(base + (d & 0xffffu), img + (int64_t)(y * W + x) * C3 + chan);
+        }
       }
     }
     if (++lwx == p.nWx) {
@@ -103,7 +117,6 @@ __global__ void __launch_bounds__(Geo<M>::THREADS) fwd_kernel(const FwdParams p)
     }
   };
 
-  // Start the first windows' loads before the one-off staging below.
   // This head's bias fragments and the class mask bits (built by the plan in this
   // kernel's fragment order) travel in the first copy group, with window 0.
   {
@@ -117,7 +130,7 @@ __global__ void __launch_bounds__(Geo<M>::THREADS) fwd_kernel(const FwdParams p)
   }
 #pragma unroll
   for (int st = 0; st < STAGES - 1; ++st) {
-    if (st < nwin) issue(st);
+    if (st < nwin) issue(st * G::STAGE_BYTES);
     cp_async_commit();
   }
 
@@ -130,23 +143,31 @@ __global__ void __launch_bounds__(Geo<M>::THREADS) fwd_kernel(const FwdParams p)
           make_uint4(0u, 0u, 0u, 0u);
     }
   }
-  const float mask_l2 = kMaskValue * kLog2e;
   const float4* bfrag = sbias + warp * NT * 32 + lane;
+  const float c_l2 = p.qk_scale_log2;            // scale * log2(e)
+  const float mask_z = kMaskValue * kInvScale;  // the -100 mask in units of z
   // Output slots of this lane: rows warp*16 + g + {0, 8}, 16-byte chunk t.
   const int os0 = warp * 16 + g, os1 = os0 + 8;
   const int oly0 = os0 / M, olx0 = os0 % M, oly1 = os1 / M, olx1 = os1 % M;
   // B operand of all ones: one extra m16n8 tile of P V yields the row sums of the very
   // bf16 P values that weight V.
   const uint32_t ones = 0x3F803F80u;
+  // Lane parts of the ldmatrix addresses (tile-relative; key tile nt adds nt*512 bytes,
+  // value k-step kk adds kk*1024 bytes).
+  const int mi = lane >> 3, r8 = lane & 7, r16 = r8 + ((mi & 1) << 3);
+  const uint32_t q_off0 = tile_off(warp * 16 + r16, mi >> 1);
+  const uint32_t q_off1 = tile_off(warp * 16 + r16, 2 + (mi >> 1));
+  const uint32_t k_off = G::TILE_BYTES + tile_off(r8, mi);
+  const uint32_t v_off0 = 2 * G::TILE_BYTES + tile_off(r16, mi >> 1);
+  const uint32_t v_off1 = 2 * G::TILE_BYTES + tile_off(r16, 2 + (mi >> 1));
 
+  uint32_t cur_off = 0, nxt_off = (STAGES - 1) * G::STAGE_BYTES;
   for (int it = 0; it < nwin; ++it) {
     cp_async_wait<STAGES - 2>();
     __syncthreads();
-    {
-      const int nx = it + STAGES - 1;
-      if (nx < nwin) issue(nx % STAGES);
-      cp_async_commit();
-    }
+    if (it + STAGES - 1 < nwin) issue(nxt_off);
+    cp_async_commit();
+    nxt_off = nxt_off + G::STAGE_BYTES == STAGES * G::STAGE_BYTES ? 0 : nxt_off + G::STAGE_BYTES;
     const int b = cb, wy = cwy, wx = cwx;
     if (++cwx == p.nWx) {
       cwx = 0;
@@ -155,40 +176,31 @@ __global__ void __launch_bounds__(Geo<M>::THREADS) fwd_kernel(const FwdParams p)
         ++cb;
       }
     }
-    unsigned char* tq = stiles + (it % STAGES) * G::STAGE_BYTES;
-    const uint32_t qb = smem_u32(tq), kb = qb + G::TILE_BYTES, vb = kb + G::TILE_BYTES;
+    unsigned char* tq = stiles + cur_off;
+    const uint32_t tb = tiles_u32 + cur_off;
+    cur_off = cur_off + G::STAGE_BYTES == STAGES * G::STAGE_BYTES ? 0 : cur_off + G::STAGE_BYTES;
 
-    // ---- S = Q K^T -------------------------------------------------------------
+    // ---- z = Q K^T + bias/scale: the accumulators start from the bias fragment ------
     uint32_t qa[2][4];
-    {
-      const int mi = lane >> 3, row = warp * 16 + (lane & 7) + ((mi & 1) << 3);
-#pragma unroll
-      for (int kk = 0; kk < 2; ++kk)
-        ldsm_x4(qb + tile_off(row, 2 * kk + (mi >> 1)), qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
-    }
+    ldsm_x4(tb + q_off0, qa[0][0], qa[0][1], qa[0][2], qa[0][3]);
+    ldsm_x4(tb + q_off1, qa[1][0], qa[1][1], qa[1][2], qa[1][3]);
     float sacc[NT][4];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.0f;
+      const float4 bb = bfrag[nt * 32];
+      sacc[nt][0] = bb.x;
+      sacc[nt][1] = bb.y;
+      sacc[nt][2] = bb.z;
+      sacc[nt][3] = bb.w;
       uint32_t b0, b1, b2, b3;
-      ldsm_x4(kb + tile_off(nt * 8 + (lane & 7), lane >> 3), b0, b1, b2, b3);
+      ldsm_x4(tb + k_off + nt * 512, b0, b1, b2, b3);
       mma_bf16(sacc[nt], qa[0][0], qa[0][1], qa[0][2], qa[0][3], b0, b1);
       mma_bf16(sacc[nt], qa[1][0], qa[1][1], qa[1][2], qa[1][3], b2, b3);
     }
 
-    // ---- logits (log2 domain): scale, bias, mask; row max ----------------------
-    int cls = 0;
-    if (p.mask_frag != nullptr) cls = (wy == p.nWy - 1 ? 2 : 0) | (wx == p.nWx - 1 ? 1 : 0);
-    float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      const float4 bb = bfrag[nt * 32];
-      sacc[nt][0] = fmaf(sacc[nt][0], p.qk_scale_log2, bb.x);
-      sacc[nt][1] = fmaf(sacc[nt][1], p.qk_scale_log2, bb.y);
-      sacc[nt][2] = fmaf(sacc[nt][2], p.qk_scale_log2, bb.z);
-      sacc[nt][3] = fmaf(sacc[nt][3], p.qk_scale_log2, bb.w);
-    }
-    if (cls) {  // boundary windows only: add the mask from the class bit pattern
+    // ---- mask (boundary windows only) and row max --------------------------------
+    if (p.mask_frag != nullptr && (wy == p.nWy - 1 || wx == p.nWx - 1)) {
+      const int cls = (wy == p.nWy - 1 ? 2 : 0) | (wx == p.nWx - 1 ? 1 : 0);
       uint32_t mb[MW];
 #pragma unroll
       for (int m = 0; m < MW; ++m) mb[m] = smask[(cls * MW + m) * THREADS + tid];
@@ -196,25 +208,33 @@ __global__ void __launch_bounds__(Geo<M>::THREADS) fwd_kernel(const FwdParams p)
       for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
         for (int q = 0; q < 4; ++q)
-          if ((mb[(nt * 4 + q) >> 5] >> ((nt * 4 + q) & 31)) & 1u) sacc[nt][q] += mask_l2;
+          if ((mb[(nt * 4 + q) >> 5] >> ((nt * 4 + q) & 31)) & 1u) sacc[nt][q] += mask_z;
     }
+    // two interleaved max chains per row halve the dependency depth
+    float m0a = -INFINITY, m0b = -INFINITY, m1a = -INFINITY, m1b = -INFINITY;
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      mx0 = fmaxf(mx0, fmaxf(sacc[nt][0], sacc[nt][1]));
-      mx1 = fmaxf(mx1, fmaxf(sacc[nt][2], sacc[nt][3]));
+    for (int nt = 0; nt < NT; nt += 2) {
+      m0a = fmaxf(m0a, fmaxf(sacc[nt][0], sacc[nt][1]));
+      m1a = fmaxf(m1a, fmaxf(sacc[nt][2], sacc[nt][3]));
+      if (nt + 1 < NT) {
+        m0b = fmaxf(m0b, fmaxf(sacc[nt + 1][0], sacc[nt + 1][1]));
+        m1b = fmaxf(m1b, fmaxf(sacc[nt + 1][2], sacc[nt + 1][3]));
+      }
     }
+    float mx0 = fmaxf(m0a, m0b), mx1 = fmaxf(m1a, m1b);
     mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
     mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
     mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
 
-    // ---- softmax numerators -------------------------------------------------------
+    // ---- softmax numerators: exp2((z - max) * scale * log2e) ------------------------
+    const float nm0 = -mx0 * c_l2, nm1 = -mx1 * c_l2;
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      sacc[nt][0] = fast_exp2(sacc[nt][0] - mx0);
-      sacc[nt][1] = fast_exp2(sacc[nt][1] - mx0);
-      sacc[nt][2] = fast_exp2(sacc[nt][2] - mx1);
-      sacc[nt][3] = fast_exp2(sacc[nt][3] - mx1);
+      sacc[nt][0] = fast_exp2(fmaf(sacc[nt][0], c_l2, nm0));
+      sacc[nt][1] = fast_exp2(fmaf(sacc[nt][1], c_l2, nm0));
+      sacc[nt][2] = fast_exp2(fmaf(sacc[nt][2], c_l2, nm1));
+      sacc[nt][3] = fast_exp2(fmaf(sacc[nt][3], c_l2, nm1));
     }
 
     // ---- O = P V, row sums from the ones tile ---------------------------------------
@@ -230,14 +250,13 @@ __global__ void __launch_bounds__(Geo<M>::THREADS) fwd_kernel(const FwdParams p)
         a2 = pack_bf16(sacc[2 * kk + 1][0], sacc[2 * kk + 1][1]);
         a3 = pack_bf16(sacc[2 * kk + 1][2], sacc[2 * kk + 1][3]);
       }
-      const int mi = lane >> 3, row = kk * 16 + (lane & 7) + ((mi & 1) << 3);
-#pragma unroll
-      for (int pr = 0; pr < 2; ++pr) {
-        uint32_t v0, v1, v2, v3;
-        ldsm_x4_t(vb + tile_off(row, 2 * pr + (mi >> 1)), v0, v1, v2, v3);
-        mma_bf16(o[2 * pr], a0, a1, a2, a3, v0, v1);
-        mma_bf16(o[2 * pr + 1], a0, a1, a2, a3, v2, v3);
-      }
+      uint32_t v0, v1, v2, v3;
+      ldsm_x4_t(tb + v_off0 + kk * 1024, v0, v1, v2, v3);
+      mma_bf16(o[0], a0, a1, a2, a3, v0, v1);
+      mma_bf16(o[1], a0, a1, a2, a3, v2, v3);
+      ldsm_x4_t(tb + v_off1 + kk * 1024, v0, v1, v2, v3);
+      mma_bf16(o[2], a0, a1, a2, a3, v0, v1);
+      mma_bf16(o[3], a0, a1, a2, a3, v2, v3);
       mma_bf16(lsum, a0, a1, a2, a3, ones, ones);
     }
 
@@ -333,7 +352,7 @@ static cudaError_t launch_t(const Plan& pl, const FwdLaunch& L, const void* qkv,
   p.nW = pl.nW;
   p.total_windows = (int64_t)pl.B * pl.nW;
   p.chunks = L.chunks;
-  p.qk_scale_log2 = kLog2e / sqrtf((float)kHeadDim);
+  p.qk_scale_log2 = kLog2e / kInvScale;
   fwd_kernel<M, TIO, STAGES><<<L.grid, L.threads, L.smem, st>>>(p);
   return cudaGetLastError();
 }

@@ -54,7 +54,9 @@ __global__ void relidx_kernel(int M, int32_t* __restrict__ out) {
 
 // The dense bias and the mask re-laid out once per plan in the order the attention
 // kernels consume them (lane (g, t) of warp wp, key tile nt: rows 16wp+g, +8; columns
-// 8nt+2t, +1), so a CTA stages its head's block with plain 16-byte copies.
+// 8nt+2t, +1), so a CTA stages its head's block with plain 16-byte copies. The bias is
+// stored divided by the softmax scale (it seeds the q.k accumulators), -inf in padded
+// key columns and 0 in padded query rows.
 template <int M>
 __global__ void fragments_kernel(const float* __restrict__ dense, const float* __restrict__ mask,
                                  int nH, int nWy, int nWx, float4* __restrict__ bias_frag,
@@ -74,7 +76,7 @@ __global__ void fragments_kernel(const float* __restrict__ dense, const float* _
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const int r = r0 + 8 * (q >> 1), c = c0 + (q & 1);
-        v[q] = c >= N ? -INFINITY : (r >= N ? 0.0f : db[r * N + c] * kLog2e);
+        v[q] = c >= N ? -INFINITY : (r >= N ? 0.0f : db[r * N + c] * kInvScale);
       }
       bias_frag[e] = make_float4(v[0], v[1], v[2], v[3]);
     } else {
