@@ -201,7 +201,7 @@ __global__ void __launch_bounds__(Geo<M>::THREADS) bwd_kernel(const BwdParams p)
   // P and dS tiles (hi and lo) start zeroed: columns NT*8..NPAD-1 are never written.
   for (int e = tid; e < 4 * BG::PS_BYTES / 16; e += THREADS)
     reinterpret_cast<uint4*>(sP)[e] = make_uint4(0u, 0u, 0u, 0u);
-  const float mask_l2 = kMaskValue * kLog2e;
+  const float mask_z = kMaskValue * kInvScale;  // the -100 mask in units of z
   const float4* bfrag = sbias + warp * NT * 32 + lane;
   const int r0 = warp * 16 + g, r1 = r0 + 8;
   float dtacc[NT][4];
@@ -237,7 +237,11 @@ __global__ void __launch_bounds__(Geo<M>::THREADS) bwd_kernel(const BwdParams p)
         ldsm_x4(qb + tile_off(row, 2 * kk + (mi >> 1)), qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
-        pr[nt][0] = pr[nt][1] = pr[nt][2] = pr[nt][3] = 0.0f;
+        const float4 bb = bfrag[nt * 32];  // z = q.k + bias/scale starts from the bias
+        pr[nt][0] = bb.x;
+        pr[nt][1] = bb.y;
+        pr[nt][2] = bb.z;
+        pr[nt][3] = bb.w;
         uint32_t b0, b1, b2, b3;
         ldsm_x4(kb + tile_off(nt * 8 + (lane & 7), lane >> 3), b0, b1, b2, b3);
         mma_bf16(pr[nt], qa[0][0], qa[0][1], qa[0][2], qa[0][3], b0, b1);
@@ -252,36 +256,28 @@ __global__ void __launch_bounds__(Geo<M>::THREADS) bwd_kernel(const BwdParams p)
     float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      const float4 bb = bfrag[nt * 32];
-      float z0 = fmaf(pr[nt][0], p.qk_scale_log2, bb.x);
-      float z1 = fmaf(pr[nt][1], p.qk_scale_log2, bb.y);
-      float z2 = fmaf(pr[nt][2], p.qk_scale_log2, bb.z);
-      float z3 = fmaf(pr[nt][3], p.qk_scale_log2, bb.w);
       if (cls) {
         const uint32_t word = mb[(nt * 4) >> 5], sh = (nt * 4) & 31;
-        if ((word >> sh) & 1u) z0 += mask_l2;
-        if ((word >> (sh + 1)) & 1u) z1 += mask_l2;
-        if ((word >> (sh + 2)) & 1u) z2 += mask_l2;
-        if ((word >> (sh + 3)) & 1u) z3 += mask_l2;
+        if ((word >> sh) & 1u) pr[nt][0] += mask_z;
+        if ((word >> (sh + 1)) & 1u) pr[nt][1] += mask_z;
+        if ((word >> (sh + 2)) & 1u) pr[nt][2] += mask_z;
+        if ((word >> (sh + 3)) & 1u) pr[nt][3] += mask_z;
       }
-      pr[nt][0] = z0;
-      pr[nt][1] = z1;
-      pr[nt][2] = z2;
-      pr[nt][3] = z3;
-      mx0 = fmaxf(mx0, fmaxf(z0, z1));
-      mx1 = fmaxf(mx1, fmaxf(z2, z3));
+      mx0 = fmaxf(mx0, fmaxf(pr[nt][0], pr[nt][1]));
+      mx1 = fmaxf(mx1, fmaxf(pr[nt][2], pr[nt][3]));
     }
     mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
     mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
     mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
     mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+    const float nm0 = -mx0 * p.qk_scale_log2, nm1 = -mx1 * p.qk_scale_log2;
     float l0 = 0.0f, l1 = 0.0f;
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      pr[nt][0] = fast_exp2(pr[nt][0] - mx0);
-      pr[nt][1] = fast_exp2(pr[nt][1] - mx0);
-      pr[nt][2] = fast_exp2(pr[nt][2] - mx1);
-      pr[nt][3] = fast_exp2(pr[nt][3] - mx1);
+      pr[nt][0] = fast_exp2(fmaf(pr[nt][0], p.qk_scale_log2, nm0));
+      pr[nt][1] = fast_exp2(fmaf(pr[nt][1], p.qk_scale_log2, nm0));
+      pr[nt][2] = fast_exp2(fmaf(pr[nt][2], p.qk_scale_log2, nm1));
+      pr[nt][3] = fast_exp2(fmaf(pr[nt][3], p.qk_scale_log2, nm1));
       l0 += pr[nt][0] + pr[nt][1];
       l1 += pr[nt][2] + pr[nt][3];
     }
@@ -512,8 +508,8 @@ static cudaError_t blaunch_t(const Plan& pl, const BwdLaunch& L, const void* qkv
   p.nW = pl.nW;
   p.total_windows = (int64_t)pl.B * pl.nW;
   p.chunks = L.chunks;
-  p.scale = 1.0f / sqrtf((float)kHeadDim);
-  p.qk_scale_log2 = p.scale * kLog2e;
+  p.scale = 1.0f / kInvScale;
+  p.qk_scale_log2 = kLog2e / kInvScale;
   bwd_kernel<M, TIO, STAGES><<<L.grid, L.threads, L.smem, st>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
