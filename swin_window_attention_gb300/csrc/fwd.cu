@@ -37,8 +37,12 @@ constexpr int fwd_smem_bytes() {
   return Geo<M>::BIAS_BYTES + Geo<M>::MASK_BYTES + STAGES * Geo<M>::STAGE_BYTES;
 }
 
+// Resident CTAs per SM the register budget is sized for.
+template <int M> struct FwdMinBlocks { static constexpr int value = 4; };
+template <> struct FwdMinBlocks<12> { static constexpr int value = 1; };
+
 template <int M, typename TIO, int STAGES>
-__global__ void __launch_bounds__(Geo<M>::THREADS) fwd_kernel(const FwdParams p) {
+__global__ void __launch_bounds__(Geo<M>::THREADS, FwdMinBlocks<M>::value) fwd_kernel(const FwdParams p) {
   using G = Geo<M>;
   constexpr int N = G::N, NT = G::NT, KT = G::KT, MW = G::MW, THREADS = G::THREADS;
   constexpr int CH_ITERS = G::CH_ITERS;
@@ -160,6 +164,9 @@ __global__ void __launch_bounds__(Geo<M>::THREADS) fwd_kernel(const FwdParams p)
   const uint32_t k_off = G::TILE_BYTES + tile_off(r8, mi);
   const uint32_t v_off0 = 2 * G::TILE_BYTES + tile_off(r16, mi >> 1);
   const uint32_t v_off1 = 2 * G::TILE_BYTES + tile_off(r16, 2 + (mi >> 1));
+  // stmatrix row addresses: matrix mi = (row half mi & 1, column chunk 2*call + (mi >> 1))
+  const uint32_t st_off0 = tile_off(warp * 16 + r8 + ((mi & 1) << 3), mi >> 1);
+  const uint32_t st_off1 = tile_off(warp * 16 + r8 + ((mi & 1) << 3), 2 + (mi >> 1));
 
   uint32_t cur_off = 0, nxt_off = (STAGES - 1) * G::STAGE_BYTES;
   for (int it = 0; it < nwin; ++it) {
@@ -188,13 +195,9 @@ __global__ void __launch_bounds__(Geo<M>::THREADS) fwd_kernel(const FwdParams p)
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       const float4 bb = bfrag[nt * 32];
-      sacc[nt][0] = bb.x;
-      sacc[nt][1] = bb.y;
-      sacc[nt][2] = bb.z;
-      sacc[nt][3] = bb.w;
       uint32_t b0, b1, b2, b3;
       ldsm_x4(tb + k_off + nt * 512, b0, b1, b2, b3);
-      mma_bf16(sacc[nt], qa[0][0], qa[0][1], qa[0][2], qa[0][3], b0, b1);
+      mma_bf16_c(sacc[nt], qa[0][0], qa[0][1], qa[0][2], qa[0][3], b0, b1, bb.x, bb.y, bb.z, bb.w);
       mma_bf16(sacc[nt], qa[1][0], qa[1][1], qa[1][2], qa[1][3], b2, b3);
     }
 
@@ -210,15 +213,15 @@ __global__ void __launch_bounds__(Geo<M>::THREADS) fwd_kernel(const FwdParams p)
         for (int q = 0; q < 4; ++q)
           if ((mb[(nt * 4 + q) >> 5] >> ((nt * 4 + q) & 31)) & 1u) sacc[nt][q] += mask_z;
     }
-    // two interleaved max chains per row halve the dependency depth
+    // two interleaved three-input max chains per row
     float m0a = -INFINITY, m0b = -INFINITY, m1a = -INFINITY, m1b = -INFINITY;
 #pragma unroll
     for (int nt = 0; nt < NT; nt += 2) {
-      m0a = fmaxf(m0a, fmaxf(sacc[nt][0], sacc[nt][1]));
-      m1a = fmaxf(m1a, fmaxf(sacc[nt][2], sacc[nt][3]));
+      m0a = fmax3(m0a, sacc[nt][0], sacc[nt][1]);
+      m1a = fmax3(m1a, sacc[nt][2], sacc[nt][3]);
       if (nt + 1 < NT) {
-        m0b = fmaxf(m0b, fmaxf(sacc[nt + 1][0], sacc[nt + 1][1]));
-        m1b = fmaxf(m1b, fmaxf(sacc[nt + 1][2], sacc[nt + 1][3]));
+        m0b = fmax3(m0b, sacc[nt + 1][0], sacc[nt + 1][1]);
+        m1b = fmax3(m1b, sacc[nt + 1][2], sacc[nt + 1][3]);
       }
     }
     float mx0 = fmaxf(m0a, m0b), mx1 = fmaxf(m1a, m1b);
@@ -238,9 +241,7 @@ __global__ void __launch_bounds__(Geo<M>::THREADS) fwd_kernel(const FwdParams p)
     }
 
     // ---- O = P V, row sums from the ones tile ---------------------------------------
-    float o[4][4], lsum[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-    for (int nd = 0; nd < 4; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.0f;
+    float o[4][4], lsum[4];
 #pragma unroll
     for (int kk = 0; kk < KT; ++kk) {
       const uint32_t a0 = pack_bf16(sacc[2 * kk][0], sacc[2 * kk][1]);
@@ -250,14 +251,22 @@ __global__ void __launch_bounds__(Geo<M>::THREADS) fwd_kernel(const FwdParams p)
         a2 = pack_bf16(sacc[2 * kk + 1][0], sacc[2 * kk + 1][1]);
         a3 = pack_bf16(sacc[2 * kk + 1][2], sacc[2 * kk + 1][3]);
       }
-      uint32_t v0, v1, v2, v3;
+      uint32_t v0, v1, v2, v3, w0, w1, w2, w3;
       ldsm_x4_t(tb + v_off0 + kk * 1024, v0, v1, v2, v3);
-      mma_bf16(o[0], a0, a1, a2, a3, v0, v1);
-      mma_bf16(o[1], a0, a1, a2, a3, v2, v3);
-      ldsm_x4_t(tb + v_off1 + kk * 1024, v0, v1, v2, v3);
-      mma_bf16(o[2], a0, a1, a2, a3, v0, v1);
-      mma_bf16(o[3], a0, a1, a2, a3, v2, v3);
-      mma_bf16(lsum, a0, a1, a2, a3, ones, ones);
+      ldsm_x4_t(tb + v_off1 + kk * 1024, w0, w1, w2, w3);
+      if (kk == 0) {
+        mma_bf16_c(o[0], a0, a1, a2, a3, v0, v1, 0.f, 0.f, 0.f, 0.f);
+        mma_bf16_c(o[1], a0, a1, a2, a3, v2, v3, 0.f, 0.f, 0.f, 0.f);
+        mma_bf16_c(o[2], a0, a1, a2, a3, w0, w1, 0.f, 0.f, 0.f, 0.f);
+        mma_bf16_c(o[3], a0, a1, a2, a3, w2, w3, 0.f, 0.f, 0.f, 0.f);
+        mma_bf16_c(lsum, a0, a1, a2, a3, ones, ones, 0.f, 0.f, 0.f, 0.f);
+      } else {
+        mma_bf16(o[0], a0, a1, a2, a3, v0, v1);
+        mma_bf16(o[1], a0, a1, a2, a3, v2, v3);
+        mma_bf16(o[2], a0, a1, a2, a3, w0, w1);
+        mma_bf16(o[3], a0, a1, a2, a3, w2, w3);
+        mma_bf16(lsum, a0, a1, a2, a3, ones, ones);
+      }
     }
 
     // ---- normalise and store at the gathered token positions ----------------------
@@ -272,16 +281,12 @@ __global__ void __launch_bounds__(Geo<M>::THREADS) fwd_kernel(const FwdParams p)
     const int64_t tok0 = img + ya * W + xa, tok1 = img + yb * W + xb;
     if constexpr (sizeof(TIO) == 2) {
       // Stage the warp's 16 x 32 bf16 rows in its own Q rows (only this warp reads
-      // them, and they are consumed), then write 64 contiguous bytes per token.
-#pragma unroll
-      for (int nd = 0; nd < 4; ++nd) {  // columns 8nd..8nd+7 = 16-byte chunk nd
-        if (os0 < N)
-          *reinterpret_cast<uint32_t*>(tq + tile_off(os0, nd) + 4 * t) =
-              pack_bf16(o[nd][0] * inv0, o[nd][1] * inv0);
-        if (os1 < N)
-          *reinterpret_cast<uint32_t*>(tq + tile_off(os1, nd) + 4 * t) =
-              pack_bf16(o[nd][2] * inv1, o[nd][3] * inv1);
-      }
+      // them, and they are consumed) with two stmatrix, then write 64 contiguous bytes
+      // per token. Padded rows receive finite values that are never stored.
+      stsm_x4(tb + st_off0, pack_bf16(o[0][0] * inv0, o[0][1] * inv0), pack_bf16(o[0][2] * inv1, o[0][3] * inv1),
+              pack_bf16(o[1][0] * inv0, o[1][1] * inv0), pack_bf16(o[1][2] * inv1, o[1][3] * inv1));
+      stsm_x4(tb + st_off1, pack_bf16(o[2][0] * inv0, o[2][1] * inv0), pack_bf16(o[2][2] * inv1, o[2][3] * inv1),
+              pack_bf16(o[3][0] * inv0, o[3][1] * inv0), pack_bf16(o[3][2] * inv1, o[3][3] * inv1));
       __syncwarp();
       __nv_bfloat16* outp = reinterpret_cast<__nv_bfloat16*>(p.out) + h * kHeadDim + t * 8;
       if (os0 < N)
