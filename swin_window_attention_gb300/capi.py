@@ -33,6 +33,8 @@ SIGNATURES = {
     "swin_wattn_fwd_host": ([_vp, _vp, _vp, _vp, _vp, _vp], _i),
     "swin_wattn_bwd": ([_vp, _vp, _vp, _vp, _vp, _vp], _i),
     "swin_wattn_debug_maps": ([_vp, _vp, _vp, _vp, _vp, _vp], _i),
+    "swin_wattn_sync": ([_vp, _vp], _i),
+    "swin_wattn_debug_withhold": ([_vp, ctypes.c_longlong], _i),
     "swin_wattn_destroy": ([_vp], _i),
     "swin_wattn_status_string": ([_i], _cp),
     "swin_wattn_last_error": ([], _cp),
@@ -98,6 +100,14 @@ def swin_wattn_bwd(plan, qkv_ptr, dout_ptr, dqkv_ptr, dtable_ptr, stream):
 def swin_wattn_debug_maps(plan, gather_ptr, relidx_ptr, mask_ptr, dense_bias_ptr, stream):
     return load().swin_wattn_debug_maps(plan, gather_ptr, relidx_ptr, mask_ptr, dense_bias_ptr,
                                         stream)
+
+
+def swin_wattn_sync(plan, stream):
+    return load().swin_wattn_sync(plan, stream)
+
+
+def swin_wattn_debug_withhold(plan, window):
+    return load().swin_wattn_debug_withhold(plan, window)
 
 
 def swin_wattn_destroy(plan):
@@ -178,6 +188,12 @@ class WindowAttention:
         if rc != OK:
             raise SwinWAttnError("swin_wattn_bwd", rc)
         return dqkv, dtable
+
+    def sync(self, stream=None):
+        """Wait for the stream; raise if a kernel of this plan gave up on a device wait."""
+        rc = swin_wattn_sync(self.handle, _stream_handle(stream))
+        if rc != OK:
+            raise SwinWAttnError("swin_wattn_sync", rc)
 
     def debug_maps(self, stream=None):
         import torch
