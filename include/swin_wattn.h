@@ -126,6 +126,30 @@ int swin_wattn_bwd(swin_wattn_plan_t plan, const void* qkv, const void* dout, vo
                    float* dtable, struct CUstream_st* stream);
 
 /*
+ * Backward without any device allocation (the pages have no counterpart: this entry
+ * point exists for callers that cannot allocate device memory when they run the
+ * backward, e.g. runtimes that fix their device memory plan at start-up and forbid any
+ * later cudaMalloc, or frameworks whose own allocator must own every device byte; such
+ * callers cannot create a plan, because a plan allocates).
+ *
+ * Same arguments and results as swin_wattn_plan followed by swin_wattn_bwd (qkv, dout,
+ * dqkv, dtable and the bias table are the caller's device buffers; window must be 4 or
+ * 7), but no plan is made and nothing is allocated or freed: the working memory (bias
+ * fragments, mask bits, per-CTA table-gradient partials) lives in one fixed 2 MiB
+ * device array inside the library, which every GPU that loads the library holds until
+ * the process exits. A shape whose working memory exceeds 2 MiB is refused with
+ * SWIN_WATTN_ERR_UNSUPPORTED and the reason in swin_wattn_last_error().
+ *
+ * The first call on a device looks up the array's device address (cudaGetSymbolAddress)
+ * with that device current; make that first call before any stream capture. Every call
+ * on a device shares the one array and overwrites it completely, so two calls that
+ * overlap on the GPU (different streams without ordering between them) race: order them.
+ */
+int swin_wattn_bwd_noalloc(const void* qkv, const void* dout, void* dqkv, float* dtable,
+                           const float* bias_table, int B, int H, int W, int C, int num_heads,
+                           int window, int shift, int dtype, struct CUstream_st* stream);
+
+/*
  * Debug dumps of the plan's index maps and preprocessed tensors (device pointers, any
  * may be NULL to skip):
  *   gather     int32 [nW, M^2]: original token index y*W + x that window w, slot i

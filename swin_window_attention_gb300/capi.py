@@ -34,6 +34,7 @@ SIGNATURES = {
     "swin_wattn_bwd": ([_vp, _vp, _vp, _vp, _vp, _vp], _i),
     "swin_wattn_debug_maps": ([_vp, _vp, _vp, _vp, _vp, _vp], _i),
     "swin_wattn_sync": ([_vp, _vp], _i),
+    "swin_wattn_bwd_noalloc": ([_vp, _vp, _vp, _vp, _vp] + [_i] * 8 + [_vp], _i),
     "swin_wattn_debug_withhold": ([_vp, ctypes.c_longlong], _i),
     "swin_wattn_destroy": ([_vp], _i),
     "swin_wattn_status_string": ([_i], _cp),
@@ -100,6 +101,14 @@ def swin_wattn_bwd(plan, qkv_ptr, dout_ptr, dqkv_ptr, dtable_ptr, stream):
 def swin_wattn_debug_maps(plan, gather_ptr, relidx_ptr, mask_ptr, dense_bias_ptr, stream):
     return load().swin_wattn_debug_maps(plan, gather_ptr, relidx_ptr, mask_ptr, dense_bias_ptr,
                                         stream)
+
+
+def swin_wattn_bwd_noalloc(qkv_ptr, dout_ptr, dqkv_ptr, dtable_ptr, table_ptr, B, H, W, C,
+                           num_heads, window, shift, dtype, stream):
+    """Backward with no plan and no device allocation (fixed working memory in the
+    library); see include/swin_wattn.h."""
+    return load().swin_wattn_bwd_noalloc(qkv_ptr, dout_ptr, dqkv_ptr, dtable_ptr, table_ptr, B, H,
+                                         W, C, num_heads, window, shift, dtype, stream)
 
 
 def swin_wattn_sync(plan, stream):

@@ -19,6 +19,10 @@
 // per-(i,j) dS sums stay in registers across the CTA's windows; at the end one thread
 // per table row folds them in a fixed order into a per-CTA partial, and a second
 // kernel sums the partials in a fixed order: the result is deterministic.
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
 #include "common.cuh"
 
 namespace swin {
@@ -549,4 +553,192 @@ cudaError_t bwd_launch(const Plan& pl, const BwdLaunch& L, const void* qkv, cons
   }
 }
 
+// ---- backward without device allocation --------------------------------------------
+//
+// Some callers cannot allocate device memory at the point where they run the backward:
+// runtimes that fix their device memory plan at start-up and forbid any later
+// cudaMalloc (real-time or certified inference/training stacks), and frameworks whose own
+// allocator must account for every device byte. A plan allocates (its dense bias, mask
+// and reduction buffers), so such a caller cannot create one. swin_wattn_bwd_noalloc
+// runs the same backward with all of its working memory in one fixed array below.
+
+// Working memory of swin_wattn_bwd_noalloc: bias fragments, class mask bits and the
+// per-CTA table-gradient partials, packed at 256-byte boundaries.
+constexpr size_t kNoAllocScratchBytes = size_t(2) << 20;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+// Bias fragments straight from the table (no dense bias) and mask bits straight from
+// the region labels (no mask tensor): the same values fragments_kernel derives from the
+// plan's dense bias and mask.
+template <int M>
+__global__ void noalloc_fragments_kernel(const float* __restrict__ table, int nH, int H, int W,
+                                         int s, float4* __restrict__ bias_frag,
+                                         uint32_t* __restrict__ mask_frag) {
+  using G = Geo<M>;
+  constexpr int N = G::N, NT = G::NT, MW = G::MW, THREADS = G::THREADS;
+  const int nWy = H / M, nWx = W / M;
+  const int per_head = G::WARPS * NT * 32;
+  const int nbias = nH * per_head;
+  const int nmask = mask_frag ? 4 * THREADS : 0;
+  for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < nbias + nmask; e += gridDim.x * blockDim.x) {
+    if (e < nbias) {
+      const int h = e / per_head, f = e % per_head;
+      const int ln = f & 31, nt = (f >> 5) % NT, wp = (f >> 5) / NT;
+      const int r0 = wp * 16 + (ln >> 2), c0 = nt * 8 + 2 * (ln & 3);
+      float v[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int r = r0 + 8 * (q >> 1), c = c0 + (q & 1);
+        v[q] = c >= N ? -INFINITY : (r >= N ? 0.0f : table[(int64_t)rel_index(r, c, M) * nH + h] * kInvScale);
+      }
+      bias_frag[e] = make_float4(v[0], v[1], v[2], v[3]);
+    } else {
+      const int f = e - nbias, cls = f / THREADS, tid = f % THREADS;
+      const int warp = tid >> 5, g = (tid & 31) >> 2, t = tid & 3;
+      const int wy = (cls & 2) ? nWy - 1 : 0, wx = (cls & 1) ? nWx - 1 : 0;
+      uint32_t bits[MW];
+#pragma unroll
+      for (int m = 0; m < MW; ++m) bits[m] = 0u;
+      if (cls != 0) {
+        for (int nt = 0; nt < NT; ++nt)
+          for (int q = 0; q < 4; ++q) {
+            const int r = warp * 16 + g + 8 * (q >> 1), c = nt * 8 + 2 * t + (q & 1);
+            if (r < N && c < N &&
+                region_label(wy * M + r / M, wx * M + r % M, H, W, M, s) !=
+                    region_label(wy * M + c / M, wx * M + c % M, H, W, M, s))
+              bits[(nt * 4 + q) >> 5] |= 1u << ((nt * 4 + q) & 31);
+          }
+      }
+#pragma unroll
+      for (int m = 0; m < MW; ++m) mask_frag[(cls * MW + m) * THREADS + tid] = bits[m];
+    }
+  }
+}
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+unsigned char* g_noalloc_ptr[kMaxDevices] = {};
+
+size_t round256(size_t n) { return (n + 255) & ~size_t(255); }
+
+// Device address of the scratch array on the current device, looked up once per device.
+cudaError_t noalloc_scratch(int device, unsigned char** out) {
+  if (device < 0 || device >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (g_noalloc_ptr[device] == nullptr) {
+    void* ptr = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    g_noalloc_ptr[device] = static_cast<unsigned char*>(ptr);
+  }
+  *out = g_noalloc_ptr[device];
+  return cudaSuccess;
+}
+
+template <int M, typename TIO>
+cudaError_t noalloc_bwd_t(Plan& pl, const float* table, const void* qkv, const void* dout,
+                          void* dqkv, float* dtable, cudaStream_t st, size_t* need) {
+  constexpr int STAGES = BwdStages<M>::value;
+  BwdLaunch L;
+  cudaError_t e = bconfig_t<M, TIO, STAGES>(pl, &L);
+  if (e != cudaSuccess) return e;
+  const size_t bias_bytes = round256((size_t)pl.nH * Geo<M>::BIAS_BYTES);
+  const size_t mask_bytes = round256(Geo<M>::MASK_BYTES);
+  const size_t part_bytes = round256((size_t)L.partial_rows * BGeo<M>::R * sizeof(float));
+  *need = bias_bytes + mask_bytes + part_bytes;
+  if (*need > kNoAllocScratchBytes) return cudaErrorMemoryAllocation;
+  unsigned char* base = nullptr;
+  e = noalloc_scratch(pl.device, &base);
+  if (e != cudaSuccess) return e;
+  pl.bias_frag = reinterpret_cast<float4*>(base);
+  pl.mask_frag = pl.s > 0 ? reinterpret_cast<uint32_t*>(base + bias_bytes) : nullptr;
+  pl.dt_partial = reinterpret_cast<float*>(base + bias_bytes + mask_bytes);
+  const int nfrag = pl.nH * Geo<M>::WARPS * Geo<M>::NT * 32 + (pl.s > 0 ? 4 * Geo<M>::THREADS : 0);
+  noalloc_fragments_kernel<M><<<(nfrag + 255) / 256, 256, 0, st>>>(table, pl.nH, pl.H, pl.W, pl.s,
+                                                                   pl.bias_frag, pl.mask_frag);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  return blaunch_t<M, TIO, STAGES>(pl, L, qkv, dout, dqkv, dtable, st);
+}
+
+}  // namespace
+
 }  // namespace swin
+
+namespace swin {
+void set_last_error(const char* msg);
+int check_device_ptr_abi(const void* ptr, size_t align);
+}
+
+extern "C" int swin_wattn_bwd_noalloc(const void* qkv, const void* dout, void* dqkv, float* dtable,
+                                      const float* bias_table, int B, int H, int W, int C,
+                                      int num_heads, int window, int shift, int dtype,
+                                      struct CUstream_st* stream) {
+  if (B < 0 || H <= 0 || W <= 0 || C <= 0 || num_heads <= 0) return SWIN_WATTN_ERR_INVALID_ARG;
+  if (dtype != SWIN_WATTN_BF16 && dtype != SWIN_WATTN_FP32) return SWIN_WATTN_ERR_INVALID_ARG;
+  if (window != 4 && window != 7) return SWIN_WATTN_ERR_UNSUPPORTED;
+  if (shift < 0 || shift >= window) return SWIN_WATTN_ERR_INVALID_ARG;
+  if (H % window != 0 || W % window != 0) return SWIN_WATTN_ERR_UNSUPPORTED;
+  if (C % num_heads != 0 || C / num_heads != swin::kHeadDim) return SWIN_WATTN_ERR_UNSUPPORTED;
+  if ((int64_t)B * H * W * 3 * C >= ((int64_t)1 << 40)) return SWIN_WATTN_ERR_UNSUPPORTED;
+  int rc = swin::check_device_ptr_abi(dtable, 4);
+  if (rc == SWIN_WATTN_OK) rc = swin::check_device_ptr_abi(bias_table, 4);
+  if (rc != SWIN_WATTN_OK) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (B == 0) {
+    const size_t tbytes = sizeof(float) * (size_t)(2 * window - 1) * (2 * window - 1) * num_heads;
+    const cudaError_t e = cudaMemsetAsync(dtable, 0, tbytes, st);
+    if (e != cudaSuccess) {
+      swin::set_last_error(cudaGetErrorString(e));
+      return SWIN_WATTN_ERR_CUDA;
+    }
+    return SWIN_WATTN_OK;
+  }
+  if ((rc = swin::check_device_ptr_abi(qkv, 16)) != SWIN_WATTN_OK) return rc;
+  if ((rc = swin::check_device_ptr_abi(dout, 16)) != SWIN_WATTN_OK) return rc;
+  if ((rc = swin::check_device_ptr_abi(dqkv, 16)) != SWIN_WATTN_OK) return rc;
+
+  swin::Plan pl;
+  std::memset(&pl, 0, sizeof(pl));
+  pl.B = B;
+  pl.H = H;
+  pl.W = W;
+  pl.C = C;
+  pl.nH = num_heads;
+  pl.M = window;
+  pl.s = shift;
+  pl.dtype = dtype;
+  pl.N = window * window;
+  pl.nWy = H / window;
+  pl.nWx = W / window;
+  pl.nW = pl.nWy * pl.nWx;
+  pl.withhold_window = -1;
+  cudaError_t e = cudaGetDevice(&pl.device);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&pl.num_sms, cudaDevAttrMultiProcessorCount, pl.device);
+  size_t need = 0;
+  if (e == cudaSuccess) {
+    const bool f32 = dtype == SWIN_WATTN_FP32;
+    if (window == 4)
+      e = f32 ? swin::noalloc_bwd_t<4, float>(pl, bias_table, qkv, dout, dqkv, dtable, st, &need)
+              : swin::noalloc_bwd_t<4, __nv_bfloat16>(pl, bias_table, qkv, dout, dqkv, dtable, st, &need);
+    else
+      e = f32 ? swin::noalloc_bwd_t<7, float>(pl, bias_table, qkv, dout, dqkv, dtable, st, &need)
+              : swin::noalloc_bwd_t<7, __nv_bfloat16>(pl, bias_table, qkv, dout, dqkv, dtable, st, &need);
+  }
+  if (e == cudaErrorMemoryAllocation) {
+    char msg[160];
+    std::snprintf(msg, sizeof(msg),
+                  "swin_wattn_bwd_noalloc: this shape needs %zu bytes of working memory, above "
+                  "the fixed %zu bytes",
+                  need, swin::kNoAllocScratchBytes);
+    swin::set_last_error(msg);
+    return SWIN_WATTN_ERR_UNSUPPORTED;
+  }
+  if (e != cudaSuccess) {
+    swin::set_last_error(cudaGetErrorString(e));
+    return SWIN_WATTN_ERR_CUDA;
+  }
+  return SWIN_WATTN_OK;
+}

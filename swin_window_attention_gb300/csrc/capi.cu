@@ -88,6 +88,11 @@ void free_plan_buffers(swin::Plan& p) {
 
 }  // namespace
 
+namespace swin {
+void set_last_error(const char* msg) { std::snprintf(g_last_error, sizeof(g_last_error), "%s", msg); }
+int check_device_ptr_abi(const void* ptr, size_t align) { return check_device_ptr(ptr, align); }
+}  // namespace swin
+
 extern "C" {
 
 const char* swin_wattn_status_string(int status) {
