@@ -40,7 +40,7 @@ constexpr int fwd_smem_bytes() {
 }
 
 // Resident CTAs per SM the register budget is sized for.
-template <int M> struct FwdMinBlocks { static constexpr int value = 4; };
+template <int M> struct FwdMinBlocks { static constexpr int value = 5; };
 template <> struct FwdMinBlocks<12> { static constexpr int value = 1; };
 
 template <int M, typename TIO, int STAGES>
@@ -411,8 +411,7 @@ static cudaError_t launch_t(const Plan& pl, const FwdLaunch& L, const void* qkv,
 
 // Pipeline depth per window size: enough windows in flight per SM while keeping the
 // shared-memory footprint within the residency target.
-template <int M> struct FwdStages { static constexpr int value = 3; };
-template <> struct FwdStages<12> { static constexpr int value = 2; };
+template <int M> struct FwdStages { static constexpr int value = 2; };
 
 #define SWIN_FWD_DISPATCH(FN, ...)                                                       \
   do {                                                                                  \
