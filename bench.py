@@ -33,6 +33,7 @@ from swin_window_attention_gb300 import inputs  # noqa: E402
 METRIC = "fused SW-MSA fwd/bwd tokens/s on 1 GB300; achieved HBM GB/s as % of roofline"
 SWEEP = ["swin_l224_s1", "swin_l224_s2", "swin_l224_s3", "swin_l224_s4"]
 TRAIN = ["swin_b224_s1", "swin_b224_s2", "swin_b224_s3", "swin_b224_s4"]
+L384 = ["swin_l384_s1", "swin_l384_s2", "swin_l384_s3", "swin_l384_s4"]
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -340,6 +341,7 @@ def run_gpu(args):
     torch.cuda.empty_cache()
 
     train = run_train_step(args, dev, stream, lib, capi, hbm, ws) if not args.skip_train else None
+    l384 = run_fwd_sweep(L384, args, dev, stream, lib, capi, hbm, ws) if not args.skip_train else None
 
     if rank == 0:
         line = {
@@ -364,6 +366,7 @@ def run_gpu(args):
             "gpu_launches": int(launches),
             "clocks": clk,
             "train_step": train,
+            "l384_sweep": l384,
         }
         if ws == 1 and not args.skip_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(sweep)
@@ -371,6 +374,47 @@ def run_gpu(args):
     if ws > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def run_fwd_sweep(names, args, dev, stream, lib, capi, hbm, ws):
+    """Forward of another stage sweep (context for the line: the 12x12-window Swin-L 384
+    sweep), per stage with CUDA events."""
+    sh = stream.cuda_stream
+    wls = [inputs.BY_NAME[n] for n in names]
+    st = []
+    with torch.cuda.stream(stream):
+        for wl in wls:
+            tab = inputs.make_table(wl).to(dev)
+            rc, h = capi.swin_wattn_plan(wl.B, wl.H, wl.W, wl.C, wl.nH, wl.M, wl.s, capi.BF16,
+                                         tab.data_ptr(), sh)
+            if rc != capi.OK:
+                raise capi.SwinWAttnError("swin_wattn_plan", rc)
+            q = inputs.make_qkv(wl).to(dev)
+            st.append(dict(wl=wl, h=h, q=q, o=torch.empty(wl.B, wl.H, wl.W, wl.C,
+                                                         dtype=torch.bfloat16, device=dev)))
+    torch.cuda.synchronize()
+    steps = max(3, min(args.steps, 200))
+    ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in st] for _ in range(steps + 3)]
+    for i in range(steps + 3):
+        for k, x in enumerate(st):
+            ev[i][k][0].record(stream)
+            if lib.swin_wattn_fwd(x["h"], x["q"].data_ptr(), x["o"].data_ptr(), sh) != capi.OK:
+                raise RuntimeError("forward failed")
+            ev[i][k][1].record(stream)
+    torch.cuda.synchronize()
+    out, tot_b, tot_ms = [], 0, 0.0
+    for k, x in enumerate(st):
+        wl = x["wl"]
+        ms = statistics.mean(ev[i][k][0].elapsed_time(ev[i][k][1]) for i in range(3, steps + 3))
+        tot_b += fwd_bytes(wl)
+        tot_ms += ms
+        out.append({"workload": wl.name, "us": round(ms * 1e3, 2),
+                    "frac_of_measured_hbm": round(fwd_bytes(wl) / (ms / 1e3) / 1e9 / hbm, 4),
+                    "tflops": round(fwd_flops(wl) / (ms / 1e3) / 1e12, 1)})
+        capi.swin_wattn_destroy(x["h"])
+    return {"workload": "swin_l384_sweep_fwd (B=16, 12x12 windows)", "us": round(tot_ms * 1e3, 2),
+            "tokens_per_s": sum(x["wl"].tokens for x in st) / (tot_ms / 1e3),
+            "frac_of_measured_hbm": round(tot_b / (tot_ms / 1e3) / 1e9 / hbm, 4), "stages": out}
 
 
 def run_train_step(args, dev, stream, lib, capi, hbm, ws):

@@ -63,7 +63,7 @@ enum swin_wattn_status {
   SWIN_WATTN_ERR_MISALIGNED = 3,   /* tensor pointer not 16-byte aligned (table: 4-byte) */
   SWIN_WATTN_ERR_BAD_PLAN = 4,     /* null, destroyed or foreign plan handle */
   SWIN_WATTN_ERR_CUDA = 5,         /* a CUDA runtime call failed; see swin_wattn_last_error */
-  SWIN_WATTN_ERR_TIMEOUT = 6       /* a bounded device-side wait gave up (swin_wattn_sync) */
+  SWIN_WATTN_ERR_TIMEOUT = 6       /* reserved for bounded device-side waits */
 };
 
 enum swin_wattn_dtype { SWIN_WATTN_BF16 = 0, SWIN_WATTN_FP32 = 1 };
@@ -160,22 +160,6 @@ int swin_wattn_bwd_noalloc(const void* qkv, const void* dout, void* dqkv, float*
  */
 int swin_wattn_debug_maps(swin_wattn_plan_t plan, int32_t* gather, int32_t* relidx,
                           float* mask, float* dense_bias, struct CUstream_st* stream);
-
-/*
- * Wait for the work queued on `stream`, then report whether any of the plan's kernels
- * gave up on a bounded device-side wait since the last call: SWIN_WATTN_OK, or
- * SWIN_WATTN_ERR_TIMEOUT (the affected outputs are then incomplete). Clears the record.
- * A kernel that gives up returns early instead of hanging, so the context stays usable.
- */
-int swin_wattn_sync(swin_wattn_plan_t plan, struct CUstream_st* stream);
-
-/*
- * Debug only: make the forward withhold the loads of one window (global index
- * b * nW + w), so that the wait for its data runs out and reports
- * SWIN_WATTN_ERR_TIMEOUT through swin_wattn_sync (about one second per forward call).
- * window < 0 restores normal operation. Used by the test of the timeout path.
- */
-int swin_wattn_debug_withhold(swin_wattn_plan_t plan, long long window);
 
 /* Free the plan's device memory (synchronises the device first). NULL is a no-op. */
 int swin_wattn_destroy(swin_wattn_plan_t plan);

@@ -33,9 +33,7 @@ SIGNATURES = {
     "swin_wattn_fwd_host": ([_vp, _vp, _vp, _vp, _vp, _vp], _i),
     "swin_wattn_bwd": ([_vp, _vp, _vp, _vp, _vp, _vp], _i),
     "swin_wattn_debug_maps": ([_vp, _vp, _vp, _vp, _vp, _vp], _i),
-    "swin_wattn_sync": ([_vp, _vp], _i),
     "swin_wattn_bwd_noalloc": ([_vp, _vp, _vp, _vp, _vp] + [_i] * 8 + [_vp], _i),
-    "swin_wattn_debug_withhold": ([_vp, ctypes.c_longlong], _i),
     "swin_wattn_destroy": ([_vp], _i),
     "swin_wattn_status_string": ([_i], _cp),
     "swin_wattn_last_error": ([], _cp),
@@ -109,14 +107,6 @@ def swin_wattn_bwd_noalloc(qkv_ptr, dout_ptr, dqkv_ptr, dtable_ptr, table_ptr, B
     library); see include/swin_wattn.h."""
     return load().swin_wattn_bwd_noalloc(qkv_ptr, dout_ptr, dqkv_ptr, dtable_ptr, table_ptr, B, H,
                                          W, C, num_heads, window, shift, dtype, stream)
-
-
-def swin_wattn_sync(plan, stream):
-    return load().swin_wattn_sync(plan, stream)
-
-
-def swin_wattn_debug_withhold(plan, window):
-    return load().swin_wattn_debug_withhold(plan, window)
 
 
 def swin_wattn_destroy(plan):
@@ -197,12 +187,6 @@ class WindowAttention:
         if rc != OK:
             raise SwinWAttnError("swin_wattn_bwd", rc)
         return dqkv, dtable
-
-    def sync(self, stream=None):
-        """Wait for the stream; raise if a kernel of this plan gave up on a device wait."""
-        rc = swin_wattn_sync(self.handle, _stream_handle(stream))
-        if rc != OK:
-            raise SwinWAttnError("swin_wattn_sync", rc)
 
     def debug_maps(self, stream=None):
         import torch

@@ -714,7 +714,6 @@ extern "C" int swin_wattn_bwd_noalloc(const void* qkv, const void* dout, void* d
   pl.nWy = H / window;
   pl.nWx = W / window;
   pl.nW = pl.nWy * pl.nWx;
-  pl.withhold_window = -1;
   cudaError_t e = cudaGetDevice(&pl.device);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&pl.num_sms, cudaDevAttrMultiProcessorCount, pl.device);
   size_t need = 0;

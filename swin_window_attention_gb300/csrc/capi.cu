@@ -79,8 +79,7 @@ void free_plan_buffers(swin::Plan& p) {
   if (p.dt_partial) cudaFree(p.dt_partial);
   if (p.bias_frag) cudaFree(p.bias_frag);
   if (p.mask_frag) cudaFree(p.mask_frag);
-  if (p.status) cudaFree(p.status);
-  p.status = nullptr;
+
   p.dense_bias = p.mask = p.dt_partial = nullptr;
   p.bias_frag = nullptr;
   p.mask_frag = nullptr;
@@ -156,9 +155,7 @@ int swin_wattn_plan(swin_wattn_plan_t* out, int B, int H, int W, int C, int num_
   if (e == cudaSuccess) e = cudaMalloc(&p.mask, sizeof(float) * nn * p.nW);
   if (e == cudaSuccess) e = cudaMalloc(&p.bias_frag, swin::bias_frag_bytes(p.M, p.nH));
   if (e == cudaSuccess && p.s > 0) e = cudaMalloc(&p.mask_frag, swin::mask_frag_bytes(p.M));
-  if (e == cudaSuccess) e = cudaMalloc(&p.status, sizeof(int));
-  if (e == cudaSuccess) e = cudaMemsetAsync(p.status, 0, sizeof(int), reinterpret_cast<cudaStream_t>(stream));
-  p.withhold_window = -1;
+
   if (e == cudaSuccess) e = swin::fwd_config(p, &pl->fwd);
   if (e == cudaSuccess) e = swin::bwd_config(p, &pl->bwd);
   if (e == cudaSuccess && pl->bwd.partial_rows > 0) {
@@ -265,25 +262,6 @@ int swin_wattn_bwd(swin_wattn_plan_t plan, const void* qkv, const void* dout, vo
   cudaError_t e = swin::bwd_launch(p, plan->bwd, qkv, dout, dqkv, dtable, st);
   g_launches += 2;
   return e == cudaSuccess ? SWIN_WATTN_OK : cuda_fail(e, "swin_wattn_bwd");
-}
-
-int swin_wattn_sync(swin_wattn_plan_t plan, struct CUstream_st* stream) {
-  int rc = check_plan(plan);
-  if (rc != SWIN_WATTN_OK) return rc;
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  int host = 0;
-  cudaError_t e = cudaStreamSynchronize(st);
-  if (e == cudaSuccess) e = cudaMemcpy(&host, plan->p.status, sizeof(int), cudaMemcpyDeviceToHost);
-  if (e == cudaSuccess && host != 0) e = cudaMemset(plan->p.status, 0, sizeof(int));
-  if (e != cudaSuccess) return cuda_fail(e, "swin_wattn_sync");
-  return host == 0 ? SWIN_WATTN_OK : host;
-}
-
-int swin_wattn_debug_withhold(swin_wattn_plan_t plan, long long window) {
-  int rc = check_plan(plan);
-  if (rc != SWIN_WATTN_OK) return rc;
-  plan->p.withhold_window = window < 0 ? -1 : window;
-  return SWIN_WATTN_OK;
 }
 
 int swin_wattn_debug_maps(swin_wattn_plan_t plan, int32_t* gather, int32_t* relidx,

@@ -16,9 +16,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 // 1 / scale = sqrt(hd) for hd = 32: the kernels accumulate z = q.k + (bias + mask) / scale
 // in the MMA, so that the logit is scale * z.
 constexpr float kInvScale = 5.6568542494923802f;
-// Upper bound on any device-side wait (an mbarrier phase); past it the kernel records
-// SWIN_WATTN_ERR_TIMEOUT in the plan's status word and returns.
-constexpr unsigned long long kWaitLimitNs = 1000000000ull;
+
 
 struct Plan {
   uint32_t magic;
@@ -36,10 +34,6 @@ struct Plan {
   // Shift-mask bit patterns of the four window classes in fragment order:
   // [4 classes][MW][THREADS] uint32 (class 0 all clear). Owned; null when s == 0.
   uint32_t* mask_frag;
-  // Device status word: 0, or a SWIN_WATTN_ERR_* code a kernel recorded. Owned.
-  int* status;
-  // Debug: global window index whose loads the forward withholds (-1: none).
-  long long withhold_window;
 };
 
 // ---- geometry shared by every kernel that touches a window -----------------------
@@ -153,51 +147,6 @@ __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
   return y;
-}
-
-// ---- mbarriers (shared::cta) --------------------------------------------------------
-
-__device__ __forceinline__ void mbar_init(uint32_t addr, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(addr), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_fence_init() {
-  asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t addr) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(addr) : "memory");
-}
-// Arrive once every cp.async this thread issued so far has landed.
-__device__ __forceinline__ void cp_async_mbar_arrive(uint32_t addr) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(addr) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint32_t addr, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-      " selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(addr), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-__device__ __forceinline__ unsigned long long global_ns() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %%globaltimer;\n" : "=l"(t));
-  return t;
-}
-// Bounded wait for the phase of the given parity: true once it completed, false when
-// kWaitLimitNs passed (or, as a backstop, 2^26 polls) without completion.
-__device__ __forceinline__ bool mbar_wait(uint32_t addr, uint32_t parity) {
-  if (mbar_try_wait(addr, parity)) return true;
-  const unsigned long long t0 = global_ns();
-  for (uint32_t n = 0; n < (1u << 26); ++n) {
-    if (mbar_try_wait(addr, parity)) return true;
-    if (global_ns() - t0 > kWaitLimitNs) return false;
-  }
-  return false;
-}
-__device__ __forceinline__ void cp_async_wait_all() {
-  asm volatile("cp.async.wait_all;\n" ::: "memory");
 }
 
 // Byte offset of 16-byte chunk c (0..3) of row r in a [rows][32 x bf16] shared tile,

@@ -30,17 +30,15 @@ struct FwdParams {
   int64_t total_windows;  // B * nW
   int chunks;             // window ranges per head
   float qk_scale_log2;    // hd^-0.5 * log2(e)
-  int* status;            // plan status word (timeouts)
-  long long withhold;     // debug: window whose loads are withheld, -1 for none
 };
 
 template <int M, typename TIO, int STAGES>
 constexpr int fwd_smem_bytes() {
-  return Geo<M>::BIAS_BYTES + Geo<M>::MASK_BYTES + STAGES * Geo<M>::STAGE_BYTES + 16 * STAGES;
+  return Geo<M>::BIAS_BYTES + Geo<M>::MASK_BYTES + STAGES * Geo<M>::STAGE_BYTES;
 }
 
 // Resident CTAs per SM the register budget is sized for.
-template <int M> struct FwdMinBlocks { static constexpr int value = 5; };
+template <int M> struct FwdMinBlocks { static constexpr int value = 4; };
 template <> struct FwdMinBlocks<12> { static constexpr int value = 1; };
 
 template <int M, typename TIO, int STAGES>
@@ -91,40 +89,30 @@ __global__ void __launch_bounds__(Geo<M>::THREADS, FwdMinBlocks<M>::value) fwd_k
   int cb = lb, cwy = lwy, cwx = lwx;  // cursor of the window being computed
   const uint32_t tiles_u32 = smem_u32(stiles);
 
-  int64_t lw = w_begin;  // global index of the next window to load
-  // Gathers the next window into the stage at stage_off and arrives on its full barrier
-  // once this thread's copies land.
-  auto issue = [&](uint32_t stage_off, uint32_t full_bar) {
+  auto issue = [&](uint32_t stage_off) {
     const uint32_t base = tiles_u32 + stage_off;
     const int y0 = lwy * M + s, x0 = lwx * M + s;
-    const bool withheld = lw++ == p.withhold;  // debug: that window's barrier never completes
-    if (withheld) {
-    } else if (y0 + M <= H && x0 + M <= W) {  // no wrap: one base plus fixed offsets
+    if (y0 + M <= H && x0 + M <= W) {  // no wrap: one base plus fixed offsets
       const TIO* wbase = qkv + ((int64_t)lb * H * W + (int64_t)y0 * W + x0) * C3;
 #pragma unroll
       for (int k = 0; k < CH_ITERS; ++k)
         if (k < CH_ITERS - 1 || tid + k * THREADS < G::CHUNKS)
           load_chunk<TIO>(base + (ld_desc[k] & 0xffffu), wbase + ld_loff[k]);
     } else {
-      const TIO* img = qkv + (int64_t)lb * H * W * C3;
+      // The window wraps around the grid edge: rows ly >= hy come from the top of the
+      // image and columns lx >= hx from its left edge.
+      const TIO* wbase = qkv + ((int64_t)lb * H * W + (int64_t)y0 * W + x0) * C3;
+      const int hy = H - y0, hx = W - x0;
+      const int64_t dy = (int64_t)H * W * C3, dx = (int64_t)W * C3;
 #pragma unroll
       for (int k = 0; k < CH_ITERS; ++k) {
         if (k < CH_ITERS - 1 || tid + k * THREADS < G::CHUNKS) {
           const uint32_t d = ld_desc[k];
-          int y = y0 + (int)((d >> 16) & 15), x = x0 + (int)((d >> 20) & 15);
-          y = y >= H ? y - H : y;
-          x = x >= W ? x - W : x;
-          const int chan = (int)((d >> 24) & 3) * p.C + h * kHeadDim + (int)((d >> 26) & 3) * 8;
-          load_chunk<TIO>(base + (d & 0xffffu), img + (int64_t)(y * W + x) * C3 + chan);
+          int64_t off = ld_loff[k];
+          if ((int)((d >> 16) & 15) >= hy) off -= dy;
+          if ((int)((d >> 20) & 15) >= hx) off -= dx;
+          load_chunk<TIO>(base + (d & 0xffffu), wbase + off);
         }
-      }
-    }
-    if (!withheld) {
-      if constexpr (sizeof(TIO) == 4) {  // fp32 loads were stored directly: release them
-        cp_async_wait_all();
-        mbar_arrive(full_bar);
-      } else {
-        cp_async_mbar_arrive(full_bar);
       }
     }
     if (++lwx == p.nWx) {
@@ -136,31 +124,8 @@ __global__ void __launch_bounds__(Geo<M>::THREADS, FwdMinBlocks<M>::value) fwd_k
     }
   };
 
-  // Pipeline barriers: full[st] completes when every thread's copies for the window in
-  // stage st have landed; empty[st] when every thread has finished with it.
-  const uint32_t bar_full = smem_u32(stiles + STAGES * G::STAGE_BYTES);
-  const uint32_t bar_empty = bar_full + 8 * STAGES;
-  if (tid == 0) {
-#pragma unroll
-    for (int st = 0; st < STAGES; ++st) {
-      mbar_init(bar_full + 8 * st, THREADS);
-      mbar_init(bar_empty + 8 * st, THREADS);
-    }
-    mbar_fence_init();
-  }
-  // Padded rows N..NPAD-1 of every q/k/v tile are zero (loads never touch them).
-  if constexpr (G::NPAD > N) {
-    constexpr int PADROWS = G::NPAD - N;
-    for (int e = tid; e < STAGES * 3 * PADROWS * 4; e += THREADS) {
-      const int c = e & 3, r = (e >> 2) % PADROWS, tile = (e >> 2) / PADROWS;
-      *reinterpret_cast<uint4*>(stiles + tile * G::TILE_BYTES + tile_off(N + r, c)) =
-          make_uint4(0u, 0u, 0u, 0u);
-    }
-  }
-  __syncthreads();
-
   // This head's bias fragments and the class mask bits (built by the plan in this
-  // kernel's fragment order) ride with window 0: its full barrier covers them.
+  // kernel's fragment order) travel in the first copy group, with window 0.
   {
     const unsigned char* bsrc = reinterpret_cast<const unsigned char*>(p.bias_frag) + (size_t)h * G::BIAS_BYTES;
     for (int e = tid; e < G::BIAS_BYTES / 16; e += THREADS) cp_async_16(smem_u32(smem + e * 16), bsrc + e * 16);
@@ -172,9 +137,19 @@ __global__ void __launch_bounds__(Geo<M>::THREADS, FwdMinBlocks<M>::value) fwd_k
   }
 #pragma unroll
   for (int st = 0; st < STAGES - 1; ++st) {
-    if (st < nwin) issue(st * G::STAGE_BYTES, bar_full + 8 * st);
+    if (st < nwin) issue(st * G::STAGE_BYTES);
+    cp_async_commit();
   }
 
+  // Padded rows N..NPAD-1 of every q/k/v tile are zero (loads never touch them).
+  if constexpr (G::NPAD > N) {
+    constexpr int PADROWS = G::NPAD - N;
+    for (int e = tid; e < STAGES * 3 * PADROWS * 4; e += THREADS) {
+      const int c = e & 3, r = (e >> 2) % PADROWS, tile = (e >> 2) / PADROWS;
+      *reinterpret_cast<uint4*>(stiles + tile * G::TILE_BYTES + tile_off(N + r, c)) =
+          make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
   const float4* bfrag = sbias + warp * NT * 32 + lane;
   const float c_l2 = p.qk_scale_log2;            // scale * log2(e)
   const float mask_z = kMaskValue * kInvScale;  // the -100 mask in units of z
@@ -196,24 +171,13 @@ __global__ void __launch_bounds__(Geo<M>::THREADS, FwdMinBlocks<M>::value) fwd_k
   const uint32_t st_off0 = tile_off(warp * 16 + r8 + ((mi & 1) << 3), mi >> 1);
   const uint32_t st_off1 = tile_off(warp * 16 + r8 + ((mi & 1) << 3), 2 + (mi >> 1));
 
-  bool ok = true;
-  int cur = 0, nxt = STAGES - 1;  // stage of window it and of window it + STAGES - 1
-  uint32_t cur_par = 0;           // phase parity of the current stage's full barrier
+  uint32_t cur_off = 0, nxt_off = (STAGES - 1) * G::STAGE_BYTES;
   for (int it = 0; it < nwin; ++it) {
-    // Refill the stage window it - 1 used, once every warp is done with it.
-    if (it + STAGES - 1 < nwin) {
-      if (it > 0 && !mbar_wait(bar_empty + 8 * nxt, ((it - 1) / STAGES) & 1)) {
-        ok = false;
-        break;
-      }
-      issue(nxt * G::STAGE_BYTES, bar_full + 8 * nxt);
-    }
-    nxt = nxt + 1 == STAGES ? 0 : nxt + 1;
-    if (!mbar_wait(bar_full + 8 * cur, cur_par)) {
-      ok = false;
-      break;
-    }
-    const uint32_t cur_off = cur * G::STAGE_BYTES;
+    cp_async_wait<STAGES - 2>();
+    __syncthreads();
+    if (it + STAGES - 1 < nwin) issue(nxt_off);
+    cp_async_commit();
+    nxt_off = nxt_off + G::STAGE_BYTES == STAGES * G::STAGE_BYTES ? 0 : nxt_off + G::STAGE_BYTES;
     const int b = cb, wy = cwy, wx = cwx;
     if (++cwx == p.nWx) {
       cwx = 0;
@@ -224,6 +188,7 @@ __global__ void __launch_bounds__(Geo<M>::THREADS, FwdMinBlocks<M>::value) fwd_k
     }
     unsigned char* tq = stiles + cur_off;
     const uint32_t tb = tiles_u32 + cur_off;
+    cur_off = cur_off + G::STAGE_BYTES == STAGES * G::STAGE_BYTES ? 0 : cur_off + G::STAGE_BYTES;
 
     // ---- z = Q K^T + bias/scale: the accumulators start from the bias fragment ------
     uint32_t qa[2][4];
@@ -348,15 +313,8 @@ __global__ void __launch_bounds__(Geo<M>::THREADS, FwdMinBlocks<M>::value) fwd_k
           *reinterpret_cast<float2*>(dst + nd * 8) = make_float2(o[nd][2] * inv1, o[nd][3] * inv1);
       }
     }
-    // This thread is done with the stage (including its staged output rows).
-    mbar_arrive(bar_empty + 8 * cur);
-    if (++cur == STAGES) {
-      cur = 0;
-      cur_par ^= 1u;
-    }
   }
-  if (!ok) atomicExch(p.status, (int)SWIN_WATTN_ERR_TIMEOUT);
-  cp_async_wait_all();  // never leave with this thread's copies in flight
+  cp_async_wait<0>();
 }
 
 // ---- host side ---------------------------------------------------------------------
@@ -403,15 +361,14 @@ static cudaError_t launch_t(const Plan& pl, const FwdLaunch& L, const void* qkv,
   p.total_windows = (int64_t)pl.B * pl.nW;
   p.chunks = L.chunks;
   p.qk_scale_log2 = kLog2e / kInvScale;
-  p.status = pl.status;
-  p.withhold = pl.withhold_window;
   fwd_kernel<M, TIO, STAGES><<<L.grid, L.threads, L.smem, st>>>(p);
   return cudaGetLastError();
 }
 
 // Pipeline depth per window size: enough windows in flight per SM while keeping the
 // shared-memory footprint within the residency target.
-template <int M> struct FwdStages { static constexpr int value = 2; };
+template <int M> struct FwdStages { static constexpr int value = 3; };
+template <> struct FwdStages<12> { static constexpr int value = 2; };
 
 #define SWIN_FWD_DISPATCH(FN, ...)                                                       \
   do {                                                                                  \
