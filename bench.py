@@ -257,28 +257,52 @@ def run_gpu(args):
         step()
     torch.cuda.synchronize()
 
+    # The step as one CUDA graph (four forward launches), replayed for the headline
+    # number: no host launch gaps between the stages.
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream, capture_error_mode="relaxed"):
+        step()
+    torch.cuda.synchronize()
+    for _ in range(args.warmup):
+        with torch.cuda.stream(stream):
+            graph.replay()
+    torch.cuda.synchronize()
+
     ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in sweep]
           for _ in range(args.steps)]
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
-    capi.swin_wattn_launch_count(reset=True)
     barrier(ws)
     torch.cuda.synchronize()
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     clocks.mark(True)
-    t_start.record(stream)
-    for i in range(args.steps):
-        step(ev[i])
-    t_end.record(stream)
+    with torch.cuda.stream(stream):
+        t_start.record(stream)
+        for i in range(args.steps):
+            graph.replay()
+        t_end.record(stream)
     torch.cuda.synchronize()
-    clocks.mark(False)
     barrier(ws)
-    launches = capi.swin_wattn_launch_count()
-    clk = clocks.stop()
     total_ms = t_start.elapsed_time(t_end)
     total_ms = max_over_ranks(total_ms, ws)
+    launches = len(sweep) * args.steps  # kernels inside the replayed graphs
+
+    # Second timed region, same steps launched one by one with CUDA events around every
+    # launch: per-stage durations for the roofline of each kernel.
+    capi.swin_wattn_launch_count(reset=True)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        step(ev[i])
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clocks.mark(False)
+    eager_ms = max_over_ranks(e0.elapsed_time(e1), ws)
+    eager_launches = capi.swin_wattn_launch_count()
+    clk = clocks.stop()
     per_stage_ms = [statistics.mean(ev[i][k][0].elapsed_time(ev[i][k][1])
                                     for i in range(args.steps)) for k in range(len(sweep))]
 
@@ -364,6 +388,11 @@ def run_gpu(args):
                       "stages": stages},
             "e2e": e2e,
             "gpu_launches": int(launches),
+            "timing": {"value_from": "CUDA-graph replays of the step (4 forward launches each)",
+                       "eager_ms_per_step": eager_ms / args.steps,
+                       "eager_launches": int(eager_launches),
+                       "per_stage_from": "CUDA events around each launch in a second, eager "
+                                         "timed region of the same steps"},
             "clocks": clk,
             "train_step": train,
             "l384_sweep": l384,
