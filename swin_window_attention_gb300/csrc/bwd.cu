@@ -69,13 +69,15 @@ __device__ __forceinline__ void store_rows(float (&acc)[4][4], float mul, unsign
   constexpr int N = M * M;
   const int g = lane >> 2, t = lane & 3;
   if constexpr (sizeof(TIO) == 2) {
-#pragma unroll
-    for (int nd = 0; nd < 4; ++nd) {
-      *reinterpret_cast<uint32_t*>(stg + tile_off(g, nd) + 4 * t) =
-          pack_bf16(acc[nd][0] * mul, acc[nd][1] * mul);
-      *reinterpret_cast<uint32_t*>(stg + tile_off(g + 8, nd) + 4 * t) =
-          pack_bf16(acc[nd][2] * mul, acc[nd][3] * mul);
-    }
+    // two stmatrix: matrix (row half mi & 1, column chunk 2 * call + (mi >> 1))
+    const int mi = lane >> 3, rr = (lane & 7) + ((mi & 1) << 3);
+    const uint32_t sb = smem_u32(stg);
+    stsm_x4(sb + tile_off(rr, mi >> 1), pack_bf16(acc[0][0] * mul, acc[0][1] * mul),
+            pack_bf16(acc[0][2] * mul, acc[0][3] * mul), pack_bf16(acc[1][0] * mul, acc[1][1] * mul),
+            pack_bf16(acc[1][2] * mul, acc[1][3] * mul));
+    stsm_x4(sb + tile_off(rr, 2 + (mi >> 1)), pack_bf16(acc[2][0] * mul, acc[2][1] * mul),
+            pack_bf16(acc[2][2] * mul, acc[2][3] * mul), pack_bf16(acc[3][0] * mul, acc[3][1] * mul),
+            pack_bf16(acc[3][2] * mul, acc[3][3] * mul));
     __syncwarp();
 #pragma unroll
     for (int e = lane; e < 64; e += 32) {
@@ -242,13 +244,9 @@ __global__ void __launch_bounds__(Geo<M>::THREADS) bwd_kernel(const BwdParams p)
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
         const float4 bb = bfrag[nt * 32];  // z = q.k + bias/scale starts from the bias
-        pr[nt][0] = bb.x;
-        pr[nt][1] = bb.y;
-        pr[nt][2] = bb.z;
-        pr[nt][3] = bb.w;
         uint32_t b0, b1, b2, b3;
         ldsm_x4(kb + tile_off(nt * 8 + (lane & 7), lane >> 3), b0, b1, b2, b3);
-        mma_bf16(pr[nt], qa[0][0], qa[0][1], qa[0][2], qa[0][3], b0, b1);
+        mma_bf16_c(pr[nt], qa[0][0], qa[0][1], qa[0][2], qa[0][3], b0, b1, bb.x, bb.y, bb.z, bb.w);
         mma_bf16(pr[nt], qa[1][0], qa[1][1], qa[1][2], qa[1][3], b2, b3);
       }
     }
@@ -257,19 +255,27 @@ __global__ void __launch_bounds__(Geo<M>::THREADS) bwd_kernel(const BwdParams p)
     uint32_t mb[MW];
 #pragma unroll
     for (int m = 0; m < MW; ++m) mb[m] = cls ? smask[(cls * MW + m) * THREADS + tid] : 0u;
-    float mx0 = -INFINITY, mx1 = -INFINITY;
+    if (cls) {
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      if (cls) {
+      for (int nt = 0; nt < NT; ++nt) {
         const uint32_t word = mb[(nt * 4) >> 5], sh = (nt * 4) & 31;
         if ((word >> sh) & 1u) pr[nt][0] += mask_z;
         if ((word >> (sh + 1)) & 1u) pr[nt][1] += mask_z;
         if ((word >> (sh + 2)) & 1u) pr[nt][2] += mask_z;
         if ((word >> (sh + 3)) & 1u) pr[nt][3] += mask_z;
       }
-      mx0 = fmaxf(mx0, fmaxf(pr[nt][0], pr[nt][1]));
-      mx1 = fmaxf(mx1, fmaxf(pr[nt][2], pr[nt][3]));
     }
+    float m0a = -INFINITY, m0b = -INFINITY, m1a = -INFINITY, m1b = -INFINITY;
+#pragma unroll
+    for (int nt = 0; nt < NT; nt += 2) {
+      m0a = fmax3(m0a, pr[nt][0], pr[nt][1]);
+      m1a = fmax3(m1a, pr[nt][2], pr[nt][3]);
+      if (nt + 1 < NT) {
+        m0b = fmax3(m0b, pr[nt + 1][0], pr[nt + 1][1]);
+        m1b = fmax3(m1b, pr[nt + 1][2], pr[nt + 1][3]);
+      }
+    }
+    float mx0 = fmaxf(m0a, m0b), mx1 = fmaxf(m1a, m1b);
     mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
     mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
     mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
@@ -327,32 +333,46 @@ __global__ void __launch_bounds__(Geo<M>::THREADS) bwd_kernel(const BwdParams p)
     D0 += __shfl_xor_sync(0xffffffffu, D0, 2);
     D1 += __shfl_xor_sync(0xffffffffu, D1, 1);
     D1 += __shfl_xor_sync(0xffffffffu, D1, 2);
+    // P and dS go to shared memory (and dS also stays in registers for dQ) as bf16
+    // hi/lo pairs: the lo term is the rounding residual of the hi term, so the MMAs that
+    // read them keep ~16 bits of each.
+    uint32_t dsh[NT][2], dsl[NT][2];
+    {
+      uint32_t ph[NT][2], pl[NT][2];
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      ds[nt][0] = pr[nt][0] * (ds[nt][0] - D0);
-      ds[nt][1] = pr[nt][1] * (ds[nt][1] - D0);
-      ds[nt][2] = pr[nt][2] * (ds[nt][2] - D1);
-      ds[nt][3] = pr[nt][3] * (ds[nt][3] - D1);
-      dtacc[nt][0] += ds[nt][0];
-      dtacc[nt][1] += ds[nt][1];
-      dtacc[nt][2] += ds[nt][2];
-      dtacc[nt][3] += ds[nt][3];
-      // P and dS go to shared memory as bf16 hi/lo pairs (the lo term is the rounding
-      // residual of the hi term), so the MMAs that read them keep ~16 bits of each.
-      const int col2 = (nt * 8 + 2 * t) * 2;
-      uint32_t hi, lo;
-      split_bf16(pr[nt][0], pr[nt][1], hi, lo);
-      *reinterpret_cast<uint32_t*>(sP + r0 * PS + col2) = hi;
-      *reinterpret_cast<uint32_t*>(sPlo + r0 * PS + col2) = lo;
-      split_bf16(pr[nt][2], pr[nt][3], hi, lo);
-      *reinterpret_cast<uint32_t*>(sP + r1 * PS + col2) = hi;
-      *reinterpret_cast<uint32_t*>(sPlo + r1 * PS + col2) = lo;
-      split_bf16(ds[nt][0], ds[nt][1], hi, lo);
-      *reinterpret_cast<uint32_t*>(sdS + r0 * PS + col2) = hi;
-      *reinterpret_cast<uint32_t*>(sdSlo + r0 * PS + col2) = lo;
-      split_bf16(ds[nt][2], ds[nt][3], hi, lo);
-      *reinterpret_cast<uint32_t*>(sdS + r1 * PS + col2) = hi;
-      *reinterpret_cast<uint32_t*>(sdSlo + r1 * PS + col2) = lo;
+      for (int nt = 0; nt < NT; ++nt) {
+        ds[nt][0] = pr[nt][0] * (ds[nt][0] - D0);
+        ds[nt][1] = pr[nt][1] * (ds[nt][1] - D0);
+        ds[nt][2] = pr[nt][2] * (ds[nt][2] - D1);
+        ds[nt][3] = pr[nt][3] * (ds[nt][3] - D1);
+        dtacc[nt][0] += ds[nt][0];
+        dtacc[nt][1] += ds[nt][1];
+        dtacc[nt][2] += ds[nt][2];
+        dtacc[nt][3] += ds[nt][3];
+        split_bf16(pr[nt][0], pr[nt][1], ph[nt][0], pl[nt][0]);
+        split_bf16(pr[nt][2], pr[nt][3], ph[nt][1], pl[nt][1]);
+        split_bf16(ds[nt][0], ds[nt][1], dsh[nt][0], dsl[nt][0]);
+        split_bf16(ds[nt][2], ds[nt][3], dsh[nt][1], dsl[nt][1]);
+      }
+      // stmatrix: matrix (n-tile nt + (mi >> 1), row half mi & 1) per 8-lane group
+      const int mi = lane >> 3;
+      const uint32_t rowoff = (uint32_t)((warp * 16 + 8 * (mi & 1) + (lane & 7)) * PS + (mi >> 1) * 16);
+      const uint32_t aP = smem_u32(sP) + rowoff, aPl = smem_u32(sPlo) + rowoff;
+      const uint32_t aS = smem_u32(sdS) + rowoff, aSl = smem_u32(sdSlo) + rowoff;
+#pragma unroll
+      for (int nt = 0; nt + 1 < NT; nt += 2) {
+        stsm_x4(aP + nt * 16, ph[nt][0], ph[nt][1], ph[nt + 1][0], ph[nt + 1][1]);
+        stsm_x4(aPl + nt * 16, pl[nt][0], pl[nt][1], pl[nt + 1][0], pl[nt + 1][1]);
+        stsm_x4(aS + nt * 16, dsh[nt][0], dsh[nt][1], dsh[nt + 1][0], dsh[nt + 1][1]);
+        stsm_x4(aSl + nt * 16, dsl[nt][0], dsl[nt][1], dsl[nt + 1][0], dsl[nt + 1][1]);
+      }
+      if constexpr (NT % 2 == 1) {
+        constexpr int nt = NT - 1;
+        stsm_x2(aP + nt * 16, ph[nt][0], ph[nt][1]);
+        stsm_x2(aPl + nt * 16, pl[nt][0], pl[nt][1]);
+        stsm_x2(aS + nt * 16, dsh[nt][0], dsh[nt][1]);
+        stsm_x2(aSl + nt * 16, dsl[nt][0], dsl[nt][1]);
+      }
     }
 
     // ---- dQ = scale dS K --------------------------------------------------------------
@@ -362,12 +382,13 @@ __global__ void __launch_bounds__(Geo<M>::THREADS) bwd_kernel(const BwdParams p)
       for (int nd = 0; nd < 4; ++nd) dq[nd][0] = dq[nd][1] = dq[nd][2] = dq[nd][3] = 0.0f;
 #pragma unroll
       for (int kk = 0; kk < KT; ++kk) {
-        uint32_t a0, a1, a2 = 0u, a3 = 0u, l0, l1, l2 = 0u, l3 = 0u;
-        split_bf16(ds[2 * kk][0], ds[2 * kk][1], a0, l0);
-        split_bf16(ds[2 * kk][2], ds[2 * kk][3], a1, l1);
+        const uint32_t a0 = dsh[2 * kk][0], a1 = dsh[2 * kk][1], l0 = dsl[2 * kk][0], l1 = dsl[2 * kk][1];
+        uint32_t a2 = 0u, a3 = 0u, l2 = 0u, l3 = 0u;
         if (2 * kk + 1 < NT) {
-          split_bf16(ds[2 * kk + 1][0], ds[2 * kk + 1][1], a2, l2);
-          split_bf16(ds[2 * kk + 1][2], ds[2 * kk + 1][3], a3, l3);
+          a2 = dsh[2 * kk + 1][0];
+          a3 = dsh[2 * kk + 1][1];
+          l2 = dsl[2 * kk + 1][0];
+          l3 = dsl[2 * kk + 1][1];
         }
         const int mi = lane >> 3, row = kk * 16 + (lane & 7) + ((mi & 1) << 3);
 #pragma unroll
