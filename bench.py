@@ -514,6 +514,31 @@ def run_train_step(args, dev, stream, lib, capi, hbm, ws):
             "stages": stages}
 
 
+def run_bwd_only(args):
+    """Backward launches of one workload (warm-up + timed), for kernel profiling."""
+    from swin_window_attention_gb300 import build, capi
+    build.build()
+    wl = inputs.BY_NAME[args.bwd_workload]
+    dev = torch.device("cuda", 0)
+    att = capi.WindowAttention(wl.B, wl.H, wl.W, wl.C, wl.nH, wl.M, wl.s,
+                               inputs.make_table(wl).to(dev))
+    q, d = inputs.make_qkv(wl).to(dev), inputs.make_dout(wl).to(dev)
+    dq, dt = torch.empty_like(q), torch.empty((2 * wl.M - 1) ** 2, wl.nH, device=dev)
+    for _ in range(args.warmup):
+        att.bwd(q, d, dq, dt)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(args.steps):
+        att.bwd(q, d, dq, dt)
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / args.steps
+    print(json.dumps({"workload": wl.name, "bwd_us": ms * 1e3,
+                      "frac_of_measured_hbm": bwd_bytes(wl) / (ms / 1e3) / 1e9 / load_peaks()[0]["hbm_gbs"]}))
+    att.close()
+
+
 # ---- reference arm: the oracle --------------------------------------------------------
 
 def run_reference(args):
@@ -564,6 +589,8 @@ def main():
     ap.add_argument("--workload", action="append", choices=sorted(inputs.BY_NAME),
                     help="time only these forward workloads instead of the Swin-L 224 sweep "
                          "(profiling runs)")
+    ap.add_argument("--bwd-workload", choices=sorted(n for n, w in inputs.BY_NAME.items() if w.bwd),
+                    help="profiling run: only the backward of this workload, a few launches")
     ap.add_argument("--skip-train", action="store_true")
     ap.add_argument("--skip-cpu-baseline", action="store_true")
     args = ap.parse_args()
@@ -571,6 +598,8 @@ def main():
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.bwd_workload:
+        run_bwd_only(args)
     else:
         run_gpu(args)
 
