@@ -72,12 +72,17 @@ __device__ __forceinline__ void store_rows(float (&acc)[4][4], float mul, unsign
     // two stmatrix: matrix (row half mi & 1, column chunk 2 * call + (mi >> 1))
     const int mi = lane >> 3, rr = (lane & 7) + ((mi & 1) << 3);
     const uint32_t sb = smem_u32(stg);
-    stsm_x4(sb + tile_off(rr, mi >> 1), pack_bf16(acc[0][0] * mul, acc[0][1] * mul),
-            pack_bf16(acc[0][2] * mul, acc[0][3] * mul), pack_bf16(acc[1][0] * mul, acc[1][1] * mul),
-            pack_bf16(acc[1][2] * mul, acc[1][3] * mul));
-    stsm_x4(sb + tile_off(rr, 2 + (mi >> 1)), pack_bf16(acc[2][0] * mul, acc[2][1] * mul),
-            pack_bf16(acc[2][2] * mul, acc[2][3] * mul), pack_bf16(acc[3][0] * mul, acc[3][1] * mul),
-            pack_bf16(acc[3][2] * mul, acc[3][3] * mul));
+    const float2 m2 = make_float2(mul, mul);
+    uint32_t w[4][2];
+#pragma unroll
+    for (int nd = 0; nd < 4; ++nd) {
+      const float2 a = __fmul2_rn(make_float2(acc[nd][0], acc[nd][1]), m2);
+      const float2 c = __fmul2_rn(make_float2(acc[nd][2], acc[nd][3]), m2);
+      w[nd][0] = pack_bf16(a.x, a.y);
+      w[nd][1] = pack_bf16(c.x, c.y);
+    }
+    stsm_x4(sb + tile_off(rr, mi >> 1), w[0][0], w[0][1], w[1][0], w[1][1]);
+    stsm_x4(sb + tile_off(rr, 2 + (mi >> 1)), w[2][0], w[2][1], w[3][0], w[3][1]);
     __syncwarp();
 #pragma unroll
     for (int e = lane; e < 64; e += 32) {
@@ -280,29 +285,39 @@ __global__ void __launch_bounds__(Geo<M>::THREADS) bwd_kernel(const BwdParams p)
     mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
     mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
     mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-    const float nm0 = -mx0 * p.qk_scale_log2, nm1 = -mx1 * p.qk_scale_log2;
-    float l0 = 0.0f, l1 = 0.0f;
+    const float2 c2 = make_float2(p.qk_scale_log2, p.qk_scale_log2);
+    const float2 nm0 = make_float2(-mx0 * p.qk_scale_log2, -mx0 * p.qk_scale_log2);
+    const float2 nm1 = make_float2(-mx1 * p.qk_scale_log2, -mx1 * p.qk_scale_log2);
+    float2 l0v = make_float2(0.0f, 0.0f), l1v = make_float2(0.0f, 0.0f);
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      pr[nt][0] = fast_exp2(fmaf(pr[nt][0], p.qk_scale_log2, nm0));
-      pr[nt][1] = fast_exp2(fmaf(pr[nt][1], p.qk_scale_log2, nm0));
-      pr[nt][2] = fast_exp2(fmaf(pr[nt][2], p.qk_scale_log2, nm1));
-      pr[nt][3] = fast_exp2(fmaf(pr[nt][3], p.qk_scale_log2, nm1));
-      l0 += pr[nt][0] + pr[nt][1];
-      l1 += pr[nt][2] + pr[nt][3];
+      const float2 e0 = __ffma2_rn(make_float2(pr[nt][0], pr[nt][1]), c2, nm0);
+      const float2 e1 = __ffma2_rn(make_float2(pr[nt][2], pr[nt][3]), c2, nm1);
+      pr[nt][0] = fast_exp2(e0.x);
+      pr[nt][1] = fast_exp2(e0.y);
+      pr[nt][2] = fast_exp2(e1.x);
+      pr[nt][3] = fast_exp2(e1.y);
+      l0v = __fadd2_rn(l0v, make_float2(pr[nt][0], pr[nt][1]));
+      l1v = __fadd2_rn(l1v, make_float2(pr[nt][2], pr[nt][3]));
     }
+    float l0 = l0v.x + l0v.y, l1 = l1v.x + l1v.y;
     l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
     l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
     l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
     l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
     // Normalised probabilities; padded query rows are zeroed so they add nothing below.
     const float inv0 = r0 < N ? 1.0f / l0 : 0.0f, inv1 = r1 < N ? 1.0f / l1 : 0.0f;
+    {
+      const float2 i0 = make_float2(inv0, inv0), i1 = make_float2(inv1, inv1);
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      pr[nt][0] *= inv0;
-      pr[nt][1] *= inv0;
-      pr[nt][2] *= inv1;
-      pr[nt][3] *= inv1;
+      for (int nt = 0; nt < NT; ++nt) {
+        const float2 a = __fmul2_rn(make_float2(pr[nt][0], pr[nt][1]), i0);
+        const float2 c = __fmul2_rn(make_float2(pr[nt][2], pr[nt][3]), i1);
+        pr[nt][0] = a.x;
+        pr[nt][1] = a.y;
+        pr[nt][2] = c.x;
+        pr[nt][3] = c.y;
+      }
     }
 
     // ---- dP = dO V^T ---------------------------------------------------------------
@@ -323,12 +338,13 @@ __global__ void __launch_bounds__(Geo<M>::THREADS) bwd_kernel(const BwdParams p)
       }
     }
     // ---- D = rowsum(P o dP), dS = P o (dP - D) ---------------------------------------
-    float D0 = 0.0f, D1 = 0.0f;
+    float2 D0v = make_float2(0.0f, 0.0f), D1v = make_float2(0.0f, 0.0f);
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      D0 = fmaf(pr[nt][0], ds[nt][0], fmaf(pr[nt][1], ds[nt][1], D0));
-      D1 = fmaf(pr[nt][2], ds[nt][2], fmaf(pr[nt][3], ds[nt][3], D1));
+      D0v = __ffma2_rn(make_float2(pr[nt][0], pr[nt][1]), make_float2(ds[nt][0], ds[nt][1]), D0v);
+      D1v = __ffma2_rn(make_float2(pr[nt][2], pr[nt][3]), make_float2(ds[nt][2], ds[nt][3]), D1v);
     }
+    float D0 = D0v.x + D0v.y, D1 = D1v.x + D1v.y;
     D0 += __shfl_xor_sync(0xffffffffu, D0, 1);
     D0 += __shfl_xor_sync(0xffffffffu, D0, 2);
     D1 += __shfl_xor_sync(0xffffffffu, D1, 1);
@@ -341,14 +357,21 @@ __global__ void __launch_bounds__(Geo<M>::THREADS) bwd_kernel(const BwdParams p)
       uint32_t ph[NT][2], pl[NT][2];
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
-        ds[nt][0] = pr[nt][0] * (ds[nt][0] - D0);
-        ds[nt][1] = pr[nt][1] * (ds[nt][1] - D0);
-        ds[nt][2] = pr[nt][2] * (ds[nt][2] - D1);
-        ds[nt][3] = pr[nt][3] * (ds[nt][3] - D1);
-        dtacc[nt][0] += ds[nt][0];
-        dtacc[nt][1] += ds[nt][1];
-        dtacc[nt][2] += ds[nt][2];
-        dtacc[nt][3] += ds[nt][3];
+        // dS = P o (dP - D): one packed subtract and one packed multiply per pair
+        const float2 s0 = __fmul2_rn(make_float2(pr[nt][0], pr[nt][1]),
+                                     __fadd2_rn(make_float2(ds[nt][0], ds[nt][1]), make_float2(-D0, -D0)));
+        const float2 s1 = __fmul2_rn(make_float2(pr[nt][2], pr[nt][3]),
+                                     __fadd2_rn(make_float2(ds[nt][2], ds[nt][3]), make_float2(-D1, -D1)));
+        ds[nt][0] = s0.x;
+        ds[nt][1] = s0.y;
+        ds[nt][2] = s1.x;
+        ds[nt][3] = s1.y;
+        const float2 t0 = __fadd2_rn(make_float2(dtacc[nt][0], dtacc[nt][1]), s0);
+        const float2 t1 = __fadd2_rn(make_float2(dtacc[nt][2], dtacc[nt][3]), s1);
+        dtacc[nt][0] = t0.x;
+        dtacc[nt][1] = t0.y;
+        dtacc[nt][2] = t1.x;
+        dtacc[nt][3] = t1.y;
         split_bf16(pr[nt][0], pr[nt][1], ph[nt][0], pl[nt][0]);
         split_bf16(pr[nt][2], pr[nt][3], ph[nt][1], pl[nt][1]);
         split_bf16(ds[nt][0], ds[nt][1], dsh[nt][0], dsl[nt][0]);

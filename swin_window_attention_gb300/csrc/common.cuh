@@ -142,11 +142,18 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return r;
 }
 
+// a - b on a pair with one packed FFMA2 (a + (-1) * b).
+__device__ __forceinline__ float2 fsub2(float2 a, float2 b) {
+  return __ffma2_rn(b, make_float2(-1.0f, -1.0f), a);
+}
+
 // (a, b) = hi + lo with hi the bf16x2 rounding of (a, b) and lo the bf16x2 rounding of
 // the residual: the pair carries ~16 significant bits of each value into a bf16 MMA.
 __device__ __forceinline__ void split_bf16(float a, float b, uint32_t& hi, uint32_t& lo) {
   hi = pack_bf16(a, b);
-  lo = pack_bf16(a - __uint_as_float(hi << 16), b - __uint_as_float(hi & 0xffff0000u));
+  const float2 r = fsub2(make_float2(a, b), make_float2(__uint_as_float(hi << 16),
+                                                                    __uint_as_float(hi & 0xffff0000u)));
+  lo = pack_bf16(r.x, r.y);
 }
 
 __device__ __forceinline__ float fast_exp2(float x) {

@@ -234,13 +234,17 @@ __global__ void __launch_bounds__(Geo<M>::THREADS, FwdMinBlocks<M>::value) fwd_k
     mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
 
     // ---- softmax numerators: exp2((z - max) * scale * log2e) ------------------------
-    const float nm0 = -mx0 * c_l2, nm1 = -mx1 * c_l2;
+    // (pairs of one row share the shift: one packed FFMA2 per pair)
+    const float2 c2 = make_float2(c_l2, c_l2);
+    const float2 nm0 = make_float2(-mx0 * c_l2, -mx0 * c_l2), nm1 = make_float2(-mx1 * c_l2, -mx1 * c_l2);
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      sacc[nt][0] = fast_exp2(fmaf(sacc[nt][0], c_l2, nm0));
-      sacc[nt][1] = fast_exp2(fmaf(sacc[nt][1], c_l2, nm0));
-      sacc[nt][2] = fast_exp2(fmaf(sacc[nt][2], c_l2, nm1));
-      sacc[nt][3] = fast_exp2(fmaf(sacc[nt][3], c_l2, nm1));
+      const float2 e0 = __ffma2_rn(make_float2(sacc[nt][0], sacc[nt][1]), c2, nm0);
+      const float2 e1 = __ffma2_rn(make_float2(sacc[nt][2], sacc[nt][3]), c2, nm1);
+      sacc[nt][0] = fast_exp2(e0.x);
+      sacc[nt][1] = fast_exp2(e0.y);
+      sacc[nt][2] = fast_exp2(e1.x);
+      sacc[nt][3] = fast_exp2(e1.y);
     }
 
     // ---- O = P V, row sums from the ones tile ---------------------------------------
@@ -286,10 +290,17 @@ __global__ void __launch_bounds__(Geo<M>::THREADS, FwdMinBlocks<M>::value) fwd_k
       // Stage the warp's 16 x 32 bf16 rows in its own Q rows (only this warp reads
       // them, and they are consumed) with two stmatrix, then write 64 contiguous bytes
       // per token. Padded rows receive finite values that are never stored.
-      stsm_x4(tb + st_off0, pack_bf16(o[0][0] * inv0, o[0][1] * inv0), pack_bf16(o[0][2] * inv1, o[0][3] * inv1),
-              pack_bf16(o[1][0] * inv0, o[1][1] * inv0), pack_bf16(o[1][2] * inv1, o[1][3] * inv1));
-      stsm_x4(tb + st_off1, pack_bf16(o[2][0] * inv0, o[2][1] * inv0), pack_bf16(o[2][2] * inv1, o[2][3] * inv1),
-              pack_bf16(o[3][0] * inv0, o[3][1] * inv0), pack_bf16(o[3][2] * inv1, o[3][3] * inv1));
+      const float2 i0 = make_float2(inv0, inv0), i1 = make_float2(inv1, inv1);
+      uint32_t ow[4][2];
+#pragma unroll
+      for (int nd = 0; nd < 4; ++nd) {
+        const float2 a = __fmul2_rn(make_float2(o[nd][0], o[nd][1]), i0);
+        const float2 c = __fmul2_rn(make_float2(o[nd][2], o[nd][3]), i1);
+        ow[nd][0] = pack_bf16(a.x, a.y);
+        ow[nd][1] = pack_bf16(c.x, c.y);
+      }
+      stsm_x4(tb + st_off0, ow[0][0], ow[0][1], ow[1][0], ow[1][1]);
+      stsm_x4(tb + st_off1, ow[2][0], ow[2][1], ow[3][0], ow[3][1]);
       __syncwarp();
       __nv_bfloat16* outp = reinterpret_cast<__nv_bfloat16*>(p.out) + h * kHeadDim + t * 8;
       if (os0 < N)
