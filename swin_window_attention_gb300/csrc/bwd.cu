@@ -30,9 +30,13 @@ namespace swin {
 template <int M>
 struct BGeo {
   using G = Geo<M>;
+  // Tiles hold the N rows of a window plus one zero row (row N): every padded row an MMA
+  // operand needs (query or key index >= N) is read from that zero row.
+  static constexpr int ROWS = G::N + 1;
+  static constexpr int TILE = (ROWS * 64 + 127) / 128 * 128;  // one of q, k, v, dO
   static constexpr int PS_STRIDE = G::NPAD * 2 + 16;  // bytes per row of the P / dS tiles
-  static constexpr int PS_BYTES = G::NPAD * PS_STRIDE;
-  static constexpr int STAGE_BYTES = 4 * G::TILE_BYTES;  // q, k, v, dO
+  static constexpr int PS_BYTES = ROWS * PS_STRIDE;
+  static constexpr int STAGE_BYTES = 4 * TILE;
   static constexpr int CHUNKS = 4 * G::N * 4;
   static constexpr int CH_ITERS = (CHUNKS + G::THREADS - 1) / G::THREADS;
   static constexpr int STG_BYTES = G::WARPS * 16 * 64;  // per-warp bf16 output staging
@@ -111,12 +115,16 @@ __device__ __forceinline__ void store_rows(float (&acc)[4][4], float mul, unsign
   }
 }
 
+// Resident CTAs per SM the register budget is sized for (shared memory allows three).
+template <int M> struct BwdMinBlocks { static constexpr int value = 3; };
+
 template <int M, typename TIO, int STAGES>
-__global__ void __launch_bounds__(Geo<M>::THREADS) bwd_kernel(const BwdParams p) {
+__global__ void __launch_bounds__(Geo<M>::THREADS, BwdMinBlocks<M>::value) bwd_kernel(const BwdParams p) {
   using G = Geo<M>;
   using BG = BGeo<M>;
   constexpr int N = G::N, NT = G::NT, KT = G::KT, MW = G::MW, THREADS = G::THREADS;
   constexpr int PS = BG::PS_STRIDE;
+  auto zr = [](int r) { return r < N ? r : N; };  // row, or the zero row for padding
   extern __shared__ __align__(128) unsigned char smem[];
   float4* sbias = reinterpret_cast<float4*>(smem);
   uint32_t* smask = reinterpret_cast<uint32_t*>(smem + G::BIAS_BYTES);
@@ -144,7 +152,7 @@ __global__ void __launch_bounds__(Geo<M>::THREADS) bwd_kernel(const BwdParams p)
     const int id = tid + k * THREADS;
     const int c = id & 3, rest = id >> 2;
     const int i = rest % N, tt = (rest / N) & 3;
-    ld_desc[k] = (uint32_t)(tt * G::TILE_BYTES + tile_off(i, c)) | ((uint32_t)(i / M) << 16) |
+    ld_desc[k] = (uint32_t)(tt * BG::TILE + tile_off(i, c)) | ((uint32_t)(i / M) << 16) |
                  ((uint32_t)(i % M) << 20) | ((uint32_t)tt << 24) | ((uint32_t)c << 26);
   }
   int lb, lwy, lwx;
@@ -201,13 +209,10 @@ __global__ void __launch_bounds__(Geo<M>::THREADS) bwd_kernel(const BwdParams p)
     cp_async_commit();
   }
 
-  if constexpr (G::NPAD > N) {
-    constexpr int PADROWS = G::NPAD - N;
-    for (int e = tid; e < STAGES * 4 * PADROWS * 4; e += THREADS) {
-      const int c = e & 3, r = (e >> 2) % PADROWS, tile = (e >> 2) / PADROWS;
-      *reinterpret_cast<uint4*>(stiles + tile * G::TILE_BYTES + tile_off(N + r, c)) =
-          make_uint4(0u, 0u, 0u, 0u);
-    }
+  // The zero row (row N) of every q/k/v/dO tile; loads never touch it.
+  for (int e = tid; e < STAGES * 4 * 4; e += THREADS) {
+    const int c = e & 3, tile = e >> 2;
+    *reinterpret_cast<uint4*>(stiles + tile * BG::TILE + tile_off(N, c)) = make_uint4(0u, 0u, 0u, 0u);
   }
   // P and dS tiles (hi and lo) start zeroed: columns NT*8..NPAD-1 are never written.
   for (int e = tid; e < 4 * BG::PS_BYTES / 16; e += THREADS)
@@ -236,13 +241,13 @@ __global__ void __launch_bounds__(Geo<M>::THREADS) bwd_kernel(const BwdParams p)
       }
     }
     const uint32_t qb = smem_u32(stiles + (it % STAGES) * BG::STAGE_BYTES);
-    const uint32_t kb = qb + G::TILE_BYTES, vb = kb + G::TILE_BYTES, ob = vb + G::TILE_BYTES;
+    const uint32_t kb = qb + BG::TILE, vb = kb + BG::TILE, ob = vb + BG::TILE;
 
     // ---- recompute S and P ---------------------------------------------------------
     float pr[NT][4];
     {
       uint32_t qa[2][4];
-      const int mi = lane >> 3, row = warp * 16 + (lane & 7) + ((mi & 1) << 3);
+      const int mi = lane >> 3, row = zr(warp * 16 + (lane & 7) + ((mi & 1) << 3));
 #pragma unroll
       for (int kk = 0; kk < 2; ++kk)
         ldsm_x4(qb + tile_off(row, 2 * kk + (mi >> 1)), qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
@@ -250,7 +255,7 @@ __global__ void __launch_bounds__(Geo<M>::THREADS) bwd_kernel(const BwdParams p)
       for (int nt = 0; nt < NT; ++nt) {
         const float4 bb = bfrag[nt * 32];  // z = q.k + bias/scale starts from the bias
         uint32_t b0, b1, b2, b3;
-        ldsm_x4(kb + tile_off(nt * 8 + (lane & 7), lane >> 3), b0, b1, b2, b3);
+        ldsm_x4(kb + tile_off(zr(nt * 8 + (lane & 7)), lane >> 3), b0, b1, b2, b3);
         mma_bf16_c(pr[nt], qa[0][0], qa[0][1], qa[0][2], qa[0][3], b0, b1, bb.x, bb.y, bb.z, bb.w);
         mma_bf16(pr[nt], qa[1][0], qa[1][1], qa[1][2], qa[1][3], b2, b3);
       }
@@ -324,7 +329,7 @@ __global__ void __launch_bounds__(Geo<M>::THREADS) bwd_kernel(const BwdParams p)
     float ds[NT][4];
     {
       uint32_t da[2][4];
-      const int mi = lane >> 3, row = warp * 16 + (lane & 7) + ((mi & 1) << 3);
+      const int mi = lane >> 3, row = zr(warp * 16 + (lane & 7) + ((mi & 1) << 3));
 #pragma unroll
       for (int kk = 0; kk < 2; ++kk)
         ldsm_x4(ob + tile_off(row, 2 * kk + (mi >> 1)), da[kk][0], da[kk][1], da[kk][2], da[kk][3]);
@@ -332,7 +337,7 @@ __global__ void __launch_bounds__(Geo<M>::THREADS) bwd_kernel(const BwdParams p)
       for (int nt = 0; nt < NT; ++nt) {
         ds[nt][0] = ds[nt][1] = ds[nt][2] = ds[nt][3] = 0.0f;
         uint32_t b0, b1, b2, b3;
-        ldsm_x4(vb + tile_off(nt * 8 + (lane & 7), lane >> 3), b0, b1, b2, b3);
+        ldsm_x4(vb + tile_off(zr(nt * 8 + (lane & 7)), lane >> 3), b0, b1, b2, b3);
         mma_bf16(ds[nt], da[0][0], da[0][1], da[0][2], da[0][3], b0, b1);
         mma_bf16(ds[nt], da[1][0], da[1][1], da[1][2], da[1][3], b2, b3);
       }
@@ -379,7 +384,8 @@ __global__ void __launch_bounds__(Geo<M>::THREADS) bwd_kernel(const BwdParams p)
       }
       // stmatrix: matrix (n-tile nt + (mi >> 1), row half mi & 1) per 8-lane group
       const int mi = lane >> 3;
-      const uint32_t rowoff = (uint32_t)((warp * 16 + 8 * (mi & 1) + (lane & 7)) * PS + (mi >> 1) * 16);
+      // padded rows (all zero) land on the zero row
+      const uint32_t rowoff = (uint32_t)(zr(warp * 16 + 8 * (mi & 1) + (lane & 7)) * PS + (mi >> 1) * 16);
       const uint32_t aP = smem_u32(sP) + rowoff, aPl = smem_u32(sPlo) + rowoff;
       const uint32_t aS = smem_u32(sdS) + rowoff, aSl = smem_u32(sdSlo) + rowoff;
 #pragma unroll
@@ -413,7 +419,7 @@ __global__ void __launch_bounds__(Geo<M>::THREADS) bwd_kernel(const BwdParams p)
           l2 = dsl[2 * kk + 1][0];
           l3 = dsl[2 * kk + 1][1];
         }
-        const int mi = lane >> 3, row = kk * 16 + (lane & 7) + ((mi & 1) << 3);
+        const int mi = lane >> 3, row = zr(kk * 16 + (lane & 7) + ((mi & 1) << 3));
 #pragma unroll
         for (int pp = 0; pp < 2; ++pp) {
           uint32_t v0, v1, v2, v3;
@@ -440,13 +446,13 @@ __global__ void __launch_bounds__(Geo<M>::THREADS) bwd_kernel(const BwdParams p)
       const int mi = lane >> 3;
 #pragma unroll
       for (int kk = 0; kk < KT; ++kk) {
-        const int rowA = kk * 16 + (lane & 7) + 8 * (mi >> 1), chA = 2 * warp + (mi & 1);
+        const int rowA = zr(kk * 16 + (lane & 7) + 8 * (mi >> 1)), chA = 2 * warp + (mi & 1);
         uint32_t a0, a1, a2, a3, f0, f1, f2, f3, p0, p1, p2, p3, e0, e1, e2, e3;
         ldsm_x4_t(smem_u32(sdS + rowA * PS + chA * 16), a0, a1, a2, a3);
         ldsm_x4_t(smem_u32(sdSlo + rowA * PS + chA * 16), f0, f1, f2, f3);
         ldsm_x4_t(smem_u32(sP + rowA * PS + chA * 16), p0, p1, p2, p3);
         ldsm_x4_t(smem_u32(sPlo + rowA * PS + chA * 16), e0, e1, e2, e3);
-        const int rowB = kk * 16 + (lane & 7) + ((mi & 1) << 3);
+        const int rowB = zr(kk * 16 + (lane & 7) + ((mi & 1) << 3));
 #pragma unroll
         for (int pp = 0; pp < 2; ++pp) {
           uint32_t q0, q1, q2, q3, d0, d1, d2, d3;
@@ -516,7 +522,7 @@ template <int M, typename TIO, int STAGES>
 static cudaError_t bconfig_t(const Plan& pl, BwdLaunch* L) {
   using G = Geo<M>;
   constexpr int smem = bwd_smem_bytes<M, STAGES>();
-  static_assert(G::NPAD * G::NPAD * 4 <= STAGES * BGeo<M>::STAGE_BYTES, "dS sums must fit the tiles");
+  static_assert(G::N * G::N * 4 <= STAGES * BGeo<M>::STAGE_BYTES, "dS sums must fit the tiles");
   auto kern = bwd_kernel<M, TIO, STAGES>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
