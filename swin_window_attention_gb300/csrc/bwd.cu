@@ -128,7 +128,6 @@ __global__ void __launch_bounds__(Geo<M>::THREADS, BwdMinBlocks<M>::value) bwd_k
   extern __shared__ __align__(128) unsigned char smem[];
   float4* sbias = reinterpret_cast<float4*>(smem);
   uint32_t* smask = reinterpret_cast<uint32_t*>(smem + G::BIAS_BYTES);
-  const float4* smtab = reinterpret_cast<const float4*>(smem + G::BIAS_BYTES + G::MASK_TAB_OFF);
   unsigned char* sP = smem + G::BIAS_BYTES + G::MASK_BYTES;
   unsigned char* sPlo = sP + BG::PS_BYTES;
   unsigned char* sdS = sPlo + BG::PS_BYTES;
@@ -218,6 +217,7 @@ __global__ void __launch_bounds__(Geo<M>::THREADS, BwdMinBlocks<M>::value) bwd_k
   // P and dS tiles (hi and lo) start zeroed: columns NT*8..NPAD-1 are never written.
   for (int e = tid; e < 4 * BG::PS_BYTES / 16; e += THREADS)
     reinterpret_cast<uint4*>(sP)[e] = make_uint4(0u, 0u, 0u, 0u);
+  const float mask_z = kMaskValue * kInvScale;  // the -100 mask in units of z
   const float4* bfrag = sbias + warp * NT * 32 + lane;
   const int r0 = warp * 16 + g, r1 = r0 + 8;
   float dtacc[NT][4];
@@ -251,25 +251,28 @@ __global__ void __launch_bounds__(Geo<M>::THREADS, BwdMinBlocks<M>::value) bwd_k
 #pragma unroll
       for (int kk = 0; kk < 2; ++kk)
         ldsm_x4(qb + tile_off(row, 2 * kk + (mi >> 1)), qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
-      // z = q.k + (bias + mask)/scale starts from the bias fragment; boundary windows add
-      // the mask picked from the table by each n-tile's four mask bits
-      const int cls = p.mask_frag != nullptr ? (wy == p.nWy - 1 ? 2 : 0) | (wx == p.nWx - 1 ? 1 : 0) : 0;
-      uint32_t mb[MW];
-#pragma unroll
-      for (int m = 0; m < MW; ++m) mb[m] = cls ? smask[(cls * MW + m) * THREADS + tid] : 0u;
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
-        float4 bb = bfrag[nt * 32];
-        if (cls) {
-          const float4 mv = smtab[(mb[(nt * 4) >> 5] >> ((nt * 4) & 31)) & 15u];
-          const float2 s01 = __fadd2_rn(make_float2(bb.x, bb.y), make_float2(mv.x, mv.y));
-          const float2 s23 = __fadd2_rn(make_float2(bb.z, bb.w), make_float2(mv.z, mv.w));
-          bb = make_float4(s01.x, s01.y, s23.x, s23.y);
-        }
+        const float4 bb = bfrag[nt * 32];  // z = q.k + bias/scale starts from the bias
         uint32_t b0, b1, b2, b3;
         ldsm_x4(kb + tile_off(zr(nt * 8 + (lane & 7)), lane >> 3), b0, b1, b2, b3);
         mma_bf16_c(pr[nt], qa[0][0], qa[0][1], qa[0][2], qa[0][3], b0, b1, bb.x, bb.y, bb.z, bb.w);
         mma_bf16(pr[nt], qa[1][0], qa[1][1], qa[1][2], qa[1][3], b2, b3);
+      }
+    }
+    int cls = 0;
+    if (p.mask_frag != nullptr) cls = (wy == p.nWy - 1 ? 2 : 0) | (wx == p.nWx - 1 ? 1 : 0);
+    uint32_t mb[MW];
+#pragma unroll
+    for (int m = 0; m < MW; ++m) mb[m] = cls ? smask[(cls * MW + m) * THREADS + tid] : 0u;
+    if (cls) {
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const uint32_t word = mb[(nt * 4) >> 5], sh = (nt * 4) & 31;
+        if ((word >> sh) & 1u) pr[nt][0] += mask_z;
+        if ((word >> (sh + 1)) & 1u) pr[nt][1] += mask_z;
+        if ((word >> (sh + 2)) & 1u) pr[nt][2] += mask_z;
+        if ((word >> (sh + 3)) & 1u) pr[nt][3] += mask_z;
       }
     }
     float m0a = -INFINITY, m0b = -INFINITY, m1a = -INFINITY, m1b = -INFINITY;
@@ -626,7 +629,7 @@ __global__ void noalloc_fragments_kernel(const float* __restrict__ table, int nH
   const int nWy = H / M, nWx = W / M;
   const int per_head = G::WARPS * NT * 32;
   const int nbias = nH * per_head;
-  const int nmask = mask_frag ? 4 * THREADS + 16 : 0;
+  const int nmask = mask_frag ? 4 * THREADS : 0;
   for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < nbias + nmask; e += gridDim.x * blockDim.x) {
     if (e < nbias) {
       const int h = e / per_head, f = e % per_head;
@@ -639,11 +642,6 @@ __global__ void noalloc_fragments_kernel(const float* __restrict__ table, int nH
         v[q] = c >= N ? -INFINITY : (r >= N ? 0.0f : table[(int64_t)rel_index(r, c, M) * nH + h] * kInvScale);
       }
       bias_frag[e] = make_float4(v[0], v[1], v[2], v[3]);
-    } else if (e >= nbias + 4 * THREADS) {
-      const int k = e - nbias - 4 * THREADS;  // table entry: mask of the set bits
-      const float mz = kMaskValue * kInvScale;
-      reinterpret_cast<float4*>(reinterpret_cast<unsigned char*>(mask_frag) + G::MASK_TAB_OFF)[k] =
-          make_float4(k & 1 ? mz : 0.0f, k & 2 ? mz : 0.0f, k & 4 ? mz : 0.0f, k & 8 ? mz : 0.0f);
     } else {
       const int f = e - nbias, cls = f / THREADS, tid = f % THREADS;
       const int warp = tid >> 5, g = (tid & 31) >> 2, t = tid & 3;
@@ -707,7 +705,7 @@ cudaError_t noalloc_bwd_t(Plan& pl, const float* table, const void* qkv, const v
   pl.bias_frag = reinterpret_cast<float4*>(base);
   pl.mask_frag = pl.s > 0 ? reinterpret_cast<uint32_t*>(base + bias_bytes) : nullptr;
   pl.dt_partial = reinterpret_cast<float*>(base + bias_bytes + mask_bytes);
-  const int nfrag = pl.nH * Geo<M>::WARPS * Geo<M>::NT * 32 + (pl.s > 0 ? 4 * Geo<M>::THREADS + 16 : 0);
+  const int nfrag = pl.nH * Geo<M>::WARPS * Geo<M>::NT * 32 + (pl.s > 0 ? 4 * Geo<M>::THREADS : 0);
   noalloc_fragments_kernel<M><<<(nfrag + 255) / 256, 256, 0, st>>>(table, pl.nH, pl.H, pl.W, pl.s,
                                                                    pl.bias_frag, pl.mask_frag);
   e = cudaGetLastError();

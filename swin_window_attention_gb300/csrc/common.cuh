@@ -187,10 +187,7 @@ struct Geo {
   static constexpr int TILE_BYTES = NPAD * 64;
   static constexpr int STAGE_BYTES = 3 * TILE_BYTES;
   static constexpr int BIAS_BYTES = WARPS * NT * 32 * 16;
-  // class mask bits [4][MW][THREADS], then a 16-entry float4 table: entry e holds the
-  // mask (in units of z) for the four elements whose bits are set in e
-  static constexpr int MASK_TAB_OFF = 4 * MW * THREADS * 4;
-  static constexpr int MASK_BYTES = MASK_TAB_OFF + 16 * 16;
+  static constexpr int MASK_BYTES = 4 * MW * THREADS * 4;
   static_assert(NT * 8 <= NPAD, "key tiles must fit the padded tile");
 };
 

@@ -49,7 +49,6 @@ __global__ void __launch_bounds__(Geo<M>::THREADS, FwdMinBlocks<M>::value) fwd_k
   extern __shared__ __align__(128) unsigned char smem[];
   float4* sbias = reinterpret_cast<float4*>(smem);
   uint32_t* smask = reinterpret_cast<uint32_t*>(smem + G::BIAS_BYTES);
-  const float4* smtab = reinterpret_cast<const float4*>(smem + G::BIAS_BYTES + G::MASK_TAB_OFF);
   unsigned char* stiles = smem + G::BIAS_BYTES + G::MASK_BYTES;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -153,6 +152,7 @@ __global__ void __launch_bounds__(Geo<M>::THREADS, FwdMinBlocks<M>::value) fwd_k
   }
   const float4* bfrag = sbias + warp * NT * 32 + lane;
   const float c_l2 = p.qk_scale_log2;            // scale * log2(e)
+  const float mask_z = kMaskValue * kInvScale;  // the -100 mask in units of z
   // Output slots of this lane: rows warp*16 + g + {0, 8}, 16-byte chunk t.
   const int os0 = warp * 16 + g, os1 = os0 + 8;
   const int oly0 = os0 / M, olx0 = os0 % M, oly1 = os1 / M, olx1 = os1 % M;
@@ -194,37 +194,28 @@ __global__ void __launch_bounds__(Geo<M>::THREADS, FwdMinBlocks<M>::value) fwd_k
     uint32_t qa[2][4];
     ldsm_x4(tb + q_off0, qa[0][0], qa[0][1], qa[0][2], qa[0][3]);
     ldsm_x4(tb + q_off1, qa[1][0], qa[1][1], qa[1][2], qa[1][3]);
-    // Boundary windows add the shift mask to the seeds: each n-tile's four mask bits pick
-    // one float4 of the mask table.
-    const bool masked = p.mask_frag != nullptr && (wy == p.nWy - 1 || wx == p.nWx - 1);
     float sacc[NT][4];
-    if (masked) {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const float4 bb = bfrag[nt * 32];
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4(tb + k_off + nt * 512, b0, b1, b2, b3);
+      mma_bf16_c(sacc[nt], qa[0][0], qa[0][1], qa[0][2], qa[0][3], b0, b1, bb.x, bb.y, bb.z, bb.w);
+      mma_bf16(sacc[nt], qa[1][0], qa[1][1], qa[1][2], qa[1][3], b2, b3);
+    }
+
+    // ---- mask (boundary windows only) and row max --------------------------------
+    if (p.mask_frag != nullptr && (wy == p.nWy - 1 || wx == p.nWx - 1)) {
       const int cls = (wy == p.nWy - 1 ? 2 : 0) | (wx == p.nWx - 1 ? 1 : 0);
       uint32_t mb[MW];
 #pragma unroll
       for (int m = 0; m < MW; ++m) mb[m] = smask[(cls * MW + m) * THREADS + tid];
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        const float4 bb = bfrag[nt * 32];
-        const float4 mv = smtab[(mb[(nt * 4) >> 5] >> ((nt * 4) & 31)) & 15u];
-        const float2 s01 = __fadd2_rn(make_float2(bb.x, bb.y), make_float2(mv.x, mv.y));
-        const float2 s23 = __fadd2_rn(make_float2(bb.z, bb.w), make_float2(mv.z, mv.w));
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(tb + k_off + nt * 512, b0, b1, b2, b3);
-        mma_bf16_c(sacc[nt], qa[0][0], qa[0][1], qa[0][2], qa[0][3], b0, b1, s01.x, s01.y, s23.x, s23.y);
-        mma_bf16(sacc[nt], qa[1][0], qa[1][1], qa[1][2], qa[1][3], b2, b3);
-      }
-    } else {
+      for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        const float4 bb = bfrag[nt * 32];
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(tb + k_off + nt * 512, b0, b1, b2, b3);
-        mma_bf16_c(sacc[nt], qa[0][0], qa[0][1], qa[0][2], qa[0][3], b0, b1, bb.x, bb.y, bb.z, bb.w);
-        mma_bf16(sacc[nt], qa[1][0], qa[1][1], qa[1][2], qa[1][3], b2, b3);
-      }
+        for (int q = 0; q < 4; ++q)
+          if ((mb[(nt * 4 + q) >> 5] >> ((nt * 4 + q) & 31)) & 1u) sacc[nt][q] += mask_z;
     }
-
     // two interleaved three-input max chains per row
     float m0a = -INFINITY, m0b = -INFINITY, m1a = -INFINITY, m1b = -INFINITY;
 #pragma unroll

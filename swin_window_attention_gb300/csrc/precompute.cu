@@ -65,7 +65,7 @@ __global__ void fragments_kernel(const float* __restrict__ dense, const float* _
   constexpr int N = G::N, NT = G::NT, MW = G::MW, THREADS = G::THREADS;
   const int per_head = G::WARPS * NT * 32;
   const int nbias = nH * per_head;
-  const int nmask = mask ? 4 * THREADS + 16 : 0;
+  const int nmask = mask ? 4 * THREADS : 0;
   for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < nbias + nmask; e += gridDim.x * blockDim.x) {
     if (e < nbias) {
       const int h = e / per_head, f = e % per_head;
@@ -79,11 +79,6 @@ __global__ void fragments_kernel(const float* __restrict__ dense, const float* _
         v[q] = c >= N ? -INFINITY : (r >= N ? 0.0f : db[r * N + c] * kInvScale);
       }
       bias_frag[e] = make_float4(v[0], v[1], v[2], v[3]);
-    } else if (e >= nbias + 4 * THREADS) {
-      const int k = e - nbias - 4 * THREADS;  // table entry: mask of the set bits
-      const float mz = kMaskValue * kInvScale;
-      reinterpret_cast<float4*>(reinterpret_cast<unsigned char*>(mask_frag) + G::MASK_TAB_OFF)[k] =
-          make_float4(k & 1 ? mz : 0.0f, k & 2 ? mz : 0.0f, k & 4 ? mz : 0.0f, k & 8 ? mz : 0.0f);
     } else {
       // one (class, thread) pair: bits of that thread's fragment elements
       const int f = e - nbias, cls = f / THREADS, tid = f % THREADS;
@@ -146,7 +141,7 @@ size_t mask_frag_bytes(int M) {
 
 cudaError_t launch_fragments(const Plan& p, cudaStream_t st) {
   const float* mask = p.s > 0 ? p.mask : nullptr;
-  const int64_t n = (int64_t)bias_frag_bytes(p.M, p.nH) / 16 + (mask ? 4 * 32 * ((p.M * p.M + 15) / 16) + 16 : 0);
+  const int64_t n = (int64_t)bias_frag_bytes(p.M, p.nH) / 16 + (mask ? 4 * 32 * ((p.M * p.M + 15) / 16) : 0);
   const int grid = grid_for(n, 256);
   switch (p.M) {
     case 4:
