@@ -104,11 +104,14 @@ int swin_wattn_fwd(swin_wattn_plan_t plan, const void* qkv, void* out,
 /*
  * Forward on host-resident activations, for callers whose data lives in host memory:
  * copies qkv_host [B,H,W,3C] into the caller-owned device buffer dev_qkv, runs the same
- * kernel as swin_wattn_fwd into dev_out, and copies dev_out back to out_host [B,H,W,C],
- * all in order on `stream` (synchronise the stream before reading out_host). Host
- * buffers should be page-locked (cudaHostAlloc, or torch pin_memory) for the copies to
- * be asynchronous. Host pointers that the GPU cannot reach are fine here; dev_qkv and
- * dev_out must be device pointers (16-byte aligned).
+ * kernel as swin_wattn_fwd into dev_out, and copies dev_out back to out_host [B,H,W,C].
+ * The batch is cut into up to four chunks that flow through a copy-in queue, `stream`
+ * (the kernels) and a copy-out queue, so both copy directions and the compute overlap;
+ * `stream` waits for the last copy-out, so the whole call is ordered on `stream`
+ * (synchronise it before reading out_host). The two copy queues and their events are
+ * created by the plan's first call. Host buffers should be page-locked (cudaHostAlloc,
+ * or torch pin_memory) for the copies to be asynchronous. dev_qkv and dev_out must be
+ * device pointers (16-byte aligned).
  */
 int swin_wattn_fwd_host(swin_wattn_plan_t plan, const void* qkv_host, void* out_host,
                         void* dev_qkv, void* dev_out, struct CUstream_st* stream);

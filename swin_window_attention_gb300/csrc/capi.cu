@@ -20,15 +20,28 @@ size_t mask_frag_bytes(int M);
 cudaError_t fwd_config(const Plan& pl, FwdLaunch* L);
 cudaError_t fwd_launch(const Plan& pl, const FwdLaunch& L, const void* qkv, void* out,
                        cudaStream_t st);
+cudaError_t fwd_launch_batch(const Plan& pl, const FwdLaunch& L, const void* qkv, void* out,
+                             int batch, cudaStream_t st);
 cudaError_t bwd_config(const Plan& pl, BwdLaunch* L);
 cudaError_t bwd_launch(const Plan& pl, const BwdLaunch& L, const void* qkv, const void* dout,
                        void* dqkv, float* dtable, cudaStream_t st);
 }  // namespace swin
 
+// Streams and events of the host-buffer forward's copy/compute pipeline, created on
+// its first use.
+constexpr int kHostChunks = 4;
+struct HostPipe {
+  bool ready = false;
+  cudaStream_t in = nullptr, out = nullptr;
+  cudaEvent_t start = nullptr, done = nullptr;
+  cudaEvent_t loaded[kHostChunks] = {}, computed[kHostChunks] = {};
+};
+
 struct swin_wattn_plan_s {
   swin::Plan p;
   swin::FwdLaunch fwd;
   swin::BwdLaunch bwd;
+  HostPipe pipe;
 };
 
 namespace {
@@ -71,6 +84,19 @@ int check_plan(const swin_wattn_plan_s* pl) {
   }
   if (pl->p.magic != swin::kPlanMagic) return SWIN_WATTN_ERR_BAD_PLAN;
   return SWIN_WATTN_OK;
+}
+
+void free_pipe(HostPipe& hp) {
+  if (!hp.ready) return;
+  for (int c = 0; c < kHostChunks; ++c) {
+    cudaEventDestroy(hp.loaded[c]);
+    cudaEventDestroy(hp.computed[c]);
+  }
+  cudaEventDestroy(hp.start);
+  cudaEventDestroy(hp.done);
+  cudaStreamDestroy(hp.in);
+  cudaStreamDestroy(hp.out);
+  hp.ready = false;
 }
 
 void free_plan_buffers(swin::Plan& p) {
@@ -231,15 +257,50 @@ int swin_wattn_fwd_host(swin_wattn_plan_t plan, const void* qkv_host, void* out_
   if ((rc = check_device_ptr(dev_qkv, 16)) != SWIN_WATTN_OK) return rc;
   if ((rc = check_device_ptr(dev_out, 16)) != SWIN_WATTN_OK) return rc;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  const size_t esz = p.dtype == SWIN_WATTN_FP32 ? 4 : 2;
-  const size_t tokens = (size_t)p.B * p.H * p.W;
-  cudaError_t e = cudaMemcpyAsync(dev_qkv, qkv_host, tokens * 3 * p.C * esz, cudaMemcpyHostToDevice, st);
-  if (e == cudaSuccess) {
-    e = swin::fwd_launch(p, plan->fwd, dev_qkv, dev_out, st);
-    ++g_launches;
+  cudaError_t e = cudaSuccess;
+  HostPipe& hp = plan->pipe;
+  if (!hp.ready) {
+    e = cudaStreamCreateWithFlags(&hp.in, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&hp.out, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&hp.start, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&hp.done, cudaEventDisableTiming);
+    for (int c = 0; c < kHostChunks && e == cudaSuccess; ++c) {
+      e = cudaEventCreateWithFlags(&hp.loaded[c], cudaEventDisableTiming);
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&hp.computed[c], cudaEventDisableTiming);
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "swin_wattn_fwd_host");
+    hp.ready = true;
   }
-  if (e == cudaSuccess)
-    e = cudaMemcpyAsync(out_host, dev_out, tokens * p.C * esz, cudaMemcpyDeviceToHost, st);
+  // Batch chunks flow through three queues: copy-in, compute (the caller's stream) and
+  // copy-out, so the two copy directions and the kernels overlap; the caller's stream
+  // finally waits for the last copy-out, keeping the call ordered on `stream`.
+  const size_t esz = p.dtype == SWIN_WATTN_FP32 ? 4 : 2;
+  const size_t img_in = (size_t)p.H * p.W * 3 * p.C * esz, img_out = (size_t)p.H * p.W * p.C * esz;
+  const int nchunk = p.B < kHostChunks ? p.B : kHostChunks;
+  e = cudaEventRecord(hp.start, st);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(hp.in, hp.start, 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(hp.out, hp.start, 0);
+  for (int c = 0; c < nchunk && e == cudaSuccess; ++c) {
+    const int b0 = (int)((int64_t)p.B * c / nchunk), b1 = (int)((int64_t)p.B * (c + 1) / nchunk);
+    const size_t n_in = img_in * (b1 - b0), n_out = img_out * (b1 - b0);
+    const char* hsrc = static_cast<const char*>(qkv_host) + img_in * b0;
+    char* dq = static_cast<char*>(dev_qkv) + img_in * b0;
+    char* dout = static_cast<char*>(dev_out) + img_out * b0;
+    e = cudaMemcpyAsync(dq, hsrc, n_in, cudaMemcpyHostToDevice, hp.in);
+    if (e == cudaSuccess) e = cudaEventRecord(hp.loaded[c], hp.in);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(st, hp.loaded[c], 0);
+    if (e == cudaSuccess) {
+      e = swin::fwd_launch_batch(p, plan->fwd, dq, dout, b1 - b0, st);
+      ++g_launches;
+    }
+    if (e == cudaSuccess) e = cudaEventRecord(hp.computed[c], st);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(hp.out, hp.computed[c], 0);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(static_cast<char*>(out_host) + img_out * b0, dout, n_out,
+                          cudaMemcpyDeviceToHost, hp.out);
+  }
+  if (e == cudaSuccess) e = cudaEventRecord(hp.done, hp.out);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(st, hp.done, 0);
   return e == cudaSuccess ? SWIN_WATTN_OK : cuda_fail(e, "swin_wattn_fwd_host");
 }
 
@@ -304,6 +365,7 @@ int swin_wattn_destroy(swin_wattn_plan_t plan) {
   }
   cudaError_t e = cudaDeviceSynchronize();
   plan->p.magic = 0;
+  free_pipe(plan->pipe);
   free_plan_buffers(plan->p);
   delete plan;
   return e == cudaSuccess ? SWIN_WATTN_OK : cuda_fail(e, "swin_wattn_destroy");

@@ -215,6 +215,7 @@ __device__ __forceinline__ void load_chunk<float>(uint32_t dst, const float* src
 
 struct FwdLaunch {
   int grid = 0, threads = 0, smem = 0, chunks = 0;
+  int ctas_per_sm = 0;
 };
 struct BwdLaunch {
   int grid = 0, threads = 0, smem = 0, chunks = 0, partial_rows = 0;

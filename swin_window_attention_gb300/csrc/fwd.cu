@@ -350,12 +350,24 @@ static cudaError_t config_t(const Plan& pl, FwdLaunch* L) {
   L->grid = (int)(chunks * pl.nH);
   L->threads = G::THREADS;
   L->smem = smem;
+  L->ctas_per_sm = occ;
   return cudaSuccess;
 }
 
+// Forward over `batch` images starting at the given pointers (batch <= the plan's B): one
+// wave of CTAs sized as in config_t for that many windows.
 template <int M, typename TIO, int STAGES>
-static cudaError_t launch_t(const Plan& pl, const FwdLaunch& L, const void* qkv, void* out,
-                            cudaStream_t st) {
+static cudaError_t launch_t(const Plan& pl, const FwdLaunch& L0, const void* qkv, void* out,
+                            int batch, cudaStream_t st) {
+  FwdLaunch L = L0;
+  if (batch != pl.B) {
+    const int64_t total = (int64_t)batch * pl.nW;
+    int64_t chunks = ((int64_t)pl.num_sms * L0.ctas_per_sm) / pl.nH;
+    if (chunks < 1) chunks = 1;
+    if (chunks > total) chunks = total;
+    L.chunks = (int)chunks;
+    L.grid = (int)(chunks * pl.nH);
+  }
   FwdParams p;
   p.qkv = qkv;
   p.out = out;
@@ -369,7 +381,7 @@ static cudaError_t launch_t(const Plan& pl, const FwdLaunch& L, const void* qkv,
   p.nWy = pl.nWy;
   p.nWx = pl.nWx;
   p.nW = pl.nW;
-  p.total_windows = (int64_t)pl.B * pl.nW;
+  p.total_windows = (int64_t)batch * pl.nW;
   p.chunks = L.chunks;
   p.qk_scale_log2 = kLog2e / kInvScale;
   fwd_kernel<M, TIO, STAGES><<<L.grid, L.threads, L.smem, st>>>(p);
@@ -403,7 +415,12 @@ cudaError_t fwd_config(const Plan& pl, FwdLaunch* L) { SWIN_FWD_DISPATCH(config_
 
 cudaError_t fwd_launch(const Plan& pl, const FwdLaunch& L, const void* qkv, void* out,
                        cudaStream_t st) {
-  SWIN_FWD_DISPATCH(launch_t, pl, L, qkv, out, st);
+  SWIN_FWD_DISPATCH(launch_t, pl, L, qkv, out, pl.B, st);
+}
+
+cudaError_t fwd_launch_batch(const Plan& pl, const FwdLaunch& L, const void* qkv, void* out,
+                             int batch, cudaStream_t st) {
+  SWIN_FWD_DISPATCH(launch_t, pl, L, qkv, out, batch, st);
 }
 
 }  // namespace swin

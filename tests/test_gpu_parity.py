@@ -217,3 +217,23 @@ def test_batch_shards_concatenate_exactly():
     assert torch.equal(torch.cat([p[1] for p in parts]), dq)
     assert_close("dtable shard sum", parts[0][2] + parts[1][2], dt.double().cpu().numpy())
     full.close()
+
+
+@pytest.mark.parametrize("name,batch", [("swin_t_s1_swmsa", 32), ("tiny", 1), ("swin_l224_s3", 3)])
+def test_fwd_host_buffers_match_device_path(name, batch):
+    """swin_wattn_fwd_host (pinned host in/out, chunked copy/compute pipeline) gives the
+    device path's output bit for bit."""
+    wl = inputs.BY_NAME[name].with_batch(batch)
+    qkv, table = inputs.make_qkv(wl), inputs.make_table(wl)
+    att = plan(wl, table.to(DEV))
+    ref = att.fwd(qkv.to(DEV)).cpu()
+    qh = qkv.pin_memory()
+    oh = torch.empty(ref.shape, dtype=ref.dtype).pin_memory()
+    dq = torch.empty(qkv.shape, dtype=qkv.dtype, device=DEV)
+    do = torch.empty(ref.shape, dtype=ref.dtype, device=DEV)
+    for _ in range(2):
+        oh.zero_()
+        att.fwd_host(qh, oh, dq, do)
+        torch.cuda.synchronize()
+        assert torch.equal(oh, ref)
+    att.close()
