@@ -37,8 +37,8 @@ struct BGeo {
   static constexpr int PS_STRIDE = G::NPAD * 2 + 16;  // bytes per row of the P / dS tiles
   static constexpr int PS_BYTES = ROWS * PS_STRIDE;
   static constexpr int STAGE_BYTES = 4 * TILE;
-  static constexpr int CHUNKS = 4 * G::N * 4;
-  static constexpr int CH_ITERS = (CHUNKS + G::THREADS - 1) / G::THREADS;
+  static constexpr int TCH = G::N * 4;                            // 16-byte chunks per tensor
+  static constexpr int TI = (TCH + G::THREADS - 1) / G::THREADS;  // per-thread chunks per tensor
   static constexpr int STG_BYTES = G::WARPS * 16 * 64;  // per-warp bf16 output staging
   static constexpr int R = (2 * M - 1) * (2 * M - 1);
 };
@@ -144,16 +144,18 @@ __global__ void __launch_bounds__(Geo<M>::THREADS, BwdMinBlocks<M>::value) bwd_k
   const int C = p.C, H = p.H, W = p.W, s = p.s;
   unsigned char* stg = sstg + warp * 16 * 64;
 
-  // Per-thread gather descriptors, packed: shared offset (bits 0-15), window row (16-19),
-  // window column (20-23), slice q/k/v/dO (24-25), 16-byte chunk (26-27).
-  uint32_t ld_desc[BG::CH_ITERS];
+  // Per-thread gather slots, the same for all four tensors (q, k, v from qkv; dO from
+  // dout): chunk j of this thread is 16-byte chunk c of window slot i = (ly, lx).
+  uint32_t ld_soff[BG::TI];  // tile-relative shared offset
+  int ld_rc[BG::TI];         // (ly << 8) | lx
+  int ld_chan[BG::TI];       // h * 32 + c * 8
 #pragma unroll
-  for (int k = 0; k < BG::CH_ITERS; ++k) {
-    const int id = tid + k * THREADS;
-    const int c = id & 3, rest = id >> 2;
-    const int i = rest % N, tt = (rest / N) & 3;
-    ld_desc[k] = (uint32_t)(tt * BG::TILE + tile_off(i, c)) | ((uint32_t)(i / M) << 16) |
-                 ((uint32_t)(i % M) << 20) | ((uint32_t)tt << 24) | ((uint32_t)c << 26);
+  for (int j = 0; j < BG::TI; ++j) {
+    const int id = tid + j * THREADS;
+    const int c = id & 3, i = (id >> 2) < N ? (id >> 2) : 0;
+    ld_soff[j] = tile_off(i, c);
+    ld_rc[j] = ((i / M) << 8) | (i % M);
+    ld_chan[j] = h * kHeadDim + c * 8;
   }
   int lb, lwy, lwx;
   {
@@ -165,22 +167,23 @@ __global__ void __launch_bounds__(Geo<M>::THREADS, BwdMinBlocks<M>::value) bwd_k
   int cb = lb, cwy = lwy, cwx = lwx;
 
   auto issue = [&](int stage) {
-    unsigned char* base = stiles + stage * BG::STAGE_BYTES;
-    const int64_t img = (int64_t)lb * H * W;
+    const uint32_t base = smem_u32(stiles + stage * BG::STAGE_BYTES);
     const int y0 = lwy * M + s, x0 = lwx * M + s;
+    const int hy = H - y0, hx = W - x0;  // window rows ly >= hy / columns lx >= hx wrap
+    const int64_t tok0 = ((int64_t)lb * H + y0) * W + x0;
+    const TIO* qbase = reinterpret_cast<const TIO*>(p.qkv) + tok0 * 3 * C;
+    const TIO* obase = reinterpret_cast<const TIO*>(p.dout) + tok0 * C;
 #pragma unroll
-    for (int k = 0; k < BG::CH_ITERS; ++k) {
-      if (k < BG::CH_ITERS - 1 || tid + k * THREADS < BG::CHUNKS) {
-        const uint32_t d = ld_desc[k];
-        const int tt = (d >> 24) & 3, c = (d >> 26) & 3;
-        int y = y0 + (int)((d >> 16) & 15), x = x0 + (int)((d >> 20) & 15);
-        y = y >= H ? y - H : y;
-        x = x >= W ? x - W : x;
-        const int64_t tok = img + y * W + x;
-        const TIO* src = tt < 3
-            ? reinterpret_cast<const TIO*>(p.qkv) + tok * 3 * C + tt * C + h * kHeadDim + c * 8
-            : reinterpret_cast<const TIO*>(p.dout) + tok * C + h * kHeadDim + c * 8;
-        load_chunk<TIO>(smem_u32(base + (d & 0xffffu)), src);
+    for (int j = 0; j < BG::TI; ++j) {
+      if (j < BG::TI - 1 || tid + j * THREADS < BG::TCH) {
+        const int ly = ld_rc[j] >> 8, lx = ld_rc[j] & 255;
+        int64_t rel = (int64_t)ly * W + lx;  // token offset from the window's first token
+        if (ly >= hy) rel -= (int64_t)H * W;
+        if (lx >= hx) rel -= W;
+#pragma unroll
+        for (int tt = 0; tt < 3; ++tt)
+          load_chunk<TIO>(base + tt * BG::TILE + ld_soff[j], qbase + rel * 3 * C + tt * C + ld_chan[j]);
+        load_chunk<TIO>(base + 3 * BG::TILE + ld_soff[j], obase + rel * C + ld_chan[j]);
       }
     }
     if (++lwx == p.nWx) {
