@@ -45,7 +45,6 @@ template <int M, typename TIO, int STAGES>
 __global__ void __launch_bounds__(Geo<M>::THREADS, FwdMinBlocks<M>::value) fwd_kernel(const FwdParams p) {
   using G = Geo<M>;
   constexpr int N = G::N, NT = G::NT, KT = G::KT, MW = G::MW, THREADS = G::THREADS;
-  constexpr int CH_ITERS = G::CH_ITERS;
   extern __shared__ __align__(128) unsigned char smem[];
   float4* sbias = reinterpret_cast<float4*>(smem);
   uint32_t* smask = reinterpret_cast<uint32_t*>(smem + G::BIAS_BYTES);
@@ -60,22 +59,19 @@ __global__ void __launch_bounds__(Geo<M>::THREADS, FwdMinBlocks<M>::value) fwd_k
   const int C3 = 3 * p.C, H = p.H, W = p.W, s = p.s;
   const TIO* __restrict__ qkv = reinterpret_cast<const TIO*>(p.qkv);
 
-  // Per-thread gather descriptors, fixed for every window: chunk k of this thread is
-  // 16-byte chunk c of slice tt (q, k or v) of window slot i = (ly, lx). ld_loff is the
-  // element offset of that chunk from the window's first token when the window does not
-  // wrap around the grid edge.
-  // Packed: shared offset (bits 0-15), window row (16-19), window column (20-23), slice
-  // (24-25), chunk (26-27).
-  uint32_t ld_desc[CH_ITERS];
-  int ld_loff[CH_ITERS];
+  // Per-thread gather slots, the same for q, k and v: chunk j of this thread is 16-byte
+  // chunk c of window slot i = (ly, lx) of each of the three tensors.
+  constexpr int TCH = N * 4, TI = (TCH + THREADS - 1) / THREADS;
+  uint32_t ld_soff[TI];  // tile-relative shared offset
+  int ld_rc[TI];         // (ly << 8) | lx
+  int ld_chan[TI];       // h * 32 + c * 8
 #pragma unroll
-  for (int k = 0; k < CH_ITERS; ++k) {
-    const int id = tid + k * THREADS;
-    const int c = id & 3, rest = id >> 2;
-    const int i = rest % N, tt = (rest / N) & 3;
-    ld_desc[k] = (uint32_t)(tt * G::TILE_BYTES + tile_off(i, c)) | ((uint32_t)(i / M) << 16) |
-                 ((uint32_t)(i % M) << 20) | ((uint32_t)tt << 24) | ((uint32_t)c << 26);
-    ld_loff[k] = ((i / M) * W + i % M) * C3 + tt * p.C + h * kHeadDim + c * 8;
+  for (int j = 0; j < TI; ++j) {
+    const int id = tid + j * THREADS;
+    const int c = id & 3, i = (id >> 2) < N ? (id >> 2) : 0;
+    ld_soff[j] = tile_off(i, c);
+    ld_rc[j] = ((i / M) << 8) | (i % M);
+    ld_chan[j] = h * kHeadDim + c * 8;
   }
   // Window cursor of the next window to load: (b, wy, wx) advanced one window at a time.
   int lb, lwy, lwx;
@@ -92,27 +88,19 @@ __global__ void __launch_bounds__(Geo<M>::THREADS, FwdMinBlocks<M>::value) fwd_k
   auto issue = [&](uint32_t stage_off) {
     const uint32_t base = tiles_u32 + stage_off;
     const int y0 = lwy * M + s, x0 = lwx * M + s;
-    if (y0 + M <= H && x0 + M <= W) {  // no wrap: one base plus fixed offsets
-      const TIO* wbase = qkv + ((int64_t)lb * H * W + (int64_t)y0 * W + x0) * C3;
+    const int hy = H - y0, hx = W - x0;  // window rows ly >= hy / columns lx >= hx wrap
+    const TIO* wbase = qkv + (((int64_t)lb * H + y0) * W + x0) * C3;
 #pragma unroll
-      for (int k = 0; k < CH_ITERS; ++k)
-        if (k < CH_ITERS - 1 || tid + k * THREADS < G::CHUNKS)
-          load_chunk<TIO>(base + (ld_desc[k] & 0xffffu), wbase + ld_loff[k]);
-    } else {
-      // The window wraps around the grid edge: rows ly >= hy come from the top of the
-      // image and columns lx >= hx from its left edge.
-      const TIO* wbase = qkv + ((int64_t)lb * H * W + (int64_t)y0 * W + x0) * C3;
-      const int hy = H - y0, hx = W - x0;
-      const int64_t dy = (int64_t)H * W * C3, dx = (int64_t)W * C3;
+    for (int j = 0; j < TI; ++j) {
+      if (j < TI - 1 || tid + j * THREADS < TCH) {
+        const int ly = ld_rc[j] >> 8, lx = ld_rc[j] & 255;
+        int64_t rel = (int64_t)ly * W + lx;  // token offset from the window's first token
+        if (ly >= hy) rel -= (int64_t)H * W;
+        if (lx >= hx) rel -= W;
+        const TIO* src = wbase + rel * C3 + ld_chan[j];
 #pragma unroll
-      for (int k = 0; k < CH_ITERS; ++k) {
-        if (k < CH_ITERS - 1 || tid + k * THREADS < G::CHUNKS) {
-          const uint32_t d = ld_desc[k];
-          int64_t off = ld_loff[k];
-          if ((int)((d >> 16) & 15) >= hy) off -= dy;
-          if ((int)((d >> 20) & 15) >= hx) off -= dx;
-          load_chunk<TIO>(base + (d & 0xffffu), wbase + off);
-        }
+        for (int tt = 0; tt < 3; ++tt)
+          load_chunk<TIO>(base + tt * G::TILE_BYTES + ld_soff[j], src + tt * p.C);
       }
     }
     if (++lwx == p.nWx) {
