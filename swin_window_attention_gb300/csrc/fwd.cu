@@ -17,8 +17,6 @@
 // [16w, 16w+16): S = Q K^T on bf16 tensor cores (m16n8k16, fp32 accumulate), fused
 // scale + bias + mask, a register softmax with quad shuffles, P (bf16) V, and the
 // normalised rows go back to the token positions they were read from.
-#include <type_traits>
-
 #include "common.cuh"
 
 namespace swin {
@@ -318,314 +316,17 @@ __global__ void __launch_bounds__(Geo<M>::THREADS, FwdMinBlocks<M>::value) fwd_k
   cp_async_wait<0>();
 }
 
-
-// ---- 12x12 windows: two warps per query tile ------------------------------------------
-//
-// A 144-token window gives each warp of the generic kernel 72 score registers, which caps
-// a CTA at nine warps per SM. Here every 16-row query tile has two warps: the first takes
-// keys 0..79 (ten n8 tiles), the second keys 80..143 (eight). They exchange row maxima
-// through shared memory, each forms its part of P V (with its row sums), the first hands
-// its partial to the second, which normalises and stores. 18 warps per SM, same plan
-// fragments (a warp reads its m-tile's fragments for its key tiles).
-constexpr int kW12Warps = 18, kW12Threads = kW12Warps * 32, kW12Split = 10;
-
-struct F12Layout {
-  using G = Geo<12>;
-  static constexpr int XM_OFF = 0;                                // [9 tiles][2 halves][16 rows] fp32
-  static constexpr int XO_OFF = XM_OFF + 9 * 2 * 16 * 4;          // [9][4 nd][32 lanes] float4
-  static constexpr int XL_OFF = XO_OFF + 9 * 4 * 32 * 16;         // [9][32 lanes] float2
-  static constexpr int XCH_BYTES = XL_OFF + 9 * 32 * 8;
-};
-
-template <int STAGES>
-constexpr int fwd12_smem_bytes() {
-  return Geo<12>::BIAS_BYTES + Geo<12>::MASK_BYTES + STAGES * Geo<12>::STAGE_BYTES + F12Layout::XCH_BYTES;
-}
-
-template <typename TIO, int STAGES>
-__global__ void __launch_bounds__(kW12Threads, 1) fwd12_kernel(const FwdParams p) {
-  using G = Geo<12>;
-  using X = F12Layout;
-  constexpr int M = 12, N = G::N, NT = G::NT, MW = G::MW, THREADS = kW12Threads;
-  extern __shared__ __align__(128) unsigned char smem[];
-  const float4* sbias = reinterpret_cast<const float4*>(smem);
-  const uint32_t* smask = reinterpret_cast<const uint32_t*>(smem + G::BIAS_BYTES);
-  unsigned char* stiles = smem + G::BIAS_BYTES + G::MASK_BYTES;
-  unsigned char* xch = stiles + STAGES * G::STAGE_BYTES;
-  float* xm = reinterpret_cast<float*>(xch + X::XM_OFF);
-  float4* xo = reinterpret_cast<float4*>(xch + X::XO_OFF);
-  float2* xl = reinterpret_cast<float2*>(xch + X::XL_OFF);
-
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int g = lane >> 2, t = lane & 3;
-  const int mt = warp >> 1, kh = warp & 1;  // query tile and key half of this warp
-  const int h = blockIdx.x % p.nH;
-  const int chunk = blockIdx.x / p.nH;
-  const int64_t w_begin = p.total_windows * chunk / p.chunks;
-  const int nwin = (int)(p.total_windows * (chunk + 1) / p.chunks - w_begin);
-  const int C3 = 3 * p.C, H = p.H, W = p.W, s = p.s;
-  const TIO* __restrict__ qkv = reinterpret_cast<const TIO*>(p.qkv);
-
-  // One 16-byte chunk of each of q, k, v per thread: chunk c of window slot i.
-  const int ld_i = tid >> 2, ld_c = tid & 3;
-  const uint32_t ld_soff = tile_off(ld_i, ld_c);
-  const int ld_ly = ld_i / M, ld_lx = ld_i % M, ld_chan = h * kHeadDim + ld_c * 8;
-  int lb, lwy, lwx;
-  {
-    lb = (int)(w_begin / p.nW);
-    const int w = (int)(w_begin - (int64_t)lb * p.nW);
-    lwy = w / p.nWx;
-    lwx = w - lwy * p.nWx;
-  }
-  int cb = lb, cwy = lwy, cwx = lwx;
-  const uint32_t tiles_u32 = smem_u32(stiles);
-  auto issue = [&](uint32_t stage_off) {
-    const int y0 = lwy * M + s, x0 = lwx * M + s;
-    int64_t rel = (int64_t)ld_ly * W + ld_lx;
-    if (ld_ly >= H - y0) rel -= (int64_t)H * W;
-    if (ld_lx >= W - x0) rel -= W;
-    const TIO* src = qkv + ((((int64_t)lb * H + y0) * W + x0) + rel) * C3 + ld_chan;
-#pragma unroll
-    for (int tt = 0; tt < 3; ++tt)
-      load_chunk<TIO>(tiles_u32 + stage_off + tt * G::TILE_BYTES + ld_soff, src + tt * p.C);
-    if (++lwx == p.nWx) {
-      lwx = 0;
-      if (++lwy == p.nWy) {
-        lwy = 0;
-        ++lb;
-      }
-    }
-  };
-
-  {
-    const unsigned char* bsrc = reinterpret_cast<const unsigned char*>(p.bias_frag) + (size_t)h * G::BIAS_BYTES;
-    for (int e = tid; e < G::BIAS_BYTES / 16; e += THREADS) cp_async_16(smem_u32(smem + e * 16), bsrc + e * 16);
-    if (p.mask_frag != nullptr) {
-      const unsigned char* msrc = reinterpret_cast<const unsigned char*>(p.mask_frag);
-      for (int e = tid; e < G::MASK_BYTES / 16; e += THREADS)
-        cp_async_16(smem_u32(smem + G::BIAS_BYTES + e * 16), msrc + e * 16);
-    }
-  }
-#pragma unroll
-  for (int st = 0; st < STAGES - 1; ++st) {
-    if (st < nwin) issue(st * G::STAGE_BYTES);
-    cp_async_commit();
-  }
-
-  const float c_l2 = p.qk_scale_log2;
-  const float mask_z = kMaskValue * kInvScale;
-  const uint32_t ones = 0x3F803F80u;
-  const int mi = lane >> 3, r8 = lane & 7, r16 = r8 + ((mi & 1) << 3);
-  const uint32_t q_off0 = tile_off(mt * 16 + r16, mi >> 1);
-  const uint32_t q_off1 = tile_off(mt * 16 + r16, 2 + (mi >> 1));
-  const uint32_t k_off = G::TILE_BYTES + tile_off(r8, mi);
-  const uint32_t v_off0 = 2 * G::TILE_BYTES + tile_off(r16, mi >> 1);
-  const uint32_t v_off1 = 2 * G::TILE_BYTES + tile_off(r16, 2 + (mi >> 1));
-  const uint32_t st_off0 = tile_off(mt * 16 + r8 + ((mi & 1) << 3), mi >> 1);
-  const uint32_t st_off1 = tile_off(mt * 16 + r8 + ((mi & 1) << 3), 2 + (mi >> 1));
-  const int os0 = mt * 16 + g, os1 = os0 + 8;
-  const int oly0 = os0 / M, olx0 = os0 % M, oly1 = os1 / M, olx1 = os1 % M;
-  const int pair_bar = 1 + mt;  // named barrier of this warp pair (64 threads)
-
-  // One window's work for key half KH (compile-time n-tile range).
-  auto body = [&](auto khc, uint32_t tb, unsigned char* tq, int b, int wy, int wx) {
-    constexpr int KH = decltype(khc)::value;
-    constexpr int NT0 = KH == 0 ? 0 : kW12Split, NTK = KH == 0 ? kW12Split : NT - kW12Split;
-    uint32_t qa[2][4];
-    ldsm_x4(tb + q_off0, qa[0][0], qa[0][1], qa[0][2], qa[0][3]);
-    ldsm_x4(tb + q_off1, qa[1][0], qa[1][1], qa[1][2], qa[1][3]);
-    const float4* bfrag = sbias + (mt * NT + NT0) * 32 + lane;
-    float sacc[NTK][4];
-#pragma unroll
-    for (int n = 0; n < NTK; ++n) {
-      const float4 bb = bfrag[n * 32];
-      uint32_t b0, b1, b2, b3;
-      ldsm_x4(tb + k_off + (NT0 + n) * 512, b0, b1, b2, b3);
-      mma_bf16_c(sacc[n], qa[0][0], qa[0][1], qa[0][2], qa[0][3], b0, b1, bb.x, bb.y, bb.z, bb.w);
-      mma_bf16(sacc[n], qa[1][0], qa[1][1], qa[1][2], qa[1][3], b2, b3);
-    }
-    if (p.mask_frag != nullptr && (wy == p.nWy - 1 || wx == p.nWx - 1)) {
-      const int cls = (wy == p.nWy - 1 ? 2 : 0) | (wx == p.nWx - 1 ? 1 : 0);
-      const uint32_t* mrow = smask + (cls * MW) * G::THREADS + mt * 32 + lane;
-#pragma unroll
-      for (int n = 0; n < NTK; ++n)
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int bit = (NT0 + n) * 4 + q;
-          if ((mrow[(bit >> 5) * G::THREADS] >> (bit & 31)) & 1u) sacc[n][q] += mask_z;
-        }
-    }
-    float m0a = -INFINITY, m0b = -INFINITY, m1a = -INFINITY, m1b = -INFINITY;
-#pragma unroll
-    for (int n = 0; n < NTK; n += 2) {
-      m0a = fmax3(m0a, sacc[n][0], sacc[n][1]);
-      m1a = fmax3(m1a, sacc[n][2], sacc[n][3]);
-      if (n + 1 < NTK) {
-        m0b = fmax3(m0b, sacc[n + 1][0], sacc[n + 1][1]);
-        m1b = fmax3(m1b, sacc[n + 1][2], sacc[n + 1][3]);
-      }
-    }
-    float mx0 = fmaxf(m0a, m0b), mx1 = fmaxf(m1a, m1b);
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-    // exchange the row maxima of the two key halves
-    float* xmt = xm + mt * 32;
-    if (t == 0) {
-      xmt[KH * 16 + g] = mx0;
-      xmt[KH * 16 + g + 8] = mx1;
-    }
-    asm volatile("bar.sync %0, 64;\n" ::"r"(pair_bar) : "memory");
-    mx0 = fmaxf(mx0, xmt[(1 - KH) * 16 + g]);
-    mx1 = fmaxf(mx1, xmt[(1 - KH) * 16 + g + 8]);
-
-    const float2 c2 = make_float2(c_l2, c_l2);
-    const float2 nm0 = make_float2(-mx0 * c_l2, -mx0 * c_l2), nm1 = make_float2(-mx1 * c_l2, -mx1 * c_l2);
-#pragma unroll
-    for (int n = 0; n < NTK; ++n) {
-      const float2 e0 = __ffma2_rn(make_float2(sacc[n][0], sacc[n][1]), c2, nm0);
-      const float2 e1 = __ffma2_rn(make_float2(sacc[n][2], sacc[n][3]), c2, nm1);
-      sacc[n][0] = fast_exp2(e0.x);
-      sacc[n][1] = fast_exp2(e0.y);
-      sacc[n][2] = fast_exp2(e1.x);
-      sacc[n][3] = fast_exp2(e1.y);
-    }
-    float o[4][4], lsum[4];
-#pragma unroll
-    for (int kk = 0; kk < NTK / 2; ++kk) {
-      const uint32_t a0 = pack_bf16(sacc[2 * kk][0], sacc[2 * kk][1]);
-      const uint32_t a1 = pack_bf16(sacc[2 * kk][2], sacc[2 * kk][3]);
-      const uint32_t a2 = pack_bf16(sacc[2 * kk + 1][0], sacc[2 * kk + 1][1]);
-      const uint32_t a3 = pack_bf16(sacc[2 * kk + 1][2], sacc[2 * kk + 1][3]);
-      uint32_t v0, v1, v2, v3, w0, w1, w2, w3;
-      ldsm_x4_t(tb + v_off0 + (NT0 / 2 + kk) * 1024, v0, v1, v2, v3);
-      ldsm_x4_t(tb + v_off1 + (NT0 / 2 + kk) * 1024, w0, w1, w2, w3);
-      if (kk == 0) {
-        mma_bf16_c(o[0], a0, a1, a2, a3, v0, v1, 0.f, 0.f, 0.f, 0.f);
-        mma_bf16_c(o[1], a0, a1, a2, a3, v2, v3, 0.f, 0.f, 0.f, 0.f);
-        mma_bf16_c(o[2], a0, a1, a2, a3, w0, w1, 0.f, 0.f, 0.f, 0.f);
-        mma_bf16_c(o[3], a0, a1, a2, a3, w2, w3, 0.f, 0.f, 0.f, 0.f);
-        mma_bf16_c(lsum, a0, a1, a2, a3, ones, ones, 0.f, 0.f, 0.f, 0.f);
-      } else {
-        mma_bf16(o[0], a0, a1, a2, a3, v0, v1);
-        mma_bf16(o[1], a0, a1, a2, a3, v2, v3);
-        mma_bf16(o[2], a0, a1, a2, a3, w0, w1);
-        mma_bf16(o[3], a0, a1, a2, a3, w2, w3);
-        mma_bf16(lsum, a0, a1, a2, a3, ones, ones);
-      }
-    }
-    float4* xot = xo + mt * 4 * 32 + lane;
-    float2* xlt = xl + mt * 32 + lane;
-    if constexpr (KH == 0) {
-      // hand the partial products and row sums to the other warp of the pair
-#pragma unroll
-      for (int nd = 0; nd < 4; ++nd) xot[nd * 32] = make_float4(o[nd][0], o[nd][1], o[nd][2], o[nd][3]);
-      *xlt = make_float2(lsum[0], lsum[2]);
-      asm volatile("bar.sync %0, 64;\n" ::"r"(pair_bar) : "memory");
-    } else {
-      asm volatile("bar.sync %0, 64;\n" ::"r"(pair_bar) : "memory");
-#pragma unroll
-      for (int nd = 0; nd < 4; ++nd) {
-        const float4 a = xot[nd * 32];
-        const float2 u = __fadd2_rn(make_float2(o[nd][0], o[nd][1]), make_float2(a.x, a.y));
-        const float2 v = __fadd2_rn(make_float2(o[nd][2], o[nd][3]), make_float2(a.z, a.w));
-        o[nd][0] = u.x;
-        o[nd][1] = u.y;
-        o[nd][2] = v.x;
-        o[nd][3] = v.y;
-      }
-      const float2 lp = *xlt;
-      const float inv0 = 1.0f / (lsum[0] + lp.x), inv1 = 1.0f / (lsum[2] + lp.y);
-      const int y0 = wy * M + s, x0 = wx * M + s;
-      int ya = y0 + oly0, xa = x0 + olx0, yb = y0 + oly1, xb = x0 + olx1;
-      ya = ya >= H ? ya - H : ya;
-      xa = xa >= W ? xa - W : xa;
-      yb = yb >= H ? yb - H : yb;
-      xb = xb >= W ? xb - W : xb;
-      const int64_t img = (int64_t)b * H * W;
-      const int64_t tok0 = img + ya * W + xa, tok1 = img + yb * W + xb;
-      if constexpr (sizeof(TIO) == 2) {
-        // stage the 16 x 32 rows in this tile's Q rows (the first warp of the pair is
-        // done with them: it passed the barrier above after its last Q read)
-        const float2 i0 = make_float2(inv0, inv0), i1 = make_float2(inv1, inv1);
-        uint32_t ow[4][2];
-#pragma unroll
-        for (int nd = 0; nd < 4; ++nd) {
-          const float2 a = __fmul2_rn(make_float2(o[nd][0], o[nd][1]), i0);
-          const float2 c = __fmul2_rn(make_float2(o[nd][2], o[nd][3]), i1);
-          ow[nd][0] = pack_bf16(a.x, a.y);
-          ow[nd][1] = pack_bf16(c.x, c.y);
-        }
-        stsm_x4(tb + st_off0, ow[0][0], ow[0][1], ow[1][0], ow[1][1]);
-        stsm_x4(tb + st_off1, ow[2][0], ow[2][1], ow[3][0], ow[3][1]);
-        __syncwarp();
-        __nv_bfloat16* outp = reinterpret_cast<__nv_bfloat16*>(p.out) + h * kHeadDim + t * 8;
-        *reinterpret_cast<uint4*>(outp + tok0 * p.C) = *reinterpret_cast<const uint4*>(tq + tile_off(os0, t));
-        *reinterpret_cast<uint4*>(outp + tok1 * p.C) = *reinterpret_cast<const uint4*>(tq + tile_off(os1, t));
-      } else {
-        float* outp = reinterpret_cast<float*>(p.out) + h * kHeadDim + 2 * t;
-        float* d0 = outp + tok0 * p.C;
-        float* d1 = outp + tok1 * p.C;
-#pragma unroll
-        for (int nd = 0; nd < 4; ++nd) {
-          *reinterpret_cast<float2*>(d0 + nd * 8) = make_float2(o[nd][0] * inv0, o[nd][1] * inv0);
-          *reinterpret_cast<float2*>(d1 + nd * 8) = make_float2(o[nd][2] * inv1, o[nd][3] * inv1);
-        }
-      }
-    }
-  };
-
-  uint32_t cur_off = 0, nxt_off = (STAGES - 1) * G::STAGE_BYTES;
-  for (int it = 0; it < nwin; ++it) {
-    cp_async_wait<STAGES - 2>();
-    __syncthreads();
-    if (it + STAGES - 1 < nwin) issue(nxt_off);
-    cp_async_commit();
-    nxt_off = nxt_off + G::STAGE_BYTES == STAGES * G::STAGE_BYTES ? 0 : nxt_off + G::STAGE_BYTES;
-    const int b = cb, wy = cwy, wx = cwx;
-    if (++cwx == p.nWx) {
-      cwx = 0;
-      if (++cwy == p.nWy) {
-        cwy = 0;
-        ++cb;
-      }
-    }
-    unsigned char* tq = stiles + cur_off;
-    const uint32_t tb = tiles_u32 + cur_off;
-    cur_off = cur_off + G::STAGE_BYTES == STAGES * G::STAGE_BYTES ? 0 : cur_off + G::STAGE_BYTES;
-    if (kh == 0)
-      body(std::integral_constant<int, 0>{}, tb, tq, b, wy, wx);
-    else
-      body(std::integral_constant<int, 1>{}, tb, tq, b, wy, wx);
-  }
-  cp_async_wait<0>();
-}
-
 // ---- host side ---------------------------------------------------------------------
 
 template <int M, typename TIO, int STAGES>
-struct FwdKernel {
-  static constexpr int threads = Geo<M>::THREADS;
-  static constexpr int smem = fwd_smem_bytes<M, TIO, STAGES>();
-  static constexpr auto fn = fwd_kernel<M, TIO, STAGES>;
-};
-template <typename TIO, int STAGES>
-struct FwdKernel<12, TIO, STAGES> {
-  static constexpr int threads = kW12Threads;
-  static constexpr int smem = fwd12_smem_bytes<STAGES>();
-  static constexpr auto fn = fwd12_kernel<TIO, STAGES>;
-};
-
-template <int M, typename TIO, int STAGES>
 static cudaError_t config_t(const Plan& pl, FwdLaunch* L) {
-  using K = FwdKernel<M, TIO, STAGES>;
-  constexpr int smem = K::smem;
-  auto kern = K::fn;
+  using G = Geo<M>;
+  constexpr int smem = fwd_smem_bytes<M, TIO, STAGES>();
+  auto kern = fwd_kernel<M, TIO, STAGES>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   int occ = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, K::threads, smem);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, G::THREADS, smem);
   if (e != cudaSuccess) return e;
   if (occ < 1) return cudaErrorInvalidConfiguration;
   const int64_t total = (int64_t)pl.B * pl.nW;
@@ -635,7 +336,7 @@ static cudaError_t config_t(const Plan& pl, FwdLaunch* L) {
   if (chunks > total) chunks = total;
   L->chunks = (int)chunks;
   L->grid = (int)(chunks * pl.nH);
-  L->threads = K::threads;
+  L->threads = G::THREADS;
   L->smem = smem;
   L->ctas_per_sm = occ;
   return cudaSuccess;
@@ -671,13 +372,14 @@ static cudaError_t launch_t(const Plan& pl, const FwdLaunch& L0, const void* qkv
   p.total_windows = (int64_t)batch * pl.nW;
   p.chunks = L.chunks;
   p.qk_scale_log2 = kLog2e / kInvScale;
-  FwdKernel<M, TIO, STAGES>::fn<<<L.grid, L.threads, L.smem, st>>>(p);
+  fwd_kernel<M, TIO, STAGES><<<L.grid, L.threads, L.smem, st>>>(p);
   return cudaGetLastError();
 }
 
 // Pipeline depth per window size: enough windows in flight per SM while keeping the
 // shared-memory footprint within the residency target.
 template <int M> struct FwdStages { static constexpr int value = 3; };
+template <> struct FwdStages<12> { static constexpr int value = 2; };
 
 #define SWIN_FWD_DISPATCH(FN, ...)                                                       \
   do {                                                                                  \
