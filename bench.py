@@ -28,7 +28,7 @@ if ROOT not in sys.path:
 
 import torch  # noqa: E402
 
-from swin_window_attention_gb300 import inputs  # noqa: E402
+from swin_window_attention_gb300 import dp, inputs  # noqa: E402
 
 METRIC = "fused SW-MSA fwd/bwd tokens/s on 1 GB300; achieved HBM GB/s as % of roofline"
 SWEEP = ["swin_l224_s1", "swin_l224_s2", "swin_l224_s3", "swin_l224_s4"]
@@ -478,6 +478,10 @@ def run_train_step(args, dev, stream, lib, capi, hbm, ws):
                 events[k][2].record(stream)
             ok &= lib.swin_wattn_bwd(x["h"], x["q"].data_ptr(), x["d"].data_ptr(),
                                      x["dq"].data_ptr(), x["dt"].data_ptr(), sh) == capi.OK
+            if ws > 1:
+                # the one exchange of the path: the bias-table gradient summed over ranks
+                with torch.cuda.stream(stream):
+                    dp.allreduce_table_grad(x["dt"])
             if events is not None:
                 events[k][3].record(stream)
             if not ok:
@@ -509,7 +513,8 @@ def run_train_step(args, dev, stream, lib, capi, hbm, ws):
                        "bwd_tflops": round(bwd_flops(wl) / (b_ms / 1e3) / 1e12, 1)})
     for x in st:
         capi.swin_wattn_destroy(x["h"])
-    return {"workload": "swin_b224_train_step (B=128, 4 stages: set_bias + fwd + bwd)",
+    return {"workload": "swin_b224_train_step (B=128 per GPU, 4 stages: set_bias + fwd + bwd"
+                        + (", table-gradient all-reduce" if ws > 1 else "") + ")",
             "steps": steps, "ms_per_step": ms, "tokens_per_s": ws * tokens / (ms / 1e3),
             "stages": stages}
 
