@@ -122,7 +122,7 @@ template <int M, typename TIO, int STAGES>
 __global__ void __launch_bounds__(Geo<M>::THREADS, BwdMinBlocks<M>::value) bwd_kernel(const BwdParams p) {
   using G = Geo<M>;
   using BG = BGeo<M>;
-  constexpr int N = G::N, NT = G::NT, KT = G::KT, MW = G::MW, THREADS = G::THREADS;
+  constexpr int N = G::N, NT = G::NT, KT = G::KT, THREADS = G::THREADS;
   constexpr int PS = BG::PS_STRIDE;
   auto zr = [](int r) { return r < N ? r : N; };  // row, or the zero row for padding
   extern __shared__ __align__(128) unsigned char smem[];
@@ -195,7 +195,7 @@ __global__ void __launch_bounds__(Geo<M>::THREADS, BwdMinBlocks<M>::value) bwd_k
     }
   };
 
-  // This head's bias fragments and the class mask bits (built by the plan in this
+  // This head's bias fragments and the class mask fragments (built by the plan in this
   // kernel's fragment order) travel in the first copy group, with window 0.
   {
     const unsigned char* bsrc = reinterpret_cast<const unsigned char*>(p.bias_frag) + (size_t)h * G::BIAS_BYTES;
@@ -220,9 +220,10 @@ __global__ void __launch_bounds__(Geo<M>::THREADS, BwdMinBlocks<M>::value) bwd_k
   // P and dS tiles (hi and lo) start zeroed: columns NT*8..NPAD-1 are never written.
   for (int e = tid; e < 4 * BG::PS_BYTES / 16; e += THREADS)
     reinterpret_cast<uint4*>(sP)[e] = make_uint4(0u, 0u, 0u, 0u);
-  const float mask_z = kMaskValue * kInvScale;  // the -100 mask in units of z
   const float4* bfrag = sbias + warp * NT * 32 + lane;
   const int r0 = warp * 16 + g, r1 = r0 + 8;
+  // U operand of the shift-mask MMA for rows r0, r1 (k-slots 8..15 are zero).
+  const uint32_t mu0 = mask_u_frag(r0, t, M, s), mu1 = mask_u_frag(r1, t, M, s);
   float dtacc[NT][4];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) dtacc[nt][0] = dtacc[nt][1] = dtacc[nt][2] = dtacc[nt][3] = 0.0f;
@@ -263,19 +264,17 @@ __global__ void __launch_bounds__(Geo<M>::THREADS, BwdMinBlocks<M>::value) bwd_k
         mma_bf16(pr[nt], qa[1][0], qa[1][1], qa[1][2], qa[1][3], b2, b3);
       }
     }
-    int cls = 0;
-    if (p.mask_frag != nullptr) cls = (wy == p.nWy - 1 ? 2 : 0) | (wx == p.nWx - 1 ? 1 : 0);
-    uint32_t mb[MW];
+    // shift mask (boundary windows only): z += U V^T, one k16 MMA per key tile
+    if (p.mask_frag != nullptr && (wy == p.nWy - 1 || wx == p.nWx - 1)) {
+      const int cls = (wy == p.nWy - 1 ? 2 : 0) | (wx == p.nWx - 1 ? 1 : 0);
+      const uint4* mv = reinterpret_cast<const uint4*>(smask) + (cls - 1) * (G::NTP / 4) * 32 + lane;
 #pragma unroll
-    for (int m = 0; m < MW; ++m) mb[m] = cls ? smask[(cls * MW + m) * THREADS + tid] : 0u;
-    if (cls) {
+      for (int q4 = 0; q4 < G::NTP / 4; ++q4) {
+        const uint4 v = mv[q4 * 32];
+        const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        const uint32_t word = mb[(nt * 4) >> 5], sh = (nt * 4) & 31;
-        if ((word >> sh) & 1u) pr[nt][0] += mask_z;
-        if ((word >> (sh + 1)) & 1u) pr[nt][1] += mask_z;
-        if ((word >> (sh + 2)) & 1u) pr[nt][2] += mask_z;
-        if ((word >> (sh + 3)) & 1u) pr[nt][3] += mask_z;
+        for (int u = 0; u < 4; ++u)
+          if (q4 * 4 + u < NT) mma_bf16(pr[q4 * 4 + u], mu0, mu1, 0u, 0u, vw[u], 0u);
       }
     }
     float m0a = -INFINITY, m0b = -INFINITY, m1a = -INFINITY, m1b = -INFINITY;
@@ -615,24 +614,22 @@ cudaError_t bwd_launch(const Plan& pl, const BwdLaunch& L, const void* qkv, cons
 // and reduction buffers), so such a caller cannot create one. swin_wattn_bwd_noalloc
 // runs the same backward with all of its working memory in one fixed array below.
 
-// Working memory of swin_wattn_bwd_noalloc: bias fragments, class mask bits and the
+// Working memory of swin_wattn_bwd_noalloc: bias fragments, class mask fragments and the
 // per-CTA table-gradient partials, packed at 256-byte boundaries.
 constexpr size_t kNoAllocScratchBytes = size_t(2) << 20;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-// Bias fragments straight from the table (no dense bias) and mask bits straight from
-// the region labels (no mask tensor): the same values fragments_kernel derives from the
-// plan's dense bias and mask.
+// Bias fragments straight from the table (no dense bias); the mask fragments come from
+// the region labels exactly as in the plan's fragment kernel.
 template <int M>
 __global__ void noalloc_fragments_kernel(const float* __restrict__ table, int nH, int H, int W,
                                          int s, float4* __restrict__ bias_frag,
                                          uint32_t* __restrict__ mask_frag) {
   using G = Geo<M>;
-  constexpr int N = G::N, NT = G::NT, MW = G::MW, THREADS = G::THREADS;
-  const int nWy = H / M, nWx = W / M;
+  constexpr int N = G::N, NT = G::NT;
   const int per_head = G::WARPS * NT * 32;
   const int nbias = nH * per_head;
-  const int nmask = mask_frag ? 4 * THREADS : 0;
+  const int nmask = mask_frag ? G::MASK_BYTES / 4 : 0;
   for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < nbias + nmask; e += gridDim.x * blockDim.x) {
     if (e < nbias) {
       const int h = e / per_head, f = e % per_head;
@@ -646,24 +643,7 @@ __global__ void noalloc_fragments_kernel(const float* __restrict__ table, int nH
       }
       bias_frag[e] = make_float4(v[0], v[1], v[2], v[3]);
     } else {
-      const int f = e - nbias, cls = f / THREADS, tid = f % THREADS;
-      const int warp = tid >> 5, g = (tid & 31) >> 2, t = tid & 3;
-      const int wy = (cls & 2) ? nWy - 1 : 0, wx = (cls & 1) ? nWx - 1 : 0;
-      uint32_t bits[MW];
-#pragma unroll
-      for (int m = 0; m < MW; ++m) bits[m] = 0u;
-      if (cls != 0) {
-        for (int nt = 0; nt < NT; ++nt)
-          for (int q = 0; q < 4; ++q) {
-            const int r = warp * 16 + g + 8 * (q >> 1), c = nt * 8 + 2 * t + (q & 1);
-            if (r < N && c < N &&
-                region_label(wy * M + r / M, wx * M + r % M, H, W, M, s) !=
-                    region_label(wy * M + c / M, wx * M + c % M, H, W, M, s))
-              bits[(nt * 4 + q) >> 5] |= 1u << ((nt * 4 + q) & 31);
-          }
-      }
-#pragma unroll
-      for (int m = 0; m < MW; ++m) mask_frag[(cls * MW + m) * THREADS + tid] = bits[m];
+      mask_frag[e - nbias] = mask_frag_word<M>(e - nbias, H, W, s);
     }
   }
 }
@@ -708,7 +688,7 @@ cudaError_t noalloc_bwd_t(Plan& pl, const float* table, const void* qkv, const v
   pl.bias_frag = reinterpret_cast<float4*>(base);
   pl.mask_frag = pl.s > 0 ? reinterpret_cast<uint32_t*>(base + bias_bytes) : nullptr;
   pl.dt_partial = reinterpret_cast<float*>(base + bias_bytes + mask_bytes);
-  const int nfrag = pl.nH * Geo<M>::WARPS * Geo<M>::NT * 32 + (pl.s > 0 ? 4 * Geo<M>::THREADS : 0);
+  const int nfrag = pl.nH * Geo<M>::WARPS * Geo<M>::NT * 32 + (pl.s > 0 ? Geo<M>::MASK_BYTES / 4 : 0);
   noalloc_fragments_kernel<M><<<(nfrag + 255) / 256, 256, 0, st>>>(table, pl.nH, pl.H, pl.W, pl.s,
                                                                    pl.bias_frag, pl.mask_frag);
   e = cudaGetLastError();

@@ -31,8 +31,8 @@ struct Plan {
   // Per-head dense bias in the kernels' mma-fragment order, log2(e)-scaled, -inf in
   // padded key columns: [nH][WARPS][NT][32 lanes] float4. Owned.
   float4* bias_frag;
-  // Shift-mask bit patterns of the four window classes in fragment order:
-  // [4 classes][MW][THREADS] uint32 (class 0 all clear). Owned; null when s == 0.
+  // Shift-mask B fragments of the three boundary window classes (see mask_v_word):
+  // [3 classes][NTP / 4][32 lanes][4] uint32. Owned; null when s == 0.
   uint32_t* mask_frag;
 };
 
@@ -181,15 +181,63 @@ struct Geo {
   static constexpr int NPAD = MT * 16;      // rows of the shared q/k/v tiles
   static constexpr int WARPS = MT;
   static constexpr int THREADS = WARPS * 32;
-  static constexpr int MW = (NT * 4 + 31) / 32;  // mask words per thread per class
+  static constexpr int NTP = (NT + 3) & ~3;      // key tiles rounded to whole uint4 loads
   static constexpr int CHUNKS = 3 * N * 4;       // 16-byte bf16 chunks per window-head
   static constexpr int CH_ITERS = (CHUNKS + THREADS - 1) / THREADS;
   static constexpr int TILE_BYTES = NPAD * 64;
   static constexpr int STAGE_BYTES = 3 * TILE_BYTES;
   static constexpr int BIAS_BYTES = WARPS * NT * 32 * 16;
-  static constexpr int MASK_BYTES = 4 * MW * THREADS * 4;
+  static constexpr int MASK_BYTES = 3 * NTP * 32 * 4;
   static_assert(NT * 8 <= NPAD, "key tiles must fit the padded tile");
 };
+
+// ---- the shift mask as one extra k16 MMA per key tile -------------------------------
+//
+// In a boundary window (class 1: last window column, 2: last window row, 3: both) slot
+// i = (ly, lx) lies in the local region c(i) = 2 [ly >= M - s] + [lx >= M - s], and the
+// region labels of query slot i and key slot j differ exactly when mism(c(i), j) does,
+// where mism(c, j) compares j with any slot of region c. The mask in z units,
+// -100 * sqrt(hd) * mism(c(i), j), is therefore the k16 product U V^T with
+//   U[i][4e + c] = -100 * [c == c(i)],   V[j][4e + c] = part_e * mism(c, j),   e = 0, 1,
+// part_0 = bf16(sqrt(hd)), part_1 = bf16(sqrt(hd) - part_0), and k-slots 8..15 zero. One
+// c is set per row, so an accumulator receives -100 * (part_0 + part_1) (within 2e-4 of
+// -100 * sqrt(hd); every product is exact in fp32) or nothing.
+constexpr uint32_t kMaskUBits = 0xC2C8u;       // bf16 of -100
+constexpr float kMaskPartHi = 5.65625f;        // bf16 of sqrt(32)
+constexpr uint32_t kMaskPartHiBits = 0x40B5u;  // its bit pattern
+
+// U fragment word of query row r for lane column t (k-slots 2t, 2t+1); zero for padding.
+__device__ __forceinline__ uint32_t mask_u_frag(int r, int t, int M, int s) {
+  if (r >= M * M) return 0u;
+  const int c = ((r / M) >= M - s ? 2 : 0) | ((r % M) >= M - s ? 1 : 0);
+  return (((2 * t) & 3) == c ? kMaskUBits : 0u) | (((2 * t + 1) & 3) == c ? kMaskUBits << 16 : 0u);
+}
+
+// V fragment word (b0 of key tile nt: k-slots 2t, 2t+1 of key j = 8 nt + g) of class cls.
+__device__ __forceinline__ uint32_t mask_v_word(int cls, int lane, int nt, int H, int W, int M, int s) {
+  const int j = nt * 8 + (lane >> 2), t = lane & 3;
+  if (j >= M * M) return 0u;
+  const int y0 = (cls & 2) ? (H / M - 1) * M : 0, x0 = (cls & 1) ? (W / M - 1) * M : 0;
+  const int lj = region_label(y0 + j / M, x0 + j % M, H, W, M, s);
+  const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(kInvScale - kMaskPartHi));
+  uint32_t word = 0u;
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    const int k = 2 * t + q, c = k & 3;
+    const int li = region_label(y0 + ((c & 2) ? M - 1 : 0), x0 + ((c & 1) ? M - 1 : 0), H, W, M, s);
+    if (li != lj) word |= (k < 4 ? kMaskPartHiBits : lo) << (16 * q);
+  }
+  return word;
+}
+
+// Word e of the [3 classes][NTP / 4][32 lanes][4] mask fragment array.
+template <int M>
+__device__ __forceinline__ uint32_t mask_frag_word(int e, int H, int W, int s) {
+  using G = Geo<M>;
+  const int cls = 1 + e / (G::NTP * 32), r = e % (G::NTP * 32);
+  const int nt = (r >> 7) * 4 + (r & 3), lane = (r >> 2) & 31;
+  return nt < G::NT ? mask_v_word(cls, lane, nt, H, W, M, s) : 0u;
+}
 
 // One 16-byte bf16 chunk (8 channels) of a token's head slice into shared memory: a
 // cp.async for bf16 sources; fp32 sources are read, rounded to bf16 (nearest even) and

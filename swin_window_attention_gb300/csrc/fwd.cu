@@ -8,10 +8,10 @@
 // for the single fused WindowAttention kernel staging HBM -> shared -> registers).
 //
 // Work decomposition. A CTA owns one head h and a contiguous range of windows (across
-// the batch). Its dense bias (already log2(e)-scaled, in mma-fragment order) and the
-// shift-mask bit patterns of the four window classes (interior, last column, last row,
-// corner: the only patterns the region labels can form) are staged in shared memory
-// once. Each window's q/k/v head slices (64 bytes per token each) are gathered with
+// the batch). Its dense bias (divided by the softmax scale, in mma-fragment order) and
+// the shift-mask V fragments of the three boundary window classes (last column, last
+// row, corner: with the interior, the only patterns the region labels can form; the
+// mask enters as one extra k16 MMA per key tile) are staged in shared memory once. Each window's q/k/v head slices (64 bytes per token each) are gathered with
 // 16-byte cp.async straight from the rolled positions into a swizzled shared tile,
 // STAGES deep, so several windows are in flight per CTA. Warp w owns query rows
 // [16w, 16w+16): S = Q K^T on bf16 tensor cores (m16n8k16, fp32 accumulate), fused
@@ -25,7 +25,7 @@ struct FwdParams {
   const void* qkv;
   void* out;
   const float4* bias_frag;    // plan fragments [nH][WARPS][NT][32]
-  const uint32_t* mask_frag;  // plan class bit patterns [4][MW][THREADS] or null
+  const uint32_t* mask_frag;  // plan boundary-class mask V fragments, or null
   int H, W, C, nH, s, nWy, nWx, nW;
   int64_t total_windows;  // B * nW
   int chunks;             // window ranges per head
@@ -44,7 +44,7 @@ template <> struct FwdMinBlocks<12> { static constexpr int value = 1; };
 template <int M, typename TIO, int STAGES>
 __global__ void __launch_bounds__(Geo<M>::THREADS, FwdMinBlocks<M>::value) fwd_kernel(const FwdParams p) {
   using G = Geo<M>;
-  constexpr int N = G::N, NT = G::NT, KT = G::KT, MW = G::MW, THREADS = G::THREADS;
+  constexpr int N = G::N, NT = G::NT, KT = G::KT, THREADS = G::THREADS;
   extern __shared__ __align__(128) unsigned char smem[];
   float4* sbias = reinterpret_cast<float4*>(smem);
   uint32_t* smask = reinterpret_cast<uint32_t*>(smem + G::BIAS_BYTES);
@@ -112,7 +112,7 @@ __global__ void __launch_bounds__(Geo<M>::THREADS, FwdMinBlocks<M>::value) fwd_k
     }
   };
 
-  // This head's bias fragments and the class mask bits (built by the plan in this
+  // This head's bias fragments and the class mask fragments (built by the plan in this
   // kernel's fragment order) travel in the first copy group, with window 0.
   {
     const unsigned char* bsrc = reinterpret_cast<const unsigned char*>(p.bias_frag) + (size_t)h * G::BIAS_BYTES;
@@ -140,10 +140,11 @@ __global__ void __launch_bounds__(Geo<M>::THREADS, FwdMinBlocks<M>::value) fwd_k
   }
   const float4* bfrag = sbias + warp * NT * 32 + lane;
   const float c_l2 = p.qk_scale_log2;            // scale * log2(e)
-  const float mask_z = kMaskValue * kInvScale;  // the -100 mask in units of z
   // Output slots of this lane: rows warp*16 + g + {0, 8}, 16-byte chunk t.
   const int os0 = warp * 16 + g, os1 = os0 + 8;
   const int oly0 = os0 / M, olx0 = os0 % M, oly1 = os1 / M, olx1 = os1 % M;
+  // U operand of the shift-mask MMA for these two rows (k-slots 8..15 are zero).
+  const uint32_t mu0 = mask_u_frag(os0, t, M, s), mu1 = mask_u_frag(os1, t, M, s);
   // B operand of all ones: one extra m16n8 tile of P V yields the row sums of the very
   // bf16 P values that weight V.
   const uint32_t ones = 0x3F803F80u;
@@ -192,17 +193,18 @@ __global__ void __launch_bounds__(Geo<M>::THREADS, FwdMinBlocks<M>::value) fwd_k
       mma_bf16(sacc[nt], qa[1][0], qa[1][1], qa[1][2], qa[1][3], b2, b3);
     }
 
-    // ---- mask (boundary windows only) and row max --------------------------------
+    // ---- shift mask (boundary windows only): z += U V^T, one k16 MMA per key tile ----
     if (p.mask_frag != nullptr && (wy == p.nWy - 1 || wx == p.nWx - 1)) {
       const int cls = (wy == p.nWy - 1 ? 2 : 0) | (wx == p.nWx - 1 ? 1 : 0);
-      uint32_t mb[MW];
+      const uint4* mv = reinterpret_cast<const uint4*>(smask) + (cls - 1) * (G::NTP / 4) * 32 + lane;
 #pragma unroll
-      for (int m = 0; m < MW; ++m) mb[m] = smask[(cls * MW + m) * THREADS + tid];
+      for (int q4 = 0; q4 < G::NTP / 4; ++q4) {
+        const uint4 v = mv[q4 * 32];
+        const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-          if ((mb[(nt * 4 + q) >> 5] >> ((nt * 4 + q) & 31)) & 1u) sacc[nt][q] += mask_z;
+        for (int u = 0; u < 4; ++u)
+          if (q4 * 4 + u < NT) mma_bf16(sacc[q4 * 4 + u], mu0, mu1, 0u, 0u, vw[u], 0u);
+      }
     }
     // two interleaved three-input max chains per row
     float m0a = -INFINITY, m0b = -INFINITY, m1a = -INFINITY, m1b = -INFINITY;

@@ -52,20 +52,20 @@ __global__ void relidx_kernel(int M, int32_t* __restrict__ out) {
     out[e] = rel_index(e / N, e % N, M);
 }
 
-// The dense bias and the mask re-laid out once per plan in the order the attention
-// kernels consume them (lane (g, t) of warp wp, key tile nt: rows 16wp+g, +8; columns
-// 8nt+2t, +1), so a CTA stages its head's block with plain 16-byte copies. The bias is
-// stored divided by the softmax scale (it seeds the q.k accumulators), -inf in padded
-// key columns and 0 in padded query rows.
+// The dense bias re-laid out once per plan in the order the attention kernels consume
+// it (lane (g, t) of warp wp, key tile nt: rows 16wp+g, +8; columns 8nt+2t, +1), so a CTA
+// stages its head's block with plain 16-byte copies. The bias is stored divided by the
+// softmax scale (it seeds the q.k accumulators), -inf in padded key columns and 0 in
+// padded query rows. The shift-mask V fragments of the three boundary classes follow
+// (mask_frag_word), built from the same region labels as the dense mask.
 template <int M>
-__global__ void fragments_kernel(const float* __restrict__ dense, const float* __restrict__ mask,
-                                 int nH, int nWy, int nWx, float4* __restrict__ bias_frag,
-                                 uint32_t* __restrict__ mask_frag) {
+__global__ void fragments_kernel(const float* __restrict__ dense, int nH, int H, int W, int s,
+                                 float4* __restrict__ bias_frag, uint32_t* __restrict__ mask_frag) {
   using G = Geo<M>;
-  constexpr int N = G::N, NT = G::NT, MW = G::MW, THREADS = G::THREADS;
+  constexpr int N = G::N, NT = G::NT;
   const int per_head = G::WARPS * NT * 32;
   const int nbias = nH * per_head;
-  const int nmask = mask ? 4 * THREADS : 0;
+  const int nmask = mask_frag ? G::MASK_BYTES / 4 : 0;
   for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < nbias + nmask; e += gridDim.x * blockDim.x) {
     if (e < nbias) {
       const int h = e / per_head, f = e % per_head;
@@ -80,23 +80,7 @@ __global__ void fragments_kernel(const float* __restrict__ dense, const float* _
       }
       bias_frag[e] = make_float4(v[0], v[1], v[2], v[3]);
     } else {
-      // one (class, thread) pair: bits of that thread's fragment elements
-      const int f = e - nbias, cls = f / THREADS, tid = f % THREADS;
-      const int warp = tid >> 5, g = (tid & 31) >> 2, t = tid & 3;
-      const int wy = (cls & 2) ? nWy - 1 : 0, wx = (cls & 1) ? nWx - 1 : 0;
-      const float* mw = mask + (int64_t)(wy * nWx + wx) * N * N;
-      uint32_t bits[MW];
-#pragma unroll
-      for (int m = 0; m < MW; ++m) bits[m] = 0u;
-      if (cls != 0) {
-        for (int nt = 0; nt < NT; ++nt)
-          for (int q = 0; q < 4; ++q) {
-            const int r = warp * 16 + g + 8 * (q >> 1), c = nt * 8 + 2 * t + (q & 1);
-            if (r < N && c < N && mw[r * N + c] != 0.0f) bits[(nt * 4 + q) >> 5] |= 1u << ((nt * 4 + q) & 31);
-          }
-      }
-#pragma unroll
-      for (int m = 0; m < MW; ++m) mask_frag[(cls * MW + m) * THREADS + tid] = bits[m];
+      mask_frag[e - nbias] = mask_frag_word<M>(e - nbias, H, W, s);
     }
   }
 }
@@ -140,18 +124,18 @@ size_t mask_frag_bytes(int M) {
 }
 
 cudaError_t launch_fragments(const Plan& p, cudaStream_t st) {
-  const float* mask = p.s > 0 ? p.mask : nullptr;
-  const int64_t n = (int64_t)bias_frag_bytes(p.M, p.nH) / 16 + (mask ? 4 * 32 * ((p.M * p.M + 15) / 16) : 0);
+  uint32_t* mask = p.s > 0 ? p.mask_frag : nullptr;
+  const int64_t n = (int64_t)bias_frag_bytes(p.M, p.nH) / 16 + (mask ? mask_frag_bytes(p.M) / 4 : 0);
   const int grid = grid_for(n, 256);
   switch (p.M) {
     case 4:
-      fragments_kernel<4><<<grid, 256, 0, st>>>(p.dense_bias, mask, p.nH, p.nWy, p.nWx, p.bias_frag, p.mask_frag);
+      fragments_kernel<4><<<grid, 256, 0, st>>>(p.dense_bias, p.nH, p.H, p.W, p.s, p.bias_frag, mask);
       break;
     case 7:
-      fragments_kernel<7><<<grid, 256, 0, st>>>(p.dense_bias, mask, p.nH, p.nWy, p.nWx, p.bias_frag, p.mask_frag);
+      fragments_kernel<7><<<grid, 256, 0, st>>>(p.dense_bias, p.nH, p.H, p.W, p.s, p.bias_frag, mask);
       break;
     case 12:
-      fragments_kernel<12><<<grid, 256, 0, st>>>(p.dense_bias, mask, p.nH, p.nWy, p.nWx, p.bias_frag, p.mask_frag);
+      fragments_kernel<12><<<grid, 256, 0, st>>>(p.dense_bias, p.nH, p.H, p.W, p.s, p.bias_frag, mask);
       break;
     default:
       return cudaErrorInvalidValue;
