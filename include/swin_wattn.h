@@ -63,10 +63,18 @@ enum swin_wattn_status {
   SWIN_WATTN_ERR_MISALIGNED = 3,   /* tensor pointer not 16-byte aligned (table: 4-byte) */
   SWIN_WATTN_ERR_BAD_PLAN = 4,     /* null, destroyed or foreign plan handle */
   SWIN_WATTN_ERR_CUDA = 5,         /* a CUDA runtime call failed; see swin_wattn_last_error */
-  SWIN_WATTN_ERR_TIMEOUT = 6       /* reserved for bounded device-side waits */
+  SWIN_WATTN_ERR_TIMEOUT = 6       /* a bounded device-side wait ran out (see
+                                      swin_wattn_device_status) */
 };
 
 enum swin_wattn_dtype { SWIN_WATTN_BF16 = 0, SWIN_WATTN_FP32 = 1 };
+
+/* Forward kernels (swin_wattn_set_fwd_kernel). */
+enum swin_wattn_kernel {
+  SWIN_WATTN_KERNEL_AUTO = 0,      /* the faster kernel as measured: mma.sync (default) */
+  SWIN_WATTN_KERNEL_MMA_SYNC = 1,  /* warp-level mma.sync kernel: every M, both dtypes */
+  SWIN_WATTN_KERNEL_TCGEN05 = 2    /* tensor-memory kernel: M = 7 with bf16 only */
+};
 
 /*
  * Create a plan for one layer shape and run the preprocessing on `stream`:
@@ -163,6 +171,23 @@ int swin_wattn_bwd_noalloc(const void* qkv, const void* dout, void* dqkv, float*
  */
 int swin_wattn_debug_maps(swin_wattn_plan_t plan, int32_t* gather, int32_t* relidx,
                           float* mask, float* dense_bias, struct CUstream_st* stream);
+
+/*
+ * Choose the plan's forward kernel (SWIN_WATTN_KERNEL_*). Both kernels compute the same
+ * function to the same tolerance; AUTO is the default. Asking for TCGEN05 where it does not apply returns SWIN_WATTN_ERR_UNSUPPORTED
+ * and leaves the plan unchanged. Host-side only; call it between launches.
+ */
+int swin_wattn_set_fwd_kernel(swin_wattn_plan_t plan, int kernel);
+
+/* The forward kernel the plan launches (MMA_SYNC or TCGEN05), or -1 for a bad handle. */
+int swin_wattn_fwd_kernel(swin_wattn_plan_t plan);
+
+/*
+ * Synchronise `stream` and report the plan's device error word: SWIN_WATTN_ERR_TIMEOUT
+ * if a kernel's bounded wait on the tensor core (1 s) ran out since the last call, in
+ * which case that launch's output is not valid; the word is cleared. Otherwise OK.
+ */
+int swin_wattn_device_status(swin_wattn_plan_t plan, struct CUstream_st* stream);
 
 /* Free the plan's device memory (synchronises the device first). NULL is a no-op. */
 int swin_wattn_destroy(swin_wattn_plan_t plan);

@@ -23,6 +23,9 @@ ERR_CUDA = 5
 ERR_TIMEOUT = 6
 BF16 = 0
 FP32 = 1
+KERNEL_AUTO = 0
+KERNEL_MMA_SYNC = 1
+KERNEL_TCGEN05 = 2
 
 # Every symbol include/swin_wattn.h declares, with (argtypes, restype).
 _vp, _i, _cp = ctypes.c_void_p, ctypes.c_int, ctypes.c_char_p
@@ -34,6 +37,9 @@ SIGNATURES = {
     "swin_wattn_bwd": ([_vp, _vp, _vp, _vp, _vp, _vp], _i),
     "swin_wattn_debug_maps": ([_vp, _vp, _vp, _vp, _vp, _vp], _i),
     "swin_wattn_bwd_noalloc": ([_vp, _vp, _vp, _vp, _vp] + [_i] * 8 + [_vp], _i),
+    "swin_wattn_set_fwd_kernel": ([_vp, _i], _i),
+    "swin_wattn_fwd_kernel": ([_vp], _i),
+    "swin_wattn_device_status": ([_vp, _vp], _i),
     "swin_wattn_destroy": ([_vp], _i),
     "swin_wattn_status_string": ([_i], _cp),
     "swin_wattn_last_error": ([], _cp),
@@ -109,6 +115,18 @@ def swin_wattn_bwd_noalloc(qkv_ptr, dout_ptr, dqkv_ptr, dtable_ptr, table_ptr, B
                                          W, C, num_heads, window, shift, dtype, stream)
 
 
+def swin_wattn_set_fwd_kernel(plan, kernel):
+    return load().swin_wattn_set_fwd_kernel(plan, kernel)
+
+
+def swin_wattn_fwd_kernel(plan):
+    return load().swin_wattn_fwd_kernel(plan)
+
+
+def swin_wattn_device_status(plan, stream):
+    return load().swin_wattn_device_status(plan, stream)
+
+
 def swin_wattn_destroy(plan):
     return load().swin_wattn_destroy(plan)
 
@@ -151,6 +169,22 @@ class WindowAttention:
         if rc != OK:
             raise SwinWAttnError("swin_wattn_plan", rc)
         self.handle = h
+
+    def set_fwd_kernel(self, kernel):
+        """KERNEL_AUTO, KERNEL_MMA_SYNC or KERNEL_TCGEN05 for later forwards."""
+        rc = swin_wattn_set_fwd_kernel(self.handle, kernel)
+        if rc != OK:
+            raise SwinWAttnError("swin_wattn_set_fwd_kernel", rc)
+
+    @property
+    def fwd_kernel(self):
+        return swin_wattn_fwd_kernel(self.handle)
+
+    def device_status(self, stream=None):
+        """Synchronise and raise if a bounded device wait ran out since the last check."""
+        rc = swin_wattn_device_status(self.handle, _stream_handle(stream))
+        if rc != OK:
+            raise SwinWAttnError("swin_wattn_device_status", rc)
 
     def set_bias(self, table, stream=None):
         rc = swin_wattn_set_bias(self.handle, table.data_ptr(), _stream_handle(stream))

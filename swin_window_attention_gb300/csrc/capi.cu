@@ -105,10 +105,12 @@ void free_plan_buffers(swin::Plan& p) {
   if (p.dt_partial) cudaFree(p.dt_partial);
   if (p.bias_frag) cudaFree(p.bias_frag);
   if (p.mask_frag) cudaFree(p.mask_frag);
+  if (p.err) cudaFree(p.err);
 
   p.dense_bias = p.mask = p.dt_partial = nullptr;
   p.bias_frag = nullptr;
   p.mask_frag = nullptr;
+  p.err = nullptr;
 }
 
 }  // namespace
@@ -181,6 +183,8 @@ int swin_wattn_plan(swin_wattn_plan_t* out, int B, int H, int W, int C, int num_
   if (e == cudaSuccess) e = cudaMalloc(&p.mask, sizeof(float) * nn * p.nW);
   if (e == cudaSuccess) e = cudaMalloc(&p.bias_frag, swin::bias_frag_bytes(p.M, p.nH));
   if (e == cudaSuccess && p.s > 0) e = cudaMalloc(&p.mask_frag, swin::mask_frag_bytes(p.M));
+  if (e == cudaSuccess) e = cudaMalloc(&p.err, sizeof(int));
+  if (e == cudaSuccess) e = cudaMemsetAsync(p.err, 0, sizeof(int), reinterpret_cast<cudaStream_t>(stream));
 
   if (e == cudaSuccess) e = swin::fwd_config(p, &pl->fwd);
   if (e == cudaSuccess) e = swin::bwd_config(p, &pl->bwd);
@@ -353,6 +357,51 @@ int swin_wattn_debug_maps(swin_wattn_plan_t plan, int32_t* gather, int32_t* reli
                         cudaMemcpyDeviceToDevice, st);
   }
   return e == cudaSuccess ? SWIN_WATTN_OK : cuda_fail(e, "swin_wattn_debug_maps");
+}
+
+int swin_wattn_set_fwd_kernel(swin_wattn_plan_t plan, int kernel) {
+  int rc = check_plan(plan);
+  if (rc != SWIN_WATTN_OK) return rc;
+  if (kernel != SWIN_WATTN_KERNEL_AUTO && kernel != SWIN_WATTN_KERNEL_MMA_SYNC &&
+      kernel != SWIN_WATTN_KERNEL_TCGEN05)
+    return SWIN_WATTN_ERR_INVALID_ARG;
+  swin::Plan& p = plan->p;
+  const int old = p.fwd_kernel;
+  p.fwd_kernel = kernel;
+  swin::FwdLaunch L;
+  cudaError_t e = swin::fwd_config(p, &L);
+  if (e == cudaErrorNotSupported) {
+    p.fwd_kernel = old;
+    return SWIN_WATTN_ERR_UNSUPPORTED;
+  }
+  if (e != cudaSuccess) {
+    p.fwd_kernel = old;
+    return cuda_fail(e, "swin_wattn_set_fwd_kernel");
+  }
+  plan->fwd = L;
+  return SWIN_WATTN_OK;
+}
+
+int swin_wattn_fwd_kernel(swin_wattn_plan_t plan) {
+  if (check_plan(plan) != SWIN_WATTN_OK) return -1;
+  return plan->fwd.tc ? SWIN_WATTN_KERNEL_TCGEN05 : SWIN_WATTN_KERNEL_MMA_SYNC;
+}
+
+int swin_wattn_device_status(swin_wattn_plan_t plan, struct CUstream_st* stream) {
+  int rc = check_plan(plan);
+  if (rc != SWIN_WATTN_OK) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int word = 0;
+  cudaError_t e = cudaMemcpyAsync(&word, plan->p.err, sizeof(int), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e == cudaSuccess && word != 0) e = cudaMemsetAsync(plan->p.err, 0, sizeof(int), st);
+  if (e == cudaSuccess && word != 0) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "swin_wattn_device_status");
+  if (word != 0) {
+    swin::set_last_error("a bounded device wait ran out (tensor-core completion never arrived)");
+    return SWIN_WATTN_ERR_TIMEOUT;
+  }
+  return SWIN_WATTN_OK;
 }
 
 int swin_wattn_destroy(swin_wattn_plan_t plan) {

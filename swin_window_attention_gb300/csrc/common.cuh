@@ -34,6 +34,11 @@ struct Plan {
   // Shift-mask B fragments of the three boundary window classes (see mask_v_word):
   // [3 classes][NTP / 4][32 lanes][4] uint32. Owned; null when s == 0.
   uint32_t* mask_frag;
+  // Device error word written by kernels with bounded waits (bit 0: a wait ran out).
+  // Owned.
+  int* err;
+  // Forward kernel request: SWIN_WATTN_KERNEL_AUTO, _MMA_SYNC or _TCGEN05.
+  int fwd_kernel;
 };
 
 // ---- geometry shared by every kernel that touches a window -----------------------
@@ -213,21 +218,25 @@ __device__ __forceinline__ uint32_t mask_u_frag(int r, int t, int M, int s) {
   return (((2 * t) & 3) == c ? kMaskUBits : 0u) | (((2 * t + 1) & 3) == c ? kMaskUBits << 16 : 0u);
 }
 
+// mism(c, j) in a window of boundary class cls: do key slot j and the slots of local
+// region c carry different region labels?
+__device__ __forceinline__ bool mask_mismatch(int cls, int c, int j, int H, int W, int M, int s) {
+  const int y0 = (cls & 2) ? (H / M - 1) * M : 0, x0 = (cls & 1) ? (W / M - 1) * M : 0;
+  const int lj = region_label(y0 + j / M, x0 + j % M, H, W, M, s);
+  const int lc = region_label(y0 + ((c & 2) ? M - 1 : 0), x0 + ((c & 1) ? M - 1 : 0), H, W, M, s);
+  return lc != lj;
+}
+
+// bf16 bit pattern of V[j][k] (k < 8) for class cls; zero for padded keys.
+__device__ __forceinline__ uint32_t mask_v_bits(int cls, int j, int k, int H, int W, int M, int s) {
+  if (j >= M * M || k >= 8 || !mask_mismatch(cls, k & 3, j, H, W, M, s)) return 0u;
+  return k < 4 ? kMaskPartHiBits : (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(kInvScale - kMaskPartHi));
+}
+
 // V fragment word (b0 of key tile nt: k-slots 2t, 2t+1 of key j = 8 nt + g) of class cls.
 __device__ __forceinline__ uint32_t mask_v_word(int cls, int lane, int nt, int H, int W, int M, int s) {
   const int j = nt * 8 + (lane >> 2), t = lane & 3;
-  if (j >= M * M) return 0u;
-  const int y0 = (cls & 2) ? (H / M - 1) * M : 0, x0 = (cls & 1) ? (W / M - 1) * M : 0;
-  const int lj = region_label(y0 + j / M, x0 + j % M, H, W, M, s);
-  const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(kInvScale - kMaskPartHi));
-  uint32_t word = 0u;
-#pragma unroll
-  for (int q = 0; q < 2; ++q) {
-    const int k = 2 * t + q, c = k & 3;
-    const int li = region_label(y0 + ((c & 2) ? M - 1 : 0), x0 + ((c & 1) ? M - 1 : 0), H, W, M, s);
-    if (li != lj) word |= (k < 4 ? kMaskPartHiBits : lo) << (16 * q);
-  }
-  return word;
+  return mask_v_bits(cls, j, 2 * t, H, W, M, s) | (mask_v_bits(cls, j, 2 * t + 1, H, W, M, s) << 16);
 }
 
 // Word e of the [3 classes][NTP / 4][32 lanes][4] mask fragment array.
@@ -264,6 +273,7 @@ __device__ __forceinline__ void load_chunk<float>(uint32_t dst, const float* src
 struct FwdLaunch {
   int grid = 0, threads = 0, smem = 0, chunks = 0;
   int ctas_per_sm = 0;
+  bool tc = false;  // the tcgen05 kernel (fwd_tc.cu) rather than the mma.sync one
 };
 struct BwdLaunch {
   int grid = 0, threads = 0, smem = 0, chunks = 0, partial_rows = 0;

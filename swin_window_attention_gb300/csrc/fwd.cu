@@ -401,16 +401,38 @@ template <> struct FwdStages<12> { static constexpr int value = 2; };
     }                                                                                   \
   } while (0)
 
-cudaError_t fwd_config(const Plan& pl, FwdLaunch* L) { SWIN_FWD_DISPATCH(config_t, pl, L); }
+static cudaError_t mma_config(const Plan& pl, FwdLaunch* L) { SWIN_FWD_DISPATCH(config_t, pl, L); }
+
+static cudaError_t mma_launch(const Plan& pl, const FwdLaunch& L, const void* qkv, void* out, int batch,
+                              cudaStream_t st) {
+  SWIN_FWD_DISPATCH(launch_t, pl, L, qkv, out, batch, st);
+}
+
+bool fwd_tc_applies(const Plan& pl);
+cudaError_t fwd_tc_config(const Plan& pl, FwdLaunch* L);
+cudaError_t fwd_tc_launch(const Plan& pl, const FwdLaunch& L, const void* qkv, void* out, int batch,
+                          cudaStream_t st);
+
+// Kernel choice: the tcgen05 kernel when the plan asks for it (7x7 windows, bf16), else
+// the mma.sync kernel (the default: the faster of the two as measured).
+cudaError_t fwd_config(const Plan& pl, FwdLaunch* L) {
+  *L = FwdLaunch();
+  if (pl.fwd_kernel == SWIN_WATTN_KERNEL_TCGEN05 && !fwd_tc_applies(pl)) return cudaErrorNotSupported;
+  if (pl.fwd_kernel == SWIN_WATTN_KERNEL_TCGEN05) {
+    L->tc = true;
+    return fwd_tc_config(pl, L);
+  }
+  return mma_config(pl, L);
+}
 
 cudaError_t fwd_launch(const Plan& pl, const FwdLaunch& L, const void* qkv, void* out,
                        cudaStream_t st) {
-  SWIN_FWD_DISPATCH(launch_t, pl, L, qkv, out, pl.B, st);
+  return L.tc ? fwd_tc_launch(pl, L, qkv, out, pl.B, st) : mma_launch(pl, L, qkv, out, pl.B, st);
 }
 
 cudaError_t fwd_launch_batch(const Plan& pl, const FwdLaunch& L, const void* qkv, void* out,
                              int batch, cudaStream_t st) {
-  SWIN_FWD_DISPATCH(launch_t, pl, L, qkv, out, batch, st);
+  return L.tc ? fwd_tc_launch(pl, L, qkv, out, batch, st) : mma_launch(pl, L, qkv, out, batch, st);
 }
 
 }  // namespace swin

@@ -1,0 +1,98 @@
+"""The two forward kernels (tcgen05 + tensor memory, and warp-level mma.sync) on the
+same inputs: each against the fp64 oracle, the kernel choice itself, and the tcgen05
+kernel's device status word after its bounded waits."""
+import pytest
+import torch
+
+import oracle
+from swin_window_attention_gb300 import capi, inputs
+from tests.gpu_util import assert_close, oracle_fwd, plan, workload
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    from swin_window_attention_gb300 import build
+    build.build()
+    oracle.build()
+    capi.load()
+
+
+KERNELS = [capi.KERNEL_TCGEN05, capi.KERNEL_MMA_SYNC]
+
+SMALL_M7 = [
+    # B, H, W, C, nH, s: windows per CTA range over 1 (a pair with one window), 2 and 3
+    (1, 7, 7, 64, 2, 3),
+    (1, 14, 21, 64, 2, 3),
+    (2, 14, 14, 96, 3, 3),
+    (3, 21, 28, 64, 2, 3),
+    (2, 14, 14, 96, 3, 0),
+    (2, 7, 7, 64, 2, 6),
+    (5, 7, 7, 1536, 48, 0),
+    (4, 56, 56, 192, 6, 3),
+    (3, 28, 35, 128, 4, 5),
+]
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("B,H,W,C,nH,s", SMALL_M7)
+def test_fwd_kernel_against_oracle(kernel, B, H, W, C, nH, s):
+    wl = workload(B, H, W, C, nH, 7, s, "bf16", seed=11 * B + H + W + s)
+    qkv, table = inputs.make_qkv(wl), inputs.make_table(wl)
+    att = plan(wl, table.to(DEV))
+    att.set_fwd_kernel(kernel)
+    assert att.fwd_kernel == kernel
+    y = att.fwd(qkv.to(DEV))
+    att.device_status()
+    assert_close("Y", y, oracle_fwd(qkv, table, wl))
+    att.close()
+
+
+@pytest.mark.parametrize("name", [w.name for w in inputs.WORKLOADS if w.M == 7 and w.dtype == "bf16"])
+def test_fwd_kernels_agree_on_workloads(name):
+    """Full-size workloads: the tcgen05 kernel against the oracle on sampled images and
+    against the mma.sync kernel everywhere (both within the tolerance of the oracle)."""
+    wl = inputs.BY_NAME[name]
+    qkv, table = inputs.make_qkv(wl), inputs.make_table(wl)
+    att = plan(wl, table.to(DEV))
+    att.set_fwd_kernel(capi.KERNEL_TCGEN05)
+    q = qkv.to(DEV)
+    y_tc = att.fwd(q)
+    att.device_status()
+    att.set_fwd_kernel(capi.KERNEL_MMA_SYNC)
+    y_mma = att.fwd(q)
+    torch.cuda.synchronize()
+    att.close()
+    sample = sorted({0, wl.B // 2, wl.B - 1})
+    assert_close(f"{name} Y tcgen05", y_tc.cpu()[sample], oracle_fwd(qkv, table, wl, batches=sample))
+    d = (y_tc.float() - y_mma.float()).abs().max().item()
+    assert d <= 2e-2, f"kernels differ by {d}"
+
+
+def test_tcgen05_kernel_is_deterministic():
+    wl = inputs.BY_NAME["swin_l224_s2"]
+    qkv, table = inputs.make_qkv(wl), inputs.make_table(wl)
+    att = plan(wl, table.to(DEV))
+    att.set_fwd_kernel(capi.KERNEL_TCGEN05)
+    q = qkv.to(DEV)
+    a, b = att.fwd(q), att.fwd(q)
+    att.device_status()
+    assert torch.equal(a, b)
+    att.close()
+
+
+@pytest.mark.parametrize("M,dt", [(4, "bf16"), (12, "bf16"), (7, "fp32")])
+def test_tcgen05_kernel_refused_where_it_does_not_apply(M, dt):
+    wl = workload(1, 2 * M, 2 * M, 64, 2, M, 1, dt)
+    table = inputs.make_table(wl)
+    att = plan(wl, table.to(DEV))
+    assert att.fwd_kernel == capi.KERNEL_MMA_SYNC
+    rc = capi.swin_wattn_set_fwd_kernel(att.handle, capi.KERNEL_TCGEN05)
+    assert rc == capi.ERR_UNSUPPORTED
+    assert att.fwd_kernel == capi.KERNEL_MMA_SYNC
+    assert capi.swin_wattn_set_fwd_kernel(att.handle, 7) == capi.ERR_INVALID_ARG
+    att.close()
