@@ -232,10 +232,7 @@ def run_gpu(args):
         for wl in sweep:
             q = inputs.make_qkv(wl)
             tab = inputs.make_table(wl).to(dev)
-            rc, h = capi.swin_wattn_plan(wl.B, wl.H, wl.W, wl.C, wl.nH, wl.M, wl.s, capi.BF16,
-                                         tab.data_ptr(), sh)
-            if rc != capi.OK:
-                raise capi.SwinWAttnError("swin_wattn_plan", rc)
+            h = make_plan(capi, wl, tab, sh, args)
             plans.append(h)
             qkvs.append(q.to(dev))
             outs.append(torch.empty(wl.B, wl.H, wl.W, wl.C, dtype=torch.bfloat16, device=dev))
@@ -328,7 +325,7 @@ def run_gpu(args):
     khash = kernel_source_hash()
     roofline = {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s",
                 "frac": round(ach / hbm, 4), "traffic": ncu_traffic(khash) if kdom == 0 else None,
-                "kernel": f"fwd_kernel<7,bf16> on {wdom.name}",
+                "kernel": f"{kernel_name(capi, plans[kdom])} on {wdom.name}",
                 "bytes_per_launch": fwd_bytes(wdom), "peak_source": peak_src + " hbm_gbs",
                 "kernel_source_hash": khash}
 
@@ -380,7 +377,8 @@ def run_gpu(args):
                        "l2": f"step working set {sweep_bytes / 1e6:.0f} MB > 129 MB L2 "
                              "(stages run in turn; each stage's inputs are evicted by the "
                              "others' before they are read again); no flush",
-                       "parallelism": f"dp{ws} (independent batch shards, no collective)"},
+                       "parallelism": f"dp{ws} (independent batch shards, no collective)",
+                       "fwd_kernel": kernel_name(capi, plans[0])},
             "roofline": roofline,
             "sweep": {"us": round(sweep_ms * 1e3, 2),
                       "GBps": round(sweep_bytes / (sweep_ms / 1e3) / 1e9, 1),
@@ -414,10 +412,7 @@ def run_fwd_sweep(names, args, dev, stream, lib, capi, hbm, ws):
     with torch.cuda.stream(stream):
         for wl in wls:
             tab = inputs.make_table(wl).to(dev)
-            rc, h = capi.swin_wattn_plan(wl.B, wl.H, wl.W, wl.C, wl.nH, wl.M, wl.s, capi.BF16,
-                                         tab.data_ptr(), sh)
-            if rc != capi.OK:
-                raise capi.SwinWAttnError("swin_wattn_plan", rc)
+            h = make_plan(capi, wl, tab, sh, args)
             q = inputs.make_qkv(wl).to(dev)
             st.append(dict(wl=wl, h=h, q=q, o=torch.empty(wl.B, wl.H, wl.W, wl.C,
                                                          dtype=torch.bfloat16, device=dev)))
@@ -455,10 +450,7 @@ def run_train_step(args, dev, stream, lib, capi, hbm, ws):
     with torch.cuda.stream(stream):
         for wl in wls:
             tab = inputs.make_table(wl).to(dev)
-            rc, h = capi.swin_wattn_plan(wl.B, wl.H, wl.W, wl.C, wl.nH, wl.M, wl.s, capi.BF16,
-                                         tab.data_ptr(), sh)
-            if rc != capi.OK:
-                raise capi.SwinWAttnError("swin_wattn_plan", rc)
+            h = make_plan(capi, wl, tab, sh, args)
             q = inputs.make_qkv(wl).to(dev)
             d = inputs.make_dout(wl).to(dev)
             st.append(dict(wl=wl, h=h, tab=tab, q=q, d=d, o=torch.empty_like(d),
@@ -517,6 +509,29 @@ def run_train_step(args, dev, stream, lib, capi, hbm, ws):
                         + (", table-gradient all-reduce" if ws > 1 else "") + ")",
             "steps": steps, "ms_per_step": ms, "tokens_per_s": ws * tokens / (ms / 1e3),
             "stages": stages}
+
+
+FWD_KERNELS = {"auto": 0, "mma_sync": 1, "tcgen05": 2}
+
+
+def kernel_name(capi, h):
+    """The forward kernel a plan launches, as named in the library's sources."""
+    return ("fwd_tc_kernel (tcgen05)" if capi.swin_wattn_fwd_kernel(h) == capi.KERNEL_TCGEN05
+            else "fwd_kernel<7,bf16,3> (mma.sync)")
+
+
+def make_plan(capi, wl, tab, sh, args):
+    """A bf16 plan for the workload, with the forward kernel --fwd-kernel asks for."""
+    rc, h = capi.swin_wattn_plan(wl.B, wl.H, wl.W, wl.C, wl.nH, wl.M, wl.s, capi.BF16,
+                                 tab.data_ptr(), sh)
+    if rc != capi.OK:
+        raise capi.SwinWAttnError("swin_wattn_plan", rc)
+    kernel = FWD_KERNELS[args.fwd_kernel]
+    if kernel != 0:
+        rc = capi.swin_wattn_set_fwd_kernel(h, kernel)
+        if rc != capi.OK:
+            raise capi.SwinWAttnError("swin_wattn_set_fwd_kernel", rc)
+    return h
 
 
 def run_bwd_only(args):
@@ -596,6 +611,8 @@ def main():
                          "(profiling runs)")
     ap.add_argument("--bwd-workload", choices=sorted(n for n, w in inputs.BY_NAME.items() if w.bwd),
                     help="profiling run: only the backward of this workload, a few launches")
+    ap.add_argument("--fwd-kernel", default="auto", choices=sorted(FWD_KERNELS),
+                    help="forward kernel of every plan (auto: the library's default)")
     ap.add_argument("--skip-train", action="store_true")
     ap.add_argument("--skip-cpu-baseline", action="store_true")
     args = ap.parse_args()

@@ -15,6 +15,8 @@ cudaError_t launch_build_mask(int H, int W, int M, int s, float* mask, cudaStrea
 cudaError_t launch_gather_map(int H, int W, int M, int s, int32_t* out, cudaStream_t st);
 cudaError_t launch_relidx(int M, int32_t* out, cudaStream_t st);
 cudaError_t launch_fragments(const Plan& p, cudaStream_t st);
+size_t tc_tables_bytes(const Plan& pl);
+cudaError_t launch_tc_tables(const Plan& pl, cudaStream_t st);
 size_t bias_frag_bytes(int M, int nH);
 size_t mask_frag_bytes(int M);
 cudaError_t fwd_config(const Plan& pl, FwdLaunch* L);
@@ -106,11 +108,13 @@ void free_plan_buffers(swin::Plan& p) {
   if (p.bias_frag) cudaFree(p.bias_frag);
   if (p.mask_frag) cudaFree(p.mask_frag);
   if (p.err) cudaFree(p.err);
+  if (p.tc_tables) cudaFree(p.tc_tables);
 
   p.dense_bias = p.mask = p.dt_partial = nullptr;
   p.bias_frag = nullptr;
   p.mask_frag = nullptr;
   p.err = nullptr;
+  p.tc_tables = nullptr;
 }
 
 }  // namespace
@@ -184,6 +188,7 @@ int swin_wattn_plan(swin_wattn_plan_t* out, int B, int H, int W, int C, int num_
   if (e == cudaSuccess) e = cudaMalloc(&p.bias_frag, swin::bias_frag_bytes(p.M, p.nH));
   if (e == cudaSuccess && p.s > 0) e = cudaMalloc(&p.mask_frag, swin::mask_frag_bytes(p.M));
   if (e == cudaSuccess) e = cudaMalloc(&p.err, sizeof(int));
+  if (e == cudaSuccess && swin::tc_tables_bytes(p) > 0) e = cudaMalloc(&p.tc_tables, swin::tc_tables_bytes(p));
   if (e == cudaSuccess) e = cudaMemsetAsync(p.err, 0, sizeof(int), reinterpret_cast<cudaStream_t>(stream));
 
   if (e == cudaSuccess) e = swin::fwd_config(p, &pl->fwd);
@@ -204,6 +209,10 @@ int swin_wattn_plan(swin_wattn_plan_t* out, int B, int H, int W, int C, int num_
   }
   if (e == cudaSuccess) {
     e = swin::launch_fragments(p, st);
+    ++g_launches;
+  }
+  if (e == cudaSuccess && p.tc_tables != nullptr) {
+    e = swin::launch_tc_tables(p, st);
     ++g_launches;
   }
   if (e != cudaSuccess) {
@@ -233,6 +242,10 @@ int swin_wattn_set_bias(swin_wattn_plan_t plan, const float* bias_table,
   ++g_launches;
   if (e == cudaSuccess) {
     e = swin::launch_fragments(p, st);
+    ++g_launches;
+  }
+  if (e == cudaSuccess && p.tc_tables != nullptr) {
+    e = swin::launch_tc_tables(p, st);
     ++g_launches;
   }
   return e == cudaSuccess ? SWIN_WATTN_OK : cuda_fail(e, "swin_wattn_set_bias");

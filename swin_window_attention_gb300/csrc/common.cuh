@@ -34,6 +34,9 @@ struct Plan {
   // Shift-mask B fragments of the three boundary window classes (see mask_v_word):
   // [3 classes][NTP / 4][32 lanes][4] uint32. Owned; null when s == 0.
   uint32_t* mask_frag;
+  // Constant operands of the tcgen05 forward (7x7 windows): mask U, class V and the bias
+  // image per head. Owned; null for other window sizes.
+  unsigned char* tc_tables;
   // Device error word written by kernels with bounded waits (bit 0: a wait ran out).
   // Owned.
   int* err;

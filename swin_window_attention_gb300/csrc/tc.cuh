@@ -8,16 +8,21 @@
 namespace swin {
 namespace tc {
 
-// ---- shared-memory matrix descriptor (no swizzle) ----------------------------------
+// ---- shared-memory matrix descriptor ------------------------------------------------
 //
-// A tile of bf16 elements in 8-row x 16-byte core matrices (each core matrix 128
-// contiguous bytes, row r at +16 r). `lbo` is the byte stride between core matrices
-// adjacent along K, `sbo` the stride between core matrices adjacent along M (or N).
 // Bits: [0,14) address >> 4, [16,30) lbo >> 4, [32,46) sbo >> 4, [46,48) version 1,
-// swizzle mode 0 in [61,64).
-__device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+// [61,64) layout: 0 = no swizzle, 4 = 64-byte swizzle.
+// * No swizzle: bf16 elements in 8-row x 16-byte core matrices (128 contiguous bytes, row
+//   r at +16 r); `lbo` is the byte stride between core matrices adjacent along K, `sbo`
+//   along M (or N).
+// * 64-byte swizzle: 64-byte rows, 8-row atoms of 512 bytes with 16-byte chunk c of row r
+//   at chunk c ^ ((r >> 1) & 3) (the layout the copy engine writes with its 64-byte
+//   swizzle). K-major: `sbo` is the stride between 8-row atoms, and a K step inside the
+//   64-byte row advances the start address. MN-major: `lbo` is the stride between atoms
+//   along M/N (32 elements each), `sbo` the stride between 8-row atoms along K.
+__device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t sbo, uint32_t layout = 0) {
   return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
-         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | ((uint64_t)1 << 46);
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | ((uint64_t)1 << 46) | ((uint64_t)layout << 61);
 }
 
 // Instruction descriptor of kind::f16 with bf16 A and B and an fp32 accumulator:
@@ -146,6 +151,22 @@ __device__ __forceinline__ void ld33_wait(uint32_t taddr, uint32_t (&a)[32], uin
         "=r"(a[24]), "=r"(a[25]), "=r"(a[26]), "=r"(a[27]), "=r"(a[28]), "=r"(a[29]), "=r"(a[30]), "=r"(a[31]),
         "=r"(c)
       : "r"(taddr), "r"(taddr + 32)
+      : "memory");
+}
+
+// 32 columns at `a` and one column at `c` of this thread's lane.
+__device__ __forceinline__ void ld32_1_wait(uint32_t a_addr, uint32_t c_addr, uint32_t (&a)[32], uint32_t& c) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%33];\n"
+      "tcgen05.ld.sync.aligned.32x32b.x1.b32 {%32}, [%34];\n"
+      "tcgen05.wait::ld.sync.aligned;\n"
+      : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3]), "=r"(a[4]), "=r"(a[5]), "=r"(a[6]), "=r"(a[7]),
+        "=r"(a[8]), "=r"(a[9]), "=r"(a[10]), "=r"(a[11]), "=r"(a[12]), "=r"(a[13]), "=r"(a[14]), "=r"(a[15]),
+        "=r"(a[16]), "=r"(a[17]), "=r"(a[18]), "=r"(a[19]), "=r"(a[20]), "=r"(a[21]), "=r"(a[22]), "=r"(a[23]),
+        "=r"(a[24]), "=r"(a[25]), "=r"(a[26]), "=r"(a[27]), "=r"(a[28]), "=r"(a[29]), "=r"(a[30]), "=r"(a[31]),
+        "=r"(c)
+      : "r"(a_addr), "r"(c_addr)
       : "memory");
 }
 
