@@ -276,7 +276,8 @@ __device__ __forceinline__ void load_chunk<float>(uint32_t dst, const float* src
 struct FwdLaunch {
   int grid = 0, threads = 0, smem = 0, chunks = 0;
   int ctas_per_sm = 0;
-  bool tc = false;  // the tcgen05 kernel (fwd_tc.cu) rather than the mma.sync one
+  bool tc = false;   // the tcgen05 kernel (fwd_tc.cu) rather than the mma.sync one
+  bool tma = false;  // mma.sync kernel: tiles by the copy engine (7x7 windows, bf16)
 };
 struct BwdLaunch {
   int grid = 0, threads = 0, smem = 0, chunks = 0, partial_rows = 0;

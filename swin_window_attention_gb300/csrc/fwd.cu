@@ -17,7 +17,10 @@
 // [16w, 16w+16): S = Q K^T on bf16 tensor cores (m16n8k16, fp32 accumulate), fused
 // scale + bias + mask, a register softmax with quad shuffles, P (bf16) V, and the
 // normalised rows go back to the token positions they were read from.
+#include <cstring>
+
 #include "common.cuh"
+#include "tc.cuh"
 
 namespace swin {
 
@@ -30,22 +33,35 @@ struct FwdParams {
   int64_t total_windows;  // B * nW
   int chunks;             // window ranges per head
   float qk_scale_log2;    // hd^-0.5 * log2(e)
+  int* err;               // plan error word (bit 0: a bounded wait ran out)
 };
 
-template <int M, typename TIO, int STAGES>
+// With TMA loads the tiles sit on 1024-byte boundaries (the copy engine's 64-byte swizzle
+// is a function of the address; the tile layout is that swizzle), followed by one
+// mbarrier per stage.
+template <int M, typename TIO, int STAGES, bool TMA>
 constexpr int fwd_smem_bytes() {
-  return Geo<M>::BIAS_BYTES + Geo<M>::MASK_BYTES + STAGES * Geo<M>::STAGE_BYTES;
+  return Geo<M>::BIAS_BYTES + Geo<M>::MASK_BYTES + STAGES * Geo<M>::STAGE_BYTES + (TMA ? 1024 + 8 * STAGES : 0);
 }
 
 // Resident CTAs per SM the register budget is sized for.
 template <int M> struct FwdMinBlocks { static constexpr int value = 4; };
 template <> struct FwdMinBlocks<12> { static constexpr int value = 1; };
 
-template <int M, typename TIO, int STAGES>
-__global__ void __launch_bounds__(Geo<M>::THREADS, FwdMinBlocks<M>::value) fwd_kernel(const FwdParams p) {
+// Tiles come either from 16-byte cp.async gathers by every thread, or (TMA, 7x7 windows,
+// bf16) from the copy engine: one 7 x 7-token box per tensor for a window that does not
+// wrap around the image border, two row bands for one that wraps at the bottom only, and
+// the cp.async gather for the last window column of a shifted layer; a stage's mbarrier
+// then counts every thread's cp.async arrival plus the copy engine's bytes.
+template <int M, typename TIO, int STAGES, bool TMA>
+__global__ void __launch_bounds__(Geo<M>::THREADS, FwdMinBlocks<M>::value)
+    fwd_kernel(const __grid_constant__ CUtensorMap box_map, const __grid_constant__ CUtensorMap top_map,
+               const __grid_constant__ CUtensorMap bot_map, const FwdParams p) {
   using G = Geo<M>;
   constexpr int N = G::N, NT = G::NT, KT = G::KT, THREADS = G::THREADS;
-  extern __shared__ __align__(128) unsigned char smem[];
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* smem = TMA ? smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u) : smem_raw;
+  const uint32_t bar0 = smem_u32(smem) + G::BIAS_BYTES + G::MASK_BYTES + STAGES * G::STAGE_BYTES;
   float4* sbias = reinterpret_cast<float4*>(smem);
   uint32_t* smask = reinterpret_cast<uint32_t*>(smem + G::BIAS_BYTES);
   unsigned char* stiles = smem + G::BIAS_BYTES + G::MASK_BYTES;
@@ -85,10 +101,46 @@ __global__ void __launch_bounds__(Geo<M>::THREADS, FwdMinBlocks<M>::value) fwd_k
   int cb = lb, cwy = lwy, cwx = lwx;  // cursor of the window being computed
   const uint32_t tiles_u32 = smem_u32(stiles);
 
-  auto issue = [&](uint32_t stage_off) {
+  auto issue = [&](uint32_t stage_off, int stage) {
     const uint32_t base = tiles_u32 + stage_off;
     const int y0 = lwy * M + s, x0 = lwx * M + s;
     const int hy = H - y0, hx = W - x0;  // window rows ly >= hy / columns lx >= hx wrap
+    if constexpr (TMA) {
+      const uint32_t full = bar0 + 8 * stage;
+      // 0: one box per tensor; 1: two row bands (wraps at the bottom only, and the second
+      // band starts on a 128-byte boundary); 2: cp.async gather (wraps at the right)
+      const int kind = hx >= M ? (hy >= M ? 0 : (((M - s) & 1) == 0 ? 1 : 2)) : 2;
+      if (kind < 2) {
+        if (tid == 0) {
+          tc::fence_proxy_async();  // the stage's previous reads before the copy engine's writes
+          tc::mbar_expect_tx(full, 3 * N * 64);
+          const int cq = h * kHeadDim, ck = p.C + cq, cv = 2 * p.C + cq;
+          if (kind == 0) {
+            tc::box_load(base, &box_map, cq, x0, y0, lb, full);
+            tc::box_load(base + G::TILE_BYTES, &box_map, ck, x0, y0, lb, full);
+            tc::box_load(base + 2 * G::TILE_BYTES, &box_map, cv, x0, y0, lb, full);
+          } else {
+            const uint32_t bot = base + (M - s) * M * 64;
+            tc::box_load(base, &top_map, cq, x0, y0, lb, full);
+            tc::box_load(base + G::TILE_BYTES, &top_map, ck, x0, y0, lb, full);
+            tc::box_load(base + 2 * G::TILE_BYTES, &top_map, cv, x0, y0, lb, full);
+            tc::box_load(bot, &bot_map, cq, x0, 0, lb, full);
+            tc::box_load(bot + G::TILE_BYTES, &bot_map, ck, x0, 0, lb, full);
+            tc::box_load(bot + 2 * G::TILE_BYTES, &bot_map, cv, x0, 0, lb, full);
+          }
+        }
+        tc::cp_async_arrive(full);
+        if (++lwx == p.nWx) {
+          lwx = 0;
+          if (++lwy == p.nWy) {
+            lwy = 0;
+            ++lb;
+          }
+        }
+        return;
+      }
+      if (tid == 0) tc::mbar_expect_tx(full, 0);
+    }
     const TIO* wbase = qkv + (((int64_t)lb * H + y0) * W + x0) * C3;
 #pragma unroll
     for (int j = 0; j < TI; ++j) {
@@ -103,6 +155,7 @@ __global__ void __launch_bounds__(Geo<M>::THREADS, FwdMinBlocks<M>::value) fwd_k
           load_chunk<TIO>(base + tt * G::TILE_BYTES + ld_soff[j], src + tt * p.C);
       }
     }
+    if constexpr (TMA) tc::cp_async_arrive(bar0 + 8 * stage);
     if (++lwx == p.nWx) {
       lwx = 0;
       if (++lwy == p.nWy) {
@@ -123,10 +176,17 @@ __global__ void __launch_bounds__(Geo<M>::THREADS, FwdMinBlocks<M>::value) fwd_k
         cp_async_16(smem_u32(smem + G::BIAS_BYTES + e * 16), msrc + e * 16);
     }
   }
+  if constexpr (TMA) {
+    if (tid == 0) {
+      for (int st = 0; st < STAGES; ++st) tc::mbar_init(bar0 + 8 * st, THREADS + 1);
+      tc::mbar_init_fence();
+    }
+    __syncthreads();
+  }
 #pragma unroll
   for (int st = 0; st < STAGES - 1; ++st) {
-    if (st < nwin) issue(st * G::STAGE_BYTES);
-    cp_async_commit();
+    if (st < nwin) issue(st * G::STAGE_BYTES, st);
+    if constexpr (!TMA) cp_async_commit();
   }
 
   // Padded rows N..NPAD-1 of every q/k/v tile are zero (loads never touch them).
@@ -161,11 +221,24 @@ __global__ void __launch_bounds__(Geo<M>::THREADS, FwdMinBlocks<M>::value) fwd_k
   const uint32_t st_off1 = tile_off(warp * 16 + r8 + ((mi & 1) << 3), 2 + (mi >> 1));
 
   uint32_t cur_off = 0, nxt_off = (STAGES - 1) * G::STAGE_BYTES;
+  int cur_st = 0, nxt_st = STAGES - 1, bad = 0;
   for (int it = 0; it < nwin; ++it) {
-    cp_async_wait<STAGES - 2>();
-    __syncthreads();
-    if (it + STAGES - 1 < nwin) issue(nxt_off);
-    cp_async_commit();
+    if constexpr (TMA) {
+      // the window's tiles: every thread's cp.async and the copy engine's bytes (bounded)
+      const bool ok = tc::mbar_wait(bar0 + 8 * cur_st, (it / STAGES) & 1, 1000000000ull);
+      if (__syncthreads_or(ok ? 0 : 1)) {
+        bad = 1;
+        break;
+      }
+      if (it + STAGES - 1 < nwin) issue(nxt_off, nxt_st);
+    } else {
+      cp_async_wait<STAGES - 2>();
+      __syncthreads();
+      if (it + STAGES - 1 < nwin) issue(nxt_off, nxt_st);
+      cp_async_commit();
+    }
+    cur_st = cur_st + 1 == STAGES ? 0 : cur_st + 1;
+    nxt_st = nxt_st + 1 == STAGES ? 0 : nxt_st + 1;
     nxt_off = nxt_off + G::STAGE_BYTES == STAGES * G::STAGE_BYTES ? 0 : nxt_off + G::STAGE_BYTES;
     const int b = cb, wy = cwy, wx = cwx;
     if (++cwx == p.nWx) {
@@ -316,16 +389,19 @@ __global__ void __launch_bounds__(Geo<M>::THREADS, FwdMinBlocks<M>::value) fwd_k
     }
   }
   cp_async_wait<0>();
+  if (bad && tid == 0) atomicOr(p.err, 1);
 }
 
 // ---- host side ---------------------------------------------------------------------
 
-template <int M, typename TIO, int STAGES>
+template <int M, typename TIO, int STAGES, bool TMA>
 static cudaError_t config_t(const Plan& pl, FwdLaunch* L) {
   using G = Geo<M>;
-  constexpr int smem = fwd_smem_bytes<M, TIO, STAGES>();
-  auto kern = fwd_kernel<M, TIO, STAGES>;
+  constexpr int smem = fwd_smem_bytes<M, TIO, STAGES, TMA>();
+  auto kern = fwd_kernel<M, TIO, STAGES, TMA>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
   int occ = 0;
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, G::THREADS, smem);
@@ -341,12 +417,13 @@ static cudaError_t config_t(const Plan& pl, FwdLaunch* L) {
   L->threads = G::THREADS;
   L->smem = smem;
   L->ctas_per_sm = occ;
+  L->tma = TMA;
   return cudaSuccess;
 }
 
 // Forward over `batch` images starting at the given pointers (batch <= the plan's B): one
 // wave of CTAs sized as in config_t for that many windows.
-template <int M, typename TIO, int STAGES>
+template <int M, typename TIO, int STAGES, bool TMA>
 static cudaError_t launch_t(const Plan& pl, const FwdLaunch& L0, const void* qkv, void* out,
                             int batch, cudaStream_t st) {
   FwdLaunch L = L0;
@@ -357,6 +434,14 @@ static cudaError_t launch_t(const Plan& pl, const FwdLaunch& L0, const void* qkv
     if (chunks > total) chunks = total;
     L.chunks = (int)chunks;
     L.grid = (int)(chunks * pl.nH);
+  }
+  CUtensorMap gather_map, box_map, top_map, bot_map;
+  if constexpr (TMA) {
+    cudaError_t e = make_qkv_maps(pl, qkv, batch, &gather_map, &box_map, &top_map, &bot_map);
+    if (e != cudaSuccess) return e;
+  } else {
+    memset(&box_map, 0, sizeof(box_map));
+    top_map = bot_map = box_map;
   }
   FwdParams p;
   p.qkv = qkv;
@@ -374,7 +459,8 @@ static cudaError_t launch_t(const Plan& pl, const FwdLaunch& L0, const void* qkv
   p.total_windows = (int64_t)batch * pl.nW;
   p.chunks = L.chunks;
   p.qk_scale_log2 = kLog2e / kInvScale;
-  fwd_kernel<M, TIO, STAGES><<<L.grid, L.threads, L.smem, st>>>(p);
+  p.err = pl.err;
+  fwd_kernel<M, TIO, STAGES, TMA><<<L.grid, L.threads, L.smem, st>>>(box_map, top_map, bot_map, p);
   return cudaGetLastError();
 }
 
@@ -383,28 +469,39 @@ static cudaError_t launch_t(const Plan& pl, const FwdLaunch& L0, const void* qkv
 template <int M> struct FwdStages { static constexpr int value = 3; };
 template <> struct FwdStages<12> { static constexpr int value = 2; };
 
+// The copy engine feeds 7x7 bf16 windows (its boxes are 7 x 7 tokens; tokens are
+// addressed by 32-bit coordinates).
+static bool fwd_tma_applies(const Plan& pl) {
+  return pl.M == 7 && pl.dtype == SWIN_WATTN_BF16 && (int64_t)pl.B * pl.H * pl.W < ((int64_t)1 << 31);
+}
+
 #define SWIN_FWD_DISPATCH(FN, ...)                                                       \
   do {                                                                                  \
     const bool f32 = pl.dtype == SWIN_WATTN_FP32;                                       \
     switch (pl.M) {                                                                     \
       case 4:                                                                           \
-        return f32 ? FN<4, float, FwdStages<4>::value>(__VA_ARGS__)                      \
-                   : FN<4, __nv_bfloat16, FwdStages<4>::value>(__VA_ARGS__);             \
+        return f32 ? FN<4, float, FwdStages<4>::value, false>(__VA_ARGS__)               \
+                   : FN<4, __nv_bfloat16, FwdStages<4>::value, false>(__VA_ARGS__);      \
       case 7:                                                                           \
-        return f32 ? FN<7, float, FwdStages<7>::value>(__VA_ARGS__)                      \
-                   : FN<7, __nv_bfloat16, FwdStages<7>::value>(__VA_ARGS__);             \
+        if (f32) return FN<7, float, FwdStages<7>::value, false>(__VA_ARGS__);           \
+        return tma ? FN<7, __nv_bfloat16, FwdStages<7>::value, true>(__VA_ARGS__)        \
+                   : FN<7, __nv_bfloat16, FwdStages<7>::value, false>(__VA_ARGS__);      \
       case 12:                                                                          \
-        return f32 ? FN<12, float, FwdStages<12>::value>(__VA_ARGS__)                    \
-                   : FN<12, __nv_bfloat16, FwdStages<12>::value>(__VA_ARGS__);           \
+        return f32 ? FN<12, float, FwdStages<12>::value, false>(__VA_ARGS__)             \
+                   : FN<12, __nv_bfloat16, FwdStages<12>::value, false>(__VA_ARGS__);    \
       default:                                                                          \
         return cudaErrorInvalidValue;                                                   \
     }                                                                                   \
   } while (0)
 
-static cudaError_t mma_config(const Plan& pl, FwdLaunch* L) { SWIN_FWD_DISPATCH(config_t, pl, L); }
+static cudaError_t mma_config(const Plan& pl, FwdLaunch* L) {
+  const bool tma = fwd_tma_applies(pl);
+  SWIN_FWD_DISPATCH(config_t, pl, L);
+}
 
 static cudaError_t mma_launch(const Plan& pl, const FwdLaunch& L, const void* qkv, void* out, int batch,
                               cudaStream_t st) {
+  const bool tma = L.tma;
   SWIN_FWD_DISPATCH(launch_t, pl, L, qkv, out, batch, st);
 }
 

@@ -48,7 +48,6 @@ namespace {
 
 constexpr int kTM = 7, kTN = 49;
 constexpr int kGROUPS = (kTN + 3) / 4;         // gather4 row groups per window tile (13)
-constexpr int kROW_THREADS = 128;              // warps 0..3
 constexpr int kMMA_WARP = 4, kPROD_WARP = 5;
 constexpr int kTHREADS = 6 * 32;
 constexpr int kROW_BYTES = 64;                 // one token's 32 bf16 head channels
@@ -86,38 +85,6 @@ __device__ __forceinline__ uint32_t k16_off(int r, int k) {
   return (r >> 3) * 256 + (k >> 3) * 128 + (r & 7) * 16 + (k & 7) * 2;
 }
 
-__device__ __forceinline__ void mbar_arrive(uint32_t mbar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(mbar) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t mbar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(mbar), "r"(bytes) : "memory");
-}
-// Four tokens' 64-byte slices (rows r0..r3 of the [tokens, 3C] tensor map, columns col..col+31)
-// to four consecutive 64-byte rows of shared memory, completing on `mbar`.
-__device__ __forceinline__ void gather4(uint32_t dst, const CUtensorMap* map, int col, int r0, int r1, int r2, int r3,
-                                        uint32_t mbar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];\n" ::"r"(dst),
-      "l"(map), "r"(col), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(mbar)
-      : "memory");
-}
-// One window's 7 x 7 tokens (32 channels each) from the [B, H, W, 3C] tensor map to 49
-// consecutive 64-byte rows of shared memory (slot order ly * 7 + lx), completing on `mbar`.
-__device__ __forceinline__ void box_load(uint32_t dst, const CUtensorMap* map, int col, int x, int y, int b,
-                                         uint32_t mbar) {
-  asm volatile(
-      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4, %5}], [%6];\n" ::"r"(dst),
-      "l"(map), "r"(col), "r"(x), "r"(y), "r"(b), "r"(mbar)
-      : "memory");
-}
-// Contiguous global -> shared bulk copy (16-byte aligned, size a multiple of 16).
-__device__ __forceinline__ void bulk_copy(uint32_t dst, const void* src, uint32_t bytes, uint32_t mbar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(dst),
-               "l"(src), "r"(bytes), "r"(mbar)
-               : "memory");
-}
 // A bounded wait whose outcome is the same for the whole warp.
 __device__ __forceinline__ bool warp_wait(uint32_t mbar, uint32_t parity) {
   return __all_sync(0xffffffffu, tc::mbar_wait(mbar, parity, kWaitLimitNs)) != 0;
@@ -215,9 +182,9 @@ __global__ void __launch_bounds__(kTHREADS, 1) fwd_tc_kernel(const __grid_consta
     // ==== producer: TMA gathers of pair n into stage n % kSTAGES =======================
     if (lane == 0) {
       // this plan's mask operands and this head's bias image
-      mbar_expect_tx(const_bar, kMASK_BYTES + kBIAS_BYTES);
-      bulk_copy(smem0 + kOFF_U, p.tables, kMASK_BYTES, const_bar);
-      bulk_copy(smem0 + kOFF_BIAS, p.tables + kMASK_BYTES + (size_t)h * kBIAS_BYTES, kBIAS_BYTES, const_bar);
+      tc::mbar_expect_tx(const_bar, kMASK_BYTES + kBIAS_BYTES);
+      tc::bulk_copy(smem0 + kOFF_U, p.tables, kMASK_BYTES, const_bar);
+      tc::bulk_copy(smem0 + kOFF_BIAS, p.tables + kMASK_BYTES + (size_t)h * kBIAS_BYTES, kBIAS_BYTES, const_bar);
     }
     // lane: window (lane >> 4) of the pair, slot group g = lane & 15 (slots 4g..4g+3)
     const int g = lane & 15, w2 = lane >> 4;
@@ -249,7 +216,7 @@ __global__ void __launch_bounds__(kTHREADS, 1) fwd_tc_kernel(const __grid_consta
       wb.next(p.nWy, p.nWx);
       const int k_a = kind(wa), k_b = has_b ? kind(wb) : 0;
       if (lane == 0)
-        mbar_expect_tx(full_bar(st), (k_a < 2 ? kBOX_TX : kG4_TX) + (has_b ? (k_b < 2 ? kBOX_TX : kG4_TX) : 0));
+        tc::mbar_expect_tx(full_bar(st), (k_a < 2 ? kBOX_TX : kG4_TX) + (has_b ? (k_b < 2 ? kBOX_TX : kG4_TX) : 0));
       __syncwarp();
       const Cursor me = w2 ? wb : wa;
       const int mk = w2 ? k_b : k_a;
@@ -258,20 +225,20 @@ __global__ void __launch_bounds__(kTHREADS, 1) fwd_tc_kernel(const __grid_consta
         if (mk == 0) {
           if (g == 0) {
             const int x = me.wx * kTM + s, y = me.wy * kTM + s;
-            box_load(tile, &box_map, colq, x, y, me.b, full_bar(st));
-            box_load(tile + kOFF_K, &box_map, colk, x, y, me.b, full_bar(st));
-            box_load(tile + kOFF_V, &box_map, colv, x, y, me.b, full_bar(st));
+            tc::box_load(tile, &box_map, colq, x, y, me.b, full_bar(st));
+            tc::box_load(tile + kOFF_K, &box_map, colk, x, y, me.b, full_bar(st));
+            tc::box_load(tile + kOFF_V, &box_map, colv, x, y, me.b, full_bar(st));
           }
         } else if (mk == 1) {
           if (g == 0) {
             const int x = me.wx * kTM + s, y = me.wy * kTM + s;
             const uint32_t bot = tile + (kTM - s) * kTM * kROW_BYTES;
-            box_load(tile, &top_map, colq, x, y, me.b, full_bar(st));
-            box_load(tile + kOFF_K, &top_map, colk, x, y, me.b, full_bar(st));
-            box_load(tile + kOFF_V, &top_map, colv, x, y, me.b, full_bar(st));
-            box_load(bot, &bot_map, colq, x, 0, me.b, full_bar(st));
-            box_load(bot + kOFF_K, &bot_map, colk, x, 0, me.b, full_bar(st));
-            box_load(bot + kOFF_V, &bot_map, colv, x, 0, me.b, full_bar(st));
+            tc::box_load(tile, &top_map, colq, x, y, me.b, full_bar(st));
+            tc::box_load(tile + kOFF_K, &top_map, colk, x, y, me.b, full_bar(st));
+            tc::box_load(tile + kOFF_V, &top_map, colv, x, y, me.b, full_bar(st));
+            tc::box_load(bot, &bot_map, colq, x, 0, me.b, full_bar(st));
+            tc::box_load(bot + kOFF_K, &bot_map, colk, x, 0, me.b, full_bar(st));
+            tc::box_load(bot + kOFF_V, &bot_map, colv, x, 0, me.b, full_bar(st));
           }
         } else if (g < kGROUPS) {
           int row[4];
@@ -283,9 +250,9 @@ __global__ void __launch_bounds__(kTHREADS, 1) fwd_tc_kernel(const __grid_consta
             row[q] = (me.b * H + y) * W + x;
           }
           const uint32_t base = tile + g * 4 * kROW_BYTES;
-          gather4(base, &qkv_map, colq, row[0], row[1], row[2], row[3], full_bar(st));
-          gather4(base + kOFF_K, &qkv_map, colk, row[0], row[1], row[2], row[3], full_bar(st));
-          gather4(base + kOFF_V, &qkv_map, colv, row[0], row[1], row[2], row[3], full_bar(st));
+          tc::gather4(base, &qkv_map, colq, row[0], row[1], row[2], row[3], full_bar(st));
+          tc::gather4(base + kOFF_K, &qkv_map, colk, row[0], row[1], row[2], row[3], full_bar(st));
+          tc::gather4(base + kOFF_V, &qkv_map, colv, row[0], row[1], row[2], row[3], full_bar(st));
         }
       }
       cur.next(p.nWy, p.nWx);
@@ -381,7 +348,7 @@ __global__ void __launch_bounds__(kTHREADS, 1) fwd_tc_kernel(const __grid_consta
       tc::ld49_wait(trow + kS_COL + 64 * win, sa, sb, sc);
       tc::fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(s_free);
+      if (lane == 0) tc::mbar_arrive(s_free);
 
       float y[kTN];
       {
@@ -426,7 +393,7 @@ __global__ void __launch_bounds__(kTHREADS, 1) fwd_tc_kernel(const __grid_consta
       tc::wait_st();
       tc::fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(p_full);
+      if (lane == 0) tc::mbar_arrive(p_full);
 
       if (!warp_wait(o_full, n & 1)) {
         bad = 1;
@@ -437,7 +404,7 @@ __global__ void __launch_bounds__(kTHREADS, 1) fwd_tc_kernel(const __grid_consta
       tc::ld32_1_wait(trow + kO_COL + 32 * win, trow + kO_COL + 64, o, osum);
       tc::fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(o_free);
+      if (lane == 0) tc::mbar_arrive(o_free);
       if (active) {
         const float inv = 1.0f / __uint_as_float(osum);
         const float2 i2 = make_float2(inv, inv);
@@ -536,6 +503,40 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 
 }  // namespace
 
+// The q/k/v tensor [batch, H, W, 3C] (bf16) as tensor maps, all with 32-channel (one
+// head) boxes, 64-byte swizzled in shared memory:
+//   gather  [tokens, 3C], one-token rows, for tile::gather4 loads;
+//   box     [B, H, W, 3C], 7 x 7 tokens: a window that does not wrap;
+//   top/bot the same with 7 x (7 - s) and 7 x s tokens: the two row bands of a window that
+//           wraps at the bottom border only.
+cudaError_t make_qkv_maps(const Plan& pl, const void* qkv, int batch, CUtensorMap* gather, CUtensorMap* box,
+                          CUtensorMap* top, CUtensorMap* bot) {
+  PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+  if (encode == nullptr) return cudaErrorNotSupported;
+  const int64_t tokens = (int64_t)batch * pl.H * pl.W;
+  const cuuint64_t row = (cuuint64_t)(3 * pl.C) * 2;
+  const cuuint64_t dims[2] = {(cuuint64_t)(3 * pl.C), (cuuint64_t)tokens};
+  const cuuint64_t strides[1] = {row};
+  const cuuint32_t gbox[2] = {kHeadDim, 1};
+  const cuuint32_t estride[4] = {1, 1, 1, 1};
+  if (encode(gather, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(qkv), dims, strides, gbox, estride,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  const cuuint64_t bdims[4] = {(cuuint64_t)(3 * pl.C), (cuuint64_t)pl.W, (cuuint64_t)pl.H, (cuuint64_t)batch};
+  const cuuint64_t bstrides[3] = {row, row * pl.W, row * pl.W * pl.H};
+  const cuuint32_t heights[3] = {kTM, (cuuint32_t)(pl.s > 0 ? kTM - pl.s : kTM), (cuuint32_t)(pl.s > 0 ? pl.s : kTM)};
+  CUtensorMap* maps[3] = {box, top, bot};
+  for (int m = 0; m < 3; ++m) {
+    const cuuint32_t bbox[4] = {kHeadDim, kTM, heights[m], 1};
+    if (encode(maps[m], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(qkv), bdims, bstrides, bbox, estride,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  return cudaSuccess;
+}
+
 cudaError_t fwd_tc_config(const Plan& pl, FwdLaunch* L) {
   cudaError_t e = cudaFuncSetAttribute(fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSMEM);
   if (e != cudaSuccess) return e;
@@ -582,36 +583,9 @@ cudaError_t fwd_tc_launch(const Plan& pl, const FwdLaunch& L0, const void* qkv, 
     L.chunks = (int)chunks;
     L.grid = (int)(chunks * pl.nH);
   }
-  // The q/k/v tensor as a [tokens, 3C] bf16 tensor map: one-row boxes of 32 channels
-  // (a head slice), 64-byte swizzled in shared memory, for the tile::gather4 loads.
-  PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
-  if (encode == nullptr) return cudaErrorNotSupported;
-  const int64_t tokens = (int64_t)batch * pl.H * pl.W;
-  CUtensorMap map;
-  const cuuint64_t dims[2] = {(cuuint64_t)(3 * pl.C), (cuuint64_t)tokens};
-  const cuuint64_t strides[1] = {(cuuint64_t)(3 * pl.C) * 2};
-  const cuuint32_t box[2] = {kHeadDim, 1};
-  const cuuint32_t estride[2] = {1, 1};
-  if (encode(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(qkv), dims, strides, box, estride,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-    return cudaErrorInvalidValue;
-  // The same tensor as [B, H, W, 3C] with boxes of 7 tokens by 7, 7 - s and s rows (32
-  // channels): a window, and the two row bands of a window that wraps at the bottom.
-  const cuuint64_t bdims[4] = {(cuuint64_t)(3 * pl.C), (cuuint64_t)pl.W, (cuuint64_t)pl.H, (cuuint64_t)batch};
-  const cuuint64_t bstrides[3] = {(cuuint64_t)(3 * pl.C) * 2, (cuuint64_t)pl.W * (3 * pl.C) * 2,
-                                  (cuuint64_t)pl.H * pl.W * (3 * pl.C) * 2};
-  const cuuint32_t bestride[4] = {1, 1, 1, 1};
-  CUtensorMap box_map, top_map, bot_map;
-  const cuuint32_t heights[3] = {kTM, (cuuint32_t)(pl.s > 0 ? kTM - pl.s : kTM), (cuuint32_t)(pl.s > 0 ? pl.s : kTM)};
-  CUtensorMap* maps[3] = {&box_map, &top_map, &bot_map};
-  for (int m = 0; m < 3; ++m) {
-    const cuuint32_t bbox[4] = {kHeadDim, kTM, heights[m], 1};
-    if (encode(maps[m], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(qkv), bdims, bstrides, bbox, bestride,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return cudaErrorInvalidValue;
-  }
+  CUtensorMap map, box_map, top_map, bot_map;
+  cudaError_t e = make_qkv_maps(pl, qkv, batch, &map, &box_map, &top_map, &bot_map);
+  if (e != cudaSuccess) return e;
   TcParams p;
   p.out = reinterpret_cast<__nv_bfloat16*>(out);
   p.tables = pl.tc_tables;

@@ -3,6 +3,7 @@
 // completion through an mbarrier, and the per-warp tensor-memory loads and stores.
 #pragma once
 
+#include <cuda.h>
 #include <stdint.h>
 
 namespace swin {
@@ -114,6 +115,46 @@ __device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity, uint64
   }
 }
 
+// ---- copy engine (TMA) and mbarrier arrivals ---------------------------------------
+
+__device__ __forceinline__ void mbar_arrive(uint32_t mbar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(mbar) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t mbar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(mbar), "r"(bytes) : "memory");
+}
+// Four tokens' 64-byte slices (rows r0..r3 of the [tokens, 3C] tensor map, columns col..col+31)
+// to four consecutive 64-byte rows of shared memory, completing on `mbar`.
+__device__ __forceinline__ void gather4(uint32_t dst, const CUtensorMap* map, int col, int r0, int r1, int r2, int r3,
+                                        uint32_t mbar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];\n" ::"r"(dst),
+      "l"(map), "r"(col), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(mbar)
+      : "memory");
+}
+// One window's 7 x 7 tokens (32 channels each) from the [B, H, W, 3C] tensor map to 49
+// consecutive 64-byte rows of shared memory (slot order ly * 7 + lx), completing on `mbar`.
+__device__ __forceinline__ void box_load(uint32_t dst, const CUtensorMap* map, int col, int x, int y, int b,
+                                         uint32_t mbar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6];\n" ::"r"(dst),
+      "l"(map), "r"(col), "r"(x), "r"(y), "r"(b), "r"(mbar)
+      : "memory");
+}
+// Arrive on the mbarrier once this thread's earlier cp.async copies have landed (the
+// barrier's expected count includes this arrival).
+__device__ __forceinline__ void cp_async_arrive(uint32_t mbar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(mbar) : "memory");
+}
+// Contiguous global -> shared bulk copy (16-byte aligned, size a multiple of 16).
+__device__ __forceinline__ void bulk_copy(uint32_t dst, const void* src, uint32_t bytes, uint32_t mbar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(mbar)
+               : "memory");
+}
+
 // ---- tensor memory -> registers (warp w reaches lanes 32 w .. 32 w + 31) ----------
 //
 // Each load is fused with tcgen05.wait::ld in one asm statement, so no use of the
@@ -185,4 +226,10 @@ __device__ __forceinline__ void st_x32(uint32_t taddr, const uint32_t (&r)[32]) 
 __device__ __forceinline__ void wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory"); }
 
 }  // namespace tc
+
+struct Plan;
+// Tensor maps of a q/k/v tensor for the copy engine (fwd_tc.cu).
+cudaError_t make_qkv_maps(const Plan& pl, const void* qkv, int batch, CUtensorMap* gather, CUtensorMap* box,
+                          CUtensorMap* top, CUtensorMap* bot);
+
 }  // namespace swin
