@@ -129,6 +129,11 @@ __global__ void __launch_bounds__(Geo<M>::THREADS, BwdMinBlocks<M>::value) bwd_k
   float4* sbias = reinterpret_cast<float4*>(smem);
   uint32_t* smask = reinterpret_cast<uint32_t*>(smem + G::BIAS_BYTES);
   unsigned char* sP = smem + G::BIAS_BYTES + G::MASK_BYTES;
+  // The next kernel may be scheduled now; everything this one reads (activations, and the
+  // plan's fragments, which the previous kernel may just have rebuilt) waits for the
+  // previous kernel to complete.
+  pdl_launch_dependents();
+  pdl_wait();
   unsigned char* sPlo = sP + BG::PS_BYTES;
   unsigned char* sdS = sPlo + BG::PS_BYTES;
   unsigned char* sdSlo = sdS + BG::PS_BYTES;
@@ -566,8 +571,7 @@ static cudaError_t blaunch_t(const Plan& pl, const BwdLaunch& L, const void* qkv
   p.chunks = L.chunks;
   p.scale = 1.0f / kInvScale;
   p.qk_scale_log2 = kLog2e / kInvScale;
-  bwd_kernel<M, TIO, STAGES><<<L.grid, L.threads, L.smem, st>>>(p);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(bwd_kernel<M, TIO, STAGES>, dim3(L.grid), dim3(L.threads), L.smem, st, p);
   if (e != cudaSuccess) return e;
   const int R = BGeo<M>::R;
   dtable_reduce_kernel<<<(R * pl.nH + 255) / 256, 256, 0, st>>>(pl.dt_partial, R, pl.nH, L.chunks,

@@ -122,6 +122,15 @@ __device__ __forceinline__ void mma_bf16_c(float (&d)[4], uint32_t a0, uint32_t 
         "f"(c3));
 }
 
+// Programmatic dependent launch: let the next kernel in the stream be scheduled (its
+// CTAs take SMs as this kernel's CTAs leave), and wait until the previous kernel has
+// completed and its memory is visible (a no-op when this kernel was launched without
+// the programmatic attribute).
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float r;
   asm("max.f32 %0, %1, %2, %3;\n" : "=f"(r) : "f"(a), "f"(b), "f"(c));
@@ -271,6 +280,24 @@ __device__ __forceinline__ void load_chunk<float>(uint32_t dst, const float* src
   asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(dst), "r"(w0), "r"(w1), "r"(w2),
                "r"(w3)
                : "memory");
+}
+
+// Launch `kernel` on `st` with programmatic stream serialisation: it may start while the
+// previous kernel of the stream drains; it calls pdl_wait() before touching activations.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
 }
 
 struct FwdLaunch {

@@ -61,6 +61,11 @@ __global__ void __launch_bounds__(Geo<M>::THREADS, FwdMinBlocks<M>::value)
   constexpr int N = G::N, NT = G::NT, KT = G::KT, THREADS = G::THREADS;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = TMA ? smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u) : smem_raw;
+  // The next kernel may be scheduled now; everything this one reads (activations, and the
+  // plan's fragments, which the previous kernel may just have rebuilt) waits for the
+  // previous kernel to complete.
+  pdl_launch_dependents();
+  pdl_wait();
   const uint32_t bar0 = smem_u32(smem) + G::BIAS_BYTES + G::MASK_BYTES + STAGES * G::STAGE_BYTES;
   float4* sbias = reinterpret_cast<float4*>(smem);
   uint32_t* smask = reinterpret_cast<uint32_t*>(smem + G::BIAS_BYTES);
@@ -460,8 +465,8 @@ static cudaError_t launch_t(const Plan& pl, const FwdLaunch& L0, const void* qkv
   p.chunks = L.chunks;
   p.qk_scale_log2 = kLog2e / kInvScale;
   p.err = pl.err;
-  fwd_kernel<M, TIO, STAGES, TMA><<<L.grid, L.threads, L.smem, st>>>(box_map, top_map, bot_map, p);
-  return cudaGetLastError();
+  return launch_pdl(fwd_kernel<M, TIO, STAGES, TMA>, dim3(L.grid), dim3(L.threads), L.smem, st, box_map, top_map,
+                    bot_map, p);
 }
 
 // Pipeline depth per window size: enough windows in flight per SM while keeping the

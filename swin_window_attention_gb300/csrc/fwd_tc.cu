@@ -125,6 +125,11 @@ __global__ void __launch_bounds__(kTHREADS, 1) fwd_tc_kernel(const __grid_consta
   unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const float* sbias = reinterpret_cast<const float*>(smem + kOFF_BIAS);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOFF_BAR + 8 * kNBAR);
+  // The next kernel may be scheduled now; everything this one reads (activations, and the
+  // plan's tables, which the previous kernel may just have rebuilt) waits for the previous
+  // kernel to complete.
+  pdl_launch_dependents();
+  pdl_wait();
   const uint32_t smem0 = smem_u32(smem);
   const uint32_t bar0 = smem0 + kOFF_BAR;
   auto full_bar = [&](int st) { return bar0 + 8 * st; };
@@ -601,8 +606,7 @@ cudaError_t fwd_tc_launch(const Plan& pl, const FwdLaunch& L0, const void* qkv, 
   p.total_windows = total;
   p.chunks = L.chunks;
   p.qk_scale_log2 = kLog2e / kInvScale;
-  fwd_tc_kernel<<<L.grid, L.threads, L.smem, st>>>(map, box_map, top_map, bot_map, p);
-  return cudaGetLastError();
+  return launch_pdl(fwd_tc_kernel, dim3(L.grid), dim3(L.threads), L.smem, st, map, box_map, top_map, bot_map, p);
 }
 
 }  // namespace swin
