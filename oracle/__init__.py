@@ -59,6 +59,7 @@ def bind(path: str) -> ctypes.CDLL:
         "oracle_probs": ([_D, _D] + [_i] * 10 + [_D], None),
         "oracle_fwd": ([_D, _D] + [_i] * 7 + [_D], None),
         "oracle_bwd": ([_D, _D, _D] + [_i] * 7 + [_D, _D], None),
+        "oracle_qkv_proj": ([_D, _D, _D, _D, _D, _i, _i, ctypes.c_double, _D], None),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -187,6 +188,19 @@ def bwd(qkv, dY, table, nH: int, M: int, s: int):
     dtab = np.empty_like(table)
     _load().oracle_bwd(_dp(qkv), _dp(dY), _dp(table), B, H, W, C, nH, M, s, _dp(dqkv), _dp(dtab))
     return dqkv, dtab
+
+
+def qkv_proj(x, gamma, beta, w, b, eps: float = 1e-5) -> np.ndarray:
+    """LayerNorm over the last axis of x [..., C] then x W^T + b with W [3C, C], b [3C]
+    -> [..., 3C] (float64)."""
+    x, gamma, beta, w, b = _f64(x), _f64(gamma), _f64(beta), _f64(w), _f64(b)
+    C = x.shape[-1]
+    if w.shape != (3 * C, C) or b.shape != (3 * C,) or gamma.shape != (C,) or beta.shape != (C,):
+        raise ValueError("oracle: qkv_proj shapes")
+    T = int(np.prod(x.shape[:-1]))
+    out = np.empty(x.shape[:-1] + (3 * C,), dtype=np.float64)
+    _load().oracle_qkv_proj(_dp(x), _dp(gamma), _dp(beta), _dp(w), _dp(b), T, C, float(eps), _dp(out))
+    return out
 
 
 def _check(B, H, W, C, nH, M, s, table):

@@ -32,6 +32,14 @@
 //     added to the logit.
 //  R7 logit = scale*(q.k) + bias + mask, scale = hd^-0.5.
 //
+// The producer step in front of the attention (the LayerNorm and the qkv projection that
+// the NVIDIA talk's section 2 lists among the fused operations of a Swin block) follows the
+// plain definitions:
+//  R15 LayerNorm over the C channels of a token: population variance, eps inside the
+//      square root, then the per-channel affine gamma, beta.
+//  R16 qkv = LN(x) W^T + b with W [3C, C] (row n is output channel n, in the channel order
+//      of R3) and b [3C].
+//
 // Everything here runs in double precision on whatever values it is given. Inputs are
 // expected to be the bf16-rounded values the GPU path also sees, widened to double.
 
@@ -356,6 +364,32 @@ void oracle_bwd(const double* qkv, const double* dY, const double* table, int B,
   // Adjoint of partition then roll is reverse then un-roll.
   oracle_reverse(dxw.data(), B, H, W, 3 * C, M, dxr.data());
   oracle_unroll(dxr.data(), B, H, W, 3 * C, s, dqkv);
+}
+
+// R15, R16: qkv[t] = LN(x[t]) W^T + b for tokens t < T; x [T, C], W [3C, C], b [3C],
+// gamma and beta [C].
+void oracle_qkv_proj(const double* x, const double* gamma, const double* beta, const double* w,
+                     const double* b, int T, int C, double eps, double* qkv) {
+  const int N = 3 * C;
+#pragma omp parallel for schedule(static)
+  for (int64_t t = 0; t < T; ++t) {
+    const double* xr = x + t * C;
+    double mean = 0.0;
+    for (int c = 0; c < C; ++c) mean += xr[c];
+    mean /= C;
+    double var = 0.0;
+    for (int c = 0; c < C; ++c) var += (xr[c] - mean) * (xr[c] - mean);
+    var /= C;
+    const double rstd = 1.0 / std::sqrt(var + eps);
+    std::vector<double> xn(C);
+    for (int c = 0; c < C; ++c) xn[c] = (xr[c] - mean) * rstd * gamma[c] + beta[c];
+    for (int n = 0; n < N; ++n) {
+      const double* wr = w + (int64_t)n * C;
+      double acc = b[n];
+      for (int c = 0; c < C; ++c) acc += xn[c] * wr[c];
+      qkv[t * N + n] = acc;
+    }
+  }
 }
 
 }  // extern "C"

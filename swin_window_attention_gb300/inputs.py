@@ -135,6 +135,21 @@ def make_dout(wl: Workload) -> torch.Tensor:
     return _act(normal((wl.B, wl.H, wl.W, wl.C), wl.seed + 2), wl.dtype)
 
 
+def make_producer(wl: Workload):
+    """Inputs of the producer step in front of the attention (LayerNorm over C, then the
+    qkv projection), CPU: x [B,H,W,C] bf16 ~ N(0,1); gamma = 1 + 0.1 N(0,1) and
+    beta = 0.1 N(0,1), fp32 [C]; W [3C, C] bf16, trunc-normal (std 0.02, +-0.04); b fp32
+    [3C] = 0.02 N(0,1). Seeds: the workload's seed + 3, 4, 5, 6."""
+    C = wl.C
+    x = normal((wl.B, wl.H, wl.W, C), wl.seed + 3).to(torch.bfloat16)
+    gb = normal((2, C), wl.seed + 4)
+    gamma = 1.0 + 0.1 * gb[0]
+    beta = 0.1 * gb[1]
+    w = trunc_normal((3 * C, C), wl.seed + 5).to(torch.bfloat16)
+    b = 0.02 * normal((3 * C,), wl.seed + 6)
+    return x, gamma.contiguous(), beta.contiguous(), w, b
+
+
 def act_f64(x: torch.Tensor):
     """Exact float64 numpy copy of the values the GPU path sees: bf16 inputs are widened
     as they are; fp32 inputs are first rounded to bf16 (round-to-nearest-even), which
