@@ -173,6 +173,27 @@ int swin_wattn_debug_maps(swin_wattn_plan_t plan, int32_t* gather, int32_t* reli
                           float* mask, float* dense_bias, struct CUstream_st* stream);
 
 /*
+ * The producer step in front of the attention (NVIDIA talk, section 2, lists LayerNorm and
+ * the qkv GEMM among the operations fused around the window attention): for each of
+ * `tokens` tokens,
+ *   xn = (x - mean) / sqrt(var + eps) * gamma + beta   (mean, population variance over C)
+ *   qkv = xn W^T + b
+ *   x      bf16 [tokens, C] (e.g. a [B,H,W,C] activation), device, 16-byte aligned;
+ *   gamma, beta fp32 [C]; b fp32 [3C]; device;
+ *   w_qkv  bf16 [3C, C] (row n = output channel n, in the order q | k | v, head-major);
+ *   qkv    bf16 [tokens, 3C], device, 16-byte aligned, written (the attention's input);
+ *   status optional device int (may be NULL): bit 0 is OR-ed in if a bounded device wait
+ *          ran out (then qkv is not valid).
+ * C must be a multiple of 32 in [32, 1536]. LayerNorm runs in fp32 and xn is rounded to
+ * bf16 as the tensor-core operand; the product accumulates in fp32; qkv is rounded to
+ * bf16. The cyclic shift and window partition are not applied here: the attention
+ * folds them into its loads. One kernel launch on `stream`; nothing is allocated.
+ */
+int swin_wattn_qkv_proj(const void* x, const float* gamma, const float* beta, const void* w_qkv,
+                        const float* b_qkv, void* qkv, int tokens, int C, float eps, int* status,
+                        struct CUstream_st* stream);
+
+/*
  * Choose the plan's forward kernel (SWIN_WATTN_KERNEL_*). Both kernels compute the same
  * function to the same tolerance; AUTO is the default. Asking for TCGEN05 where it does not apply returns SWIN_WATTN_ERR_UNSUPPORTED
  * and leaves the plan unchanged. Host-side only; call it between launches.

@@ -37,6 +37,7 @@ SIGNATURES = {
     "swin_wattn_bwd": ([_vp, _vp, _vp, _vp, _vp, _vp], _i),
     "swin_wattn_debug_maps": ([_vp, _vp, _vp, _vp, _vp, _vp], _i),
     "swin_wattn_bwd_noalloc": ([_vp, _vp, _vp, _vp, _vp] + [_i] * 8 + [_vp], _i),
+    "swin_wattn_qkv_proj": ([_vp] * 6 + [_i, _i, ctypes.c_float, _vp, _vp], _i),
     "swin_wattn_set_fwd_kernel": ([_vp, _i], _i),
     "swin_wattn_fwd_kernel": ([_vp], _i),
     "swin_wattn_device_status": ([_vp, _vp], _i),
@@ -113,6 +114,28 @@ def swin_wattn_bwd_noalloc(qkv_ptr, dout_ptr, dqkv_ptr, dtable_ptr, table_ptr, B
     library); see include/swin_wattn.h."""
     return load().swin_wattn_bwd_noalloc(qkv_ptr, dout_ptr, dqkv_ptr, dtable_ptr, table_ptr, B, H,
                                          W, C, num_heads, window, shift, dtype, stream)
+
+
+def swin_wattn_qkv_proj(x_ptr, gamma_ptr, beta_ptr, w_ptr, b_ptr, qkv_ptr, tokens, C, eps, status_ptr,
+                        stream):
+    return load().swin_wattn_qkv_proj(x_ptr, gamma_ptr, beta_ptr, w_ptr, b_ptr, qkv_ptr, tokens, C, eps,
+                                      status_ptr, stream)
+
+
+def qkv_proj(x, gamma, beta, w, b, qkv=None, eps=1e-5, status=None, stream=None):
+    """LayerNorm over the last axis of the bf16 CUDA tensor x [..., C], then x W^T + b into
+    a bf16 [..., 3C] tensor (allocated here when not given)."""
+    import torch
+    C = x.shape[-1]
+    if qkv is None:
+        qkv = torch.empty(x.shape[:-1] + (3 * C,), dtype=torch.bfloat16, device=x.device)
+    tokens = x.numel() // C
+    rc = swin_wattn_qkv_proj(x.data_ptr(), gamma.data_ptr(), beta.data_ptr(), w.data_ptr(), b.data_ptr(),
+                             qkv.data_ptr(), tokens, C, eps, None if status is None else status.data_ptr(),
+                             _stream_handle(stream))
+    if rc != OK:
+        raise SwinWAttnError("swin_wattn_qkv_proj", rc)
+    return qkv
 
 
 def swin_wattn_set_fwd_kernel(plan, kernel):

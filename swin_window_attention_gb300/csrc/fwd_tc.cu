@@ -491,10 +491,8 @@ cudaError_t launch_tc_tables(const Plan& pl, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-namespace {
-
 // cuTensorMapEncodeTiled from the driver, looked up once.
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
     void* f = nullptr;
     cudaDriverEntryPointQueryResult q;
@@ -506,8 +504,6 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-}  // namespace
-
 // The q/k/v tensor [batch, H, W, 3C] (bf16) as tensor maps, all with 32-channel (one
 // head) boxes, 64-byte swizzled in shared memory:
 //   gather  [tokens, 3C], one-token rows, for tile::gather4 loads;
@@ -516,7 +512,7 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 //           wraps at the bottom border only.
 cudaError_t make_qkv_maps(const Plan& pl, const void* qkv, int batch, CUtensorMap* gather, CUtensorMap* box,
                           CUtensorMap* top, CUtensorMap* bot) {
-  PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+  PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder_fn();
   if (encode == nullptr) return cudaErrorNotSupported;
   const int64_t tokens = (int64_t)batch * pl.H * pl.W;
   const cuuint64_t row = (cuuint64_t)(3 * pl.C) * 2;

@@ -4,6 +4,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cudaTypedefs.h>
 #include <stdint.h>
 
 namespace swin {
@@ -148,6 +149,15 @@ __device__ __forceinline__ void box_load(uint32_t dst, const CUtensorMap* map, i
 __device__ __forceinline__ void cp_async_arrive(uint32_t mbar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(mbar) : "memory");
 }
+// A 2-D box of a tensor map (inner coordinate c0, outer c1) to shared memory, completing
+// on `mbar`.
+__device__ __forceinline__ void tile_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint32_t mbar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];\n" ::"r"(dst),
+      "l"(map), "r"(c0), "r"(c1), "r"(mbar)
+      : "memory");
+}
 // Contiguous global -> shared bulk copy (16-byte aligned, size a multiple of 16).
 __device__ __forceinline__ void bulk_copy(uint32_t dst, const void* src, uint32_t bytes, uint32_t mbar) {
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(dst),
@@ -195,6 +205,17 @@ __device__ __forceinline__ void ld33_wait(uint32_t taddr, uint32_t (&a)[32], uin
       : "memory");
 }
 
+// 16 columns of this thread's lane.
+__device__ __forceinline__ void ld16_wait(uint32_t taddr, uint32_t (&a)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n"
+      "tcgen05.wait::ld.sync.aligned;\n"
+      : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3]), "=r"(a[4]), "=r"(a[5]), "=r"(a[6]), "=r"(a[7]),
+        "=r"(a[8]), "=r"(a[9]), "=r"(a[10]), "=r"(a[11]), "=r"(a[12]), "=r"(a[13]), "=r"(a[14]), "=r"(a[15])
+      : "r"(taddr)
+      : "memory");
+}
+
 // 32 columns at `a` and one column at `c` of this thread's lane.
 __device__ __forceinline__ void ld32_1_wait(uint32_t a_addr, uint32_t c_addr, uint32_t (&a)[32], uint32_t& c) {
   asm volatile(
@@ -228,6 +249,8 @@ __device__ __forceinline__ void wait_st() { asm volatile("tcgen05.wait::st.sync.
 }  // namespace tc
 
 struct Plan;
+// cuTensorMapEncodeTiled from the driver (looked up once), or null (fwd_tc.cu).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder_fn();
 // Tensor maps of a q/k/v tensor for the copy engine (fwd_tc.cu).
 cudaError_t make_qkv_maps(const Plan& pl, const void* qkv, int batch, CUtensorMap* gather, CUtensorMap* box,
                           CUtensorMap* top, CUtensorMap* bot);

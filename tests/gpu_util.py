@@ -25,13 +25,18 @@ def errors(got, ref):
         np.linalg.norm(d) / max(np.linalg.norm(ref), 1e-30))
 
 
-def assert_close(name, got, ref):
-    ma, rl = errors(got, ref)
+def log_case(name, ma, rl):
+    """Append the measured margins of one comparison to $SWIN_PARITY_LOG (if set)."""
     log = os.environ.get("SWIN_PARITY_LOG")
     if log:
         with open(log, "a") as f:
             f.write(json.dumps({"case": os.environ.get("PYTEST_CURRENT_TEST", "").split(" ")[0],
                                 "tensor": name, "max_abs": ma, "rel_l2": rl}) + "\n")
+
+
+def assert_close(name, got, ref):
+    ma, rl = errors(got, ref)
+    log_case(name, ma, rl)
     assert ma <= TOL_ABS and rl <= TOL_REL, f"{name}: max-abs {ma:.3g}, rel-L2 {rl:.3g}"
     return ma, rl
 

@@ -1,0 +1,117 @@
+"""The producer step (LayerNorm over C, then the qkv projection) on the GPU against the
+fp64 oracle, through the C ABI: ragged token counts, every Swin channel width, the
+full-size Swin-L 224 stages on sampled images, the chain producer -> attention against the
+oracle's chain, and the error paths."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from swin_window_attention_gb300 import capi, inputs
+from tests.gpu_util import TOL_ABS, TOL_REL, assert_close, errors, log_case, plan, workload
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    from swin_window_attention_gb300 import build
+    build.build()
+    oracle.build()
+    capi.load()
+
+
+def _f64(t):
+    return t.to(torch.float64).numpy()
+
+
+# qkv is stored in bf16 and its values grow with sqrt(C) (|qkv| reaches ~3 at C = 1536
+# with W ~ 0.02): a bf16 value carries an error up to half an ulp = 2^-9 |qkv| from its own
+# rounding, and rounding the normalised operand to bf16 adds about as much again. So each
+# element must lie within 1e-2 + 2^-8 |ref| (the 1e-2 absolute bound plus one bf16 ulp of
+# the value), and the tensor within rel-L2 5e-3.
+def assert_close_qkv(name, got, ref):
+    ma, rl = errors(got, ref)
+    g = got.double().cpu().numpy() if isinstance(got, torch.Tensor) else np.asarray(got)
+    excess = float((np.abs(g - ref) - (TOL_ABS + 2.0 ** -8 * np.abs(ref))).max())
+    log_case(name, ma, rl)
+    assert excess <= 0.0 and rl <= TOL_REL, f"{name}: max-abs {ma:.3g} (bound exceeded by {excess:.3g}), rel-L2 {rl:.3g}"
+
+
+def _run(x, g, be, w, b, eps=1e-5):
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    y = capi.qkv_proj(x.to(DEV), g.to(DEV), be.to(DEV), w.to(DEV), b.to(DEV), eps=eps, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    return y
+
+
+@pytest.mark.parametrize("T,C", [(1, 32), (127, 96), (129, 128), (300, 192), (1000, 256), (77, 384),
+                                 (260, 768), (130, 1536), (4096, 192)])
+def test_qkv_proj_against_oracle(T, C):
+    wl = workload(1, 1, T, C, C // 32, 1, 0, seed=T + C)
+    x, g, be, w, b = inputs.make_producer(wl)
+    y = _run(x, g, be, w, b)
+    assert y.shape == (1, 1, T, 3 * C) and y.dtype == torch.bfloat16
+    assert_close_qkv("qkv", y, oracle.qkv_proj(_f64(x), _f64(g), _f64(be), _f64(w), _f64(b)))
+
+
+@pytest.mark.parametrize("name", ["swin_l224_s1", "swin_l224_s2", "swin_l224_s3", "swin_l224_s4"])
+def test_qkv_proj_full_size_workloads(name):
+    wl = inputs.BY_NAME[name]
+    x, g, be, w, b = inputs.make_producer(wl)
+    y = _run(x, g, be, w, b).cpu()
+    for bi in sorted({0, wl.B - 1}):
+        ref = oracle.qkv_proj(_f64(x[bi]), _f64(g), _f64(be), _f64(w), _f64(b))
+        assert_close_qkv(f"{name} qkv[{bi}]", y[bi], ref)
+
+
+def test_qkv_proj_is_deterministic_and_large_offsets_are_stable():
+    """x with a large common offset per token (LayerNorm must remove it) and a wide spread."""
+    wl = workload(2, 14, 14, 192, 6, 7, 3, seed=5)
+    x, g, be, w, b = inputs.make_producer(wl)
+    x = (x.float() * 4.0 + 30.0).to(torch.bfloat16)
+    y1 = _run(x, g, be, w, b)
+    y2 = _run(x, g, be, w, b)
+    assert torch.equal(y1, y2)
+    assert_close_qkv("qkv", y1, oracle.qkv_proj(_f64(x), _f64(g), _f64(be), _f64(w), _f64(b)))
+
+
+def test_producer_then_attention_matches_the_oracle_chain():
+    """LayerNorm + qkv projection, then the shifted-window attention, against the oracle's
+    two steps (the attention oracle applied to the oracle's fp64 qkv)."""
+    wl = workload(2, 14, 21, 96, 3, 7, 3, seed=11)
+    x, g, be, w, b = inputs.make_producer(wl)
+    table = inputs.make_table(wl)
+    qkv = _run(x, g, be, w, b)
+    att = plan(wl, table.to(DEV))
+    y = att.fwd(qkv)
+    torch.cuda.synchronize()
+    att.close()
+    qkv_ref = oracle.qkv_proj(_f64(x), _f64(g), _f64(be), _f64(w), _f64(b))
+    assert_close("Y", y, oracle.fwd(qkv_ref, table.double().numpy(), wl.nH, wl.M, wl.s))
+
+
+def test_qkv_proj_error_paths():
+    x = torch.zeros(4, 96, dtype=torch.bfloat16, device=DEV)
+    v = torch.zeros(288, dtype=torch.float32, device=DEV)
+    w = torch.zeros(288, 96, dtype=torch.bfloat16, device=DEV)
+    out = torch.full((4, 288), 3.0, dtype=torch.bfloat16, device=DEV)
+    s = torch.cuda.current_stream().cuda_stream
+    f = capi.swin_wattn_qkv_proj
+    assert f(x.data_ptr(), v.data_ptr(), v.data_ptr(), w.data_ptr(), v.data_ptr(), out.data_ptr(), 0, 96, 1e-5,
+             None, s) == capi.OK
+    torch.cuda.synchronize()
+    assert torch.all(out == 3.0)  # no tokens: nothing written
+    assert f(x.data_ptr(), v.data_ptr(), v.data_ptr(), w.data_ptr(), v.data_ptr(), out.data_ptr(), 4, 80, 1e-5,
+             None, s) == capi.ERR_UNSUPPORTED
+    assert f(x.data_ptr(), v.data_ptr(), v.data_ptr(), w.data_ptr(), v.data_ptr(), out.data_ptr(), -1, 96, 1e-5,
+             None, s) == capi.ERR_INVALID_ARG
+    host = torch.zeros(4, 96, dtype=torch.bfloat16)
+    assert f(host.data_ptr(), v.data_ptr(), v.data_ptr(), w.data_ptr(), v.data_ptr(), out.data_ptr(), 4, 96,
+             1e-5, None, s) == capi.ERR_INVALID_ARG
+    assert f(x.data_ptr() + 2, v.data_ptr(), v.data_ptr(), w.data_ptr(), v.data_ptr(), out.data_ptr(), 4, 96,
+             1e-5, None, s) == capi.ERR_MISALIGNED
