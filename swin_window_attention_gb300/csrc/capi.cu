@@ -26,7 +26,8 @@ cudaError_t fwd_launch_batch(const Plan& pl, const FwdLaunch& L, const void* qkv
                              int batch, cudaStream_t st);
 cudaError_t bwd_config(const Plan& pl, BwdLaunch* L);
 cudaError_t qkv_proj_launch(const void* x, const float* gamma, const float* beta, const void* w, const float* b,
-                            void* out, int T, int C, float eps, int* status, cudaStream_t st);
+                            void* out, int T, int C, float eps, void* workspace, int* status, cudaStream_t st);
+size_t qkv_workspace_bytes(int C);
 cudaError_t bwd_launch(const Plan& pl, const BwdLaunch& L, const void* qkv, const void* dout,
                        void* dqkv, float* dtable, cudaStream_t st);
 }  // namespace swin
@@ -374,25 +375,33 @@ int swin_wattn_debug_maps(swin_wattn_plan_t plan, int32_t* gather, int32_t* reli
   return e == cudaSuccess ? SWIN_WATTN_OK : cuda_fail(e, "swin_wattn_debug_maps");
 }
 
+size_t swin_wattn_qkv_workspace_bytes(int C) {
+  return (C < 32 || C > 1536 || C % 32 != 0) ? 0 : swin::qkv_workspace_bytes(C);
+}
+
 int swin_wattn_qkv_proj(const void* x, const float* gamma, const float* beta, const void* w_qkv,
-                        const float* b_qkv, void* qkv, int tokens, int C, float eps, int* status,
-                        struct CUstream_st* stream) {
-  if (tokens < 0 || C < 32 || C > 1536 || C % 32 != 0 || !(eps >= 0.0f) || !std::isfinite(eps))
-    return tokens < 0 || !(eps >= 0.0f) || !std::isfinite(eps) ? SWIN_WATTN_ERR_INVALID_ARG
-                                                                 : SWIN_WATTN_ERR_UNSUPPORTED;
+                        const float* b_qkv, void* qkv, int tokens, int C, float eps, void* workspace,
+                        size_t workspace_bytes, int* status, struct CUstream_st* stream) {
+  if (tokens < 0 || !(eps >= 0.0f) || !std::isfinite(eps)) return SWIN_WATTN_ERR_INVALID_ARG;
+  if (C < 32 || C > 1536 || C % 32 != 0) return SWIN_WATTN_ERR_UNSUPPORTED;
   if ((int64_t)tokens >= ((int64_t)1 << 31)) return SWIN_WATTN_ERR_UNSUPPORTED;
   if (tokens == 0) return SWIN_WATTN_OK;
+  if (workspace_bytes < swin::qkv_workspace_bytes(C)) {
+    swin::set_last_error("swin_wattn_qkv_proj: workspace smaller than swin_wattn_qkv_workspace_bytes(C)");
+    return SWIN_WATTN_ERR_INVALID_ARG;
+  }
   int rc;
   if ((rc = check_device_ptr(x, 16)) != SWIN_WATTN_OK) return rc;
   if ((rc = check_device_ptr(w_qkv, 16)) != SWIN_WATTN_OK) return rc;
   if ((rc = check_device_ptr(qkv, 16)) != SWIN_WATTN_OK) return rc;
+  if ((rc = check_device_ptr(workspace, 256)) != SWIN_WATTN_OK) return rc;
   if ((rc = check_device_ptr(gamma, 4)) != SWIN_WATTN_OK) return rc;
   if ((rc = check_device_ptr(beta, 4)) != SWIN_WATTN_OK) return rc;
   if ((rc = check_device_ptr(b_qkv, 4)) != SWIN_WATTN_OK) return rc;
   if (status != nullptr && (rc = check_device_ptr(status, 4)) != SWIN_WATTN_OK) return rc;
-  cudaError_t e = swin::qkv_proj_launch(x, gamma, beta, w_qkv, b_qkv, qkv, tokens, C, eps, status,
+  cudaError_t e = swin::qkv_proj_launch(x, gamma, beta, w_qkv, b_qkv, qkv, tokens, C, eps, workspace, status,
                                         reinterpret_cast<cudaStream_t>(stream));
-  ++g_launches;
+  g_launches += 2;
   return e == cudaSuccess ? SWIN_WATTN_OK : cuda_fail(e, "swin_wattn_qkv_proj");
 }
 

@@ -100,18 +100,19 @@ def test_qkv_proj_error_paths():
     v = torch.zeros(288, dtype=torch.float32, device=DEV)
     w = torch.zeros(288, 96, dtype=torch.bfloat16, device=DEV)
     out = torch.full((4, 288), 3.0, dtype=torch.bfloat16, device=DEV)
+    nws = capi.swin_wattn_qkv_workspace_bytes(96)
+    assert nws >= 288 * 96 * 2 + 2 * 288 * 4
+    assert capi.swin_wattn_qkv_workspace_bytes(80) == 0
+    ws = torch.empty(nws, dtype=torch.uint8, device=DEV)
     s = torch.cuda.current_stream().cuda_stream
-    f = capi.swin_wattn_qkv_proj
-    assert f(x.data_ptr(), v.data_ptr(), v.data_ptr(), w.data_ptr(), v.data_ptr(), out.data_ptr(), 0, 96, 1e-5,
-             None, s) == capi.OK
+    f = lambda xp, T, C, nb: capi.swin_wattn_qkv_proj(xp, v.data_ptr(), v.data_ptr(), w.data_ptr(), v.data_ptr(),
+                                                      out.data_ptr(), T, C, 1e-5, ws.data_ptr(), nb, None, s)
+    assert f(x.data_ptr(), 0, 96, nws) == capi.OK
     torch.cuda.synchronize()
     assert torch.all(out == 3.0)  # no tokens: nothing written
-    assert f(x.data_ptr(), v.data_ptr(), v.data_ptr(), w.data_ptr(), v.data_ptr(), out.data_ptr(), 4, 80, 1e-5,
-             None, s) == capi.ERR_UNSUPPORTED
-    assert f(x.data_ptr(), v.data_ptr(), v.data_ptr(), w.data_ptr(), v.data_ptr(), out.data_ptr(), -1, 96, 1e-5,
-             None, s) == capi.ERR_INVALID_ARG
+    assert f(x.data_ptr(), 4, 80, nws) == capi.ERR_UNSUPPORTED
+    assert f(x.data_ptr(), -1, 96, nws) == capi.ERR_INVALID_ARG
+    assert f(x.data_ptr(), 4, 96, nws - 16) == capi.ERR_INVALID_ARG  # workspace too small
     host = torch.zeros(4, 96, dtype=torch.bfloat16)
-    assert f(host.data_ptr(), v.data_ptr(), v.data_ptr(), w.data_ptr(), v.data_ptr(), out.data_ptr(), 4, 96,
-             1e-5, None, s) == capi.ERR_INVALID_ARG
-    assert f(x.data_ptr() + 2, v.data_ptr(), v.data_ptr(), w.data_ptr(), v.data_ptr(), out.data_ptr(), 4, 96,
-             1e-5, None, s) == capi.ERR_MISALIGNED
+    assert f(host.data_ptr(), 4, 96, nws) == capi.ERR_INVALID_ARG
+    assert f(x.data_ptr() + 2, 4, 96, nws) == capi.ERR_MISALIGNED
