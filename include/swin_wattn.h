@@ -182,9 +182,10 @@ int swin_wattn_debug_maps(swin_wattn_plan_t plan, int32_t* gather, int32_t* reli
  *   gamma, beta fp32 [C]; b fp32 [3C]; device;
  *   w_qkv  bf16 [3C, C] (row n = output channel n, in the order q | k | v, head-major);
  *   qkv    bf16 [tokens, 3C], device, 16-byte aligned, written (the attention's input);
- *   workspace  caller-owned device memory of at least swin_wattn_qkv_workspace_bytes(C)
- *          bytes, 256-byte aligned, overwritten (the gamma-folded weights and two
- *          per-channel vectors); one call at a time per workspace;
+ *   workspace  caller-owned device memory of at least swin_wattn_qkv_workspace_bytes(C,
+ *          tokens) bytes, 256-byte aligned, overwritten (the gamma-folded weights, two
+ *          per-channel vectors and the per-token statistics); one call at a time per
+ *          workspace;
  *   status optional device int (may be NULL): bit 0 is OR-ed in if a bounded device wait
  *          ran out (then qkv is not valid).
  * The normalisation is applied on the other side of the product:
@@ -192,10 +193,11 @@ int swin_wattn_debug_maps(swin_wattn_plan_t plan, int32_t* gather, int32_t* reli
  *   u = row sums of W', v = beta W^T + b,
  * with the row statistics in fp32 and the product accumulated in fp32 on bf16 x and W';
  * qkv is rounded to bf16. C must be a multiple of 32 in [32, 1536]. The cyclic shift and
- * window partition are not applied here: the attention folds them into its loads. Two
- * kernel launches on `stream` (the fold, the product); nothing is allocated.
+ * window partition are not applied here: the attention folds them into its loads. Three
+ * kernel launches on `stream` (the fold, the statistics, the product); nothing is
+ * allocated. swin_wattn_qkv_workspace_bytes returns 0 for an unsupported C.
  */
-size_t swin_wattn_qkv_workspace_bytes(int C);
+size_t swin_wattn_qkv_workspace_bytes(int C, int tokens);
 int swin_wattn_qkv_proj(const void* x, const float* gamma, const float* beta, const void* w_qkv,
                         const float* b_qkv, void* qkv, int tokens, int C, float eps, void* workspace,
                         size_t workspace_bytes, int* status, struct CUstream_st* stream);

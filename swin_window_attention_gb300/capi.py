@@ -37,7 +37,7 @@ SIGNATURES = {
     "swin_wattn_bwd": ([_vp, _vp, _vp, _vp, _vp, _vp], _i),
     "swin_wattn_debug_maps": ([_vp, _vp, _vp, _vp, _vp, _vp], _i),
     "swin_wattn_bwd_noalloc": ([_vp, _vp, _vp, _vp, _vp] + [_i] * 8 + [_vp], _i),
-    "swin_wattn_qkv_workspace_bytes": ([_i], ctypes.c_size_t),
+    "swin_wattn_qkv_workspace_bytes": ([_i, _i], ctypes.c_size_t),
     "swin_wattn_qkv_proj": ([_vp] * 6 + [_i, _i, ctypes.c_float, _vp, ctypes.c_size_t, _vp, _vp], _i),
     "swin_wattn_set_fwd_kernel": ([_vp, _i], _i),
     "swin_wattn_fwd_kernel": ([_vp], _i),
@@ -117,8 +117,8 @@ def swin_wattn_bwd_noalloc(qkv_ptr, dout_ptr, dqkv_ptr, dtable_ptr, table_ptr, B
                                          W, C, num_heads, window, shift, dtype, stream)
 
 
-def swin_wattn_qkv_workspace_bytes(C):
-    return int(load().swin_wattn_qkv_workspace_bytes(C))
+def swin_wattn_qkv_workspace_bytes(C, tokens):
+    return int(load().swin_wattn_qkv_workspace_bytes(C, tokens))
 
 
 def swin_wattn_qkv_proj(x_ptr, gamma_ptr, beta_ptr, w_ptr, b_ptr, qkv_ptr, tokens, C, eps, workspace_ptr,
@@ -134,9 +134,10 @@ def qkv_proj(x, gamma, beta, w, b, qkv=None, eps=1e-5, status=None, workspace=No
     C = x.shape[-1]
     if qkv is None:
         qkv = torch.empty(x.shape[:-1] + (3 * C,), dtype=torch.bfloat16, device=x.device)
-    if workspace is None:
-        workspace = torch.empty(max(swin_wattn_qkv_workspace_bytes(C), 1), dtype=torch.uint8, device=x.device)
     tokens = x.numel() // C
+    if workspace is None:
+        workspace = torch.empty(max(swin_wattn_qkv_workspace_bytes(C, tokens), 1), dtype=torch.uint8,
+                                device=x.device)
     rc = swin_wattn_qkv_proj(x.data_ptr(), gamma.data_ptr(), beta.data_ptr(), w.data_ptr(), b.data_ptr(),
                              qkv.data_ptr(), tokens, C, eps, workspace.data_ptr(), workspace.numel(),
                              None if status is None else status.data_ptr(), _stream_handle(stream))

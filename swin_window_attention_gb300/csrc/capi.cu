@@ -27,7 +27,7 @@ cudaError_t fwd_launch_batch(const Plan& pl, const FwdLaunch& L, const void* qkv
 cudaError_t bwd_config(const Plan& pl, BwdLaunch* L);
 cudaError_t qkv_proj_launch(const void* x, const float* gamma, const float* beta, const void* w, const float* b,
                             void* out, int T, int C, float eps, void* workspace, int* status, cudaStream_t st);
-size_t qkv_workspace_bytes(int C);
+size_t qkv_workspace_bytes(int C, int64_t T);
 cudaError_t bwd_launch(const Plan& pl, const BwdLaunch& L, const void* qkv, const void* dout,
                        void* dqkv, float* dtable, cudaStream_t st);
 }  // namespace swin
@@ -375,8 +375,8 @@ int swin_wattn_debug_maps(swin_wattn_plan_t plan, int32_t* gather, int32_t* reli
   return e == cudaSuccess ? SWIN_WATTN_OK : cuda_fail(e, "swin_wattn_debug_maps");
 }
 
-size_t swin_wattn_qkv_workspace_bytes(int C) {
-  return (C < 32 || C > 1536 || C % 32 != 0) ? 0 : swin::qkv_workspace_bytes(C);
+size_t swin_wattn_qkv_workspace_bytes(int C, int tokens) {
+  return (C < 32 || C > 1536 || C % 32 != 0 || tokens < 0) ? 0 : swin::qkv_workspace_bytes(C, tokens);
 }
 
 int swin_wattn_qkv_proj(const void* x, const float* gamma, const float* beta, const void* w_qkv,
@@ -386,8 +386,8 @@ int swin_wattn_qkv_proj(const void* x, const float* gamma, const float* beta, co
   if (C < 32 || C > 1536 || C % 32 != 0) return SWIN_WATTN_ERR_UNSUPPORTED;
   if ((int64_t)tokens >= ((int64_t)1 << 31)) return SWIN_WATTN_ERR_UNSUPPORTED;
   if (tokens == 0) return SWIN_WATTN_OK;
-  if (workspace_bytes < swin::qkv_workspace_bytes(C)) {
-    swin::set_last_error("swin_wattn_qkv_proj: workspace smaller than swin_wattn_qkv_workspace_bytes(C)");
+  if (workspace_bytes < swin::qkv_workspace_bytes(C, tokens)) {
+    swin::set_last_error("swin_wattn_qkv_proj: workspace smaller than swin_wattn_qkv_workspace_bytes(C, tokens)");
     return SWIN_WATTN_ERR_INVALID_ARG;
   }
   int rc;
@@ -401,7 +401,7 @@ int swin_wattn_qkv_proj(const void* x, const float* gamma, const float* beta, co
   if (status != nullptr && (rc = check_device_ptr(status, 4)) != SWIN_WATTN_OK) return rc;
   cudaError_t e = swin::qkv_proj_launch(x, gamma, beta, w_qkv, b_qkv, qkv, tokens, C, eps, workspace, status,
                                         reinterpret_cast<cudaStream_t>(stream));
-  g_launches += 2;
+  g_launches += 3;
   return e == cudaSuccess ? SWIN_WATTN_OK : cuda_fail(e, "swin_wattn_qkv_proj");
 }
 

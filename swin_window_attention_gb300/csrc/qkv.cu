@@ -9,29 +9,40 @@
 // The normalisation is moved to the other side of the product:
 //   LN(x) W^T + b = rstd * (x W'^T) - rstd * mean * u + v,
 //   W'[n][c] = bf16(gamma_c W[n][c]),  u_n = sum_c W'[n][c],  v_n = sum_c beta_c W[n][c] + b_n,
-// so the tensor cores consume the raw bf16 x tiles as they arrive, the row statistics are
-// summed from the same tiles while the MMAs run, and the epilogue applies them (u is
-// summed from the rounded W', so the mean cancels exactly against the rounded weights).
-// qkv_fold_kernel builds W', u and v once per call.
+// so the tensor cores consume the raw bf16 x tiles as they arrive and the epilogue applies
+// the row statistics (u is summed from the rounded W', so the mean cancels exactly against
+// the rounded weights). qkv_prep_kernel builds W', u and v once per call. The mean and
+// 1 / sqrt(var + eps) of each token come from one of two places:
+// * when every token tile is one work item (many tokens), statistics warps sum them from
+//   the x tiles already staged for the product, at no extra memory traffic;
+// * when the output channels of a token tile are split over several work items (few
+//   tokens, wide C), qkv_prep_kernel also computes them in one coalesced pass over x, so
+//   that no work item repeats the sums.
 //
 // A dense contraction (2 * 3C * C flops per token) on the fifth-generation tensor cores.
 // One persistent CTA per SM walks work items (128 tokens, the MMA's M, times a group of
 // output-channel tiles of N <= 256), with specialised warps whose pipelines run on across
 // items:
-// * copy warp (13): TMA loads of x chunks [128 tokens x 32 channels] and W' chunks
-//   [N tile x 32 channels], 64-byte swizzled, six stages deep;
-// * MMA warp (12), one thread: per chunk two M128 N<=256 K16 tcgen05.mma (A = the x chunk,
+// * copy warp: TMA loads of x chunks [128 tokens x 64 channels] and W' chunks
+//   [N tile x 64 channels], 128-byte swizzled, into a ring of as many stages as the rest
+//   of the shared memory holds (4 at N = 256, up to 8), so that enough bytes are in flight to cover the load
+//   latency at the tensor cores' rate (channels past C in the last chunk arrive as zeros
+//   and add nothing);
+// * MMA warp, one thread: per chunk four M128 N<=256 K16 tcgen05.mma (A = the x chunk,
 //   B = the W' chunk) into one of two tensor-memory accumulators;
-// * statistics warps (0..3): thread r sums its token row's x and x^2 (shifted by the row's
-//   first value) over the chunks of an item's first output tile, then publishes mean and
-//   1 / sqrt(var + eps);
-// * epilogue warps (4..11, two per tensor-memory lane quadrant, each taking 16 of every
-//   32 channels): thread r forms rstd * acc - rstd * mean * u + v and rounds to bf16 into
-//   a 64-byte-swizzled staging tile that one thread writes out with a TMA store (two
-//   staging tiles alternate), while the next output tile accumulates.
+// * statistics warps (four, with in-kernel statistics): thread r sums its token row's x
+//   and x^2, shifted by the row's first value, over the chunks of an item's first output
+//   tile and publishes mean and rstd;
+// * epilogue warps (eight, two per tensor-memory lane quadrant, taking alternate 32-channel
+//   slices): thread r forms rstd * acc - rstd * mean * u + v for its token row and rounds
+//   to bf16 into the warp's own 64-byte-swizzled staging tile [32 rows x 32 channels],
+//   which the warp's first lane writes out with a TMA store (two tiles per warp
+//   alternate; no barrier beyond the warp), while the next output tile accumulates.
 // Every wait is bounded (1 s); a wait that runs out sets the caller's status word (when
 // one is given) and the CTA leaves after releasing its tensor memory.
 #include <cuda.h>
+
+#include <algorithm>
 
 #include "common.cuh"
 #include "tc.cuh"
@@ -41,35 +52,43 @@ namespace swin {
 namespace {
 
 constexpr int kBM = 128;                       // tokens per work item
-constexpr int kKC = 32;                        // channels per K chunk: one 64-byte row
+constexpr int kKC = 64;                        // channels per K chunk: one 128-byte row
+constexpr int kSC = 32;                        // output channels per stored slice
 constexpr int kMaxNT = 256;                    // output channels per N tile
 constexpr int kMaxC = 1536;
-constexpr int kSTAGES = 6;
-constexpr int kXCH = kBM * 64;                 // x chunk
-constexpr int kWCH = kMaxNT * 64;              // W' chunk
-constexpr int kSTAGE = kXCH + kWCH;            // 24 KB
-constexpr int kTHREADS = 14 * 32;
-constexpr int kEPI_WARP0 = 4, kEPI_THREADS = 256, kMMA_WARP = 12, kCOPY_WARP = 13;
-constexpr int kOFF_UV = kSTAGES * kSTAGE;              // u, v: 2 x 3 kMaxC floats
-constexpr int kOFF_STATS = kOFF_UV + 6 * kMaxC * 4;    // mean, rstd: 2 buffers x 128 x 2 floats
-constexpr int kOFF_OUT = kOFF_STATS + 2 * kBM * 8;     // 2 staging tiles of 128 rows x 64 B
-constexpr int kOFF_BAR = kOFF_OUT + 2 * kBM * 64;
-constexpr int kNBAR = 2 * kSTAGES + 8;
-constexpr int kSMEM = kOFF_BAR + 8 * kNBAR + 8 + 1024;  // + alignment slack
+constexpr int kMaxSTAGES = 8;
+constexpr int kXCH = kBM * 128;                // x chunk
+// Warp roles: [statistics warps 0..3 when in-kernel], 8 epilogue warps, MMA, copy.
+template <bool IN_STATS>
+struct Roles {
+  static constexpr int kEPI0 = IN_STATS ? 4 : 0;
+  static constexpr int kMMA = kEPI0 + 8, kCOPY = kMMA + 1;
+  static constexpr int kTHREADS = (kCOPY + 1) * 32;
+};
+// Shared memory, from a 1024-byte aligned base: the stage ring (stages x stage_bytes),
+// [mean and rstd: 2 buffers x 128 x float2, with in-kernel statistics], per epilogue warp
+// two staging tiles of 32 rows x 64 bytes, the mbarriers and the tensor-memory address.
+constexpr int kSTATS_BYTES = 2 * kBM * 8;
+constexpr int kOUT_BYTES = 8 * 2 * 32 * 64;
+constexpr int kNBAR = 2 * kMaxSTAGES + 8;
+constexpr int kTAIL_BYTES = kOUT_BYTES + 8 * kNBAR + 8 + 1024;  // + alignment slack
+constexpr int kMinSMEM = 120 * 1024;  // above half of an SM: one CTA per SM
 constexpr int kTMEM_COLS = 512;                // two accumulators of up to 256 columns
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
-constexpr uint32_t kSW64 = 4;
+constexpr uint32_t kSW128 = 2;  // descriptor layout: 128-byte swizzle
 
-// More than half of the SM's shared memory: one CTA per SM, so the 512-column tensor
-// memory allocation never waits.
-static_assert(kSMEM > 233472 / 2 && kSMEM <= 232448, "one CTA per SM");
+// One CTA per SM (more than half of its shared memory), so the 512-column tensor memory
+// allocation never waits.
 
 struct QkvParams {
   __nv_bfloat16* out;     // [T, 3C]
   const float* u;         // [3C]
   const float* v;         // [3C]
+  const float2* stats;    // [T] (mean, rstd), when computed before the product
   int* status;            // optional: bit 0 set when a bounded wait ran out
   int T, C, N, NT, tiles_per_item, n_tt, n_items;
+  int stages, stage_bytes;  // the ring: stages x (x chunk + NT x 128 bytes), 1024-byte multiples
+  int off_stats, off_out, off_bar;
   float eps;
 };
 
@@ -80,29 +99,30 @@ __device__ __forceinline__ bool warp_wait(uint32_t mbar, uint32_t parity) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
-__global__ void __launch_bounds__(kTHREADS, 1)
+template <bool IN_STATS>
+__global__ void __launch_bounds__(Roles<IN_STATS>::kTHREADS, 1)
     qkv_gemm_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_constant__ CUtensorMap w_map,
                     const __grid_constant__ CUtensorMap out_map, const QkvParams p) {
+  using R = Roles<IN_STATS>;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   pdl_launch_dependents();
   pdl_wait();
   const uint32_t smem0 = smem_u32(smem);
-  float* su = reinterpret_cast<float*>(smem + kOFF_UV);
-  float* sv = su + 3 * kMaxC;
-  float2* sstats = reinterpret_cast<float2*>(smem + kOFF_STATS);  // [2][128] (mean, rstd)
-  const uint32_t bar0 = smem0 + kOFF_BAR;
+  float2* sstats = reinterpret_cast<float2*>(smem + p.off_stats);  // [2][128] (mean, rstd)
+  const uint32_t bar0 = smem0 + p.off_bar;
   auto full_bar = [&](int st) { return bar0 + 8 * st; };
-  auto empty_bar = [&](int st) { return bar0 + 8 * (kSTAGES + st); };
-  auto dfull_bar = [&](int b) { return bar0 + 8 * (2 * kSTAGES + b); };
-  auto dfree_bar = [&](int b) { return bar0 + 8 * (2 * kSTAGES + 2 + b); };
-  auto sfull_bar = [&](int b) { return bar0 + 8 * (2 * kSTAGES + 4 + b); };
-  auto sfree_bar = [&](int b) { return bar0 + 8 * (2 * kSTAGES + 6 + b); };
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOFF_BAR + 8 * kNBAR);
+  auto empty_bar = [&](int st) { return bar0 + 8 * (kMaxSTAGES + st); };
+  auto dfull_bar = [&](int b) { return bar0 + 8 * (2 * kMaxSTAGES + b); };
+  auto dfree_bar = [&](int b) { return bar0 + 8 * (2 * kMaxSTAGES + 2 + b); };
+  auto sfull_bar = [&](int b) { return bar0 + 8 * (2 * kMaxSTAGES + 4 + b); };
+  auto sfree_bar = [&](int b) { return bar0 + 8 * (2 * kMaxSTAGES + 6 + b); };
+  const int stages = p.stages;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + p.off_bar + 8 * kNBAR);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n_tiles = p.N / p.NT;
-  const int kcn = p.C / kKC;
+  const int kcn = (p.C + kKC - 1) / kKC;
   // Work item i: token tile i % n_tt, output-channel tiles [j0, j0 + ntile) of group i / n_tt.
   auto item_tiles = [&](int i, int& t0, int& j0, int& ntile) {
     t0 = (i % p.n_tt) * kBM;
@@ -110,11 +130,11 @@ __global__ void __launch_bounds__(kTHREADS, 1)
     ntile = min(p.tiles_per_item, n_tiles - j0);  // >= 1 by construction
   };
 
-  if (warp == kMMA_WARP) tc::tmem_alloc<kTMEM_COLS>(smem_u32(tmem_slot));
+  if (warp == R::kMMA) tc::tmem_alloc<kTMEM_COLS>(smem_u32(tmem_slot));
   if (tid == 0) {
-    for (int st = 0; st < kSTAGES; ++st) {
+    for (int st = 0; st < stages; ++st) {
       tc::mbar_init(full_bar(st), 1);
-      tc::mbar_init(empty_bar(st), 1 + 4);  // the MMA commit and the four statistics warps
+      tc::mbar_init(empty_bar(st), IN_STATS ? 1 + 4 : 1);  // the MMA commit [and the statistics warps]
     }
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(dfull_bar(b), 1);
@@ -124,42 +144,44 @@ __global__ void __launch_bounds__(kTHREADS, 1)
     }
     tc::mbar_init_fence();
   }
-  for (int c = tid; c < p.N; c += kTHREADS) {
-    su[c] = p.u[c];
-    sv[c] = p.v[c];
-  }
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
   int bad = 0;
 
-  if (warp == kCOPY_WARP) {
-    // ==== copies: x chunk and W' chunk of step q into stage q % kSTAGES ==============
+  if (warp == R::kCOPY) {
+    // ==== copies: x chunk and W' chunk of each step into the next ring stage ==========
     if (lane == 0) {
-      int q = 0, st = 0;
+      int st = 0;
+      uint32_t ph = 0, first = 1;  // ring phase; the first pass needs no free stage
       for (int it = blockIdx.x; it < p.n_items && !bad; it += gridDim.x) {
         int t0, j0, ntile;
         item_tiles(it, t0, j0, ntile);
-        for (int s_ = 0; s_ < ntile * kcn; ++s_, ++q) {
-          if (q >= kSTAGES && !tc::mbar_wait(empty_bar(st), ((q / kSTAGES) - 1) & 1, kWaitLimitNs)) {
+        for (int s_ = 0; s_ < ntile * kcn; ++s_) {
+          if (!first && !tc::mbar_wait(empty_bar(st), ph ^ 1, kWaitLimitNs)) {
             bad = 1;
             break;
           }
           const int kc = s_ % kcn, n0 = (j0 + s_ / kcn) * p.NT;
-          const uint32_t base = smem0 + st * kSTAGE;
-          tc::mbar_expect_tx(full_bar(st), kXCH + p.NT * 64);
+          const uint32_t base = smem0 + st * p.stage_bytes;
+          tc::mbar_expect_tx(full_bar(st), p.stage_bytes);
           tc::tile_load_2d(base, &x_map, kc * kKC, t0, full_bar(st));
           tc::tile_load_2d(base + kXCH, &w_map, kc * kKC, n0, full_bar(st));
-          st = st + 1 == kSTAGES ? 0 : st + 1;
+          if (++st == stages) {
+            st = 0;
+            ph ^= 1;
+            first = 0;
+          }
         }
       }
     }
     __syncwarp();
-  } else if (warp == kMMA_WARP) {
+  } else if (warp == R::kMMA) {
     // ==== MMA issue: one thread; the warp waits together ==============================
     const uint32_t idesc = tc::idesc_bf16(128, p.NT, false);
-    int q = 0, st = 0, g = 0;  // global step and output-tile counters
+    int st = 0, g = 0;  // ring stage and output-tile counter
+    uint32_t ph = 0;    // ring phase
     for (int it = blockIdx.x; it < p.n_items && !bad; it += gridDim.x) {
       int t0, j0, ntile;
       item_tiles(it, t0, j0, ntile);
@@ -169,45 +191,50 @@ __global__ void __launch_bounds__(kTHREADS, 1)
           bad = 1;
           break;
         }
-        for (int kc = 0; kc < kcn; ++kc, ++q) {
-          if (!warp_wait(full_bar(st), (q / kSTAGES) & 1)) {
+        for (int kc = 0; kc < kcn; ++kc) {
+          if (!warp_wait(full_bar(st), ph)) {
             bad = 1;
             break;
           }
           if (lane == 0) {
             tc::fence_after_sync();
-            const uint32_t a = smem0 + st * kSTAGE, w = a + kXCH;
+            const uint32_t a = smem0 + st * p.stage_bytes, w = a + kXCH;
 #pragma unroll
-            for (int kk = 0; kk < 2; ++kk)
-              tc::mma_ss(tmem + buf * kMaxNT, tc::sdesc(a + kk * 32, 16, 512, kSW64),
-                         tc::sdesc(w + kk * 32, 16, 512, kSW64), idesc, kc > 0 || kk > 0);
+            for (int kk = 0; kk < 4; ++kk)
+              tc::mma_ss(tmem + buf * kMaxNT, tc::sdesc(a + kk * 32, 16, 1024, kSW128),
+                         tc::sdesc(w + kk * 32, 16, 1024, kSW128), idesc, kc > 0 || kk > 0);
             tc::commit(empty_bar(st));
             if (kc == kcn - 1) tc::commit(dfull_bar(buf));
           }
           __syncwarp();
-          st = st + 1 == kSTAGES ? 0 : st + 1;
+          if (++st == stages) {
+            st = 0;
+            ph ^= 1;
+          }
         }
       }
     }
-  } else if (warp < kEPI_WARP0) {
+  } else if (warp < R::kEPI0) {
     // ==== statistics warps: shifted sums of row r over the item's first output tile =====
     const int r = tid;
-    int q = 0, st = 0, k = 0;  // global step and item counters
+    int st = 0, k = 0;  // ring stage and item counter
+    uint32_t ph = 0;    // ring phase
     for (int it = blockIdx.x; it < p.n_items && !bad; it += gridDim.x, ++k) {
       int t0, j0, ntile;
       item_tiles(it, t0, j0, ntile);
       float shift = 0.0f;
       float2 sh2 = make_float2(0.0f, 0.0f), s1v = make_float2(0.0f, 0.0f), s2v = make_float2(0.0f, 0.0f);
-      for (int s_ = 0; s_ < ntile * kcn; ++s_, ++q) {
-        if (!warp_wait(full_bar(st), (q / kSTAGES) & 1)) {
+      for (int s_ = 0; s_ < ntile * kcn; ++s_) {
+        if (!warp_wait(full_bar(st), ph)) {
           bad = 1;
           break;
         }
         if (s_ < kcn) {
-          const unsigned char* xc = smem + st * kSTAGE;
+          const unsigned char* xc = smem + st * p.stage_bytes;
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const uint4 w4 = *reinterpret_cast<const uint4*>(xc + r * 64 + ((c ^ ((r >> 1) & 3)) << 4));
+          for (int c = 0; c < 8; ++c) {
+            if (s_ * kKC + c * 8 >= p.C) break;  // zero fill past C (C is a multiple of 8)
+            const uint4 w4 = *reinterpret_cast<const uint4*>(xc + r * 128 + ((c ^ (r & 7)) << 4));
             const uint32_t in[4] = {w4.x, w4.y, w4.z, w4.w};
             if (s_ == 0 && c == 0) {
               shift = bf16_lo(in[0]);
@@ -223,7 +250,10 @@ __global__ void __launch_bounds__(kTHREADS, 1)
         }
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(empty_bar(st));
-        st = st + 1 == kSTAGES ? 0 : st + 1;
+        if (++st == stages) {
+          st = 0;
+          ph ^= 1;
+        }
         if (s_ == kcn - 1) {
           // mean = shift + s1 / C; var = s2 / C - (s1 / C)^2 (shifted sums)
           const float m1 = (s1v.x + s1v.y) / p.C;
@@ -241,23 +271,28 @@ __global__ void __launch_bounds__(kTHREADS, 1)
     }
   } else {
     // ==== epilogue warps: rstd * acc - rstd * mean * u + v, bf16, staged TMA stores =====
-    const int ew = warp - kEPI_WARP0, row = (ew & 3) * 32 + lane, half = ew >> 2;  // 16-channel half
-    const int et = ew * 32 + lane;  // 0 .. 255
-    const uint32_t trow = tmem + ((uint32_t)((ew & 3) * 32) << 16);
-    unsigned char* stage_out = smem + kOFF_OUT;
-    int g = 0, k = 0, m = 0;  // output tiles, items, 32-channel slices
+    const int ew = warp - R::kEPI0, quad = ew & 3, parity = ew >> 2;
+    const int row = quad * 32 + lane;
+    const uint32_t trow = tmem + ((uint32_t)(quad * 32) << 16);
+    unsigned char* wstage = smem + p.off_out + ew * (2 * 32 * 64);
+    int g = 0, k = 0, m = 0;  // output tiles, items, slices stored by this warp
     for (int it = blockIdx.x; it < p.n_items && !bad; it += gridDim.x, ++k) {
       int t0, j0, ntile;
       item_tiles(it, t0, j0, ntile);
-      const int sb = k & 1;
-      if (!warp_wait(sfull_bar(sb), (k >> 1) & 1)) {
-        bad = 1;
-        break;
+      float2 ms;
+      if constexpr (IN_STATS) {
+        const int sb = k & 1;
+        if (!warp_wait(sfull_bar(sb), (k >> 1) & 1)) {
+          bad = 1;
+          break;
+        }
+        ms = sstats[sb * kBM + row];
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(sfree_bar(sb));
+      } else {
+        ms = t0 + row < p.T ? p.stats[t0 + row] : make_float2(0.0f, 0.0f);
       }
-      const float2 ms = sstats[sb * kBM + row];
       const float rstd = ms.y, nmr = -ms.x * ms.y;
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(sfree_bar(sb));
       const float2 r2 = make_float2(rstd, rstd), nm2 = make_float2(nmr, nmr);
       for (int jj = 0; jj < ntile; ++jj, ++g) {
         const int buf = g & 1;
@@ -267,22 +302,23 @@ __global__ void __launch_bounds__(kTHREADS, 1)
         }
         tc::fence_after_sync();
         const int n0 = (j0 + jj) * p.NT;
-        for (int c0 = 0; c0 < p.NT; c0 += 32, ++m) {
-          unsigned char* so = stage_out + (m & 1) * (kBM * 64);
+        for (int c0 = parity * kSC; c0 < p.NT; c0 += 2 * kSC, ++m) {
+          unsigned char* so = wstage + (m & 1) * (32 * 64);
           if (m >= 2) {
-            if (et == 0) tc::bulk_wait_read<1>();  // the store of slice m - 2 has read its tile
-            asm volatile("bar.sync 1, %0;\n" ::"n"(kEPI_THREADS) : "memory");
+            if (lane == 0) tc::bulk_wait_read<1>();  // the store of slice m - 2 has read its tile
+            __syncwarp();
           }
-          uint32_t a[16];
-          tc::ld16_wait(trow + buf * kMaxNT + c0 + 16 * half, a);
-          const float4* uu = reinterpret_cast<const float4*>(su + n0 + c0 + 16 * half);
-          const float4* vv = reinterpret_cast<const float4*>(sv + n0 + c0 + 16 * half);
+          uint32_t a[32];
+          tc::ld32_wait(trow + buf * kMaxNT + c0, a);
+          // u and v: the same 32 channels for every lane (broadcast loads through L1)
+          const float4* uu = reinterpret_cast<const float4*>(p.u + n0 + c0);
+          const float4* vv = reinterpret_cast<const float4*>(p.v + n0 + c0);
 #pragma unroll
-          for (int c = 0; c < 2; ++c) {
+          for (int c = 0; c < 4; ++c) {
             uint32_t o[4];
 #pragma unroll
             for (int w2 = 0; w2 < 2; ++w2) {
-              const float4 u4 = uu[2 * c + w2], v4 = vv[2 * c + w2];
+              const float4 u4 = __ldg(uu + 2 * c + w2), v4 = __ldg(vv + 2 * c + w2);
               const int e = 8 * c + 4 * w2;
               const float2 c0v = __ffma2_rn(nm2, make_float2(u4.x, u4.y), make_float2(v4.x, v4.y));
               const float2 c1v = __ffma2_rn(nm2, make_float2(u4.z, u4.w), make_float2(v4.z, v4.w));
@@ -292,14 +328,13 @@ __global__ void __launch_bounds__(kTHREADS, 1)
               o[2 * w2] = pack_bf16(y0.x, y0.y);
               o[2 * w2 + 1] = pack_bf16(y1.x, y1.y);
             }
-            const int chunk = 2 * half + c;
-            *reinterpret_cast<uint4*>(so + row * 64 + ((chunk ^ ((row >> 1) & 3)) << 4)) =
+            *reinterpret_cast<uint4*>(so + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4)) =
                 make_uint4(o[0], o[1], o[2], o[3]);
           }
           tc::fence_proxy_async();  // the staging tile to the copy engine
-          asm volatile("bar.sync 1, %0;\n" ::"n"(kEPI_THREADS) : "memory");
-          if (et == 0) {
-            tc::tile_store_2d(&out_map, n0 + c0, t0, smem_u32(so));
+          __syncwarp();
+          if (lane == 0) {
+            tc::tile_store_2d(&out_map, n0 + c0, t0 + quad * 32, smem_u32(so));
             tc::bulk_commit();
           }
         }
@@ -308,49 +343,99 @@ __global__ void __launch_bounds__(kTHREADS, 1)
         if (lane == 0) tc::mbar_arrive(dfree_bar(buf));
       }
     }
-    if (et == 0) tc::bulk_wait_all();
+    if (lane == 0) tc::bulk_wait_all();
   }
   if (bad && p.status != nullptr) atomicOr(p.status, 1);
 
   tc::fence_before_sync();
   __syncthreads();
-  if (warp == kMMA_WARP) tc::tmem_dealloc<kTMEM_COLS>(tmem);
+  if (warp == R::kMMA) tc::tmem_dealloc<kTMEM_COLS>(tmem);
 }
 
-// W'[n][c] = bf16(gamma_c W[n][c]); u_n = sum_c W'[n][c]; v_n = sum_c beta_c W[n][c] + b_n.
-// One warp per output channel n.
-__global__ void qkv_fold_kernel(const __nv_bfloat16* __restrict__ w, const float* __restrict__ gamma,
+// Blocks [0, fold_blocks): W'[n][c] = bf16(gamma_c W[n][c]), u_n = sum_c W'[n][c],
+// v_n = sum_c beta_c W[n][c] + b_n, one warp per output channel n.
+// Blocks from fold_blocks on (when stats is given): (mean, 1 / sqrt(var + eps)) of each
+// token's C channels, four tokens per warp with their loads in flight together; shifted
+// sums (by the row's first value) in fp32, reduced across the warp.
+__global__ void qkv_prep_kernel(const __nv_bfloat16* __restrict__ w, const float* __restrict__ gamma,
                                 const float* __restrict__ beta, const float* __restrict__ b, int C, int N,
-                                __nv_bfloat16* __restrict__ wf, float* __restrict__ u, float* __restrict__ v) {
-  const int lane = threadIdx.x & 31;
-  for (int n = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); n < N; n += gridDim.x * (blockDim.x >> 5)) {
-    float su_ = 0.0f, sv_ = 0.0f;
-    for (int c = lane; c < C; c += 32) {
-      const float wv = __bfloat162float(w[(int64_t)n * C + c]);
-      const __nv_bfloat16 f = __float2bfloat16_rn(gamma[c] * wv);
-      wf[(int64_t)n * C + c] = f;
-      su_ += __bfloat162float(f);
-      sv_ = fmaf(beta[c], wv, sv_);
+                                __nv_bfloat16* __restrict__ wf, float* __restrict__ u, float* __restrict__ v,
+                                int fold_blocks, const __nv_bfloat16* __restrict__ x, int T, float eps,
+                                float2* __restrict__ stats) {
+  const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5, wpb = blockDim.x >> 5;
+  if ((int)blockIdx.x < fold_blocks) {
+    for (int n = blockIdx.x * wpb + wib; n < N; n += fold_blocks * wpb) {
+      float su_ = 0.0f, sv_ = 0.0f;
+      for (int c = lane; c < C; c += 32) {
+        const float wv = __bfloat162float(w[(int64_t)n * C + c]);
+        const __nv_bfloat16 f = __float2bfloat16_rn(gamma[c] * wv);
+        wf[(int64_t)n * C + c] = f;
+        su_ += __bfloat162float(f);
+        sv_ = fmaf(beta[c], wv, sv_);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        su_ += __shfl_xor_sync(0xffffffffu, su_, o);
+        sv_ += __shfl_xor_sync(0xffffffffu, sv_, o);
+      }
+      if (lane == 0) {
+        u[n] = su_;
+        v[n] = sv_ + b[n];
+      }
+    }
+    return;
+  }
+  const int sblocks = gridDim.x - fold_blocks;
+  for (int64_t t0 = ((int64_t)(blockIdx.x - fold_blocks) * wpb + wib) * 4; t0 < T; t0 += (int64_t)sblocks * wpb * 4) {
+    const int nr = T - t0 < 4 ? (int)(T - t0) : 4;
+    float shift[4];
+    float2 s1[4], s2[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      shift[r] = r < nr ? __bfloat162float(x[(t0 + r) * C]) : 0.0f;
+      s1[r] = make_float2(0.0f, 0.0f);
+      s2[r] = make_float2(0.0f, 0.0f);
+    }
+    for (int c = lane; c < C / 8; c += 32) {
+      uint4 w4[4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+        w4[r] = r < nr ? reinterpret_cast<const uint4*>(x + (t0 + r) * C)[c] : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const uint32_t in[4] = {w4[r].x, w4[r].y, w4[r].z, w4[r].w};
+        const float2 sh2 = make_float2(-shift[r], -shift[r]);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float2 a = __fadd2_rn(make_float2(bf16_lo(in[k]), bf16_hi(in[k])), sh2);
+          s1[r] = __fadd2_rn(s1[r], a);
+          s2[r] = __ffma2_rn(a, a, s2[r]);
+        }
+      }
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      su_ += __shfl_xor_sync(0xffffffffu, su_, o);
-      sv_ += __shfl_xor_sync(0xffffffffu, sv_, o);
-    }
-    if (lane == 0) {
-      u[n] = su_;
-      v[n] = sv_ + b[n];
+    for (int r = 0; r < 4; ++r) {
+      float a1 = s1[r].x + s1[r].y, a2 = s2[r].x + s2[r].y;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        a1 += __shfl_xor_sync(0xffffffffu, a1, o);
+        a2 += __shfl_xor_sync(0xffffffffu, a2, o);
+      }
+      if (lane == 0 && r < nr) {
+        const float m1 = a1 / C;  // mean = shift + m1; var = a2 / C - m1^2
+        stats[t0 + r] = make_float2(shift[r] + m1, rsqrtf(fmaxf(a2 / C - m1 * m1, 0.0f) + eps));
+      }
     }
   }
 }
 
 }  // namespace
 
-// Workspace of one call: W' [3C, C] bf16, then u and v [3C] fp32, each 256-byte aligned.
-size_t qkv_workspace_bytes(int C) {
-  const size_t wf = ((size_t)3 * C * C * 2 + 255) & ~(size_t)255;
-  const size_t uv = ((size_t)3 * C * 4 + 255) & ~(size_t)255;
-  return wf + 2 * uv;
+// Workspace of one call: W' [3C, C] bf16, u and v [3C] fp32, then the token statistics
+// [T] (mean, rstd), each part 256-byte aligned.
+static size_t align256(size_t n) { return (n + 255) & ~(size_t)255; }
+size_t qkv_workspace_bytes(int C, int64_t T) {
+  return align256((size_t)3 * C * C * 2) + 2 * align256((size_t)3 * C * 4) + align256((size_t)T * 8);
 }
 
 // Output-channel tile: the largest multiple of 32 up to 256 that divides 3C (C is a
@@ -364,52 +449,19 @@ static int qkv_tile(int N) {
 cudaError_t qkv_proj_launch(const void* x, const float* gamma, const float* beta, const void* w, const float* b,
                             void* out, int T, int C, float eps, void* workspace, int* status, cudaStream_t st) {
   if (T <= 0) return cudaSuccess;
-  if (C % kKC != 0 || C < kKC || C > kMaxC) return cudaErrorInvalidValue;
+  if (C % 32 != 0 || C < 32 || C > kMaxC) return cudaErrorInvalidValue;
   PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder_fn();
   if (encode == nullptr) return cudaErrorNotSupported;
   const int N = 3 * C, NT = qkv_tile(N);
   unsigned char* ws = static_cast<unsigned char*>(workspace);
   __nv_bfloat16* wf = reinterpret_cast<__nv_bfloat16*>(ws);
-  float* u = reinterpret_cast<float*>(ws + (((size_t)N * C * 2 + 255) & ~(size_t)255));
-  float* v = u + ((((size_t)N * 4 + 255) & ~(size_t)255) / 4);
-  qkv_fold_kernel<<<(N + 7) / 8, 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(w), gamma, beta, b, C, N, wf,
-                                               u, v);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  CUtensorMap x_map, w_map;
-  const cuuint32_t es[2] = {1, 1};
-  {
-    const cuuint64_t dims[2] = {(cuuint64_t)C, (cuuint64_t)T};
-    const cuuint64_t strides[1] = {(cuuint64_t)C * 2};
-    const cuuint32_t box[2] = {kKC, kBM};
-    if (encode(&x_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(x), dims, strides, box, es,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return cudaErrorInvalidValue;
-  }
-  {
-    const cuuint64_t dims[2] = {(cuuint64_t)C, (cuuint64_t)N};
-    const cuuint64_t strides[1] = {(cuuint64_t)C * 2};
-    const cuuint32_t box[2] = {kKC, (cuuint32_t)NT};
-    if (encode(&w_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, wf, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-               CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
-        CUDA_SUCCESS)
-      return cudaErrorInvalidValue;
-  }
-  CUtensorMap out_map;
-  {
-    const cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)T};
-    const cuuint64_t strides[1] = {(cuuint64_t)N * 2};
-    const cuuint32_t box[2] = {kKC, kBM};
-    if (encode(&out_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, out, dims, strides, box, es,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return cudaErrorInvalidValue;
-  }
-  int dev = 0, sms = 0;
-  e = cudaGetDevice(&dev);
+  float* u = reinterpret_cast<float*>(ws + align256((size_t)N * C * 2));
+  float* v = u + align256((size_t)N * 4) / 4;
+  float2* stats = reinterpret_cast<float2*>(reinterpret_cast<unsigned char*>(v) + align256((size_t)N * 4));
+  int dev = 0, sms = 0, smem_max = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(qkv_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSMEM);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&smem_max, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
   if (e != cudaSuccess) return e;
   // Work items: token tiles times groups of output-channel tiles, at least four per SM
   // when the channel tiles allow it; one persistent CTA per SM walks them.
@@ -419,21 +471,76 @@ cudaError_t qkv_proj_launch(const void* x, const float* gamma, const float* beta
   const int per = (n_tiles + groups - 1) / groups;
   groups = (n_tiles + per - 1) / per;
   const int n_items = n_tt * groups;
+  const bool in_stats = groups == 1;  // each token tile is one item: sum the statistics on chip
+  const int fold_blocks = (N + 7) / 8;
+  const int stat_blocks = in_stats ? 0 : (int)std::min<int64_t>(((int64_t)T + 31) / 32, 16 * sms);
+  qkv_prep_kernel<<<fold_blocks + stat_blocks, 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(w), gamma,
+                                                             beta, b, C, N, wf, u, v, fold_blocks,
+                                                             reinterpret_cast<const __nv_bfloat16*>(x), T, eps,
+                                                             stats);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  CUtensorMap x_map, w_map;
+  const cuuint32_t es[2] = {1, 1};
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)C, (cuuint64_t)T};
+    const cuuint64_t strides[1] = {(cuuint64_t)C * 2};
+    const cuuint32_t box[2] = {kKC, kBM};
+    if (encode(&x_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(x), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)C, (cuuint64_t)N};
+    const cuuint64_t strides[1] = {(cuuint64_t)C * 2};
+    const cuuint32_t box[2] = {kKC, (cuuint32_t)NT};
+    if (encode(&w_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, wf, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
+        CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  CUtensorMap out_map;
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)T};
+    const cuuint64_t strides[1] = {(cuuint64_t)N * 2};
+    const cuuint32_t box[2] = {kSC, 32};
+    if (encode(&out_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, out, dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
   QkvParams p;
   p.out = reinterpret_cast<__nv_bfloat16*>(out);
   p.u = u;
   p.v = v;
+  p.stats = in_stats ? nullptr : stats;
   p.status = status;
   p.T = T;
   p.C = C;
   p.N = N;
   p.NT = NT;
   p.tiles_per_item = per;
+  p.stage_bytes = kXCH + NT * 128;
+  const int fixed = (in_stats ? kSTATS_BYTES : 0) + kTAIL_BYTES;
+  p.stages = std::min(kMaxSTAGES, (smem_max - fixed) / p.stage_bytes);
+  if (p.stages < 2) return cudaErrorInvalidConfiguration;
+  p.off_stats = p.stages * p.stage_bytes;
+  p.off_out = p.off_stats + (in_stats ? kSTATS_BYTES : 0);
+  p.off_bar = p.off_out + kOUT_BYTES;
+  const int smem = std::max(kMinSMEM, p.stages * p.stage_bytes + fixed);
   p.n_tt = n_tt;
   p.n_items = n_items;
   p.eps = eps;
-  return launch_pdl(qkv_gemm_kernel, dim3(n_items < sms ? n_items : sms), dim3(kTHREADS), kSMEM, st, x_map, w_map,
-                    out_map, p);
+  const dim3 grid(n_items < sms ? n_items : sms);
+  if (in_stats) {
+    e = cudaFuncSetAttribute(qkv_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(qkv_gemm_kernel<true>, grid, dim3(Roles<true>::kTHREADS), smem, st, x_map, w_map, out_map, p);
+  }
+  e = cudaFuncSetAttribute(qkv_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(qkv_gemm_kernel<false>, grid, dim3(Roles<false>::kTHREADS), smem, st, x_map, w_map, out_map, p);
 }
 
 }  // namespace swin

@@ -231,6 +231,20 @@ __device__ __forceinline__ void ld16_wait(uint32_t taddr, uint32_t (&a)[16]) {
       : "memory");
 }
 
+// 32 columns of this thread's lane.
+__device__ __forceinline__ void ld32_wait(uint32_t taddr, uint32_t (&a)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
+      "tcgen05.wait::ld.sync.aligned;\n"
+      : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3]), "=r"(a[4]), "=r"(a[5]), "=r"(a[6]), "=r"(a[7]),
+        "=r"(a[8]), "=r"(a[9]), "=r"(a[10]), "=r"(a[11]), "=r"(a[12]), "=r"(a[13]), "=r"(a[14]), "=r"(a[15]),
+        "=r"(a[16]), "=r"(a[17]), "=r"(a[18]), "=r"(a[19]), "=r"(a[20]), "=r"(a[21]), "=r"(a[22]), "=r"(a[23]),
+        "=r"(a[24]), "=r"(a[25]), "=r"(a[26]), "=r"(a[27]), "=r"(a[28]), "=r"(a[29]), "=r"(a[30]), "=r"(a[31])
+      : "r"(taddr)
+      : "memory");
+}
+
 // 32 columns at `a` and one column at `c` of this thread's lane.
 __device__ __forceinline__ void ld32_1_wait(uint32_t a_addr, uint32_t c_addr, uint32_t (&a)[32], uint32_t& c) {
   asm volatile(

@@ -50,7 +50,7 @@ def _run(x, g, be, w, b, eps=1e-5):
 
 
 @pytest.mark.parametrize("T,C", [(1, 32), (127, 96), (129, 128), (300, 192), (1000, 256), (77, 384),
-                                 (260, 768), (130, 1536), (4096, 192)])
+                                 (260, 768), (130, 1536), (4096, 192), (555, 160)])
 def test_qkv_proj_against_oracle(T, C):
     wl = workload(1, 1, T, C, C // 32, 1, 0, seed=T + C)
     x, g, be, w, b = inputs.make_producer(wl)
@@ -67,6 +67,25 @@ def test_qkv_proj_full_size_workloads(name):
     for bi in sorted({0, wl.B - 1}):
         ref = oracle.qkv_proj(_f64(x[bi]), _f64(g), _f64(be), _f64(w), _f64(b))
         assert_close_qkv(f"{name} qkv[{bi}]", y[bi], ref)
+
+
+@pytest.mark.parametrize("C", [160, 96])
+def test_qkv_proj_many_tokens_statistics_on_chip(C):
+    """Enough tokens (over four 128-token tiles per SM) that every token tile is one work
+    item and the statistics are summed from the staged x tiles; C not a multiple of the
+    64-channel chunk (zero-filled tail), a ragged last token tile and a large common offset
+    per token. Compared on sampled rows (the operation is row-independent)."""
+    T = 80001
+    wl = workload(1, 1, T, C, C // 32, 1, 0, seed=C)
+    x, g, be, w, b = inputs.make_producer(wl)
+    x = (x.float() * 3.0 + 20.0).to(torch.bfloat16)
+    y = _run(x, g, be, w, b).cpu().reshape(T, 3 * C)
+    xs = x.reshape(T, C)
+    gen = torch.Generator().manual_seed(C)
+    rows = torch.cat([torch.arange(0, 256), torch.randint(256, T - 256, (512,), generator=gen),
+                      torch.arange(T - 256, T)])
+    ref = oracle.qkv_proj(_f64(xs[rows]), _f64(g), _f64(be), _f64(w), _f64(b))
+    assert_close_qkv(f"qkv T={T} C={C} (sampled rows)", y[rows], ref)
 
 
 def test_qkv_proj_is_deterministic_and_large_offsets_are_stable():
@@ -100,9 +119,9 @@ def test_qkv_proj_error_paths():
     v = torch.zeros(288, dtype=torch.float32, device=DEV)
     w = torch.zeros(288, 96, dtype=torch.bfloat16, device=DEV)
     out = torch.full((4, 288), 3.0, dtype=torch.bfloat16, device=DEV)
-    nws = capi.swin_wattn_qkv_workspace_bytes(96)
-    assert nws >= 288 * 96 * 2 + 2 * 288 * 4
-    assert capi.swin_wattn_qkv_workspace_bytes(80) == 0
+    nws = capi.swin_wattn_qkv_workspace_bytes(96, 4)
+    assert nws >= 288 * 96 * 2 + 2 * 288 * 4 + 4 * 8
+    assert capi.swin_wattn_qkv_workspace_bytes(80, 4) == 0
     ws = torch.empty(nws, dtype=torch.uint8, device=DEV)
     s = torch.cuda.current_stream().cuda_stream
     f = lambda xp, T, C, nb: capi.swin_wattn_qkv_proj(xp, v.data_ptr(), v.data_ptr(), w.data_ptr(), v.data_ptr(),
