@@ -60,6 +60,7 @@ def bind(path: str) -> ctypes.CDLL:
         "oracle_fwd": ([_D, _D] + [_i] * 7 + [_D], None),
         "oracle_bwd": ([_D, _D, _D] + [_i] * 7 + [_D, _D], None),
         "oracle_qkv_proj": ([_D, _D, _D, _D, _D, _i, _i, ctypes.c_double, _D], None),
+        "oracle_proj_residual": ([_D, _D, _D, _D, _i, _i, _D], None),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -200,6 +201,19 @@ def qkv_proj(x, gamma, beta, w, b, eps: float = 1e-5) -> np.ndarray:
     T = int(np.prod(x.shape[:-1]))
     out = np.empty(x.shape[:-1] + (3 * C,), dtype=np.float64)
     _load().oracle_qkv_proj(_dp(x), _dp(gamma), _dp(beta), _dp(w), _dp(b), T, C, float(eps), _dp(out))
+    return out
+
+
+def proj_residual(o, wp, bp, residual) -> np.ndarray:
+    """residual + o Wp^T + bp over the last axis: o and residual [..., C], Wp [C, C],
+    bp [C] -> [..., C] (float64)."""
+    o, wp, bp, residual = _f64(o), _f64(wp), _f64(bp), _f64(residual)
+    C = o.shape[-1]
+    if wp.shape != (C, C) or bp.shape != (C,) or residual.shape != o.shape:
+        raise ValueError("oracle: proj_residual shapes")
+    T = int(np.prod(o.shape[:-1]))
+    out = np.empty(o.shape, dtype=np.float64)
+    _load().oracle_proj_residual(_dp(o), _dp(wp), _dp(bp), _dp(residual), T, C, _dp(out))
     return out
 
 

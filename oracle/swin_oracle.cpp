@@ -40,6 +40,13 @@
 //  R16 qkv = LN(x) W^T + b with W [3C, C] (row n is output channel n, in the channel order
 //      of R3) and b [3C].
 //
+// The consumer step after the attention (the output projection followed by the bias and
+// residual addition that the NVIDIA talk's section 3 "inference optimisation" fuses into one
+// elementwise pass, its half2 example) also follows the plain definition:
+//  R18 y = residual + O Wp^T + bp, with O the attention output [T, C] (channel order of
+//      R4), Wp [C, C] (row n is output channel n), bp [C], and the residual the block
+//      input at the same token.
+//
 // Everything here runs in double precision on whatever values it is given. Inputs are
 // expected to be the bf16-rounded values the GPU path also sees, widened to double.
 
@@ -388,6 +395,22 @@ void oracle_qkv_proj(const double* x, const double* gamma, const double* beta, c
       double acc = b[n];
       for (int c = 0; c < C; ++c) acc += xn[c] * wr[c];
       qkv[t * N + n] = acc;
+    }
+  }
+}
+
+// R18: y[t] = residual[t] + O[t] Wp^T + bp for tokens t < T; O, residual, y [T, C],
+// Wp [C, C], bp [C].
+void oracle_proj_residual(const double* o, const double* wp, const double* bp, const double* residual, int T,
+                          int C, double* y) {
+#pragma omp parallel for schedule(static)
+  for (int64_t t = 0; t < T; ++t) {
+    const double* orow = o + t * C;
+    for (int n = 0; n < C; ++n) {
+      const double* wr = wp + (int64_t)n * C;
+      double acc = 0.0;
+      for (int c = 0; c < C; ++c) acc += orow[c] * wr[c];
+      y[t * C + n] = residual[t * C + n] + (acc + bp[n]);
     }
   }
 }

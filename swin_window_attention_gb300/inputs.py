@@ -150,6 +150,20 @@ def make_producer(wl: Workload):
     return x, gamma.contiguous(), beta.contiguous(), w, b
 
 
+def make_consumer(wl: Workload):
+    """Inputs of the consumer step after the attention (the output projection, then bias
+    and residual), CPU: o [B,H,W,C] bf16 ~ N(0, 0.5^2) (the attention output, an average of
+    N(0,1) values); Wp [C, C] bf16, trunc-normal (std 0.02, +-0.04); bp fp32 [C] =
+    0.02 N(0,1); the residual (the block input) [B,H,W,C] bf16 ~ N(0,1). Seeds: the
+    workload's seed + 7, 8, 9, 10."""
+    C = wl.C
+    o = (0.5 * normal((wl.B, wl.H, wl.W, C), wl.seed + 7)).to(torch.bfloat16)
+    wp = trunc_normal((C, C), wl.seed + 8).to(torch.bfloat16)
+    bp = 0.02 * normal((C,), wl.seed + 9)
+    r = normal((wl.B, wl.H, wl.W, C), wl.seed + 10).to(torch.bfloat16)
+    return o, wp, bp.contiguous(), r
+
+
 def act_f64(x: torch.Tensor):
     """Exact float64 numpy copy of the values the GPU path sees: bf16 inputs are widened
     as they are; fp32 inputs are first rounded to bf16 (round-to-nearest-even), which
