@@ -193,14 +193,40 @@ int swin_wattn_debug_maps(swin_wattn_plan_t plan, int32_t* gather, int32_t* reli
  *   u = row sums of W', v = beta W^T + b,
  * with the row statistics in fp32 and the product accumulated in fp32 on bf16 x and W';
  * qkv is rounded to bf16. C must be a multiple of 32 in [32, 1536]. The cyclic shift and
- * window partition are not applied here: the attention folds them into its loads. Three
- * kernel launches on `stream` (the fold, the statistics, the product); nothing is
- * allocated. swin_wattn_qkv_workspace_bytes returns 0 for an unsupported C.
+ * window partition are not applied here: the attention folds them into its loads. Two
+ * kernel launches on `stream` (the weight fold, with the token statistics when the product
+ * does not sum them itself; the product); nothing is allocated.
+ * swin_wattn_qkv_workspace_bytes returns 0 for an unsupported C.
  */
 size_t swin_wattn_qkv_workspace_bytes(int C, int tokens);
 int swin_wattn_qkv_proj(const void* x, const float* gamma, const float* beta, const void* w_qkv,
                         const float* b_qkv, void* qkv, int tokens, int C, float eps, void* workspace,
                         size_t workspace_bytes, int* status, struct CUstream_st* stream);
+
+/*
+ * The consumer step after the attention: the output projection, then its bias and the
+ * residual added, fused into the product's epilogue (NVIDIA Swin talk, uticex.com article
+ * 1598, section 3 "inference optimisation": the bias-plus-residual pass in its half2
+ * example):
+ *   y[t] = residual[t] + o[t] Wp^T + bp   for each token t < tokens.
+ * Arguments (device pointers unless stated):
+ *   o        bf16 [tokens, C], 16-byte aligned: the attention output (swin_wattn_fwd's
+ *            out, channel order h*32 + d);
+ *   w_proj   bf16 [C, C] (row n = output channel n);
+ *   b_proj   fp32 [C];
+ *   residual bf16 [tokens, C], 16-byte aligned: the block input (the shortcut);
+ *   y        bf16 [tokens, C], 16-byte aligned, written. y may be the residual buffer
+ *            itself (each element is read before it is written) but must not overlap o;
+ *   status   optional device int (may be NULL): bit 0 is OR-ed in if a bounded device
+ *            wait ran out (then y is not valid).
+ * The product is accumulated in fp32 on the bf16 operands, bp and the residual are added
+ * in fp32, and y is rounded to bf16. C must be a multiple of 32 in [32, 1536]. One kernel
+ * launch on `stream`; nothing is allocated. Errors: INVALID_ARG for negative tokens,
+ * overlapping o and y, or a pointer that is not device memory; MISALIGNED for a pointer
+ * off its alignment; UNSUPPORTED for C.
+ */
+int swin_wattn_proj_residual(const void* o, const void* w_proj, const float* b_proj, const void* residual,
+                             void* y, int tokens, int C, int* status, struct CUstream_st* stream);
 
 /*
  * Choose the plan's forward kernel (SWIN_WATTN_KERNEL_*). Both kernels compute the same

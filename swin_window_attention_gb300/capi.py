@@ -39,6 +39,7 @@ SIGNATURES = {
     "swin_wattn_bwd_noalloc": ([_vp, _vp, _vp, _vp, _vp] + [_i] * 8 + [_vp], _i),
     "swin_wattn_qkv_workspace_bytes": ([_i, _i], ctypes.c_size_t),
     "swin_wattn_qkv_proj": ([_vp] * 6 + [_i, _i, ctypes.c_float, _vp, ctypes.c_size_t, _vp, _vp], _i),
+    "swin_wattn_proj_residual": ([_vp] * 5 + [_i, _i, _vp, _vp], _i),
     "swin_wattn_set_fwd_kernel": ([_vp, _i], _i),
     "swin_wattn_fwd_kernel": ([_vp], _i),
     "swin_wattn_device_status": ([_vp, _vp], _i),
@@ -144,6 +145,27 @@ def qkv_proj(x, gamma, beta, w, b, qkv=None, eps=1e-5, status=None, workspace=No
     if rc != OK:
         raise SwinWAttnError("swin_wattn_qkv_proj", rc)
     return qkv
+
+
+def swin_wattn_proj_residual(o_ptr, wp_ptr, bp_ptr, residual_ptr, y_ptr, tokens, C, status_ptr, stream):
+    return load().swin_wattn_proj_residual(o_ptr, wp_ptr, bp_ptr, residual_ptr, y_ptr, tokens, C, status_ptr,
+                                           stream)
+
+
+def proj_residual(o, wp, bp, residual, y=None, status=None, stream=None):
+    """residual + o Wp^T + bp over the last axis of the bf16 CUDA tensors o and residual
+    [..., C] into a bf16 [..., C] tensor (allocated here when not given; it may be the
+    residual itself)."""
+    import torch
+    C = o.shape[-1]
+    if y is None:
+        y = torch.empty(o.shape, dtype=torch.bfloat16, device=o.device)
+    rc = swin_wattn_proj_residual(o.data_ptr(), wp.data_ptr(), bp.data_ptr(), residual.data_ptr(), y.data_ptr(),
+                                  o.numel() // C, C, None if status is None else status.data_ptr(),
+                                  _stream_handle(stream))
+    if rc != OK:
+        raise SwinWAttnError("swin_wattn_proj_residual", rc)
+    return y
 
 
 def swin_wattn_set_fwd_kernel(plan, kernel):

@@ -28,6 +28,8 @@ cudaError_t bwd_config(const Plan& pl, BwdLaunch* L);
 cudaError_t qkv_proj_launch(const void* x, const float* gamma, const float* beta, const void* w, const float* b,
                             void* out, int T, int C, float eps, void* workspace, int* status, cudaStream_t st);
 size_t qkv_workspace_bytes(int C, int64_t T);
+cudaError_t proj_residual_launch(const void* o, const void* wp, const float* bp, const void* residual, void* y,
+                                 int T, int C, int* status, cudaStream_t st);
 cudaError_t bwd_launch(const Plan& pl, const BwdLaunch& L, const void* qkv, const void* dout,
                        void* dqkv, float* dtable, cudaStream_t st);
 }  // namespace swin
@@ -401,8 +403,33 @@ int swin_wattn_qkv_proj(const void* x, const float* gamma, const float* beta, co
   if (status != nullptr && (rc = check_device_ptr(status, 4)) != SWIN_WATTN_OK) return rc;
   cudaError_t e = swin::qkv_proj_launch(x, gamma, beta, w_qkv, b_qkv, qkv, tokens, C, eps, workspace, status,
                                         reinterpret_cast<cudaStream_t>(stream));
-  g_launches += 3;
+  g_launches += 2;
   return e == cudaSuccess ? SWIN_WATTN_OK : cuda_fail(e, "swin_wattn_qkv_proj");
+}
+
+int swin_wattn_proj_residual(const void* o, const void* w_proj, const float* b_proj, const void* residual,
+                             void* y, int tokens, int C, int* status, struct CUstream_st* stream) {
+  if (tokens < 0) return SWIN_WATTN_ERR_INVALID_ARG;
+  if (C < 32 || C > 1536 || C % 32 != 0) return SWIN_WATTN_ERR_UNSUPPORTED;
+  if ((int64_t)tokens >= ((int64_t)1 << 31)) return SWIN_WATTN_ERR_UNSUPPORTED;
+  if (tokens == 0) return SWIN_WATTN_OK;
+  int rc;
+  if ((rc = check_device_ptr(o, 16)) != SWIN_WATTN_OK) return rc;
+  if ((rc = check_device_ptr(w_proj, 16)) != SWIN_WATTN_OK) return rc;
+  if ((rc = check_device_ptr(residual, 16)) != SWIN_WATTN_OK) return rc;
+  if ((rc = check_device_ptr(y, 16)) != SWIN_WATTN_OK) return rc;
+  if ((rc = check_device_ptr(b_proj, 4)) != SWIN_WATTN_OK) return rc;
+  if (status != nullptr && (rc = check_device_ptr(status, 4)) != SWIN_WATTN_OK) return rc;
+  const uintptr_t ob = reinterpret_cast<uintptr_t>(o), yb = reinterpret_cast<uintptr_t>(y);
+  const uintptr_t bytes = (uintptr_t)tokens * (uintptr_t)C * 2;
+  if (ob < yb + bytes && yb < ob + bytes) {
+    swin::set_last_error("swin_wattn_proj_residual: y overlaps o");
+    return SWIN_WATTN_ERR_INVALID_ARG;
+  }
+  cudaError_t e = swin::proj_residual_launch(o, w_proj, b_proj, residual, y, tokens, C, status,
+                                             reinterpret_cast<cudaStream_t>(stream));
+  ++g_launches;
+  return e == cudaSuccess ? SWIN_WATTN_OK : cuda_fail(e, "swin_wattn_proj_residual");
 }
 
 int swin_wattn_set_fwd_kernel(swin_wattn_plan_t plan, int kernel) {

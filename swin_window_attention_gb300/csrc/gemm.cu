@@ -1,41 +1,49 @@
-// The producer step in front of the attention: LayerNorm over the C channels of each
-// token, then qkv = LN(x) W^T + b (W [3C, C] bf16, b [3C] fp32), written as the
-// [tokens, 3C] bf16 tensor the attention reads. The NVIDIA Swin talk (uticex.com article
-// 1598, section 2 "training optimisation") lists LayerNorm and the qkv GEMM among the
-// operations fused around the window attention; the cyclic shift and the window
-// partition that the talk fuses with them are already folded into the attention's
-// loads here, so this kernel writes qkv in plain token order.
+// The two matrix products around the attention, on the fifth-generation tensor cores.
+//
+// Producer (in front of the attention): LayerNorm over the C channels of each token, then
+// qkv = LN(x) W^T + b (W [3C, C] bf16, b [3C] fp32), written as the [tokens, 3C] bf16
+// tensor the attention reads. The NVIDIA Swin talk (uticex.com article 1598, section 2
+// "training optimisation") lists LayerNorm and the qkv GEMM among the operations fused
+// around the window attention, and its section 3 fuses the qkv GEMM with its bias; the
+// cyclic shift and the window partition that the talk fuses with them are already folded
+// into the attention's loads here, so this kernel writes qkv in plain token order.
 //
 // The normalisation is moved to the other side of the product:
 //   LN(x) W^T + b = rstd * (x W'^T) - rstd * mean * u + v,
 //   W'[n][c] = bf16(gamma_c W[n][c]),  u_n = sum_c W'[n][c],  v_n = sum_c beta_c W[n][c] + b_n,
 // so the tensor cores consume the raw bf16 x tiles as they arrive and the epilogue applies
 // the row statistics (u is summed from the rounded W', so the mean cancels exactly against
-// the rounded weights). qkv_prep_kernel builds W', u and v once per call. The mean and
+// the rounded weights). gemm_prep_kernel builds W', u and v once per call. The mean and
 // 1 / sqrt(var + eps) of each token come from one of two places:
 // * when every token tile is one work item (many tokens), statistics warps sum them from
 //   the x tiles already staged for the product, at no extra memory traffic;
 // * when the output channels of a token tile are split over several work items (few
-//   tokens, wide C), qkv_prep_kernel also computes them in one coalesced pass over x, so
+//   tokens, wide C), gemm_prep_kernel also computes them in one coalesced pass over x, so
 //   that no work item repeats the sums.
 //
-// A dense contraction (2 * 3C * C flops per token) on the fifth-generation tensor cores.
-// One persistent CTA per SM walks work items (128 tokens, the MMA's M, times a group of
-// output-channel tiles of N <= 256), with specialised warps whose pipelines run on across
+// Consumer (after the attention): y = residual + O Wp^T + bp (O the attention output
+// [tokens, C] bf16, Wp [C, C] bf16, bp [C] fp32, the residual [tokens, C] bf16), the
+// output projection with the bias and residual addition that the same talk's section 3
+// fuses into one vectorised elementwise pass (its half2 example) moved into the product's
+// epilogue, so the projection's output never goes to memory before the residual is added.
+//
+// Both are one kernel, gemm_kernel<MODE>: a dense contraction (2 K N flops per token for
+// K input and N output channels). One persistent CTA per SM walks work items (128 tokens,
+// the MMA's M, times a group of output-channel tiles of N <= 256), with specialised warps whose pipelines run on across
 // items:
-// * copy warp: TMA loads of x chunks [128 tokens x 64 channels] and W' chunks
-//   [N tile x 64 channels], 128-byte swizzled, into a ring of as many stages as the rest
+// * copy warp: TMA loads of activation chunks [128 tokens x 64 channels] and weight
+//   chunks [N tile x 64 channels], 128-byte swizzled, into a ring of as many stages as the rest
 //   of the shared memory holds (4 at N = 256, up to 8), so that enough bytes are in flight to cover the load
 //   latency at the tensor cores' rate (channels past C in the last chunk arrive as zeros
 //   and add nothing);
-// * MMA warp, one thread: per chunk four M128 N<=256 K16 tcgen05.mma (A = the x chunk,
-//   B = the W' chunk) into one of two tensor-memory accumulators;
-// * statistics warps (four, with in-kernel statistics): thread r sums its token row's x
+// * MMA warp, one thread: per chunk four M128 N<=256 K16 tcgen05.mma (A = the activation
+//   chunk, B = the weight chunk) into one of two tensor-memory accumulators;
+// * statistics warps (four, producer with in-kernel statistics): thread r sums its token row's x
 //   and x^2, shifted by the row's first value, over the chunks of an item's first output
 //   tile and publishes mean and rstd;
 // * epilogue warps (eight, two per tensor-memory lane quadrant, taking alternate 32-channel
-//   slices): thread r forms rstd * acc - rstd * mean * u + v for its token row and rounds
-//   to bf16 into the warp's own 64-byte-swizzled staging tile [32 rows x 32 channels],
+//   slices): thread r forms rstd * acc - rstd * mean * u + v (producer) or
+//   acc + bp + residual (consumer) for its token row and rounds to bf16 into the warp's own 64-byte-swizzled staging tile [32 rows x 32 channels],
 //   which the warp's first lane writes out with a TMA store (two tiles per warp
 //   alternate; no barrier beyond the warp), while the next output tile accumulates.
 // Every wait is bounded (1 s); a wait that runs out sets the caller's status word (when
@@ -58,10 +66,14 @@ constexpr int kMaxNT = 256;                    // output channels per N tile
 constexpr int kMaxC = 1536;
 constexpr int kMaxSTAGES = 8;
 constexpr int kXCH = kBM * 128;                // x chunk
-// Warp roles: [statistics warps 0..3 when in-kernel], 8 epilogue warps, MMA, copy.
-template <bool IN_STATS>
+// Epilogues: the producer with statistics from the prep pass or summed on chip, and the
+// consumer.
+enum GemmMode { kLnPrepStats = 0, kLnChipStats = 1, kBiasResidual = 2 };
+
+// Warp roles: [statistics warps 0..3 when on chip], 8 epilogue warps, MMA, copy.
+template <int MODE>
 struct Roles {
-  static constexpr int kEPI0 = IN_STATS ? 4 : 0;
+  static constexpr int kEPI0 = MODE == kLnChipStats ? 4 : 0;
   static constexpr int kMMA = kEPI0 + 8, kCOPY = kMMA + 1;
   static constexpr int kTHREADS = (kCOPY + 1) * 32;
 };
@@ -80,13 +92,14 @@ constexpr uint32_t kSW128 = 2;  // descriptor layout: 128-byte swizzle
 // One CTA per SM (more than half of its shared memory), so the 512-column tensor memory
 // allocation never waits.
 
-struct QkvParams {
-  __nv_bfloat16* out;     // [T, 3C]
-  const float* u;         // [3C]
-  const float* v;         // [3C]
-  const float2* stats;    // [T] (mean, rstd), when computed before the product
-  int* status;            // optional: bit 0 set when a bounded wait ran out
-  int T, C, N, NT, tiles_per_item, n_tt, n_items;
+struct GemmParams {
+  __nv_bfloat16* out;              // [T, N]
+  const float* u;                  // [N] producer: row sums of W'
+  const float* v;                  // [N] producer: beta W^T + b; consumer: bp
+  const float2* stats;             // [T] (mean, rstd), producer with the prep pass
+  const __nv_bfloat16* residual;   // [T, N] consumer
+  int* status;                     // optional: bit 0 set when a bounded wait ran out
+  int T, K, N, NT, tiles_per_item, n_tt, n_items;
   int stages, stage_bytes;  // the ring: stages x (x chunk + NT x 128 bytes), 1024-byte multiples
   int off_stats, off_out, off_bar;
   float eps;
@@ -99,11 +112,11 @@ __device__ __forceinline__ bool warp_wait(uint32_t mbar, uint32_t parity) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
-template <bool IN_STATS>
-__global__ void __launch_bounds__(Roles<IN_STATS>::kTHREADS, 1)
-    qkv_gemm_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_constant__ CUtensorMap w_map,
-                    const __grid_constant__ CUtensorMap out_map, const QkvParams p) {
-  using R = Roles<IN_STATS>;
+template <int MODE>
+__global__ void __launch_bounds__(Roles<MODE>::kTHREADS, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_constant__ CUtensorMap w_map,
+                const __grid_constant__ CUtensorMap out_map, const GemmParams p) {
+  using R = Roles<MODE>;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   pdl_launch_dependents();
@@ -122,7 +135,7 @@ __global__ void __launch_bounds__(Roles<IN_STATS>::kTHREADS, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n_tiles = p.N / p.NT;
-  const int kcn = (p.C + kKC - 1) / kKC;
+  const int kcn = (p.K + kKC - 1) / kKC;
   // Work item i: token tile i % n_tt, output-channel tiles [j0, j0 + ntile) of group i / n_tt.
   auto item_tiles = [&](int i, int& t0, int& j0, int& ntile) {
     t0 = (i % p.n_tt) * kBM;
@@ -134,7 +147,7 @@ __global__ void __launch_bounds__(Roles<IN_STATS>::kTHREADS, 1)
   if (tid == 0) {
     for (int st = 0; st < stages; ++st) {
       tc::mbar_init(full_bar(st), 1);
-      tc::mbar_init(empty_bar(st), IN_STATS ? 1 + 4 : 1);  // the MMA commit [and the statistics warps]
+      tc::mbar_init(empty_bar(st), MODE == kLnChipStats ? 1 + 4 : 1);  // the MMA commit [and the statistics warps]
     }
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(dfull_bar(b), 1);
@@ -233,7 +246,7 @@ __global__ void __launch_bounds__(Roles<IN_STATS>::kTHREADS, 1)
           const unsigned char* xc = smem + st * p.stage_bytes;
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
-            if (s_ * kKC + c * 8 >= p.C) break;  // zero fill past C (C is a multiple of 8)
+            if (s_ * kKC + c * 8 >= p.K) break;  // zero fill past C (C is a multiple of 8)
             const uint4 w4 = *reinterpret_cast<const uint4*>(xc + r * 128 + ((c ^ (r & 7)) << 4));
             const uint32_t in[4] = {w4.x, w4.y, w4.z, w4.w};
             if (s_ == 0 && c == 0) {
@@ -256,8 +269,8 @@ __global__ void __launch_bounds__(Roles<IN_STATS>::kTHREADS, 1)
         }
         if (s_ == kcn - 1) {
           // mean = shift + s1 / C; var = s2 / C - (s1 / C)^2 (shifted sums)
-          const float m1 = (s1v.x + s1v.y) / p.C;
-          const float var = fmaxf((s2v.x + s2v.y) / p.C - m1 * m1, 0.0f);
+          const float m1 = (s1v.x + s1v.y) / p.K;
+          const float var = fmaxf((s2v.x + s2v.y) / p.K - m1 * m1, 0.0f);
           const int sb = k & 1;
           if (k >= 2 && !warp_wait(sfree_bar(sb), ((k >> 1) - 1) & 1)) {
             bad = 1;
@@ -270,7 +283,8 @@ __global__ void __launch_bounds__(Roles<IN_STATS>::kTHREADS, 1)
       }
     }
   } else {
-    // ==== epilogue warps: rstd * acc - rstd * mean * u + v, bf16, staged TMA stores =====
+    // ==== epilogue warps: rstd * acc - rstd * mean * u + v or acc + bp + residual, bf16,
+    //      staged TMA stores ===========================================================
     const int ew = warp - R::kEPI0, quad = ew & 3, parity = ew >> 2;
     const int row = quad * 32 + lane;
     const uint32_t trow = tmem + ((uint32_t)(quad * 32) << 16);
@@ -279,8 +293,8 @@ __global__ void __launch_bounds__(Roles<IN_STATS>::kTHREADS, 1)
     for (int it = blockIdx.x; it < p.n_items && !bad; it += gridDim.x, ++k) {
       int t0, j0, ntile;
       item_tiles(it, t0, j0, ntile);
-      float2 ms;
-      if constexpr (IN_STATS) {
+      float2 ms = make_float2(0.0f, 1.0f);
+      if constexpr (MODE == kLnChipStats) {
         const int sb = k & 1;
         if (!warp_wait(sfull_bar(sb), (k >> 1) & 1)) {
           bad = 1;
@@ -289,7 +303,7 @@ __global__ void __launch_bounds__(Roles<IN_STATS>::kTHREADS, 1)
         ms = sstats[sb * kBM + row];
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(sfree_bar(sb));
-      } else {
+      } else if constexpr (MODE == kLnPrepStats) {
         ms = t0 + row < p.T ? p.stats[t0 + row] : make_float2(0.0f, 0.0f);
       }
       const float rstd = ms.y, nmr = -ms.x * ms.y;
@@ -308,6 +322,12 @@ __global__ void __launch_bounds__(Roles<IN_STATS>::kTHREADS, 1)
             if (lane == 0) tc::bulk_wait_read<1>();  // the store of slice m - 2 has read its tile
             __syncwarp();
           }
+          uint4 rv[4];  // consumer: the residual's 32 channels of this row, loaded ahead
+          if constexpr (MODE == kBiasResidual) {
+            const uint4* rr = reinterpret_cast<const uint4*>(p.residual + (int64_t)(t0 + row) * p.N + n0 + c0);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) rv[c] = t0 + row < p.T ? rr[c] : make_uint4(0, 0, 0, 0);
+          }
           uint32_t a[32];
           tc::ld32_wait(trow + buf * kMaxNT + c0, a);
           // u and v: the same 32 channels for every lane (broadcast loads through L1)
@@ -318,13 +338,23 @@ __global__ void __launch_bounds__(Roles<IN_STATS>::kTHREADS, 1)
             uint32_t o[4];
 #pragma unroll
             for (int w2 = 0; w2 < 2; ++w2) {
-              const float4 u4 = __ldg(uu + 2 * c + w2), v4 = __ldg(vv + 2 * c + w2);
               const int e = 8 * c + 4 * w2;
-              const float2 c0v = __ffma2_rn(nm2, make_float2(u4.x, u4.y), make_float2(v4.x, v4.y));
-              const float2 c1v = __ffma2_rn(nm2, make_float2(u4.z, u4.w), make_float2(v4.z, v4.w));
-              const float2 y0 = __ffma2_rn(make_float2(__uint_as_float(a[e]), __uint_as_float(a[e + 1])), r2, c0v);
-              const float2 y1 =
-                  __ffma2_rn(make_float2(__uint_as_float(a[e + 2]), __uint_as_float(a[e + 3])), r2, c1v);
+              const float2 a0 = make_float2(__uint_as_float(a[e]), __uint_as_float(a[e + 1]));
+              const float2 a1 = make_float2(__uint_as_float(a[e + 2]), __uint_as_float(a[e + 3]));
+              const float4 v4 = __ldg(vv + 2 * c + w2);
+              float2 y0, y1;
+              if constexpr (MODE == kBiasResidual) {
+                // (acc + bp) + residual, as the definition adds them
+                const uint32_t r0 = w2 ? rv[c].z : rv[c].x, r1 = w2 ? rv[c].w : rv[c].y;
+                y0 = __fadd2_rn(__fadd2_rn(a0, make_float2(v4.x, v4.y)), make_float2(bf16_lo(r0), bf16_hi(r0)));
+                y1 = __fadd2_rn(__fadd2_rn(a1, make_float2(v4.z, v4.w)), make_float2(bf16_lo(r1), bf16_hi(r1)));
+              } else {
+                const float4 u4 = __ldg(uu + 2 * c + w2);
+                const float2 c0v = __ffma2_rn(nm2, make_float2(u4.x, u4.y), make_float2(v4.x, v4.y));
+                const float2 c1v = __ffma2_rn(nm2, make_float2(u4.z, u4.w), make_float2(v4.z, v4.w));
+                y0 = __ffma2_rn(a0, r2, c0v);
+                y1 = __ffma2_rn(a1, r2, c1v);
+              }
               o[2 * w2] = pack_bf16(y0.x, y0.y);
               o[2 * w2 + 1] = pack_bf16(y1.x, y1.y);
             }
@@ -352,12 +382,12 @@ __global__ void __launch_bounds__(Roles<IN_STATS>::kTHREADS, 1)
   if (warp == R::kMMA) tc::tmem_dealloc<kTMEM_COLS>(tmem);
 }
 
-// Blocks [0, fold_blocks): W'[n][c] = bf16(gamma_c W[n][c]), u_n = sum_c W'[n][c],
+// The producer's preparation. Blocks [0, fold_blocks): W'[n][c] = bf16(gamma_c W[n][c]), u_n = sum_c W'[n][c],
 // v_n = sum_c beta_c W[n][c] + b_n, one warp per output channel n.
 // Blocks from fold_blocks on (when stats is given): (mean, 1 / sqrt(var + eps)) of each
 // token's C channels, four tokens per warp with their loads in flight together; shifted
 // sums (by the row's first value) in fp32, reduced across the warp.
-__global__ void qkv_prep_kernel(const __nv_bfloat16* __restrict__ w, const float* __restrict__ gamma,
+__global__ void gemm_prep_kernel(const __nv_bfloat16* __restrict__ w, const float* __restrict__ gamma,
                                 const float* __restrict__ beta, const float* __restrict__ b, int C, int N,
                                 __nv_bfloat16* __restrict__ wf, float* __restrict__ u, float* __restrict__ v,
                                 int fold_blocks, const __nv_bfloat16* __restrict__ x, int T, float eps,
@@ -431,116 +461,150 @@ __global__ void qkv_prep_kernel(const __nv_bfloat16* __restrict__ w, const float
 
 }  // namespace
 
-// Workspace of one call: W' [3C, C] bf16, u and v [3C] fp32, then the token statistics
-// [T] (mean, rstd), each part 256-byte aligned.
+// Producer workspace of one call: W' [3C, C] bf16, u and v [3C] fp32, then the token
+// statistics [T] (mean, rstd), each part 256-byte aligned.
 static size_t align256(size_t n) { return (n + 255) & ~(size_t)255; }
 size_t qkv_workspace_bytes(int C, int64_t T) {
   return align256((size_t)3 * C * C * 2) + 2 * align256((size_t)3 * C * 4) + align256((size_t)T * 8);
 }
 
-// Output-channel tile: the largest multiple of 32 up to 256 that divides 3C (C is a
-// multiple of 32, so 96 always qualifies).
-static int qkv_tile(int N) {
+namespace {
+
+// Output-channel tile: the largest multiple of 32 up to 256 that divides N (a multiple of
+// 32).
+int gemm_tile(int N) {
   for (int nt = kMaxNT; nt >= 32; nt -= 32)
     if (N % nt == 0) return nt;
   return 0;
 }
 
+// Work items: token tiles times groups of output-channel tiles, at least four per SM when
+// the channel tiles allow it; one persistent CTA per SM walks them.
+struct ItemPlan {
+  int sms, smem_max, NT, n_tt, per, n_items;
+  bool one_item_per_token_tile;
+};
+
+cudaError_t plan_items(int T, int N, ItemPlan* ip) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&ip->sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&ip->smem_max, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  if (e != cudaSuccess) return e;
+  ip->NT = gemm_tile(N);
+  if (ip->NT == 0) return cudaErrorInvalidValue;
+  ip->n_tt = (T + kBM - 1) / kBM;
+  const int n_tiles = N / ip->NT;
+  int groups = (4 * ip->sms + ip->n_tt - 1) / ip->n_tt;
+  groups = groups < 1 ? 1 : (groups > n_tiles ? n_tiles : groups);
+  ip->per = (n_tiles + groups - 1) / groups;
+  groups = (n_tiles + ip->per - 1) / ip->per;
+  ip->n_items = ip->n_tt * groups;
+  ip->one_item_per_token_tile = groups == 1;
+  return cudaSuccess;
+}
+
+cudaError_t encode_2d(PFN_cuTensorMapEncodeTiled_v12000 encode, CUtensorMap* map, const void* base, int inner,
+                      int outer, int box_inner, int box_outer, CUtensorMapSwizzle swz, CUtensorMapL2promotion l2) {
+  const cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
+  const cuuint64_t strides[1] = {(cuuint64_t)inner * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)box_inner, (cuuint32_t)box_outer};
+  const cuuint32_t es[2] = {1, 1};
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, swz, l2, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS
+             ? cudaSuccess
+             : cudaErrorInvalidValue;
+}
+
+template <int MODE>
+cudaError_t launch_gemm(const ItemPlan& ip, GemmParams p, const void* a, const void* w, cudaStream_t st) {
+  PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder_fn();
+  if (encode == nullptr) return cudaErrorNotSupported;
+  CUtensorMap a_map, w_map, out_map;
+  cudaError_t e = encode_2d(encode, &a_map, a, p.K, p.T, kKC, kBM, CU_TENSOR_MAP_SWIZZLE_128B,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_128B);
+  if (e == cudaSuccess)
+    e = encode_2d(encode, &w_map, w, p.K, p.N, kKC, ip.NT, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+  if (e == cudaSuccess)
+    e = encode_2d(encode, &out_map, p.out, p.N, p.T, kSC, 32, CU_TENSOR_MAP_SWIZZLE_64B,
+                  CU_TENSOR_MAP_L2_PROMOTION_NONE);
+  if (e != cudaSuccess) return e;
+  p.NT = ip.NT;
+  p.tiles_per_item = ip.per;
+  p.n_tt = ip.n_tt;
+  p.n_items = ip.n_items;
+  p.stage_bytes = kXCH + ip.NT * 128;
+  constexpr int kStatsBytes = MODE == kLnChipStats ? kSTATS_BYTES : 0;
+  const int fixed = kStatsBytes + kTAIL_BYTES;
+  p.stages = std::min(kMaxSTAGES, (ip.smem_max - fixed) / p.stage_bytes);
+  if (p.stages < 2) return cudaErrorInvalidConfiguration;
+  p.off_stats = p.stages * p.stage_bytes;
+  p.off_out = p.off_stats + kStatsBytes;
+  p.off_bar = p.off_out + kOUT_BYTES;
+  const int smem = std::max(kMinSMEM, p.stages * p.stage_bytes + fixed);
+  e = cudaFuncSetAttribute(gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(gemm_kernel<MODE>, dim3(std::min(ip.n_items, ip.sms)), dim3(Roles<MODE>::kTHREADS), smem, st,
+                    a_map, w_map, out_map, p);
+}
+
+GemmParams base_params(void* out, int T, int K, int N, int* status) {
+  GemmParams p{};
+  p.out = reinterpret_cast<__nv_bfloat16*>(out);
+  p.status = status;
+  p.T = T;
+  p.K = K;
+  p.N = N;
+  return p;
+}
+
+}  // namespace
+
+// Producer: qkv = LN(x) W^T + b. Two launches: gemm_prep_kernel, then gemm_kernel.
 cudaError_t qkv_proj_launch(const void* x, const float* gamma, const float* beta, const void* w, const float* b,
                             void* out, int T, int C, float eps, void* workspace, int* status, cudaStream_t st) {
   if (T <= 0) return cudaSuccess;
   if (C % 32 != 0 || C < 32 || C > kMaxC) return cudaErrorInvalidValue;
-  PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder_fn();
-  if (encode == nullptr) return cudaErrorNotSupported;
-  const int N = 3 * C, NT = qkv_tile(N);
+  const int N = 3 * C;
+  ItemPlan ip;
+  cudaError_t e = plan_items(T, N, &ip);
+  if (e != cudaSuccess) return e;
   unsigned char* ws = static_cast<unsigned char*>(workspace);
   __nv_bfloat16* wf = reinterpret_cast<__nv_bfloat16*>(ws);
   float* u = reinterpret_cast<float*>(ws + align256((size_t)N * C * 2));
   float* v = u + align256((size_t)N * 4) / 4;
   float2* stats = reinterpret_cast<float2*>(reinterpret_cast<unsigned char*>(v) + align256((size_t)N * 4));
-  int dev = 0, sms = 0, smem_max = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&smem_max, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-  if (e != cudaSuccess) return e;
-  // Work items: token tiles times groups of output-channel tiles, at least four per SM
-  // when the channel tiles allow it; one persistent CTA per SM walks them.
-  const int n_tt = (T + kBM - 1) / kBM, n_tiles = N / NT;
-  int groups = (4 * sms + n_tt - 1) / n_tt;
-  groups = groups < 1 ? 1 : (groups > n_tiles ? n_tiles : groups);
-  const int per = (n_tiles + groups - 1) / groups;
-  groups = (n_tiles + per - 1) / per;
-  const int n_items = n_tt * groups;
-  const bool in_stats = groups == 1;  // each token tile is one item: sum the statistics on chip
+  const bool chip_stats = ip.one_item_per_token_tile;  // each token tile is one item: sum on chip
   const int fold_blocks = (N + 7) / 8;
-  const int stat_blocks = in_stats ? 0 : (int)std::min<int64_t>(((int64_t)T + 31) / 32, 16 * sms);
-  qkv_prep_kernel<<<fold_blocks + stat_blocks, 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(w), gamma,
-                                                             beta, b, C, N, wf, u, v, fold_blocks,
-                                                             reinterpret_cast<const __nv_bfloat16*>(x), T, eps,
-                                                             stats);
+  const int stat_blocks = chip_stats ? 0 : (int)std::min<int64_t>(((int64_t)T + 31) / 32, 16 * ip.sms);
+  gemm_prep_kernel<<<fold_blocks + stat_blocks, 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(w), gamma,
+                                                              beta, b, C, N, wf, u, v, fold_blocks,
+                                                              reinterpret_cast<const __nv_bfloat16*>(x), T, eps,
+                                                              stats);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  CUtensorMap x_map, w_map;
-  const cuuint32_t es[2] = {1, 1};
-  {
-    const cuuint64_t dims[2] = {(cuuint64_t)C, (cuuint64_t)T};
-    const cuuint64_t strides[1] = {(cuuint64_t)C * 2};
-    const cuuint32_t box[2] = {kKC, kBM};
-    if (encode(&x_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(x), dims, strides, box, es,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return cudaErrorInvalidValue;
-  }
-  {
-    const cuuint64_t dims[2] = {(cuuint64_t)C, (cuuint64_t)N};
-    const cuuint64_t strides[1] = {(cuuint64_t)C * 2};
-    const cuuint32_t box[2] = {kKC, (cuuint32_t)NT};
-    if (encode(&w_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, wf, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
-        CUDA_SUCCESS)
-      return cudaErrorInvalidValue;
-  }
-  CUtensorMap out_map;
-  {
-    const cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)T};
-    const cuuint64_t strides[1] = {(cuuint64_t)N * 2};
-    const cuuint32_t box[2] = {kSC, 32};
-    if (encode(&out_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, out, dims, strides, box, es,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return cudaErrorInvalidValue;
-  }
-  QkvParams p;
-  p.out = reinterpret_cast<__nv_bfloat16*>(out);
+  GemmParams p = base_params(out, T, C, N, status);
   p.u = u;
   p.v = v;
-  p.stats = in_stats ? nullptr : stats;
-  p.status = status;
-  p.T = T;
-  p.C = C;
-  p.N = N;
-  p.NT = NT;
-  p.tiles_per_item = per;
-  p.stage_bytes = kXCH + NT * 128;
-  const int fixed = (in_stats ? kSTATS_BYTES : 0) + kTAIL_BYTES;
-  p.stages = std::min(kMaxSTAGES, (smem_max - fixed) / p.stage_bytes);
-  if (p.stages < 2) return cudaErrorInvalidConfiguration;
-  p.off_stats = p.stages * p.stage_bytes;
-  p.off_out = p.off_stats + (in_stats ? kSTATS_BYTES : 0);
-  p.off_bar = p.off_out + kOUT_BYTES;
-  const int smem = std::max(kMinSMEM, p.stages * p.stage_bytes + fixed);
-  p.n_tt = n_tt;
-  p.n_items = n_items;
   p.eps = eps;
-  const dim3 grid(n_items < sms ? n_items : sms);
-  if (in_stats) {
-    e = cudaFuncSetAttribute(qkv_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    return launch_pdl(qkv_gemm_kernel<true>, grid, dim3(Roles<true>::kTHREADS), smem, st, x_map, w_map, out_map, p);
-  }
-  e = cudaFuncSetAttribute(qkv_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (chip_stats) return launch_gemm<kLnChipStats>(ip, p, x, wf, st);
+  p.stats = stats;
+  return launch_gemm<kLnPrepStats>(ip, p, x, wf, st);
+}
+
+// Consumer: y = residual + O Wp^T + bp. One launch.
+cudaError_t proj_residual_launch(const void* o, const void* wp, const float* bp, const void* residual, void* y,
+                                 int T, int C, int* status, cudaStream_t st) {
+  if (T <= 0) return cudaSuccess;
+  if (C % 32 != 0 || C < 32 || C > kMaxC) return cudaErrorInvalidValue;
+  ItemPlan ip;
+  cudaError_t e = plan_items(T, C, &ip);
   if (e != cudaSuccess) return e;
-  return launch_pdl(qkv_gemm_kernel<false>, grid, dim3(Roles<false>::kTHREADS), smem, st, x_map, w_map, out_map, p);
+  GemmParams p = base_params(y, T, C, C, status);
+  p.v = bp;
+  p.residual = reinterpret_cast<const __nv_bfloat16*>(residual);
+  return launch_gemm<kBiasResidual>(ip, p, o, wp, st);
 }
 
 }  // namespace swin

@@ -71,3 +71,19 @@ def test_null_and_foreign_plan_handles(lib):
 def test_null_out_handle(lib):
     so = lib.load()
     assert so.swin_wattn_plan(None, 1, 8, 8, 64, 2, 4, 0, 0, None, None) == lib.ERR_INVALID_ARG
+
+
+def test_gemm_steps_reject_bad_arguments_before_touching_cuda(lib):
+    # producer: workspace size query and shape checks
+    assert lib.swin_wattn_qkv_workspace_bytes(80, 4) == 0           # C not a multiple of 32
+    assert lib.swin_wattn_qkv_workspace_bytes(1568, 4) == 0         # C above 1536
+    assert lib.swin_wattn_qkv_workspace_bytes(96, 4) >= 288 * 96 * 2 + 2 * 288 * 4 + 4 * 8
+    assert lib.swin_wattn_qkv_proj(*([None] * 6), -1, 96, 1e-5, None, 0, None, None) == lib.ERR_INVALID_ARG
+    assert lib.swin_wattn_qkv_proj(*([None] * 6), 4, 96, -1.0, None, 0, None, None) == lib.ERR_INVALID_ARG
+    assert lib.swin_wattn_qkv_proj(*([None] * 6), 4, 80, 1e-5, None, 0, None, None) == lib.ERR_UNSUPPORTED
+    assert lib.swin_wattn_qkv_proj(*([None] * 6), 0, 96, 1e-5, None, 0, None, None) == lib.OK
+    # consumer
+    assert lib.swin_wattn_proj_residual(*([None] * 5), -1, 96, None, None) == lib.ERR_INVALID_ARG
+    assert lib.swin_wattn_proj_residual(*([None] * 5), 4, 48, None, None) == lib.ERR_UNSUPPORTED
+    assert lib.swin_wattn_proj_residual(*([None] * 5), 4, 3072, None, None) == lib.ERR_UNSUPPORTED
+    assert lib.swin_wattn_proj_residual(*([None] * 5), 0, 96, None, None) == lib.OK
