@@ -4,7 +4,9 @@ A step is one pass of the hot path over the Swin-L 224 stage sweep at batch 64: 
 fused forward of each of the four stages (56x56 C=192 nH=6 s=3; 28x28 C=384 nH=12 s=3;
 14x14 C=768 nH=24 s=3; 7x7 C=1536 nH=48 s=0; window 7, bf16), with the dense bias and
 shift mask built once per plan. The line also reports the Swin-B 224 training step (bias
-re-expansion + forward + backward of its four stages) as `train_step`.
+re-expansion + forward + backward of its four stages) as `train_step`, and the whole
+attention sub-block of the same sweep (LayerNorm + qkv projection, the attention, output
+projection + bias + residual), captured as one CUDA graph, as `block_sweep`.
 
 Prints one JSON line (rank 0). `value` is tokens/s over the whole job with inputs
 resident in HBM; `e2e` is the same metric through the host-buffer entry point, with the
@@ -61,6 +63,36 @@ def fwd_flops(wl) -> int:
 
 def bwd_flops(wl) -> int:
     return 10 * wl.N * wl.N * wl.hd * wl.window_heads
+
+
+def qkv_bytes(wl) -> int:
+    """Producer: x read, qkv written, W read (bf16)."""
+    return 2 * (wl.tokens * wl.C + wl.tokens * 3 * wl.C + 3 * wl.C * wl.C)
+
+
+def qkv_flops(wl) -> int:
+    return 2 * wl.tokens * wl.C * 3 * wl.C
+
+
+def proj_bytes(wl) -> int:
+    """Consumer: attention output and residual read, y written, Wp read (bf16)."""
+    return 2 * (3 * wl.tokens * wl.C + wl.C * wl.C)
+
+
+def proj_flops(wl) -> int:
+    return 2 * wl.tokens * wl.C * wl.C
+
+
+def gemm_roofline(nbytes, flops, ms, peaks):
+    """The binding roofline of a GEMM step timed alone: the larger of its HBM time
+    (measured copy bandwidth) and its tensor time (measured bf16 burst rate)."""
+    t_hbm = nbytes / (float(peaks["hbm_gbs"]) * 1e9)
+    t_tc = flops / (float(peaks["bf16_tflops"]) * 1e12)
+    bound = "hbm" if t_hbm >= t_tc else "tensor"
+    return {"us": round(ms * 1e3, 2), "bound": bound,
+            "frac": round(max(t_hbm, t_tc) / (ms / 1e3), 4),
+            "GBps": round(nbytes / (ms / 1e3) / 1e9, 1),
+            "tflops": round(flops / (ms / 1e3) / 1e12, 1)}
 
 
 def load_peaks():
@@ -363,6 +395,7 @@ def run_gpu(args):
 
     train = run_train_step(args, dev, stream, lib, capi, hbm, ws) if not args.skip_train else None
     l384 = run_fwd_sweep(L384, args, dev, stream, lib, capi, hbm, ws) if not args.skip_train else None
+    block = run_block_sweep(SWEEP, args, dev, stream, lib, capi, peaks, ws) if not args.skip_train else None
 
     if rank == 0:
         line = {
@@ -394,6 +427,7 @@ def run_gpu(args):
             "clocks": clk,
             "train_step": train,
             "l384_sweep": l384,
+            "block_sweep": block,
         }
         if ws == 1 and not args.skip_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(sweep)
@@ -439,6 +473,100 @@ def run_fwd_sweep(names, args, dev, stream, lib, capi, hbm, ws):
     return {"workload": "swin_l384_sweep_fwd (B=16, 12x12 windows)", "us": round(tot_ms * 1e3, 2),
             "tokens_per_s": sum(x["wl"].tokens for x in st) / (tot_ms / 1e3),
             "frac_of_measured_hbm": round(tot_b / (tot_ms / 1e3) / 1e9 / hbm, 4), "stages": out}
+
+
+def run_block_sweep(names, args, dev, stream, lib, capi, peaks, ws):
+    """The attention sub-block of each stage, x -> LayerNorm + qkv projection -> shifted-
+    window attention -> output projection + bias + residual x, captured as one CUDA graph
+    (four launches per stage) and replayed; per-call times from a second, eager region with
+    CUDA events around every call."""
+    sh = stream.cuda_stream
+    st = []
+    with torch.cuda.stream(stream):
+        for name in names:
+            wl = inputs.BY_NAME[name]
+            x, g, be, w, b = [t.to(dev) for t in inputs.make_producer(wl)]
+            _, wp, bp, _ = [t.to(dev) for t in inputs.make_consumer(wl)]
+            h = make_plan(capi, wl, inputs.make_table(wl).to(dev), sh, args)
+            T = wl.tokens
+            nws = capi.swin_wattn_qkv_workspace_bytes(wl.C, T)
+            st.append(dict(wl=wl, x=x, g=g, be=be, w=w, b=b, wp=wp, bp=bp, h=h, T=T, nws=nws,
+                           ws=torch.empty(nws, dtype=torch.uint8, device=dev),
+                           qkv=torch.empty(wl.B, wl.H, wl.W, 3 * wl.C, dtype=torch.bfloat16, device=dev),
+                           o=torch.empty_like(x), y=torch.empty_like(x)))
+    torch.cuda.synchronize()
+
+    def one(events=None):
+        for k, z in enumerate(st):
+            wl = z["wl"]
+            if events is not None:
+                events[k][0].record(stream)
+            ok = lib.swin_wattn_qkv_proj(z["x"].data_ptr(), z["g"].data_ptr(), z["be"].data_ptr(),
+                                         z["w"].data_ptr(), z["b"].data_ptr(), z["qkv"].data_ptr(), z["T"],
+                                         wl.C, 1e-5, z["ws"].data_ptr(), z["nws"], None, sh) == capi.OK
+            if events is not None:
+                events[k][1].record(stream)
+            ok &= lib.swin_wattn_fwd(z["h"], z["qkv"].data_ptr(), z["o"].data_ptr(), sh) == capi.OK
+            if events is not None:
+                events[k][2].record(stream)
+            ok &= lib.swin_wattn_proj_residual(z["o"].data_ptr(), z["wp"].data_ptr(), z["bp"].data_ptr(),
+                                               z["x"].data_ptr(), z["y"].data_ptr(), z["T"], wl.C, None,
+                                               sh) == capi.OK
+            if events is not None:
+                events[k][3].record(stream)
+            if not ok:
+                raise RuntimeError("block step call failed")
+
+    for _ in range(max(3, args.warmup)):
+        one()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream, capture_error_mode="relaxed"):
+        one()
+    torch.cuda.synchronize()
+    steps = max(3, min(args.steps, 200))
+    for _ in range(3):
+        with torch.cuda.stream(stream):
+            graph.replay()
+    torch.cuda.synchronize()
+    barrier(ws)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(steps):
+            graph.replay()
+    b.record(stream)
+    torch.cuda.synchronize()
+    graph_ms = max_over_ranks(a.elapsed_time(b), ws) / steps
+    ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in st] for _ in range(steps)]
+    a.record(stream)
+    for i in range(steps):
+        one(ev[i])
+    b.record(stream)
+    torch.cuda.synchronize()
+    eager_ms = a.elapsed_time(b) / steps
+    hbm = float(peaks["hbm_gbs"])
+    stages = []
+    for k, z in enumerate(st):
+        wl = z["wl"]
+        q_ms, f_ms, p_ms = (statistics.mean(ev[i][k][j].elapsed_time(ev[i][k][j + 1]) for i in range(steps))
+                            for j in range(3))
+        stages.append({"workload": wl.name,
+                       "producer": gemm_roofline(qkv_bytes(wl), qkv_flops(wl), q_ms, peaks),
+                       "attention": {"us": round(f_ms * 1e3, 2),
+                                     "frac_of_measured_hbm": round(fwd_bytes(wl) / (f_ms / 1e3) / 1e9 / hbm, 4)},
+                       "consumer": gemm_roofline(proj_bytes(wl), proj_flops(wl), p_ms, peaks)})
+    for z in st:
+        capi.swin_wattn_destroy(z["h"])
+    tokens = sum(z["T"] for z in st)
+    return {"workload": "swin_l224 attention sub-block sweep (B=64 per GPU; per stage LayerNorm + qkv "
+                        "projection, SW-MSA, output projection + bias + residual)",
+            "steps": steps, "graph_us_per_step": round(graph_ms * 1e3, 2),
+            "eager_us_per_step": round(eager_ms * 1e3, 2), "tokens_per_s": ws * tokens / (graph_ms / 1e3),
+            "launches_per_step": 4 * len(st),
+            "roofline_note": "GEMM steps: bound = the larger of bytes / measured HBM and flops / measured "
+                             "bf16 burst rate; frac = that time / measured time",
+            "stages": stages}
 
 
 def run_train_step(args, dev, stream, lib, capi, hbm, ws):
