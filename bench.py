@@ -105,10 +105,16 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_source_hash() -> str:
+# The files the forward kernel is compiled from: its DRAM traffic recorded by ncu stays
+# valid while these are unchanged.
+FWD_KERNEL_FILES = ("common.cuh", "fwd.cu", "tc.cuh")
+
+
+def kernel_source_hash(files=FWD_KERNEL_FILES) -> str:
+    """Short hash of the named csrc files (None: every file under csrc/)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "swin_window_attention_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in sorted(os.listdir(csrc) if files is None else files):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
@@ -116,7 +122,7 @@ def kernel_source_hash() -> str:
 
 def ncu_traffic(kernel_hash: str):
     """Per-launch DRAM bytes of the forward kernel on the first sweep stage, from the
-    committed ncu summary, if it was captured on the current kernel sources."""
+    committed ncu summary, if it was captured on the forward kernel's current sources."""
     path = os.path.join(ROOT, "profiles", "fwd_swin_l224_s1_traffic.json")
     try:
         with open(path) as f:
@@ -662,6 +668,34 @@ def make_plan(capi, wl, tab, sh, args):
     return h
 
 
+def run_gemm_only(args):
+    """Producer and consumer launches of one workload (warm-up + timed), for kernel
+    profiling: each iteration is swin_wattn_qkv_proj then swin_wattn_proj_residual."""
+    from swin_window_attention_gb300 import build, capi
+    build.build()
+    wl = inputs.BY_NAME[args.gemm_workload]
+    dev = torch.device("cuda", 0)
+    x, g, be, w, b = [t.to(dev) for t in inputs.make_producer(wl)]
+    o, wp, bp, r = [t.to(dev) for t in inputs.make_consumer(wl)]
+    qkv = torch.empty(x.shape[:-1] + (3 * wl.C,), dtype=torch.bfloat16, device=dev)
+    y = torch.empty_like(o)
+    ws = torch.empty(capi.swin_wattn_qkv_workspace_bytes(wl.C, wl.tokens), dtype=torch.uint8, device=dev)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.warmup + args.steps)]
+    for i in range(args.warmup + args.steps):
+        ev[i][0].record()
+        capi.qkv_proj(x, g, be, w, b, qkv, workspace=ws)
+        ev[i][1].record()
+        capi.proj_residual(o, wp, bp, r, y)
+        ev[i][2].record()
+    torch.cuda.synchronize()
+    peaks, _ = load_peaks()
+    q_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev[args.warmup:])
+    p_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev[args.warmup:])
+    print(json.dumps({"workload": wl.name,
+                      "producer": gemm_roofline(qkv_bytes(wl), qkv_flops(wl), q_ms, peaks),
+                      "consumer": gemm_roofline(proj_bytes(wl), proj_flops(wl), p_ms, peaks)}))
+
+
 def run_bwd_only(args):
     """Backward launches of one workload (warm-up + timed), for kernel profiling."""
     from swin_window_attention_gb300 import build, capi
@@ -739,6 +773,8 @@ def main():
                          "(profiling runs)")
     ap.add_argument("--bwd-workload", choices=sorted(n for n, w in inputs.BY_NAME.items() if w.bwd),
                     help="profiling run: only the backward of this workload, a few launches")
+    ap.add_argument("--gemm-workload", choices=sorted(inputs.BY_NAME),
+                    help="profiling run: only the producer and consumer of this workload, a few launches")
     ap.add_argument("--fwd-kernel", default="auto", choices=sorted(FWD_KERNELS),
                     help="forward kernel of every plan (auto: the library's default)")
     ap.add_argument("--skip-train", action="store_true")
@@ -750,6 +786,8 @@ def main():
         run_reference(args)
     elif args.bwd_workload:
         run_bwd_only(args)
+    elif args.gemm_workload:
+        run_gemm_only(args)
     else:
         run_gpu(args)
 
