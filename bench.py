@@ -484,8 +484,10 @@ def run_fwd_sweep(names, args, dev, stream, lib, capi, hbm, ws):
 def run_block_sweep(names, args, dev, stream, lib, capi, peaks, ws):
     """The attention sub-block of each stage, x -> LayerNorm + qkv projection -> shifted-
     window attention -> output projection + bias + residual x, captured as one CUDA graph
-    (four launches per stage) and replayed; per-call times from a second, eager region with
-    CUDA events around every call."""
+    and replayed; per-call times from a second, eager region with CUDA events around every
+    call. The qkv weights are prepared once per stage (the fold of gamma into W and the
+    bias vectors), as an inference deployment does with fixed weights; the dense bias and
+    mask of each attention plan are likewise built once."""
     sh = stream.cuda_stream
     st = []
     with torch.cuda.stream(stream):
@@ -495,8 +497,9 @@ def run_block_sweep(names, args, dev, stream, lib, capi, peaks, ws):
             _, wp, bp, _ = [t.to(dev) for t in inputs.make_consumer(wl)]
             h = make_plan(capi, wl, inputs.make_table(wl).to(dev), sh, args)
             T = wl.tokens
-            nws = capi.swin_wattn_qkv_workspace_bytes(wl.C, T)
-            st.append(dict(wl=wl, x=x, g=g, be=be, w=w, b=b, wp=wp, bp=bp, h=h, T=T, nws=nws,
+            proj = capi.QkvProjection(g, be, w, b, stream=stream)
+            nws = capi.swin_wattn_qkv_stats_bytes(T)
+            st.append(dict(wl=wl, x=x, wp=wp, bp=bp, h=h, T=T, nws=nws, prep=proj.prepared,
                            ws=torch.empty(nws, dtype=torch.uint8, device=dev),
                            qkv=torch.empty(wl.B, wl.H, wl.W, 3 * wl.C, dtype=torch.bfloat16, device=dev),
                            o=torch.empty_like(x), y=torch.empty_like(x)))
@@ -507,9 +510,9 @@ def run_block_sweep(names, args, dev, stream, lib, capi, peaks, ws):
             wl = z["wl"]
             if events is not None:
                 events[k][0].record(stream)
-            ok = lib.swin_wattn_qkv_proj(z["x"].data_ptr(), z["g"].data_ptr(), z["be"].data_ptr(),
-                                         z["w"].data_ptr(), z["b"].data_ptr(), z["qkv"].data_ptr(), z["T"],
-                                         wl.C, 1e-5, z["ws"].data_ptr(), z["nws"], None, sh) == capi.OK
+            ok = lib.swin_wattn_qkv_proj_prepared(z["x"].data_ptr(), z["prep"].data_ptr(), z["qkv"].data_ptr(),
+                                                  z["T"], wl.C, 1e-5, z["ws"].data_ptr(), z["nws"], None,
+                                                  sh) == capi.OK
             if events is not None:
                 events[k][1].record(stream)
             ok &= lib.swin_wattn_fwd(z["h"], z["qkv"].data_ptr(), z["o"].data_ptr(), sh) == capi.OK
@@ -526,6 +529,9 @@ def run_block_sweep(names, args, dev, stream, lib, capi, peaks, ws):
     for _ in range(max(3, args.warmup)):
         one()
     torch.cuda.synchronize()
+    capi.swin_wattn_launch_count(reset=True)
+    one()
+    launches_per_step = capi.swin_wattn_launch_count()
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=stream, capture_error_mode="relaxed"):
         one()
@@ -569,7 +575,7 @@ def run_block_sweep(names, args, dev, stream, lib, capi, peaks, ws):
                         "projection, SW-MSA, output projection + bias + residual)",
             "steps": steps, "graph_us_per_step": round(graph_ms * 1e3, 2),
             "eager_us_per_step": round(eager_ms * 1e3, 2), "tokens_per_s": ws * tokens / (graph_ms / 1e3),
-            "launches_per_step": 4 * len(st),
+            "launches_per_step": int(launches_per_step),
             "roofline_note": "GEMM steps: bound = the larger of bytes / measured HBM and flops / measured "
                              "bf16 burst rate; frac = that time / measured time",
             "stages": stages}
@@ -670,7 +676,8 @@ def make_plan(capi, wl, tab, sh, args):
 
 def run_gemm_only(args):
     """Producer and consumer launches of one workload (warm-up + timed), for kernel
-    profiling: each iteration is swin_wattn_qkv_proj then swin_wattn_proj_residual."""
+    profiling: after one swin_wattn_qkv_prepare, each iteration is
+    swin_wattn_qkv_proj_prepared then swin_wattn_proj_residual."""
     from swin_window_attention_gb300 import build, capi
     build.build()
     wl = inputs.BY_NAME[args.gemm_workload]
@@ -679,11 +686,11 @@ def run_gemm_only(args):
     o, wp, bp, r = [t.to(dev) for t in inputs.make_consumer(wl)]
     qkv = torch.empty(x.shape[:-1] + (3 * wl.C,), dtype=torch.bfloat16, device=dev)
     y = torch.empty_like(o)
-    ws = torch.empty(capi.swin_wattn_qkv_workspace_bytes(wl.C, wl.tokens), dtype=torch.uint8, device=dev)
+    proj = capi.QkvProjection(g, be, w, b)  # the weights prepared once
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.warmup + args.steps)]
     for i in range(args.warmup + args.steps):
         ev[i][0].record()
-        capi.qkv_proj(x, g, be, w, b, qkv, workspace=ws)
+        proj(x, qkv)
         ev[i][1].record()
         capi.proj_residual(o, wp, bp, r, y)
         ev[i][2].record()

@@ -204,6 +204,26 @@ int swin_wattn_qkv_proj(const void* x, const float* gamma, const float* beta, co
                         size_t workspace_bytes, int* status, struct CUstream_st* stream);
 
 /*
+ * The producer step with its weights prepared once (NVIDIA Swin talk, section 3: inference
+ * may transform the qkv weight and bias ahead of time). swin_wattn_qkv_prepare writes W',
+ * u and v (as above) for gamma, beta, w_qkv, b_qkv into `prepared` (device, 256-byte
+ * aligned, at least swin_wattn_qkv_prepared_bytes(C) bytes; one launch). Then each
+ * swin_wattn_qkv_proj_prepared call computes qkv for x from them, with the same arithmetic
+ * and results as swin_wattn_qkv_proj; it reads `prepared` and uses `stats_workspace`
+ * (device, 16-byte aligned, at least swin_wattn_qkv_stats_bytes(tokens) bytes,
+ * overwritten; one call at a time per workspace) for the per-token statistics. One or two
+ * launches (the statistics pass where the product does not sum them itself; the product).
+ * Errors as for swin_wattn_qkv_proj. The size queries return 0 for unsupported arguments.
+ */
+size_t swin_wattn_qkv_prepared_bytes(int C);
+size_t swin_wattn_qkv_stats_bytes(int tokens);
+int swin_wattn_qkv_prepare(const float* gamma, const float* beta, const void* w_qkv, const float* b_qkv, int C,
+                           void* prepared, size_t prepared_bytes, struct CUstream_st* stream);
+int swin_wattn_qkv_proj_prepared(const void* x, const void* prepared, void* qkv, int tokens, int C, float eps,
+                                 void* stats_workspace, size_t stats_bytes, int* status,
+                                 struct CUstream_st* stream);
+
+/*
  * The consumer step after the attention: the output projection, then its bias and the
  * residual added, fused into the product's epilogue (NVIDIA Swin talk, uticex.com article
  * 1598, section 3 "inference optimisation": the bias-plus-residual pass in its half2

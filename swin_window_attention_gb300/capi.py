@@ -39,6 +39,10 @@ SIGNATURES = {
     "swin_wattn_bwd_noalloc": ([_vp, _vp, _vp, _vp, _vp] + [_i] * 8 + [_vp], _i),
     "swin_wattn_qkv_workspace_bytes": ([_i, _i], ctypes.c_size_t),
     "swin_wattn_qkv_proj": ([_vp] * 6 + [_i, _i, ctypes.c_float, _vp, ctypes.c_size_t, _vp, _vp], _i),
+    "swin_wattn_qkv_prepared_bytes": ([_i], ctypes.c_size_t),
+    "swin_wattn_qkv_stats_bytes": ([_i], ctypes.c_size_t),
+    "swin_wattn_qkv_prepare": ([_vp] * 4 + [_i, _vp, ctypes.c_size_t, _vp], _i),
+    "swin_wattn_qkv_proj_prepared": ([_vp] * 3 + [_i, _i, ctypes.c_float, _vp, ctypes.c_size_t, _vp, _vp], _i),
     "swin_wattn_proj_residual": ([_vp] * 5 + [_i, _i, _vp, _vp], _i),
     "swin_wattn_set_fwd_kernel": ([_vp, _i], _i),
     "swin_wattn_fwd_kernel": ([_vp], _i),
@@ -145,6 +149,56 @@ def qkv_proj(x, gamma, beta, w, b, qkv=None, eps=1e-5, status=None, workspace=No
     if rc != OK:
         raise SwinWAttnError("swin_wattn_qkv_proj", rc)
     return qkv
+
+
+def swin_wattn_qkv_prepared_bytes(C):
+    return int(load().swin_wattn_qkv_prepared_bytes(C))
+
+
+def swin_wattn_qkv_stats_bytes(tokens):
+    return int(load().swin_wattn_qkv_stats_bytes(tokens))
+
+
+def swin_wattn_qkv_prepare(gamma_ptr, beta_ptr, w_ptr, b_ptr, C, prepared_ptr, prepared_bytes, stream):
+    return load().swin_wattn_qkv_prepare(gamma_ptr, beta_ptr, w_ptr, b_ptr, C, prepared_ptr, prepared_bytes, stream)
+
+
+def swin_wattn_qkv_proj_prepared(x_ptr, prepared_ptr, qkv_ptr, tokens, C, eps, stats_ptr, stats_bytes, status_ptr,
+                                 stream):
+    return load().swin_wattn_qkv_proj_prepared(x_ptr, prepared_ptr, qkv_ptr, tokens, C, eps, stats_ptr,
+                                               stats_bytes, status_ptr, stream)
+
+
+class QkvProjection:
+    """The producer step with its weights prepared once: LayerNorm over the last axis of a
+    bf16 CUDA tensor x [..., C], then x W^T + b, for fixed gamma, beta, W [3C, C], b [3C]."""
+
+    def __init__(self, gamma, beta, w, b, stream=None):
+        import torch
+        self.C = int(w.shape[1])
+        self.prepared = torch.empty(max(swin_wattn_qkv_prepared_bytes(self.C), 1), dtype=torch.uint8,
+                                    device=w.device)
+        rc = swin_wattn_qkv_prepare(gamma.data_ptr(), beta.data_ptr(), w.data_ptr(), b.data_ptr(), self.C,
+                                    self.prepared.data_ptr(), self.prepared.numel(), _stream_handle(stream))
+        if rc != OK:
+            raise SwinWAttnError("swin_wattn_qkv_prepare", rc)
+        self.stats = None
+
+    def __call__(self, x, qkv=None, eps=1e-5, status=None, stream=None):
+        import torch
+        C = self.C
+        tokens = x.numel() // C
+        if qkv is None:
+            qkv = torch.empty(x.shape[:-1] + (3 * C,), dtype=torch.bfloat16, device=x.device)
+        need = max(swin_wattn_qkv_stats_bytes(tokens), 16)
+        if self.stats is None or self.stats.numel() < need:
+            self.stats = torch.empty(need, dtype=torch.uint8, device=x.device)
+        rc = swin_wattn_qkv_proj_prepared(x.data_ptr(), self.prepared.data_ptr(), qkv.data_ptr(), tokens, C, eps,
+                                          self.stats.data_ptr(), self.stats.numel(),
+                                          None if status is None else status.data_ptr(), _stream_handle(stream))
+        if rc != OK:
+            raise SwinWAttnError("swin_wattn_qkv_proj_prepared", rc)
+        return qkv
 
 
 def swin_wattn_proj_residual(o_ptr, wp_ptr, bp_ptr, residual_ptr, y_ptr, tokens, C, status_ptr, stream):

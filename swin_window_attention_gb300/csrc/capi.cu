@@ -28,6 +28,13 @@ cudaError_t bwd_config(const Plan& pl, BwdLaunch* L);
 cudaError_t qkv_proj_launch(const void* x, const float* gamma, const float* beta, const void* w, const float* b,
                             void* out, int T, int C, float eps, void* workspace, int* status, cudaStream_t st);
 size_t qkv_workspace_bytes(int C, int64_t T);
+size_t qkv_prepared_bytes(int C);
+size_t qkv_stats_bytes(int64_t T);
+cudaError_t qkv_prepare_launch(const float* gamma, const float* beta, const void* w, const float* b, int C,
+                               void* prepared, cudaStream_t st);
+cudaError_t qkv_proj_prepared_launch(const void* x, const void* prepared, void* out, int T, int C, float eps,
+                                     void* stats_workspace, int* status, cudaStream_t st);
+int qkv_launches(int T, int C, bool fold);
 cudaError_t proj_residual_launch(const void* o, const void* wp, const float* bp, const void* residual, void* y,
                                  int T, int C, int* status, cudaStream_t st);
 cudaError_t bwd_launch(const Plan& pl, const BwdLaunch& L, const void* qkv, const void* dout,
@@ -405,6 +412,54 @@ int swin_wattn_qkv_proj(const void* x, const float* gamma, const float* beta, co
                                         reinterpret_cast<cudaStream_t>(stream));
   g_launches += 2;
   return e == cudaSuccess ? SWIN_WATTN_OK : cuda_fail(e, "swin_wattn_qkv_proj");
+}
+
+size_t swin_wattn_qkv_prepared_bytes(int C) {
+  return (C < 32 || C > 1536 || C % 32 != 0) ? 0 : swin::qkv_prepared_bytes(C);
+}
+
+size_t swin_wattn_qkv_stats_bytes(int tokens) { return tokens < 0 ? 0 : swin::qkv_stats_bytes(tokens); }
+
+int swin_wattn_qkv_prepare(const float* gamma, const float* beta, const void* w_qkv, const float* b_qkv, int C,
+                           void* prepared, size_t prepared_bytes, struct CUstream_st* stream) {
+  if (C < 32 || C > 1536 || C % 32 != 0) return SWIN_WATTN_ERR_UNSUPPORTED;
+  if (prepared_bytes < swin::qkv_prepared_bytes(C)) {
+    swin::set_last_error("swin_wattn_qkv_prepare: buffer smaller than swin_wattn_qkv_prepared_bytes(C)");
+    return SWIN_WATTN_ERR_INVALID_ARG;
+  }
+  int rc;
+  if ((rc = check_device_ptr(w_qkv, 16)) != SWIN_WATTN_OK) return rc;
+  if ((rc = check_device_ptr(prepared, 256)) != SWIN_WATTN_OK) return rc;
+  if ((rc = check_device_ptr(gamma, 4)) != SWIN_WATTN_OK) return rc;
+  if ((rc = check_device_ptr(beta, 4)) != SWIN_WATTN_OK) return rc;
+  if ((rc = check_device_ptr(b_qkv, 4)) != SWIN_WATTN_OK) return rc;
+  cudaError_t e = swin::qkv_prepare_launch(gamma, beta, w_qkv, b_qkv, C, prepared,
+                                           reinterpret_cast<cudaStream_t>(stream));
+  ++g_launches;
+  return e == cudaSuccess ? SWIN_WATTN_OK : cuda_fail(e, "swin_wattn_qkv_prepare");
+}
+
+int swin_wattn_qkv_proj_prepared(const void* x, const void* prepared, void* qkv, int tokens, int C, float eps,
+                                 void* stats_workspace, size_t stats_bytes, int* status, struct CUstream_st* stream) {
+  if (tokens < 0 || !(eps >= 0.0f) || !std::isfinite(eps)) return SWIN_WATTN_ERR_INVALID_ARG;
+  if (C < 32 || C > 1536 || C % 32 != 0) return SWIN_WATTN_ERR_UNSUPPORTED;
+  if ((int64_t)tokens >= ((int64_t)1 << 31)) return SWIN_WATTN_ERR_UNSUPPORTED;
+  if (tokens == 0) return SWIN_WATTN_OK;
+  if (stats_bytes < swin::qkv_stats_bytes(tokens)) {
+    swin::set_last_error("swin_wattn_qkv_proj_prepared: statistics workspace smaller than "
+                         "swin_wattn_qkv_stats_bytes(tokens)");
+    return SWIN_WATTN_ERR_INVALID_ARG;
+  }
+  int rc;
+  if ((rc = check_device_ptr(x, 16)) != SWIN_WATTN_OK) return rc;
+  if ((rc = check_device_ptr(prepared, 256)) != SWIN_WATTN_OK) return rc;
+  if ((rc = check_device_ptr(qkv, 16)) != SWIN_WATTN_OK) return rc;
+  if ((rc = check_device_ptr(stats_workspace, 16)) != SWIN_WATTN_OK) return rc;
+  if (status != nullptr && (rc = check_device_ptr(status, 4)) != SWIN_WATTN_OK) return rc;
+  cudaError_t e = swin::qkv_proj_prepared_launch(x, prepared, qkv, tokens, C, eps, stats_workspace, status,
+                                                 reinterpret_cast<cudaStream_t>(stream));
+  g_launches += swin::qkv_launches(tokens, C, false);
+  return e == cudaSuccess ? SWIN_WATTN_OK : cuda_fail(e, "swin_wattn_qkv_proj_prepared");
 }
 
 int swin_wattn_proj_residual(const void* o, const void* w_proj, const float* b_proj, const void* residual,

@@ -13,13 +13,15 @@
 //   W'[n][c] = bf16(gamma_c W[n][c]),  u_n = sum_c W'[n][c],  v_n = sum_c beta_c W[n][c] + b_n,
 // so the tensor cores consume the raw bf16 x tiles as they arrive and the epilogue applies
 // the row statistics (u is summed from the rounded W', so the mean cancels exactly against
-// the rounded weights). gemm_prep_kernel builds W', u and v once per call. The mean and
+// the rounded weights). W', u and v depend on the weights alone: the talk's section 3 says
+// inference may transform the qkv weight and bias ahead of time, so they are built once by
+// qkv_prepare_launch (or on every call by qkv_proj_launch). The mean and
 // 1 / sqrt(var + eps) of each token come from one of two places:
 // * when every token tile is one work item (many tokens), statistics warps sum them from
 //   the x tiles already staged for the product, at no extra memory traffic;
 // * when the output channels of a token tile are split over several work items (few
-//   tokens, wide C), gemm_prep_kernel also computes them in one coalesced pass over x, so
-//   that no work item repeats the sums.
+//   tokens, wide C), gemm_prep_kernel computes them first in one coalesced pass over x,
+//   so that no work item repeats the sums.
 //
 // Consumer (after the attention): y = residual + O Wp^T + bp (O the attention output
 // [tokens, C] bf16, Wp [C, C] bf16, bp [C] fp32, the residual [tokens, C] bf16), the
@@ -29,23 +31,23 @@
 //
 // Both are one kernel, gemm_kernel<MODE>: a dense contraction (2 K N flops per token for
 // K input and N output channels). One persistent CTA per SM walks work items (128 tokens,
-// the MMA's M, times a group of output-channel tiles of N <= 256), with specialised warps whose pipelines run on across
-// items:
+// the MMA's M, times a group of output-channel tiles of N <= 256), with specialised warps
+// whose pipelines run on across items:
 // * copy warp: TMA loads of activation chunks [128 tokens x 64 channels] and weight
-//   chunks [N tile x 64 channels], 128-byte swizzled, into a ring of as many stages as the rest
-//   of the shared memory holds (4 at N = 256, up to 8), so that enough bytes are in flight to cover the load
-//   latency at the tensor cores' rate (channels past C in the last chunk arrive as zeros
-//   and add nothing);
+//   chunks [N tile x 64 channels], 128-byte swizzled, into a ring of as many stages as
+//   the rest of the shared memory holds (4 at N = 256, up to 8); channels past C in the
+//   last chunk arrive as zeros and add nothing;
 // * MMA warp, one thread: per chunk four M128 N<=256 K16 tcgen05.mma (A = the activation
 //   chunk, B = the weight chunk) into one of two tensor-memory accumulators;
-// * statistics warps (four, producer with in-kernel statistics): thread r sums its token row's x
-//   and x^2, shifted by the row's first value, over the chunks of an item's first output
-//   tile and publishes mean and rstd;
-// * epilogue warps (eight, two per tensor-memory lane quadrant, taking alternate 32-channel
-//   slices): thread r forms rstd * acc - rstd * mean * u + v (producer) or
-//   acc + bp + residual (consumer) for its token row and rounds to bf16 into the warp's own 64-byte-swizzled staging tile [32 rows x 32 channels],
-//   which the warp's first lane writes out with a TMA store (two tiles per warp
-//   alternate; no barrier beyond the warp), while the next output tile accumulates.
+// * statistics warps (four, producer with statistics on chip): thread r sums its token
+//   row's x and x^2, shifted by the row's first value, over the chunks of an item's first
+//   output tile and publishes mean and rstd;
+// * epilogue warps (eight, two per tensor-memory lane quadrant, taking alternate
+//   32-channel slices): thread r forms rstd * acc - rstd * mean * u + v (producer) or
+//   acc + bp + residual (consumer) for its token row and rounds it to bf16 into the
+//   warp's own 64-byte-swizzled staging tile [32 rows x 32 channels], which the warp's
+//   first lane writes out with a TMA store (two tiles per warp alternate; no barrier
+//   beyond the warp), while the next output tile accumulates.
 // Every wait is bounded (1 s); a wait that runs out sets the caller's status word (when
 // one is given) and the CTA leaves after releasing its tensor memory.
 #include <cuda.h>
@@ -382,8 +384,8 @@ __global__ void __launch_bounds__(Roles<MODE>::kTHREADS, 1)
   if (warp == R::kMMA) tc::tmem_dealloc<kTMEM_COLS>(tmem);
 }
 
-// The producer's preparation. Blocks [0, fold_blocks): W'[n][c] = bf16(gamma_c W[n][c]), u_n = sum_c W'[n][c],
-// v_n = sum_c beta_c W[n][c] + b_n, one warp per output channel n.
+// The producer's preparation. Blocks [0, fold_blocks): W'[n][c] = bf16(gamma_c W[n][c]),
+// u_n = sum_c W'[n][c], v_n = sum_c beta_c W[n][c] + b_n, one warp per output channel n.
 // Blocks from fold_blocks on (when stats is given): (mean, 1 / sqrt(var + eps)) of each
 // token's C channels, four tokens per warp with their loads in flight together; shifted
 // sums (by the row's first value) in fp32, reduced across the warp.
@@ -394,14 +396,36 @@ __global__ void gemm_prep_kernel(const __nv_bfloat16* __restrict__ w, const floa
                                 float2* __restrict__ stats) {
   const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5, wpb = blockDim.x >> 5;
   if ((int)blockIdx.x < fold_blocks) {
+    // gamma and beta staged once per block, read back as float4 (8 channels per lane)
+    __shared__ __align__(16) float sg[kMaxC], sb[kMaxC];
+    for (int c = threadIdx.x; c < C; c += blockDim.x) {
+      sg[c] = gamma[c];
+      sb[c] = beta[c];
+    }
+    __syncthreads();
     for (int n = blockIdx.x * wpb + wib; n < N; n += fold_blocks * wpb) {
+      const uint4* wr = reinterpret_cast<const uint4*>(w + (int64_t)n * C);
+      uint4* fr = reinterpret_cast<uint4*>(wf + (int64_t)n * C);
       float su_ = 0.0f, sv_ = 0.0f;
-      for (int c = lane; c < C; c += 32) {
-        const float wv = __bfloat162float(w[(int64_t)n * C + c]);
-        const __nv_bfloat16 f = __float2bfloat16_rn(gamma[c] * wv);
-        wf[(int64_t)n * C + c] = f;
-        su_ += __bfloat162float(f);
-        sv_ = fmaf(beta[c], wv, sv_);
+#pragma unroll 4
+      for (int c8 = lane; c8 < C / 8; c8 += 32) {  // 8 channels per lane and step
+        const uint4 w4 = wr[c8];
+        const float4 g0 = reinterpret_cast<const float4*>(sg)[2 * c8], g1 = reinterpret_cast<const float4*>(sg)[2 * c8 + 1];
+        const float4 b0 = reinterpret_cast<const float4*>(sb)[2 * c8], b1 = reinterpret_cast<const float4*>(sb)[2 * c8 + 1];
+        const float gg[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+        const float bb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+        const uint32_t in[4] = {w4.x, w4.y, w4.z, w4.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float w0 = bf16_lo(in[k]), w1 = bf16_hi(in[k]);
+          const __nv_bfloat16 f0 = __float2bfloat16_rn(gg[2 * k] * w0);
+          const __nv_bfloat16 f1 = __float2bfloat16_rn(gg[2 * k + 1] * w1);
+          su_ += __bfloat162float(f0) + __bfloat162float(f1);
+          sv_ = fmaf(bb[2 * k], w0, fmaf(bb[2 * k + 1], w1, sv_));
+          o[k] = (uint32_t)__bfloat16_as_ushort(f0) | ((uint32_t)__bfloat16_as_ushort(f1) << 16);
+        }
+        fr[c8] = make_uint4(o[0], o[1], o[2], o[3]);
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
@@ -461,12 +485,12 @@ __global__ void gemm_prep_kernel(const __nv_bfloat16* __restrict__ w, const floa
 
 }  // namespace
 
-// Producer workspace of one call: W' [3C, C] bf16, u and v [3C] fp32, then the token
-// statistics [T] (mean, rstd), each part 256-byte aligned.
+// Prepared producer weights: W' [3C, C] bf16, u and v [3C] fp32, each part 256-byte
+// aligned. The one-call workspace adds the token statistics [T] (mean, rstd).
 static size_t align256(size_t n) { return (n + 255) & ~(size_t)255; }
-size_t qkv_workspace_bytes(int C, int64_t T) {
-  return align256((size_t)3 * C * C * 2) + 2 * align256((size_t)3 * C * 4) + align256((size_t)T * 8);
-}
+size_t qkv_prepared_bytes(int C) { return align256((size_t)3 * C * C * 2) + 2 * align256((size_t)3 * C * 4); }
+size_t qkv_stats_bytes(int64_t T) { return align256((size_t)T * 8); }
+size_t qkv_workspace_bytes(int C, int64_t T) { return qkv_prepared_bytes(C) + qkv_stats_bytes(T); }
 
 namespace {
 
@@ -561,36 +585,89 @@ GemmParams base_params(void* out, int T, int K, int N, int* status) {
 
 }  // namespace
 
-// Producer: qkv = LN(x) W^T + b. Two launches: gemm_prep_kernel, then gemm_kernel.
-cudaError_t qkv_proj_launch(const void* x, const float* gamma, const float* beta, const void* w, const float* b,
-                            void* out, int T, int C, float eps, void* workspace, int* status, cudaStream_t st) {
-  if (T <= 0) return cudaSuccess;
-  if (C % 32 != 0 || C < 32 || C > kMaxC) return cudaErrorInvalidValue;
+namespace {
+
+struct Prepared {
+  __nv_bfloat16* wf;
+  float* u;
+  float* v;
+};
+
+Prepared prepared_parts(void* prepared, int C) {
+  unsigned char* p = static_cast<unsigned char*>(prepared);
+  const int N = 3 * C;
+  Prepared r;
+  r.wf = reinterpret_cast<__nv_bfloat16*>(p);
+  r.u = reinterpret_cast<float*>(p + align256((size_t)N * C * 2));
+  r.v = reinterpret_cast<float*>(p + align256((size_t)N * C * 2) + align256((size_t)N * 4));
+  return r;
+}
+
+// The fold (when w is given) and the token statistics (when the product will not sum them
+// on chip) in one launch, then the product.
+cudaError_t qkv_run(const void* x, const float* gamma, const float* beta, const void* w, const float* b,
+                    const Prepared& pw, float2* stats, void* out, int T, int C, float eps, int* status,
+                    cudaStream_t st) {
   const int N = 3 * C;
   ItemPlan ip;
   cudaError_t e = plan_items(T, N, &ip);
   if (e != cudaSuccess) return e;
-  unsigned char* ws = static_cast<unsigned char*>(workspace);
-  __nv_bfloat16* wf = reinterpret_cast<__nv_bfloat16*>(ws);
-  float* u = reinterpret_cast<float*>(ws + align256((size_t)N * C * 2));
-  float* v = u + align256((size_t)N * 4) / 4;
-  float2* stats = reinterpret_cast<float2*>(reinterpret_cast<unsigned char*>(v) + align256((size_t)N * 4));
   const bool chip_stats = ip.one_item_per_token_tile;  // each token tile is one item: sum on chip
-  const int fold_blocks = (N + 7) / 8;
+  const int fold_blocks = w != nullptr ? (N + 7) / 8 : 0;
   const int stat_blocks = chip_stats ? 0 : (int)std::min<int64_t>(((int64_t)T + 31) / 32, 16 * ip.sms);
-  gemm_prep_kernel<<<fold_blocks + stat_blocks, 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(w), gamma,
-                                                              beta, b, C, N, wf, u, v, fold_blocks,
-                                                              reinterpret_cast<const __nv_bfloat16*>(x), T, eps,
-                                                              stats);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  if (fold_blocks + stat_blocks > 0) {
+    gemm_prep_kernel<<<fold_blocks + stat_blocks, 256, 0, st>>>(
+        reinterpret_cast<const __nv_bfloat16*>(w), gamma, beta, b, C, N, pw.wf, pw.u, pw.v, fold_blocks,
+        reinterpret_cast<const __nv_bfloat16*>(x), T, eps, stats);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
   GemmParams p = base_params(out, T, C, N, status);
-  p.u = u;
-  p.v = v;
+  p.u = pw.u;
+  p.v = pw.v;
   p.eps = eps;
-  if (chip_stats) return launch_gemm<kLnChipStats>(ip, p, x, wf, st);
+  if (chip_stats) return launch_gemm<kLnChipStats>(ip, p, x, pw.wf, st);
   p.stats = stats;
-  return launch_gemm<kLnPrepStats>(ip, p, x, wf, st);
+  return launch_gemm<kLnPrepStats>(ip, p, x, pw.wf, st);
+}
+
+}  // namespace
+
+// Producer, one call: the weights are folded into the workspace, then the product. Two
+// launches (the prep kernel, the product).
+cudaError_t qkv_proj_launch(const void* x, const float* gamma, const float* beta, const void* w, const float* b,
+                            void* out, int T, int C, float eps, void* workspace, int* status, cudaStream_t st) {
+  if (T <= 0) return cudaSuccess;
+  if (C % 32 != 0 || C < 32 || C > kMaxC) return cudaErrorInvalidValue;
+  float2* stats = reinterpret_cast<float2*>(static_cast<unsigned char*>(workspace) + qkv_prepared_bytes(C));
+  return qkv_run(x, gamma, beta, w, b, prepared_parts(workspace, C), stats, out, T, C, eps, status, st);
+}
+
+// Producer weights prepared ahead of time: W', u and v into `prepared`. One launch.
+cudaError_t qkv_prepare_launch(const float* gamma, const float* beta, const void* w, const float* b, int C,
+                               void* prepared, cudaStream_t st) {
+  if (C % 32 != 0 || C < 32 || C > kMaxC) return cudaErrorInvalidValue;
+  const int N = 3 * C;
+  const Prepared pw = prepared_parts(prepared, C);
+  gemm_prep_kernel<<<(N + 7) / 8, 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(w), gamma, beta, b, C, N,
+                                                pw.wf, pw.u, pw.v, (N + 7) / 8, nullptr, 0, 0.0f, nullptr);
+  return cudaGetLastError();
+}
+
+// Producer on prepared weights: [the token statistics,] the product.
+cudaError_t qkv_proj_prepared_launch(const void* x, const void* prepared, void* out, int T, int C, float eps,
+                                     void* stats_workspace, int* status, cudaStream_t st) {
+  if (T <= 0) return cudaSuccess;
+  if (C % 32 != 0 || C < 32 || C > kMaxC) return cudaErrorInvalidValue;
+  return qkv_run(x, nullptr, nullptr, nullptr, nullptr, prepared_parts(const_cast<void*>(prepared), C),
+                 static_cast<float2*>(stats_workspace), out, T, C, eps, status, st);
+}
+
+// Launches of one producer call for T tokens of C channels with or without the fold.
+int qkv_launches(int T, int C, bool fold) {
+  ItemPlan ip;
+  if (T <= 0 || plan_items(T, 3 * C, &ip) != cudaSuccess) return 0;
+  return 1 + ((fold || !ip.one_item_per_token_tile) ? 1 : 0);
 }
 
 // Consumer: y = residual + O Wp^T + bp. One launch.

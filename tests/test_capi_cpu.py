@@ -82,6 +82,15 @@ def test_gemm_steps_reject_bad_arguments_before_touching_cuda(lib):
     assert lib.swin_wattn_qkv_proj(*([None] * 6), 4, 96, -1.0, None, 0, None, None) == lib.ERR_INVALID_ARG
     assert lib.swin_wattn_qkv_proj(*([None] * 6), 4, 80, 1e-5, None, 0, None, None) == lib.ERR_UNSUPPORTED
     assert lib.swin_wattn_qkv_proj(*([None] * 6), 0, 96, 1e-5, None, 0, None, None) == lib.OK
+    # producer on prepared weights
+    assert lib.swin_wattn_qkv_prepared_bytes(80) == 0
+    assert lib.swin_wattn_qkv_prepared_bytes(96) >= 288 * 96 * 2 + 2 * 288 * 4
+    assert lib.swin_wattn_qkv_stats_bytes(-1) == 0 and lib.swin_wattn_qkv_stats_bytes(5) >= 40
+    assert lib.swin_wattn_qkv_prepare(*([None] * 4), 80, None, 0, None) == lib.ERR_UNSUPPORTED
+    assert lib.swin_wattn_qkv_prepare(*([None] * 4), 96, None, 0, None) == lib.ERR_INVALID_ARG
+    assert lib.swin_wattn_qkv_proj_prepared(None, None, None, -1, 96, 1e-5, None, 0, None, None) == lib.ERR_INVALID_ARG
+    assert lib.swin_wattn_qkv_proj_prepared(None, None, None, 4, 80, 1e-5, None, 0, None, None) == lib.ERR_UNSUPPORTED
+    assert lib.swin_wattn_qkv_proj_prepared(None, None, None, 0, 96, 1e-5, None, 0, None, None) == lib.OK
     # consumer
     assert lib.swin_wattn_proj_residual(*([None] * 5), -1, 96, None, None) == lib.ERR_INVALID_ARG
     assert lib.swin_wattn_proj_residual(*([None] * 5), 4, 48, None, None) == lib.ERR_UNSUPPORTED

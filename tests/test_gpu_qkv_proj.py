@@ -126,3 +126,51 @@ def test_qkv_proj_error_paths():
     host = torch.zeros(4, 96, dtype=torch.bfloat16)
     assert f(host.data_ptr(), 4, 96, nws) == capi.ERR_INVALID_ARG
     assert f(x.data_ptr() + 2, 4, 96, nws) == capi.ERR_MISALIGNED
+
+
+@pytest.mark.parametrize("T,C", [(300, 192), (3136, 1536), (80001, 96)])
+def test_prepared_weights_give_the_same_bits(T, C):
+    """Weights prepared once, then two different inputs: bit-identical to the one-call form
+    (statistics from the prep pass at 300 and 3136 tokens, on chip at 80001)."""
+    wl = workload(1, 1, T, C, C // 32, 1, 0, seed=3 * T + C)
+    x, g, be, w, b = inputs.make_producer(wl)
+    gd, bed, wd, bd = g.to(DEV), be.to(DEV), w.to(DEV), b.to(DEV)
+    proj = capi.QkvProjection(gd, bed, wd, bd)
+    for xi in (x, (x.float() * 0.5 - 1.0).to(torch.bfloat16)):
+        xd = xi.to(DEV)
+        status = torch.zeros(1, dtype=torch.int32, device=DEV)
+        y1 = proj(xd, status=status)
+        y2 = capi.qkv_proj(xd, gd, bed, wd, bd, status=status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        assert torch.equal(y1, y2)
+    if T <= 4096:
+        assert_close_qkv("qkv (prepared)", y1, oracle.qkv_proj(_f64(xi), _f64(g), _f64(be), _f64(w), _f64(b)))
+
+
+def test_prepared_error_paths():
+    C, T = 96, 4
+    v = torch.zeros(3 * C, dtype=torch.float32, device=DEV)
+    w = torch.zeros(3 * C, C, dtype=torch.bfloat16, device=DEV)
+    x = torch.zeros(T, C, dtype=torch.bfloat16, device=DEV)
+    out = torch.zeros(T, 3 * C, dtype=torch.bfloat16, device=DEV)
+    npb = capi.swin_wattn_qkv_prepared_bytes(C)
+    nst = capi.swin_wattn_qkv_stats_bytes(T)
+    assert npb >= 3 * C * C * 2 + 2 * 3 * C * 4 and nst >= T * 8
+    assert capi.swin_wattn_qkv_prepared_bytes(80) == 0
+    prep = torch.empty(npb, dtype=torch.uint8, device=DEV)
+    st = torch.empty(nst, dtype=torch.uint8, device=DEV)
+    s = torch.cuda.current_stream().cuda_stream
+    pr = lambda C_, nb: capi.swin_wattn_qkv_prepare(v.data_ptr(), v.data_ptr(), w.data_ptr(), v.data_ptr(), C_,
+                                                    prep.data_ptr(), nb, s)
+    assert pr(80, npb) == capi.ERR_UNSUPPORTED
+    assert pr(C, npb - 256) == capi.ERR_INVALID_ARG
+    assert pr(C, npb) == capi.OK
+    f = lambda T_, nb, sp: capi.swin_wattn_qkv_proj_prepared(x.data_ptr(), prep.data_ptr(), out.data_ptr(), T_, C,
+                                                             1e-5, sp, nb, None, s)
+    assert f(T, nst - 8, st.data_ptr()) == capi.ERR_INVALID_ARG
+    assert f(-1, nst, st.data_ptr()) == capi.ERR_INVALID_ARG
+    assert f(T, nst, st.data_ptr() + 8) == capi.ERR_MISALIGNED
+    assert f(T, nst, st.data_ptr()) == capi.OK
+    torch.cuda.synchronize()
+    assert torch.all(out == 0)  # zero weights and biases
