@@ -362,7 +362,7 @@ def run_gpu(args):
     ach = fwd_bytes(wdom) / (per_stage_ms[kdom] / 1e3) / 1e9
     khash = kernel_source_hash()
     roofline = {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s",
-                "frac": round(ach / hbm, 4), "traffic": ncu_traffic(khash) if kdom == 0 else None,
+                "frac": round(ach / hbm, 4), "traffic": ncu_traffic(khash) if wdom.name == "swin_l224_s1" else None,
                 "kernel": f"{kernel_name(capi, plans[kdom])} on {wdom.name}",
                 "bytes_per_launch": fwd_bytes(wdom), "peak_source": peak_src + " hbm_gbs",
                 "kernel_source_hash": khash}

@@ -310,25 +310,36 @@ __global__ void __launch_bounds__(Roles<MODE>::kTHREADS, 1)
       }
       const float rstd = ms.y, nmr = -ms.x * ms.y;
       const float2 r2 = make_float2(rstd, rstd), nm2 = make_float2(nmr, nmr);
+      // consumer: the residual's 32 channels of this row for a slice, loaded one slice
+      // ahead (the first slice of a tile before its accumulator is waited for)
+      auto load_residual = [&](int n0_, int c0_, uint4* dst) {
+        const uint4* rr = reinterpret_cast<const uint4*>(p.residual + (int64_t)(t0 + row) * p.N + n0_ + c0_);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) dst[c] = t0 + row < p.T ? rr[c] : make_uint4(0, 0, 0, 0);
+      };
+      uint4 rnext[4];
       for (int jj = 0; jj < ntile; ++jj, ++g) {
         const int buf = g & 1;
+        const int n0 = (j0 + jj) * p.NT;
+        if constexpr (MODE == kBiasResidual) {
+          if (parity * kSC < p.NT) load_residual(n0, parity * kSC, rnext);
+        }
         if (!warp_wait(dfull_bar(buf), (g >> 1) & 1)) {
           bad = 1;
           break;
         }
         tc::fence_after_sync();
-        const int n0 = (j0 + jj) * p.NT;
         for (int c0 = parity * kSC; c0 < p.NT; c0 += 2 * kSC, ++m) {
           unsigned char* so = wstage + (m & 1) * (32 * 64);
           if (m >= 2) {
             if (lane == 0) tc::bulk_wait_read<1>();  // the store of slice m - 2 has read its tile
             __syncwarp();
           }
-          uint4 rv[4];  // consumer: the residual's 32 channels of this row, loaded ahead
+          uint4 rv[4];
           if constexpr (MODE == kBiasResidual) {
-            const uint4* rr = reinterpret_cast<const uint4*>(p.residual + (int64_t)(t0 + row) * p.N + n0 + c0);
 #pragma unroll
-            for (int c = 0; c < 4; ++c) rv[c] = t0 + row < p.T ? rr[c] : make_uint4(0, 0, 0, 0);
+            for (int c = 0; c < 4; ++c) rv[c] = rnext[c];
+            if (c0 + 2 * kSC < p.NT) load_residual(n0, c0 + 2 * kSC, rnext);
           }
           uint32_t a[32];
           tc::ld32_wait(trow + buf * kMaxNT + c0, a);
