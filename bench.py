@@ -350,7 +350,8 @@ def run_gpu(args):
     for wl, ms in zip(sweep, per_stage_ms):
         gbs = fwd_bytes(wl) / (ms / 1e3) / 1e9
         stages.append({"workload": wl.name, "us": round(ms * 1e3, 2),
-                       "tokens_per_s": wl.tokens / (ms / 1e3), "GBps": round(gbs, 1),
+                       "tokens_per_s": wl.tokens / (ms / 1e3),
+                       "window_heads_per_s": wl.window_heads / (ms / 1e3), "GBps": round(gbs, 1),
                        "frac_of_measured_hbm": round(gbs / hbm, 4),
                        "tflops": round(fwd_flops(wl) / (ms / 1e3) / 1e12, 1)})
     sweep_bytes = sum(fwd_bytes(wl) for wl in sweep)
@@ -420,6 +421,7 @@ def run_gpu(args):
                        "fwd_kernel": kernel_name(capi, plans[0])},
             "roofline": roofline,
             "sweep": {"us": round(sweep_ms * 1e3, 2),
+                      "window_heads_per_s": sum(wl.window_heads for wl in sweep) / (sweep_ms / 1e3),
                       "GBps": round(sweep_bytes / (sweep_ms / 1e3) / 1e9, 1),
                       "frac_of_measured_hbm": round(sweep_bytes / (sweep_ms / 1e3) / 1e9 / hbm, 4),
                       "stages": stages},
@@ -639,6 +641,7 @@ def run_train_step(args, dev, stream, lib, capi, hbm, ws):
         b_ms = statistics.mean(ev[i][k][2].elapsed_time(ev[i][k][3]) for i in range(steps))
         s_ms = statistics.mean(ev[i][k][0].elapsed_time(ev[i][k][1]) for i in range(steps))
         stages.append({"workload": wl.name, "set_bias_us": round(s_ms * 1e3, 2),
+                       "window_heads_per_s_fwd_bwd": wl.window_heads / ((f_ms + b_ms) / 1e3),
                        "fwd_us": round(f_ms * 1e3, 2), "bwd_us": round(b_ms * 1e3, 2),
                        "fwd_frac_of_measured_hbm": round(fwd_bytes(wl) / (f_ms / 1e3) / 1e9 / hbm, 4),
                        "bwd_frac_of_measured_hbm": round(bwd_bytes(wl) / (b_ms / 1e3) / 1e9 / hbm, 4),
