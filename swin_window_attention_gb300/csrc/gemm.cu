@@ -83,9 +83,16 @@ struct Roles {
 // [mean and rstd: 2 buffers x 128 x float2, with in-kernel statistics], per epilogue warp
 // two staging tiles of 32 rows x 64 bytes, the mbarriers and the tensor-memory address.
 constexpr int kSTATS_BYTES = 2 * kBM * 8;
-constexpr int kOUT_BYTES = 8 * 2 * 32 * 64;
-constexpr int kNBAR = 2 * kMaxSTAGES + 8;
-constexpr int kTAIL_BYTES = kOUT_BYTES + 8 * kNBAR + 8 + 1024;  // + alignment slack
+// Staging tiles per epilogue warp: two; three for the consumer, whose residual arrives by
+// TMA in the tile the result is then written over and stored from.
+template <int MODE>
+__host__ __device__ constexpr int out_bufs() { return MODE == 2 ? 3 : 2; }
+template <int MODE>
+__host__ __device__ constexpr int out_bytes() { return 8 * out_bufs<MODE>() * 32 * 64; }
+constexpr int kRBAR0 = 2 * kMaxSTAGES + 8;  // consumer: residual-load barriers, 3 per epilogue warp
+constexpr int kNBAR = kRBAR0 + 8 * 3;
+template <int MODE>
+__host__ __device__ constexpr int tail_bytes() { return out_bytes<MODE>() + 8 * kNBAR + 8 + 1024; }  // + alignment slack
 constexpr int kMinSMEM = 120 * 1024;  // above half of an SM: one CTA per SM
 constexpr int kTMEM_COLS = 512;                // two accumulators of up to 256 columns
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
@@ -99,7 +106,6 @@ struct GemmParams {
   const float* u;                  // [N] producer: row sums of W'
   const float* v;                  // [N] producer: beta W^T + b; consumer: bp
   const float2* stats;             // [T] (mean, rstd), producer with the prep pass
-  const __nv_bfloat16* residual;   // [T, N] consumer
   int* status;                     // optional: bit 0 set when a bounded wait ran out
   int T, K, N, NT, tiles_per_item, n_tt, n_items;
   int stages, stage_bytes;  // the ring: stages x (x chunk + NT x 128 bytes), 1024-byte multiples
@@ -117,7 +123,8 @@ __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w 
 template <int MODE>
 __global__ void __launch_bounds__(Roles<MODE>::kTHREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_constant__ CUtensorMap w_map,
-                const __grid_constant__ CUtensorMap out_map, const GemmParams p) {
+                const __grid_constant__ CUtensorMap out_map, const __grid_constant__ CUtensorMap res_map,
+                const GemmParams p) {
   using R = Roles<MODE>;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -151,6 +158,8 @@ __global__ void __launch_bounds__(Roles<MODE>::kTHREADS, 1)
       tc::mbar_init(full_bar(st), 1);
       tc::mbar_init(empty_bar(st), MODE == kLnChipStats ? 1 + 4 : 1);  // the MMA commit [and the statistics warps]
     }
+    if constexpr (MODE == kBiasResidual)
+      for (int b = 0; b < 8 * 3; ++b) tc::mbar_init(bar0 + 8 * (kRBAR0 + b), 1);
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(dfull_bar(b), 1);
       tc::mbar_init(dfree_bar(b), 8);
@@ -189,6 +198,12 @@ __global__ void __launch_bounds__(Roles<MODE>::kTHREADS, 1)
             first = 0;
           }
         }
+      }
+      if (bad) {
+        // after a timeout: let the loads still in flight land before the CTA leaves (a
+        // stage's last phase has completed already unless its bytes are still coming)
+        for (int s2 = 0; s2 < (first ? st : stages); ++s2)
+          tc::mbar_wait(full_bar(s2), s2 < st ? ph : ph ^ 1, kWaitLimitNs);
       }
     }
     __syncwarp();
@@ -287,10 +302,39 @@ __global__ void __launch_bounds__(Roles<MODE>::kTHREADS, 1)
   } else {
     // ==== epilogue warps: rstd * acc - rstd * mean * u + v or acc + bp + residual, bf16,
     //      staged TMA stores ===========================================================
+    constexpr int NB = out_bufs<MODE>();
     const int ew = warp - R::kEPI0, quad = ew & 3, parity = ew >> 2;
     const int row = quad * 32 + lane;
     const uint32_t trow = tmem + ((uint32_t)(quad * 32) << 16);
-    unsigned char* wstage = smem + p.off_out + ew * (2 * 32 * 64);
+    unsigned char* wstage = smem + p.off_out + ew * (NB * 32 * 64);
+    const bool has_slices = parity * kSC < p.NT;  // at N tile 32 the second warp of a quadrant idles
+    // Consumer: the residual of the warp's slices arrives by TMA, one slice ahead, in the
+    // staging tile the slice's result is written over. The warp's slices in order: items
+    // it, their output tiles jj, channel offsets c0 = parity * 32 + 64 i.
+    const uint32_t rbar0 = bar0 + 8 * (kRBAR0 + 3 * ew);
+    int nx_it = blockIdx.x, nx_jj = 0, nx_c0 = parity * kSC;  // the next slice to request
+    int issued = 0;                                           // residual loads requested
+    auto request_next = [&]() {
+      if (!has_slices || nx_it >= p.n_items) return;
+      int t0_, j0_, nt_;
+      item_tiles(nx_it, t0_, j0_, nt_);
+      if (lane == 0) {
+        const uint32_t rb = rbar0 + 8 * (issued % 3);
+        tc::mbar_expect_tx(rb, 32 * 64);
+        tc::tile_load_2d(smem_u32(wstage + (issued % 3) * (32 * 64)), &res_map, (j0_ + nx_jj) * p.NT + nx_c0,
+                         t0_ + quad * 32, rb);
+      }
+      ++issued;
+      nx_c0 += 2 * kSC;
+      if (nx_c0 >= p.NT) {
+        nx_c0 = parity * kSC;
+        if (++nx_jj >= nt_) {
+          nx_jj = 0;
+          nx_it += gridDim.x;
+        }
+      }
+    };
+    if constexpr (MODE == kBiasResidual) request_next();
     int g = 0, k = 0, m = 0;  // output tiles, items, slices stored by this warp
     for (int it = blockIdx.x; it < p.n_items && !bad; it += gridDim.x, ++k) {
       int t0, j0, ntile;
@@ -310,19 +354,15 @@ __global__ void __launch_bounds__(Roles<MODE>::kTHREADS, 1)
       }
       const float rstd = ms.y, nmr = -ms.x * ms.y;
       const float2 r2 = make_float2(rstd, rstd), nm2 = make_float2(nmr, nmr);
-      // consumer: the residual's 32 channels of this row for a slice, loaded one slice
-      // ahead (the first slice of a tile before its accumulator is waited for)
-      auto load_residual = [&](int n0_, int c0_, uint4* dst) {
-        const uint4* rr = reinterpret_cast<const uint4*>(p.residual + (int64_t)(t0 + row) * p.N + n0_ + c0_);
-#pragma unroll
-        for (int c = 0; c < 4; ++c) dst[c] = t0 + row < p.T ? rr[c] : make_uint4(0, 0, 0, 0);
-      };
-      uint4 rnext[4];
       for (int jj = 0; jj < ntile; ++jj, ++g) {
         const int buf = g & 1;
         const int n0 = (j0 + jj) * p.NT;
-        if constexpr (MODE == kBiasResidual) {
-          if (parity * kSC < p.NT) load_residual(n0, parity * kSC, rnext);
+        // u and v (bp for the consumer) of the next slice's 32 channels, lane = channel:
+        // one coalesced load each, one slice ahead, broadcast to the rows by shuffles
+        float un = 0.0f, vn = 0.0f;
+        if (has_slices) {
+          vn = __ldg(p.v + n0 + parity * kSC + lane);
+          if constexpr (MODE != kBiasResidual) un = __ldg(p.u + n0 + parity * kSC + lane);
         }
         if (!warp_wait(dfull_bar(buf), (g >> 1) & 1)) {
           bad = 1;
@@ -330,49 +370,48 @@ __global__ void __launch_bounds__(Roles<MODE>::kTHREADS, 1)
         }
         tc::fence_after_sync();
         for (int c0 = parity * kSC; c0 < p.NT; c0 += 2 * kSC, ++m) {
-          unsigned char* so = wstage + (m & 1) * (32 * 64);
+          unsigned char* so = wstage + (m % NB) * (32 * 64);
           if (m >= 2) {
             if (lane == 0) tc::bulk_wait_read<1>();  // the store of slice m - 2 has read its tile
             __syncwarp();
           }
-          uint4 rv[4];
-          if constexpr (MODE == kBiasResidual) {
-#pragma unroll
-            for (int c = 0; c < 4; ++c) rv[c] = rnext[c];
-            if (c0 + 2 * kSC < p.NT) load_residual(n0, c0 + 2 * kSC, rnext);
+          if constexpr (MODE == kBiasResidual) request_next();  // slice m + 1, into the tile of m - 2
+          const float uc = un, vc = vn;
+          if (c0 + 2 * kSC < p.NT) {
+            vn = __ldg(p.v + n0 + c0 + 2 * kSC + lane);
+            if constexpr (MODE != kBiasResidual) un = __ldg(p.u + n0 + c0 + 2 * kSC + lane);
           }
           uint32_t a[32];
           tc::ld32_wait(trow + buf * kMaxNT + c0, a);
-          // u and v: the same 32 channels for every lane (broadcast loads through L1)
-          const float4* uu = reinterpret_cast<const float4*>(p.u + n0 + c0);
-          const float4* vv = reinterpret_cast<const float4*>(p.v + n0 + c0);
+          if constexpr (MODE == kBiasResidual) {
+            if (!warp_wait(rbar0 + 8 * (m % 3), (m / 3) & 1)) {
+              bad = 1;
+              break;
+            }
+          }
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
+            uint4* sp = reinterpret_cast<uint4*>(so + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4));
+            uint4 rw = make_uint4(0, 0, 0, 0);
+            if constexpr (MODE == kBiasResidual) rw = *sp;  // the residual's 8 channels of this row
+            const uint32_t rr[4] = {rw.x, rw.y, rw.z, rw.w};
             uint32_t o[4];
 #pragma unroll
-            for (int w2 = 0; w2 < 2; ++w2) {
-              const int e = 8 * c + 4 * w2;
+            for (int q = 0; q < 4; ++q) {
+              const int e = 8 * c + 2 * q;
               const float2 a0 = make_float2(__uint_as_float(a[e]), __uint_as_float(a[e + 1]));
-              const float2 a1 = make_float2(__uint_as_float(a[e + 2]), __uint_as_float(a[e + 3]));
-              const float4 v4 = __ldg(vv + 2 * c + w2);
-              float2 y0, y1;
+              const float2 v2 = make_float2(__shfl_sync(0xffffffffu, vc, e), __shfl_sync(0xffffffffu, vc, e + 1));
+              float2 y;
               if constexpr (MODE == kBiasResidual) {
                 // (acc + bp) + residual, as the definition adds them
-                const uint32_t r0 = w2 ? rv[c].z : rv[c].x, r1 = w2 ? rv[c].w : rv[c].y;
-                y0 = __fadd2_rn(__fadd2_rn(a0, make_float2(v4.x, v4.y)), make_float2(bf16_lo(r0), bf16_hi(r0)));
-                y1 = __fadd2_rn(__fadd2_rn(a1, make_float2(v4.z, v4.w)), make_float2(bf16_lo(r1), bf16_hi(r1)));
+                y = __fadd2_rn(__fadd2_rn(a0, v2), make_float2(bf16_lo(rr[q]), bf16_hi(rr[q])));
               } else {
-                const float4 u4 = __ldg(uu + 2 * c + w2);
-                const float2 c0v = __ffma2_rn(nm2, make_float2(u4.x, u4.y), make_float2(v4.x, v4.y));
-                const float2 c1v = __ffma2_rn(nm2, make_float2(u4.z, u4.w), make_float2(v4.z, v4.w));
-                y0 = __ffma2_rn(a0, r2, c0v);
-                y1 = __ffma2_rn(a1, r2, c1v);
+                const float2 u2 = make_float2(__shfl_sync(0xffffffffu, uc, e), __shfl_sync(0xffffffffu, uc, e + 1));
+                y = __ffma2_rn(a0, r2, __ffma2_rn(nm2, u2, v2));
               }
-              o[2 * w2] = pack_bf16(y0.x, y0.y);
-              o[2 * w2 + 1] = pack_bf16(y1.x, y1.y);
+              o[q] = pack_bf16(y.x, y.y);
             }
-            *reinterpret_cast<uint4*>(so + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4)) =
-                make_uint4(o[0], o[1], o[2], o[3]);
+            *sp = make_uint4(o[0], o[1], o[2], o[3]);
           }
           tc::fence_proxy_async();  // the staging tile to the copy engine
           __syncwarp();
@@ -381,10 +420,15 @@ __global__ void __launch_bounds__(Roles<MODE>::kTHREADS, 1)
             tc::bulk_commit();
           }
         }
+        if (bad) break;
         tc::fence_before_sync();
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(dfree_bar(buf));
       }
+    }
+    if constexpr (MODE == kBiasResidual) {
+      // after a timeout: let the residual loads still in flight land before the CTA leaves
+      for (int q = m; q < issued; ++q) warp_wait(rbar0 + 8 * (q % 3), (q / 3) & 1);
     }
     if (lane == 0) tc::bulk_wait_all();
   }
@@ -552,7 +596,8 @@ cudaError_t encode_2d(PFN_cuTensorMapEncodeTiled_v12000 encode, CUtensorMap* map
 }
 
 template <int MODE>
-cudaError_t launch_gemm(const ItemPlan& ip, GemmParams p, const void* a, const void* w, cudaStream_t st) {
+cudaError_t launch_gemm(const ItemPlan& ip, GemmParams p, const void* a, const void* w, cudaStream_t st,
+                        const void* residual = nullptr) {
   PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder_fn();
   if (encode == nullptr) return cudaErrorNotSupported;
   CUtensorMap a_map, w_map, out_map;
@@ -564,6 +609,10 @@ cudaError_t launch_gemm(const ItemPlan& ip, GemmParams p, const void* a, const v
   if (e == cudaSuccess)
     e = encode_2d(encode, &out_map, p.out, p.N, p.T, kSC, 32, CU_TENSOR_MAP_SWIZZLE_64B,
                   CU_TENSOR_MAP_L2_PROMOTION_NONE);
+  CUtensorMap res_map = out_map;  // read only by the consumer
+  if (e == cudaSuccess && residual != nullptr)
+    e = encode_2d(encode, &res_map, residual, p.N, p.T, kSC, 32, CU_TENSOR_MAP_SWIZZLE_64B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_128B);
   if (e != cudaSuccess) return e;
   p.NT = ip.NT;
   p.tiles_per_item = ip.per;
@@ -571,17 +620,17 @@ cudaError_t launch_gemm(const ItemPlan& ip, GemmParams p, const void* a, const v
   p.n_items = ip.n_items;
   p.stage_bytes = kXCH + ip.NT * 128;
   constexpr int kStatsBytes = MODE == kLnChipStats ? kSTATS_BYTES : 0;
-  const int fixed = kStatsBytes + kTAIL_BYTES;
+  const int fixed = kStatsBytes + tail_bytes<MODE>();
   p.stages = std::min(kMaxSTAGES, (ip.smem_max - fixed) / p.stage_bytes);
   if (p.stages < 2) return cudaErrorInvalidConfiguration;
   p.off_stats = p.stages * p.stage_bytes;
   p.off_out = p.off_stats + kStatsBytes;
-  p.off_bar = p.off_out + kOUT_BYTES;
+  p.off_bar = p.off_out + out_bytes<MODE>();
   const int smem = std::max(kMinSMEM, p.stages * p.stage_bytes + fixed);
   e = cudaFuncSetAttribute(gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   return launch_pdl(gemm_kernel<MODE>, dim3(std::min(ip.n_items, ip.sms)), dim3(Roles<MODE>::kTHREADS), smem, st,
-                    a_map, w_map, out_map, p);
+                    a_map, w_map, out_map, res_map, p);
 }
 
 GemmParams base_params(void* out, int T, int K, int N, int* status) {
@@ -691,8 +740,7 @@ cudaError_t proj_residual_launch(const void* o, const void* wp, const float* bp,
   if (e != cudaSuccess) return e;
   GemmParams p = base_params(y, T, C, C, status);
   p.v = bp;
-  p.residual = reinterpret_cast<const __nv_bfloat16*>(residual);
-  return launch_gemm<kBiasResidual>(ip, p, o, wp, st);
+  return launch_gemm<kBiasResidual>(ip, p, o, wp, st, residual);
 }
 
 }  // namespace swin
