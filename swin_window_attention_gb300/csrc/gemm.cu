@@ -83,12 +83,19 @@ struct Roles {
 // [mean and rstd: 2 buffers x 128 x float2, with in-kernel statistics], per epilogue warp
 // two staging tiles of 32 rows x 64 bytes, the mbarriers and the tensor-memory address.
 constexpr int kSTATS_BYTES = 2 * kBM * 8;
-// Staging tiles per epilogue warp: two; three for the consumer, whose residual arrives by
-// TMA in the tile the result is then written over and stored from.
+// Staging tiles per epilogue warp: three where the epilogue paces the kernel, so that a
+// store has two slices' time to read its tile before the tile is needed again (for the
+// consumer the residual arrives by TMA in the tile the result is then written over and
+// stored from, one slice ahead); two for the producer with the statistics pass (few
+// tokens, wide C: the tensor cores pace it, and the ring keeps the shared memory).
 template <int MODE>
-__host__ __device__ constexpr int out_bufs() { return MODE == 2 ? 3 : 2; }
+__host__ __device__ constexpr int out_bufs() { return MODE == 0 ? 2 : 3; }
+// per epilogue warp: the staging tiles, then (where the epilogue paces the kernel) u and
+// v of its slices of the current output tile (up to 4 slices x 32 channels x 2 floats)
 template <int MODE>
-__host__ __device__ constexpr int out_bytes() { return 8 * out_bufs<MODE>() * 32 * 64; }
+__host__ __device__ constexpr int uv_warp_bytes() { return MODE == 0 ? 0 : 4 * 64 * 4; }
+template <int MODE>
+__host__ __device__ constexpr int out_bytes() { return 8 * (out_bufs<MODE>() * 32 * 64 + uv_warp_bytes<MODE>()); }
 constexpr int kRBAR0 = 2 * kMaxSTAGES + 8;  // consumer: residual-load barriers, 3 per epilogue warp
 constexpr int kNBAR = kRBAR0 + 8 * 3;
 template <int MODE>
@@ -306,7 +313,8 @@ __global__ void __launch_bounds__(Roles<MODE>::kTHREADS, 1)
     const int ew = warp - R::kEPI0, quad = ew & 3, parity = ew >> 2;
     const int row = quad * 32 + lane;
     const uint32_t trow = tmem + ((uint32_t)(quad * 32) << 16);
-    unsigned char* wstage = smem + p.off_out + ew * (NB * 32 * 64);
+    unsigned char* wstage = smem + p.off_out + ew * (NB * 32 * 64 + uv_warp_bytes<MODE>());
+    float* wuv = reinterpret_cast<float*>(wstage + NB * 32 * 64);  // [slice i][u 32 | v 32]
     const bool has_slices = parity * kSC < p.NT;  // at N tile 32 the second warp of a quadrant idles
     // Consumer: the residual of the warp's slices arrives by TMA, one slice ahead, in the
     // staging tile the slice's result is written over. The warp's slices in order: items
@@ -357,30 +365,50 @@ __global__ void __launch_bounds__(Roles<MODE>::kTHREADS, 1)
       for (int jj = 0; jj < ntile; ++jj, ++g) {
         const int buf = g & 1;
         const int n0 = (j0 + jj) * p.NT;
-        // u and v (bp for the consumer) of the next slice's 32 channels, lane = channel:
-        // one coalesced load each, one slice ahead, broadcast to the rows by shuffles
-        float un = 0.0f, vn = 0.0f;
-        if (has_slices) {
-          vn = __ldg(p.v + n0 + parity * kSC + lane);
-          if constexpr (MODE != kBiasResidual) un = __ldg(p.u + n0 + parity * kSC + lane);
+        // u and v (bp for the consumer) of the warp's slices of this tile: one coalesced
+        // word per lane and slice, loaded while the accumulator is still being summed and
+        // kept in the warp's corner of shared memory for broadcast reads (with the
+        // statistics pass the tensor cores pace the kernel: broadcast reads from global)
+        if constexpr (MODE != kLnPrepStats) {
+          float ut[4], vt[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int c = parity * kSC + 2 * kSC * i;
+            ut[i] = vt[i] = 0.0f;
+            if (c < p.NT) {
+              vt[i] = __ldg(p.v + n0 + c + lane);
+              if constexpr (MODE != kBiasResidual) ut[i] = __ldg(p.u + n0 + c + lane);
+            }
+          }
+          __syncwarp();  // the previous tile's reads of the corner are done
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            wuv[64 * i + lane] = ut[i];
+            wuv[64 * i + 32 + lane] = vt[i];
+          }
+          __syncwarp();
         }
         if (!warp_wait(dfull_bar(buf), (g >> 1) & 1)) {
           bad = 1;
           break;
         }
         tc::fence_after_sync();
-        for (int c0 = parity * kSC; c0 < p.NT; c0 += 2 * kSC, ++m) {
+        int si = 0;  // the warp's slice index within the tile
+        for (int c0 = parity * kSC; c0 < p.NT; c0 += 2 * kSC, ++m, ++si) {
           unsigned char* so = wstage + (m % NB) * (32 * 64);
-          if (m >= 2) {
-            if (lane == 0) tc::bulk_wait_read<1>();  // the store of slice m - 2 has read its tile
+          if constexpr (MODE == kBiasResidual) {
+            if (m >= 2) {
+              if (lane == 0) tc::bulk_wait_read<1>();  // the store of slice m - 2 has read its tile
+              __syncwarp();
+            }
+            request_next();  // the residual of slice m + 1, into the tile of slice m - 2
+          } else if (m >= NB) {
+            if (lane == 0) tc::bulk_wait_read<NB - 1>();  // the store of slice m - NB has read its tile
             __syncwarp();
           }
-          if constexpr (MODE == kBiasResidual) request_next();  // slice m + 1, into the tile of m - 2
-          const float uc = un, vc = vn;
-          if (c0 + 2 * kSC < p.NT) {
-            vn = __ldg(p.v + n0 + c0 + 2 * kSC + lane);
-            if constexpr (MODE != kBiasResidual) un = __ldg(p.u + n0 + c0 + 2 * kSC + lane);
-          }
+          const float4* u4s = MODE == kLnPrepStats ? reinterpret_cast<const float4*>(p.u + n0 + c0)
+                                                   : reinterpret_cast<const float4*>(wuv + 64 * si);
+          const float4* v4s = MODE == kLnPrepStats ? reinterpret_cast<const float4*>(p.v + n0 + c0) : u4s + 8;
           uint32_t a[32];
           tc::ld32_wait(trow + buf * kMaxNT + c0, a);
           if constexpr (MODE == kBiasResidual) {
@@ -395,19 +423,26 @@ __global__ void __launch_bounds__(Roles<MODE>::kTHREADS, 1)
             uint4 rw = make_uint4(0, 0, 0, 0);
             if constexpr (MODE == kBiasResidual) rw = *sp;  // the residual's 8 channels of this row
             const uint32_t rr[4] = {rw.x, rw.y, rw.z, rw.w};
+            const float4 vA = v4s[2 * c], vB = v4s[2 * c + 1];  // broadcast reads
+            const float vv[8] = {vA.x, vA.y, vA.z, vA.w, vB.x, vB.y, vB.z, vB.w};
+            float uu[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+            if constexpr (MODE != kBiasResidual) {
+              const float4 uA = u4s[2 * c], uB = u4s[2 * c + 1];
+              uu[0] = uA.x, uu[1] = uA.y, uu[2] = uA.z, uu[3] = uA.w;
+              uu[4] = uB.x, uu[5] = uB.y, uu[6] = uB.z, uu[7] = uB.w;
+            }
             uint32_t o[4];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
               const int e = 8 * c + 2 * q;
               const float2 a0 = make_float2(__uint_as_float(a[e]), __uint_as_float(a[e + 1]));
-              const float2 v2 = make_float2(__shfl_sync(0xffffffffu, vc, e), __shfl_sync(0xffffffffu, vc, e + 1));
+              const float2 v2 = make_float2(vv[2 * q], vv[2 * q + 1]);
               float2 y;
               if constexpr (MODE == kBiasResidual) {
                 // (acc + bp) + residual, as the definition adds them
                 y = __fadd2_rn(__fadd2_rn(a0, v2), make_float2(bf16_lo(rr[q]), bf16_hi(rr[q])));
               } else {
-                const float2 u2 = make_float2(__shfl_sync(0xffffffffu, uc, e), __shfl_sync(0xffffffffu, uc, e + 1));
-                y = __ffma2_rn(a0, r2, __ffma2_rn(nm2, u2, v2));
+                y = __ffma2_rn(a0, r2, __ffma2_rn(nm2, make_float2(uu[2 * q], uu[2 * q + 1]), v2));
               }
               o[q] = pack_bf16(y.x, y.y);
             }
