@@ -136,7 +136,6 @@ __global__ void __launch_bounds__(Roles<MODE>::kTHREADS, 1)
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   pdl_launch_dependents();
-  pdl_wait();
   const uint32_t smem0 = smem_u32(smem);
   float2* sstats = reinterpret_cast<float2*>(smem + p.off_stats);  // [2][128] (mean, rstd)
   const uint32_t bar0 = smem0 + p.off_bar;
@@ -179,6 +178,9 @@ __global__ void __launch_bounds__(Roles<MODE>::kTHREADS, 1)
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
+  // The prologue above touches only this CTA's shared and tensor memory, so it may overlap
+  // the previous kernel on the stream; every global read comes after this wait.
+  pdl_wait();
   int bad = 0;
 
   if (warp == R::kCOPY) {
@@ -484,6 +486,8 @@ __global__ void gemm_prep_kernel(const __nv_bfloat16* __restrict__ w, const floa
                                 __nv_bfloat16* __restrict__ wf, float* __restrict__ u, float* __restrict__ v,
                                 int fold_blocks, const __nv_bfloat16* __restrict__ x, int T, float eps,
                                 float2* __restrict__ stats) {
+  pdl_wait();  // x and the weights may come from the previous kernel on the stream
+  pdl_launch_dependents();
   const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5, wpb = blockDim.x >> 5;
   if ((int)blockIdx.x < fold_blocks) {
     // gamma and beta staged once per block, read back as float4 (8 channels per lane)
@@ -711,10 +715,9 @@ cudaError_t qkv_run(const void* x, const float* gamma, const float* beta, const 
   const int fold_blocks = w != nullptr ? (N + 7) / 8 : 0;
   const int stat_blocks = chip_stats ? 0 : (int)std::min<int64_t>(((int64_t)T + 31) / 32, 16 * ip.sms);
   if (fold_blocks + stat_blocks > 0) {
-    gemm_prep_kernel<<<fold_blocks + stat_blocks, 256, 0, st>>>(
-        reinterpret_cast<const __nv_bfloat16*>(w), gamma, beta, b, C, N, pw.wf, pw.u, pw.v, fold_blocks,
-        reinterpret_cast<const __nv_bfloat16*>(x), T, eps, stats);
-    e = cudaGetLastError();
+    e = launch_pdl(gemm_prep_kernel, dim3(fold_blocks + stat_blocks), dim3(256), 0, st,
+                   reinterpret_cast<const __nv_bfloat16*>(w), gamma, beta, b, C, N, pw.wf, pw.u, pw.v, fold_blocks,
+                   reinterpret_cast<const __nv_bfloat16*>(x), T, eps, stats);
     if (e != cudaSuccess) return e;
   }
   GemmParams p = base_params(out, T, C, N, status);
@@ -744,9 +747,9 @@ cudaError_t qkv_prepare_launch(const float* gamma, const float* beta, const void
   if (C % 32 != 0 || C < 32 || C > kMaxC) return cudaErrorInvalidValue;
   const int N = 3 * C;
   const Prepared pw = prepared_parts(prepared, C);
-  gemm_prep_kernel<<<(N + 7) / 8, 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(w), gamma, beta, b, C, N,
-                                                pw.wf, pw.u, pw.v, (N + 7) / 8, nullptr, 0, 0.0f, nullptr);
-  return cudaGetLastError();
+  return launch_pdl(gemm_prep_kernel, dim3((N + 7) / 8), dim3(256), 0, st, reinterpret_cast<const __nv_bfloat16*>(w),
+                    gamma, beta, b, C, N, pw.wf, pw.u, pw.v, (N + 7) / 8, static_cast<const __nv_bfloat16*>(nullptr), 0,
+                    0.0f, static_cast<float2*>(nullptr));
 }
 
 // Producer on prepared weights: [the token statistics,] the product.
