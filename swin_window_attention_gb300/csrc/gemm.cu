@@ -596,8 +596,11 @@ int gemm_tile(int N) {
   return 0;
 }
 
-// Work items: token tiles times groups of output-channel tiles, at least four per SM when
-// the channel tiles allow it; one persistent CTA per SM walks them.
+// Work items: token tiles times groups of output-channel tiles; one persistent CTA per SM
+// walks them. With many tokens (at least four token tiles per SM) each token tile is one
+// item, so its statistics can be summed on chip. Otherwise the group size is the one
+// that minimises the tiles of the busiest SM, ceil(items / SMs) x tiles per item (every
+// output tile costs the same), preferring larger groups on a tie.
 struct ItemPlan {
   int sms, smem_max, NT, n_tt, per, n_items;
   bool one_item_per_token_tile;
@@ -613,10 +616,20 @@ cudaError_t plan_items(int T, int N, ItemPlan* ip) {
   if (ip->NT == 0) return cudaErrorInvalidValue;
   ip->n_tt = (T + kBM - 1) / kBM;
   const int n_tiles = N / ip->NT;
-  int groups = (4 * ip->sms + ip->n_tt - 1) / ip->n_tt;
-  groups = groups < 1 ? 1 : (groups > n_tiles ? n_tiles : groups);
-  ip->per = (n_tiles + groups - 1) / groups;
-  groups = (n_tiles + ip->per - 1) / ip->per;
+  int per = n_tiles;
+  if (ip->n_tt < 4 * ip->sms) {
+    int64_t best = -1;
+    for (int q = n_tiles; q >= 1; --q) {
+      const int64_t items = (int64_t)ip->n_tt * ((n_tiles + q - 1) / q);
+      const int64_t cost = (items + ip->sms - 1) / ip->sms * q;
+      if (best < 0 || cost < best) {
+        best = cost;
+        per = q;
+      }
+    }
+  }
+  const int groups = (n_tiles + per - 1) / per;
+  ip->per = per;
   ip->n_items = ip->n_tt * groups;
   ip->one_item_per_token_tile = groups == 1;
   return cudaSuccess;
