@@ -35,8 +35,8 @@
 // whose pipelines run on across items:
 // * copy warp: TMA loads of activation chunks [128 tokens x 64 channels] and weight
 //   chunks [N tile x 64 channels], 128-byte swizzled, into a ring of as many stages as
-//   the rest of the shared memory holds (4 at N = 256, up to 8); channels past C in the
-//   last chunk arrive as zeros and add nothing;
+//   the rest of the shared memory holds (3 to 8); channels past C in the last chunk
+//   arrive as zeros and add nothing;
 // * MMA warp, one thread: per chunk four M128 N<=256 K16 tcgen05.mma (A = the activation
 //   chunk, B = the weight chunk) into one of two tensor-memory accumulators;
 // * statistics warps (four, producer with statistics on chip): thread r sums its token
@@ -44,10 +44,12 @@
 //   output tile and publishes mean and rstd;
 // * epilogue warps (eight, two per tensor-memory lane quadrant, taking alternate
 //   32-channel slices): thread r forms rstd * acc - rstd * mean * u + v (producer) or
-//   acc + bp + residual (consumer) for its token row and rounds it to bf16 into the
-//   warp's own 64-byte-swizzled staging tile [32 rows x 32 channels], which the warp's
-//   first lane writes out with a TMA store (two tiles per warp alternate; no barrier
-//   beyond the warp), while the next output tile accumulates.
+//   acc + bp + residual (consumer) for its token row and rounds it to bf16 into one of
+//   the warp's own 64-byte-swizzled staging tiles [32 rows x 32 channels], which the
+//   warp's first lane writes out with a TMA store (two or three tiles per warp rotate; no
+//   barrier beyond the warp), while the next output tile accumulates. The consumer's
+//   residual slice arrives in that staging tile by a TMA load one slice ahead; u and v
+//   (bp) of a warp's slices are staged per output tile in its corner of shared memory.
 // Every wait is bounded (1 s); a wait that runs out sets the caller's status word (when
 // one is given) and the CTA leaves after releasing its tensor memory.
 #include <cuda.h>
@@ -81,7 +83,8 @@ struct Roles {
 };
 // Shared memory, from a 1024-byte aligned base: the stage ring (stages x stage_bytes),
 // [mean and rstd: 2 buffers x 128 x float2, with in-kernel statistics], per epilogue warp
-// two staging tiles of 32 rows x 64 bytes, the mbarriers and the tensor-memory address.
+// its staging tiles of 32 rows x 64 bytes [and its u/v corner], the mbarriers and the
+// tensor-memory address.
 constexpr int kSTATS_BYTES = 2 * kBM * 8;
 // Staging tiles per epilogue warp: three where the epilogue paces the kernel, so that a
 // store has two slices' time to read its tile before the tile is needed again (for the
@@ -100,13 +103,12 @@ constexpr int kRBAR0 = 2 * kMaxSTAGES + 8;  // consumer: residual-load barriers,
 constexpr int kNBAR = kRBAR0 + 8 * 3;
 template <int MODE>
 __host__ __device__ constexpr int tail_bytes() { return out_bytes<MODE>() + 8 * kNBAR + 8 + 1024; }  // + alignment slack
-constexpr int kMinSMEM = 120 * 1024;  // above half of an SM: one CTA per SM
+// More than half of an SM's shared memory: one CTA per SM, so the 512-column tensor
+// memory allocation never waits for another CTA of this kernel.
+constexpr int kMinSMEM = 120 * 1024;
 constexpr int kTMEM_COLS = 512;                // two accumulators of up to 256 columns
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 constexpr uint32_t kSW128 = 2;  // descriptor layout: 128-byte swizzle
-
-// One CTA per SM (more than half of its shared memory), so the 512-column tensor memory
-// allocation never waits.
 
 struct GemmParams {
   __nv_bfloat16* out;              // [T, N]
