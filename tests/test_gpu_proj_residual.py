@@ -125,3 +125,22 @@ def test_proj_residual_error_paths():
     assert f(o.data_ptr() + 2, y.data_ptr(), 4, 96) == capi.ERR_MISALIGNED
     torch.cuda.synchronize()
     assert torch.all(y == 3.0)
+
+
+def test_gemm_steps_count_their_launches():
+    """The launch accounting covers the GEMM entry points: the one-call producer launches
+    the fold and the product, the prepared producer the product after at most one
+    statistics pass, and the consumer one kernel."""
+    wl = workload(1, 1, 300, 96, 3, 1, 0, seed=21)
+    x, g, be, w, b = _dev(*inputs.make_producer(wl))
+    o, wp, bp, r = _dev(*inputs.make_consumer(wl))
+    proj = capi.QkvProjection(g, be, w, b)
+    torch.cuda.synchronize()
+    capi.swin_wattn_launch_count(reset=True)
+    capi.qkv_proj(x, g, be, w, b)
+    assert capi.swin_wattn_launch_count(reset=True) == 2
+    proj(x)
+    assert capi.swin_wattn_launch_count(reset=True) in (1, 2)
+    capi.proj_residual(o, wp, bp, r)
+    assert capi.swin_wattn_launch_count(reset=True) == 1
+    torch.cuda.synchronize()
