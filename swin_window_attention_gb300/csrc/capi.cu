@@ -10,11 +10,10 @@
 #include "common.cuh"
 
 namespace swin {
-cudaError_t launch_expand_bias(const float* table, int nH, int M, float* dense, cudaStream_t st);
+cudaError_t launch_bias_tables(const Plan& p, const float* table, bool with_mask, cudaStream_t st);
 cudaError_t launch_build_mask(int H, int W, int M, int s, float* mask, cudaStream_t st);
 cudaError_t launch_gather_map(int H, int W, int M, int s, int32_t* out, cudaStream_t st);
 cudaError_t launch_relidx(int M, int32_t* out, cudaStream_t st);
-cudaError_t launch_fragments(const Plan& p, cudaStream_t st);
 size_t tc_tables_bytes(const Plan& pl);
 cudaError_t launch_tc_tables(const Plan& pl, cudaStream_t st);
 size_t bias_frag_bytes(int M, int nH);
@@ -212,21 +211,14 @@ int swin_wattn_plan(swin_wattn_plan_t* out, int B, int H, int W, int C, int num_
   }
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (e == cudaSuccess) {
-    e = swin::launch_expand_bias(bias_table, p.nH, p.M, p.dense_bias, st);
+    e = swin::launch_bias_tables(p, bias_table, true, st);
     ++g_launches;
   }
   if (e == cudaSuccess) {
     e = swin::launch_build_mask(p.H, p.W, p.M, p.s, p.mask, st);
     ++g_launches;
   }
-  if (e == cudaSuccess) {
-    e = swin::launch_fragments(p, st);
-    ++g_launches;
-  }
-  if (e == cudaSuccess && p.tc_tables != nullptr) {
-    e = swin::launch_tc_tables(p, st);
-    ++g_launches;
-  }
+  p.tc_stale = p.tc_tables != nullptr;  // built before the first tcgen05 forward
   if (e != cudaSuccess) {
     rc = cuda_fail(e, "swin_wattn_plan");
     free_plan_buffers(p);
@@ -248,19 +240,25 @@ int swin_wattn_set_bias(swin_wattn_plan_t plan, const float* bias_table,
   if (rc != SWIN_WATTN_OK) return rc;
   rc = check_device_ptr(bias_table, 4);
   if (rc != SWIN_WATTN_OK) return rc;
-  const swin::Plan& p = plan->p;
+  swin::Plan& p = plan->p;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = swin::launch_expand_bias(bias_table, p.nH, p.M, p.dense_bias, st);
+  // One launch: the mma fragments and the dense bias, both from the table. The tcgen05
+  // tables are rebuilt before the next forward that uses them.
+  cudaError_t e = swin::launch_bias_tables(p, bias_table, false, st);
   ++g_launches;
-  if (e == cudaSuccess) {
-    e = swin::launch_fragments(p, st);
-    ++g_launches;
-  }
-  if (e == cudaSuccess && p.tc_tables != nullptr) {
-    e = swin::launch_tc_tables(p, st);
-    ++g_launches;
-  }
+  p.tc_stale = p.tc_tables != nullptr;
   return e == cudaSuccess ? SWIN_WATTN_OK : cuda_fail(e, "swin_wattn_set_bias");
+}
+
+// The tcgen05 forward's constant tables, rebuilt from the dense bias on `st` when the bias
+// changed since they were last built.
+static cudaError_t ensure_tc_tables(swin_wattn_plan_s* plan, cudaStream_t st) {
+  swin::Plan& p = plan->p;
+  if (!plan->fwd.tc || !p.tc_stale) return cudaSuccess;
+  const cudaError_t e = swin::launch_tc_tables(p, st);
+  ++g_launches;
+  if (e == cudaSuccess) p.tc_stale = false;
+  return e;
 }
 
 int swin_wattn_fwd(swin_wattn_plan_t plan, const void* qkv, void* out,
@@ -271,7 +269,8 @@ int swin_wattn_fwd(swin_wattn_plan_t plan, const void* qkv, void* out,
   if (p.B == 0) return SWIN_WATTN_OK;
   if ((rc = check_device_ptr(qkv, 16)) != SWIN_WATTN_OK) return rc;
   if ((rc = check_device_ptr(out, 16)) != SWIN_WATTN_OK) return rc;
-  cudaError_t e = swin::fwd_launch(p, plan->fwd, qkv, out, reinterpret_cast<cudaStream_t>(stream));
+  cudaError_t e = ensure_tc_tables(plan, reinterpret_cast<cudaStream_t>(stream));
+  if (e == cudaSuccess) e = swin::fwd_launch(p, plan->fwd, qkv, out, reinterpret_cast<cudaStream_t>(stream));
   ++g_launches;
   return e == cudaSuccess ? SWIN_WATTN_OK : cuda_fail(e, "swin_wattn_fwd");
 }
@@ -286,7 +285,8 @@ int swin_wattn_fwd_host(swin_wattn_plan_t plan, const void* qkv_host, void* out_
   if ((rc = check_device_ptr(dev_qkv, 16)) != SWIN_WATTN_OK) return rc;
   if ((rc = check_device_ptr(dev_out, 16)) != SWIN_WATTN_OK) return rc;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = cudaSuccess;
+  cudaError_t e = ensure_tc_tables(plan, st);
+  if (e != cudaSuccess) return cuda_fail(e, "swin_wattn_fwd_host");
   HostPipe& hp = plan->pipe;
   if (!hp.ready) {
     e = cudaStreamCreateWithFlags(&hp.in, cudaStreamNonBlocking);

@@ -37,6 +37,8 @@ struct Plan {
   // Constant operands of the tcgen05 forward (7x7 windows): mask U, class V and the bias
   // image per head. Owned; null for other window sizes.
   unsigned char* tc_tables;
+  // The tables no longer match the bias (built lazily before the next tcgen05 forward).
+  bool tc_stale;
   // Device error word written by kernels with bounded waits (bit 0: a wait ran out).
   // Owned.
   int* err;

@@ -8,20 +8,6 @@
 
 namespace swin {
 
-// dense[h, i, j] = table[idx(i, j), h]
-__global__ void expand_bias_kernel(const float* __restrict__ table, int nH, int M,
-                                   float* __restrict__ dense) {
-  const int N = M * M;
-  const int64_t total = (int64_t)nH * N * N;
-  for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < total;
-       e += (int64_t)gridDim.x * blockDim.x) {
-    const int h = (int)(e / ((int64_t)N * N));
-    const int ij = (int)(e % ((int64_t)N * N));
-    const int i = ij / N, j = ij % N;
-    dense[e] = table[(int64_t)rel_index(i, j, M) * nH + h];
-  }
-}
-
 // mask[w, i, j] = 0 if the region labels of slots i and j of window w agree, else -100.
 __global__ void build_mask_kernel(int H, int W, int M, int s, float* __restrict__ mask) {
   const int N = M * M, nWx = W / M, nW = (H / M) * nWx;
@@ -52,35 +38,43 @@ __global__ void relidx_kernel(int M, int32_t* __restrict__ out) {
     out[e] = rel_index(e / N, e % N, M);
 }
 
-// The dense bias re-laid out once per plan in the order the attention kernels consume
-// it (lane (g, t) of warp wp, key tile nt: rows 16wp+g, +8; columns 8nt+2t, +1), so a CTA
-// stages its head's block with plain 16-byte copies. The bias is stored divided by the
-// softmax scale (it seeds the q.k accumulators), -inf in padded key columns and 0 in
-// padded query rows. The shift-mask V fragments of the three boundary classes follow
-// (mask_frag_word), built from the same region labels as the dense mask.
+// The bias in the order the attention kernels consume it (lane (g, t) of warp wp, key
+// tile nt: rows 16wp+g, +8; columns 8nt+2t, +1), so that a CTA stages its head's block with
+// plain 16-byte copies, read straight from the table (the same value the dense bias
+// holds). It is stored divided by the softmax scale (it seeds the q.k accumulators), -inf
+// in padded key columns and 0 in padded query rows. In the same launch: the shift-mask V
+// fragments of the three boundary classes (mask_frag_word, from the region labels the
+// dense mask uses), when mask_frag is given, and the dense bias
+// dense[h, i, j] = table[idx(i, j), h], when dense is given.
 template <int M>
-__global__ void fragments_kernel(const float* __restrict__ dense, int nH, int H, int W, int s,
-                                 float4* __restrict__ bias_frag, uint32_t* __restrict__ mask_frag) {
+__global__ void bias_tables_kernel(const float* __restrict__ table, int nH, int H, int W, int s,
+                                   float4* __restrict__ bias_frag, uint32_t* __restrict__ mask_frag,
+                                   float* __restrict__ dense) {
   using G = Geo<M>;
   constexpr int N = G::N, NT = G::NT;
   const int per_head = G::WARPS * NT * 32;
-  const int nbias = nH * per_head;
-  const int nmask = mask_frag ? G::MASK_BYTES / 4 : 0;
-  for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < nbias + nmask; e += gridDim.x * blockDim.x) {
+  const int64_t nbias = (int64_t)nH * per_head;
+  const int64_t nmask = mask_frag ? G::MASK_BYTES / 4 : 0;
+  const int64_t ndense = dense ? (int64_t)nH * N * N : 0;
+  for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < nbias + nmask + ndense;
+       e += (int64_t)gridDim.x * blockDim.x) {
     if (e < nbias) {
-      const int h = e / per_head, f = e % per_head;
+      const int h = (int)(e / per_head), f = (int)(e % per_head);
       const int ln = f & 31, nt = (f >> 5) % NT, wp = (f >> 5) / NT;
       const int r0 = wp * 16 + (ln >> 2), c0 = nt * 8 + 2 * (ln & 3);
-      const float* db = dense + (int64_t)h * N * N;
       float v[4];
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const int r = r0 + 8 * (q >> 1), c = c0 + (q & 1);
-        v[q] = c >= N ? -INFINITY : (r >= N ? 0.0f : db[r * N + c] * kInvScale);
+        v[q] = c >= N ? -INFINITY : (r >= N ? 0.0f : table[(int64_t)rel_index(r, c, M) * nH + h] * kInvScale);
       }
       bias_frag[e] = make_float4(v[0], v[1], v[2], v[3]);
+    } else if (e < nbias + nmask) {
+      mask_frag[e - nbias] = mask_frag_word<M>((int)(e - nbias), H, W, s);
     } else {
-      mask_frag[e - nbias] = mask_frag_word<M>(e - nbias, H, W, s);
+      const int64_t d = e - nbias - nmask;
+      const int h = (int)(d / (N * N)), ij = (int)(d % (N * N));
+      dense[d] = table[(int64_t)rel_index(ij / N, ij % N, M) * nH + h];
     }
   }
 }
@@ -90,13 +84,6 @@ static int grid_for(int64_t n, int threads) {
   if (g < 1) g = 1;
   if (g > 4096) g = 4096;
   return (int)g;
-}
-
-cudaError_t launch_expand_bias(const float* table, int nH, int M, float* dense,
-                               cudaStream_t st) {
-  const int64_t n = (int64_t)nH * M * M * M * M;
-  expand_bias_kernel<<<grid_for(n, 256), 256, 0, st>>>(table, nH, M, dense);
-  return cudaGetLastError();
 }
 
 cudaError_t launch_build_mask(int H, int W, int M, int s, float* mask, cudaStream_t st) {
@@ -123,19 +110,22 @@ size_t mask_frag_bytes(int M) {
   }
 }
 
-cudaError_t launch_fragments(const Plan& p, cudaStream_t st) {
-  uint32_t* mask = p.s > 0 ? p.mask_frag : nullptr;
-  const int64_t n = (int64_t)bias_frag_bytes(p.M, p.nH) / 16 + (mask ? mask_frag_bytes(p.M) / 4 : 0);
+// The plan's bias fragments and dense bias from `table` [and its mask fragments], one
+// launch.
+cudaError_t launch_bias_tables(const Plan& p, const float* table, bool with_mask, cudaStream_t st) {
+  uint32_t* mask = with_mask && p.s > 0 ? p.mask_frag : nullptr;
+  const int64_t n = (int64_t)bias_frag_bytes(p.M, p.nH) / 16 + (mask ? mask_frag_bytes(p.M) / 4 : 0) +
+                    (int64_t)p.nH * p.N * p.N;
   const int grid = grid_for(n, 256);
   switch (p.M) {
     case 4:
-      fragments_kernel<4><<<grid, 256, 0, st>>>(p.dense_bias, p.nH, p.H, p.W, p.s, p.bias_frag, mask);
+      bias_tables_kernel<4><<<grid, 256, 0, st>>>(table, p.nH, p.H, p.W, p.s, p.bias_frag, mask, p.dense_bias);
       break;
     case 7:
-      fragments_kernel<7><<<grid, 256, 0, st>>>(p.dense_bias, p.nH, p.H, p.W, p.s, p.bias_frag, mask);
+      bias_tables_kernel<7><<<grid, 256, 0, st>>>(table, p.nH, p.H, p.W, p.s, p.bias_frag, mask, p.dense_bias);
       break;
     case 12:
-      fragments_kernel<12><<<grid, 256, 0, st>>>(p.dense_bias, p.nH, p.H, p.W, p.s, p.bias_frag, mask);
+      bias_tables_kernel<12><<<grid, 256, 0, st>>>(table, p.nH, p.H, p.W, p.s, p.bias_frag, mask, p.dense_bias);
       break;
     default:
       return cudaErrorInvalidValue;

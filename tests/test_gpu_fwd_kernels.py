@@ -96,3 +96,32 @@ def test_tcgen05_kernel_refused_where_it_does_not_apply(M, dt):
     assert att.fwd_kernel == capi.KERNEL_MMA_SYNC
     assert capi.swin_wattn_set_fwd_kernel(att.handle, 7) == capi.ERR_INVALID_ARG
     att.close()
+
+
+def test_new_bias_reaches_the_tcgen05_kernel_whenever_it_is_chosen():
+    """set_bias rebuilds the mma fragments and the dense bias in one launch; the tcgen05
+    kernel's tables follow before its next forward, whether the kernel was chosen before
+    or after the new bias, and the dense bias dump matches the new table."""
+    wl = workload(2, 14, 14, 64, 2, 7, 3, "bf16", seed=31)
+    qkv, t1 = inputs.make_qkv(wl), inputs.make_table(wl)
+    t2 = inputs.trunc_normal(t1.shape, 1234) * 8
+    q = qkv.to(DEV)
+    ref2 = oracle_fwd(qkv, t2, wl)
+    # chosen after the new bias
+    att = plan(wl, t1.to(DEV))
+    att.set_bias(t2.to(DEV))
+    att.set_fwd_kernel(capi.KERNEL_TCGEN05)
+    assert_close("Y", att.fwd(q), ref2)
+    att.device_status()
+    att.close()
+    # chosen before: a forward with the first table, then the new bias
+    att = plan(wl, t1.to(DEV))
+    att.set_fwd_kernel(capi.KERNEL_TCGEN05)
+    assert_close("Y", att.fwd(q), oracle_fwd(qkv, t1, wl))
+    att.set_bias(t2.to(DEV))
+    assert_close("Y", att.fwd(q), ref2)
+    # and back to the mma.sync kernel, which reads the fragments
+    att.set_fwd_kernel(capi.KERNEL_MMA_SYNC)
+    assert_close("Y", att.fwd(q), ref2)
+    att.device_status()
+    att.close()
