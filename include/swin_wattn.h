@@ -249,6 +249,24 @@ int swin_wattn_proj_residual(const void* o, const void* w_proj, const float* b_p
                              void* y, int tokens, int C, int* status, struct CUstream_st* stream);
 
 /*
+ * Forward on 8-bit operands (7x7 windows, a SWIN_WATTN_BF16 plan): the attention of
+ * q = scale_q * q8, k = scale_k * k8, v = scale_v * v8 for
+ *   qkv8   device, 16-byte aligned: [B,H,W,3C] OCP FP8 E4M3 values, one byte each, in the
+ *          token layout of qkv (q | k | v channels of a token);
+ *   scale_q, scale_k, scale_v  one fp32 scale per tensor, finite and positive;
+ *   out    device, 16-byte aligned: [B,H,W,C] bf16, written.
+ * q8 k8^T runs on the 8-bit tensor cores (exact products, fp32 accumulation), the bias and
+ * the shift mask are those of the plan, P is rounded to fp16, and v8 is widened exactly to
+ * fp16 for P V: the result is the attention of the decoded values to the tolerance of
+ * swin_wattn_fwd, with 3C instead of 6C bytes of qkv read per token (the pages take the
+ * Swin GEMMs to 8 bits for inference, NVIDIA Swin talk section 3; here the attention's
+ * operands). One kernel launch. UNSUPPORTED for another window size or dtype,
+ * INVALID_ARG for a bad scale, and the pointer errors of swin_wattn_fwd.
+ */
+int swin_wattn_fwd_fp8(swin_wattn_plan_t plan, const void* qkv8, float scale_q, float scale_k, float scale_v,
+                       void* out, struct CUstream_st* stream);
+
+/*
  * Choose the plan's forward kernel (SWIN_WATTN_KERNEL_*). Both kernels compute the same
  * function to the same tolerance; AUTO is the default. Asking for TCGEN05 where it does not apply returns SWIN_WATTN_ERR_UNSUPPORTED
  * and leaves the plan unchanged. Host-side only; call it between launches.

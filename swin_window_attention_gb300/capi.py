@@ -44,6 +44,7 @@ SIGNATURES = {
     "swin_wattn_qkv_prepare": ([_vp] * 4 + [_i, _vp, ctypes.c_size_t, _vp], _i),
     "swin_wattn_qkv_proj_prepared": ([_vp] * 3 + [_i, _i, ctypes.c_float, _vp, ctypes.c_size_t, _vp, _vp], _i),
     "swin_wattn_proj_residual": ([_vp] * 5 + [_i, _i, _vp, _vp], _i),
+    "swin_wattn_fwd_fp8": ([_vp, _vp, ctypes.c_float, ctypes.c_float, ctypes.c_float, _vp, _vp], _i),
     "swin_wattn_set_fwd_kernel": ([_vp, _i], _i),
     "swin_wattn_fwd_kernel": ([_vp], _i),
     "swin_wattn_device_status": ([_vp, _vp], _i),
@@ -222,6 +223,10 @@ def proj_residual(o, wp, bp, residual, y=None, status=None, stream=None):
     return y
 
 
+def swin_wattn_fwd_fp8(plan, qkv8_ptr, scale_q, scale_k, scale_v, out_ptr, stream):
+    return load().swin_wattn_fwd_fp8(plan, qkv8_ptr, scale_q, scale_k, scale_v, out_ptr, stream)
+
+
 def swin_wattn_set_fwd_kernel(plan, kernel):
     return load().swin_wattn_set_fwd_kernel(plan, kernel)
 
@@ -305,6 +310,18 @@ class WindowAttention:
         rc = swin_wattn_fwd(self.handle, qkv.data_ptr(), out.data_ptr(), _stream_handle(stream))
         if rc != OK:
             raise SwinWAttnError("swin_wattn_fwd", rc)
+        return out
+
+    def fwd_fp8(self, qkv8, scales, out=None, stream=None):
+        """Forward on 8-bit operands: qkv8 a [B,H,W,3C] CUDA tensor of OCP FP8 E4M3 bytes
+        (torch.float8_e4m3fn or uint8), scales (scale_q, scale_k, scale_v); bf16 output."""
+        import torch
+        if out is None:
+            out = torch.empty(self.B, self.H, self.W, self.C, dtype=torch.bfloat16, device=qkv8.device)
+        sq, sk, sv = (float(x) for x in scales)
+        rc = swin_wattn_fwd_fp8(self.handle, qkv8.data_ptr(), sq, sk, sv, out.data_ptr(), _stream_handle(stream))
+        if rc != OK:
+            raise SwinWAttnError("swin_wattn_fwd_fp8", rc)
         return out
 
     def fwd_host(self, qkv_host, out_host, dev_qkv, dev_out, stream=None):

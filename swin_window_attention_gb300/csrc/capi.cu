@@ -11,6 +11,9 @@
 
 namespace swin {
 cudaError_t launch_bias_tables(const Plan& p, const float* table, bool with_mask, cudaStream_t st);
+bool fwd_fp8_applies(const Plan& pl);
+cudaError_t fwd_fp8_launch(const Plan& pl, const void* qkv8, float sq, float sk, float sv, void* out,
+                           cudaStream_t st);
 cudaError_t launch_build_mask(int H, int W, int M, int s, float* mask, cudaStream_t st);
 cudaError_t launch_gather_map(int H, int W, int M, int s, int32_t* out, cudaStream_t st);
 cudaError_t launch_relidx(int M, int32_t* out, cudaStream_t st);
@@ -273,6 +276,23 @@ int swin_wattn_fwd(swin_wattn_plan_t plan, const void* qkv, void* out,
   if (e == cudaSuccess) e = swin::fwd_launch(p, plan->fwd, qkv, out, reinterpret_cast<cudaStream_t>(stream));
   ++g_launches;
   return e == cudaSuccess ? SWIN_WATTN_OK : cuda_fail(e, "swin_wattn_fwd");
+}
+
+int swin_wattn_fwd_fp8(swin_wattn_plan_t plan, const void* qkv8, float scale_q, float scale_k, float scale_v,
+                       void* out, struct CUstream_st* stream) {
+  int rc = check_plan(plan);
+  if (rc != SWIN_WATTN_OK) return rc;
+  const swin::Plan& p = plan->p;
+  if (!swin::fwd_fp8_applies(p)) return SWIN_WATTN_ERR_UNSUPPORTED;
+  for (const float sc : {scale_q, scale_k, scale_v})
+    if (!(sc > 0.0f) || !std::isfinite(sc)) return SWIN_WATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale_q * scale_k) || !(scale_q * scale_k > 0.0f)) return SWIN_WATTN_ERR_INVALID_ARG;
+  if (p.B == 0) return SWIN_WATTN_OK;
+  if ((rc = check_device_ptr(qkv8, 16)) != SWIN_WATTN_OK) return rc;
+  if ((rc = check_device_ptr(out, 16)) != SWIN_WATTN_OK) return rc;
+  cudaError_t e = swin::fwd_fp8_launch(p, qkv8, scale_q, scale_k, scale_v, out, reinterpret_cast<cudaStream_t>(stream));
+  ++g_launches;
+  return e == cudaSuccess ? SWIN_WATTN_OK : cuda_fail(e, "swin_wattn_fwd_fp8");
 }
 
 int swin_wattn_fwd_host(swin_wattn_plan_t plan, const void* qkv_host, void* out_host,

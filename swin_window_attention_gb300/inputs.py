@@ -164,6 +164,32 @@ def make_consumer(wl: Workload):
     return o, wp, bp.contiguous(), r
 
 
+FP8_MAX = 448.0  # the largest finite OCP FP8 E4M3 value
+
+
+def make_qkv_fp8(wl: Workload):
+    """The workload's qkv (the same seeded N(0,1) draw as make_qkv) encoded as OCP FP8
+    E4M3 with one scale per tensor (q, k, v): scale = max|x| / 448, x8 = round(x / scale)
+    to E4M3 (torch's round-to-nearest-even cast), CPU. Returns (qkv8 [B,H,W,3C]
+    torch.float8_e4m3fn, (scale_q, scale_k, scale_v))."""
+    x = normal((wl.B, wl.H, wl.W, 3 * wl.C), wl.seed)
+    parts, scales = [], []
+    for t in range(3):
+        xt = x[..., t * wl.C:(t + 1) * wl.C]
+        sc = float(xt.abs().max()) / FP8_MAX
+        parts.append((xt / sc).to(torch.float8_e4m3fn))
+        scales.append(sc)
+    return torch.cat(parts, dim=-1), tuple(scales)
+
+
+def fp8_decoded_f64(qkv8: torch.Tensor, scales, C: int):
+    """Exact float64 numpy values of scale_t * x8 for each tensor t of an E4M3 qkv."""
+    x = qkv8.to(torch.float64)
+    for t in range(3):
+        x[..., t * C:(t + 1) * C] *= scales[t]
+    return x.numpy()
+
+
 def act_f64(x: torch.Tensor):
     """Exact float64 numpy copy of the values the GPU path sees: bf16 inputs are widened
     as they are; fp32 inputs are first rounded to bf16 (round-to-nearest-even), which

@@ -19,7 +19,7 @@ def lib():
 def _declared():
     txt = open(os.path.join(ROOT, "include", "swin_wattn.h")).read()
     txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
-    return sorted(set(re.findall(r"\b(swin_wattn_[a-z_]+)\s*\(", txt)))
+    return sorted(set(re.findall(r"\b(swin_wattn_[a-z0-9_]+)\s*\(", txt)))
 
 
 def test_header_declares_the_documented_entry_points():
@@ -96,3 +96,7 @@ def test_gemm_steps_reject_bad_arguments_before_touching_cuda(lib):
     assert lib.swin_wattn_proj_residual(*([None] * 5), 4, 48, None, None) == lib.ERR_UNSUPPORTED
     assert lib.swin_wattn_proj_residual(*([None] * 5), 4, 3072, None, None) == lib.ERR_UNSUPPORTED
     assert lib.swin_wattn_proj_residual(*([None] * 5), 0, 96, None, None) == lib.OK
+
+
+def test_fp8_forward_rejects_a_bad_plan_before_touching_cuda(lib):
+    assert lib.swin_wattn_fwd_fp8(None, None, 1.0, 1.0, 1.0, None, None) == lib.ERR_BAD_PLAN
