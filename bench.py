@@ -49,6 +49,12 @@ def fwd_bytes(wl) -> int:
     return (wl.tokens * 4 * wl.C * esz + wl.nH * nn * 4 + (wl.nW * nn * 4 if wl.s > 0 else 0))
 
 
+def fwd_fp8_bytes(wl) -> int:
+    """8-bit forward: qkv read at 3C bytes per token, bf16 output write, bias and mask."""
+    nn = wl.N * wl.N
+    return wl.tokens * 5 * wl.C + wl.nH * nn * 4 + (wl.nW * nn * 4 if wl.s > 0 else 0)
+
+
 def bwd_bytes(wl) -> int:
     """qkv (3C) + dO (C) read, dqkv (3C) write, dense bias, mask, table gradient write."""
     esz = 2 if wl.dtype == "bf16" else 4
@@ -403,6 +409,7 @@ def run_gpu(args):
     train = run_train_step(args, dev, stream, lib, capi, hbm, ws) if not args.skip_train else None
     l384 = run_fwd_sweep(L384, args, dev, stream, lib, capi, hbm, ws) if not args.skip_train else None
     block = run_block_sweep(SWEEP, args, dev, stream, lib, capi, peaks, ws) if not args.skip_train else None
+    fp8 = run_fp8_sweep(SWEEP, args, dev, stream, lib, capi, hbm, ws) if not args.skip_train else None
 
     if rank == 0:
         line = {
@@ -436,6 +443,7 @@ def run_gpu(args):
             "train_step": train,
             "l384_sweep": l384,
             "block_sweep": block,
+            "fp8_sweep": fp8,
         }
         if ws == 1 and not args.skip_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(sweep)
@@ -481,6 +489,78 @@ def run_fwd_sweep(names, args, dev, stream, lib, capi, hbm, ws):
     return {"workload": "swin_l384_sweep_fwd (B=16, 12x12 windows)", "us": round(tot_ms * 1e3, 2),
             "tokens_per_s": sum(x["wl"].tokens for x in st) / (tot_ms / 1e3),
             "frac_of_measured_hbm": round(tot_b / (tot_ms / 1e3) / 1e9 / hbm, 4), "stages": out}
+
+
+def run_fp8_sweep(names, args, dev, stream, lib, capi, hbm, ws):
+    """The same sweep's forward on 8-bit operands (OCP FP8 E4M3 q, k, v with per-tensor
+    scales, bf16 output), captured as one CUDA graph and replayed; per-stage times from an
+    eager region with CUDA events around every launch. Context for the line, not the
+    headline (which is the bf16 forward)."""
+    sh = stream.cuda_stream
+    st = []
+    with torch.cuda.stream(stream):
+        for name in names:
+            wl = inputs.BY_NAME[name]
+            q8, scales = inputs.make_qkv_fp8(wl)
+            h = make_plan(capi, wl, inputs.make_table(wl).to(dev), sh, args)
+            st.append(dict(wl=wl, h=h, q=q8.to(dev), sc=scales,
+                           o=torch.empty(wl.B, wl.H, wl.W, wl.C, dtype=torch.bfloat16, device=dev)))
+    torch.cuda.synchronize()
+
+    def one(events=None):
+        for k, z in enumerate(st):
+            if events is not None:
+                events[k][0].record(stream)
+            rc = lib.swin_wattn_fwd_fp8(z["h"], z["q"].data_ptr(), z["sc"][0], z["sc"][1], z["sc"][2],
+                                        z["o"].data_ptr(), sh)
+            if events is not None:
+                events[k][1].record(stream)
+            if rc != capi.OK:
+                raise capi.SwinWAttnError("swin_wattn_fwd_fp8", rc)
+
+    for _ in range(max(3, args.warmup)):
+        one()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream, capture_error_mode="relaxed"):
+        one()
+    torch.cuda.synchronize()
+    steps = max(3, min(args.steps, 2000))
+    for _ in range(3):
+        with torch.cuda.stream(stream):
+            graph.replay()
+    torch.cuda.synchronize()
+    barrier(ws)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(steps):
+            graph.replay()
+    b.record(stream)
+    torch.cuda.synchronize()
+    graph_ms = max_over_ranks(a.elapsed_time(b), ws) / steps
+    esteps = max(3, min(args.steps, 200))
+    ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in st] for _ in range(esteps)]
+    for i in range(esteps):
+        one(ev[i])
+    torch.cuda.synchronize()
+    stages, tot_b = [], 0
+    for k, z in enumerate(st):
+        wl = z["wl"]
+        ms = statistics.mean(ev[i][k][0].elapsed_time(ev[i][k][1]) for i in range(esteps))
+        tot_b += fwd_fp8_bytes(wl)
+        stages.append({"workload": wl.name, "us": round(ms * 1e3, 2),
+                       "frac_of_measured_hbm": round(fwd_fp8_bytes(wl) / (ms / 1e3) / 1e9 / hbm, 4),
+                       "speedup_vs_bf16_bytes": round(fwd_bytes(wl) / fwd_fp8_bytes(wl), 3)})
+    for z in st:
+        capi.swin_wattn_destroy(z["h"])
+    tokens = sum(z["wl"].tokens for z in st)
+    return {"workload": "swin_l224_sweep_fwd on OCP FP8 E4M3 q, k, v (per-tensor scales), bf16 out",
+            "steps": steps, "graph_us_per_step": round(graph_ms * 1e3, 2),
+            "tokens_per_s": ws * tokens / (graph_ms / 1e3),
+            "frac_of_measured_hbm": round(tot_b / (graph_ms / 1e3) / 1e9 / hbm, 4),
+            "bytes_per_token": "5C (qkv 3C as E4M3, out 2C as bf16) + bias + mask per launch",
+            "stages": stages}
 
 
 def run_block_sweep(names, args, dev, stream, lib, capi, peaks, ws):

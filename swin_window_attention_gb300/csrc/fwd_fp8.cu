@@ -90,7 +90,7 @@ __device__ __forceinline__ void e4m3x4_to_f16(uint32_t w, uint32_t& lo, uint32_t
       : "r"(w));
 }
 
-__global__ void __launch_bounds__(G7::THREADS, 4) fwd_fp8_kernel(const Fp8Params p) {
+__global__ void __launch_bounds__(G7::THREADS, 5) fwd_fp8_kernel(const Fp8Params p) {
   constexpr int N = G7::N, NT = G7::NT, KT = G7::KT, THREADS = G7::THREADS;
   extern __shared__ __align__(128) unsigned char smem[];
   pdl_launch_dependents();
@@ -341,6 +341,9 @@ cudaError_t fwd_fp8_launch(const Plan& pl, const void* qkv8, float sq, float sk,
                            cudaStream_t st) {
   if (!fwd_fp8_applies(pl)) return cudaErrorNotSupported;
   cudaError_t e = cudaFuncSetAttribute(fwd_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem8);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(fwd_fp8_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
   int occ = 0;
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fwd_fp8_kernel, G7::THREADS, kSmem8);
