@@ -786,6 +786,31 @@ def run_gemm_only(args):
                       "consumer": gemm_roofline(proj_bytes(wl), proj_flops(wl), p_ms, peaks)}))
 
 
+def run_fp8_only(args):
+    """Forward launches on FP8 operands for one workload (warm-up + timed), for kernel
+    profiling."""
+    from swin_window_attention_gb300 import build, capi
+    build.build()
+    wl = inputs.BY_NAME[args.fp8_workload]
+    dev = torch.device("cuda", 0)
+    q8, scales = inputs.make_qkv_fp8(wl)
+    att = capi.WindowAttention(wl.B, wl.H, wl.W, wl.C, wl.nH, wl.M, wl.s, inputs.make_table(wl).to(dev))
+    q = q8.to(dev)
+    for _ in range(args.warmup):
+        att.fwd_fp8(q, scales)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(args.steps):
+        att.fwd_fp8(q, scales)
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / args.steps
+    print(json.dumps({"workload": wl.name, "fp8_fwd_us": ms * 1e3,
+                      "frac_of_measured_hbm": fwd_fp8_bytes(wl) / (ms / 1e3) / 1e9 / load_peaks()[0]["hbm_gbs"]}))
+    att.close()
+
+
 def run_bwd_only(args):
     """Backward launches of one workload (warm-up + timed), for kernel profiling."""
     from swin_window_attention_gb300 import build, capi
@@ -863,6 +888,8 @@ def main():
                          "(profiling runs)")
     ap.add_argument("--bwd-workload", choices=sorted(n for n, w in inputs.BY_NAME.items() if w.bwd),
                     help="profiling run: only the backward of this workload, a few launches")
+    ap.add_argument("--fp8-workload", choices=sorted(n for n, w in inputs.BY_NAME.items() if w.M == 7),
+                    help="profiling run: only the forward on FP8 operands of this workload, a few launches")
     ap.add_argument("--gemm-workload", choices=sorted(inputs.BY_NAME),
                     help="profiling run: only the producer and consumer of this workload, a few launches")
     ap.add_argument("--fwd-kernel", default="auto", choices=sorted(FWD_KERNELS),
@@ -878,6 +905,8 @@ def main():
         run_bwd_only(args)
     elif args.gemm_workload:
         run_gemm_only(args)
+    elif args.fp8_workload:
+        run_fp8_only(args)
     else:
         run_gpu(args)
 
