@@ -7,7 +7,8 @@
 // is 3C bytes per token instead of 6C. The arithmetic after decoding is that of the bf16
 // forward (fwd.cu), applied to the decoded values:
 // * S = Q8 K8^T on the 8-bit tensor-core MMA (m16n8k32 e4m3: products exact in fp32,
-//   fp32 accumulation), the accumulator seeded with bias / (scale sq sk) and the shift mask
+//   fp32 accumulation), the accumulator seeded with bias / (scale sq sk) (the head's bias
+//   fragments rescaled once per CTA in shared memory) and the shift mask
 //   added as the same rank-4 bf16 MMA with its -100 rescaled by 1 / (sq sk);
 // * P = softmax(scale sq sk S) in fp32, rounded to fp16 (11 significant bits);
 // * O = P V8 on the fp16 MMA after V8 is widened to fp16 in shared memory (exact), with
@@ -193,6 +194,14 @@ __global__ void __launch_bounds__(G7::THREADS, 5) fwd_fp8_kernel(const Fp8Params
   for (int it = 0; it < nwin; ++it) {
     cp_async_wait<kStages8 - 2>();
     __syncthreads();  // this window's tiles are in; every warp is done with the last one
+    if (it == 0) {
+      // the head's bias fragments (bias / scale) to accumulator units, once per CTA
+      for (int e = tid; e < G7::BIAS_BYTES / 16; e += THREADS) {
+        const float4 v = sbias[e];
+        sbias[e] = make_float4(v.x * r_sc, v.y * r_sc, v.z * r_sc, v.w * r_sc);
+      }
+      __syncthreads();
+    }
     if (it + kStages8 - 1 < nwin) issue(nxt_off);
     cp_async_commit();
     nxt_off = nxt_off + kStage8 == kStages8 * kStage8 ? 0 : nxt_off + kStage8;
@@ -234,8 +243,7 @@ __global__ void __launch_bounds__(G7::THREADS, 5) fwd_fp8_kernel(const Fp8Params
         const int nt = 2 * np + u;
         if (nt < NT) {
           const float4 bb = bfrag[nt * 32];
-          mma_e4m3_c(sacc[nt], qa0, qa1, qa2, qa3, u ? b2 : b0, u ? b3 : b1, bb.x * r_sc, bb.y * r_sc, bb.z * r_sc,
-                     bb.w * r_sc);
+          mma_e4m3_c(sacc[nt], qa0, qa1, qa2, qa3, u ? b2 : b0, u ? b3 : b1, bb.x, bb.y, bb.z, bb.w);
         }
       }
     }
