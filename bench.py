@@ -344,8 +344,9 @@ def run_gpu(args):
     eager_ms = max_over_ranks(e0.elapsed_time(e1), ws)
     eager_launches = capi.swin_wattn_launch_count()
     clk = clocks.stop()
-    per_stage_ms = [statistics.mean(ev[i][k][0].elapsed_time(ev[i][k][1])
-                                    for i in range(args.steps)) for k in range(len(sweep))]
+    # per-stage launch times: the median over the timed steps
+    per_stage_ms = [statistics.median(ev[i][k][0].elapsed_time(ev[i][k][1])
+                                      for i in range(args.steps)) for k in range(len(sweep))]
 
     tokens_step = sum(wl.tokens for wl in sweep)
     value = ws * tokens_step * args.steps / (total_ms / 1e3)
@@ -438,7 +439,7 @@ def run_gpu(args):
                        "eager_ms_per_step": eager_ms / args.steps,
                        "eager_launches": int(eager_launches),
                        "per_stage_from": "CUDA events around each launch in a second, eager "
-                                         "timed region of the same steps"},
+                                         "timed region of the same steps (median per stage)"},
             "clocks": clk,
             "train_step": train,
             "l384_sweep": l384,
