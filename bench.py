@@ -18,6 +18,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -344,6 +345,29 @@ def run_gpu(args):
     eager_ms = max_over_ranks(e0.elapsed_time(e1), ws)
     eager_launches = capi.swin_wattn_launch_count()
     clk = clocks.stop()
+
+    # Third timed region: the same graph replayed for at least a second, so that the step
+    # time is also known at the clock the GPU settles to under sustained load (the kernels
+    # are paced by instruction issue, so their speed follows the SM clock).
+    step_s = total_ms / args.steps / 1e3
+    sus_steps = max(args.steps, int(math.ceil(1.0 / max(step_s, 1e-9))))
+    clocks2 = ClockSampler(local)
+    clocks2.start()
+    time.sleep(0.3)
+    barrier(ws)
+    torch.cuda.synchronize()
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks2.mark(True)
+    with torch.cuda.stream(stream):
+        s0.record(stream)
+        for _ in range(sus_steps):
+            graph.replay()
+        s1.record(stream)
+    torch.cuda.synchronize()
+    clocks2.mark(False)
+    barrier(ws)
+    sus_ms = max_over_ranks(s0.elapsed_time(s1), ws)
+    clk2 = clocks2.stop()
     # per-stage launch times: the median over the timed steps
     per_stage_ms = [statistics.median(ev[i][k][0].elapsed_time(ev[i][k][1])
                                       for i in range(args.steps)) for k in range(len(sweep))]
@@ -441,6 +465,18 @@ def run_gpu(args):
                        "per_stage_from": "CUDA events around each launch in a second, eager "
                                          "timed region of the same steps (median per stage)"},
             "clocks": clk,
+            "sustained": {
+                "what": "the same graph replayed for at least 1 s in a third timed region, with "
+                        "its own clock samples (reported beside the driver-length headline)",
+                "steps": sus_steps, "seconds": round(sus_ms / 1e3, 3),
+                "us_per_step": round(sus_ms / sus_steps * 1e3, 2),
+                "tokens_per_s": ws * tokens_step * sus_steps / (sus_ms / 1e3),
+                "frac_of_measured_hbm": round(sweep_bytes / (sus_ms / sus_steps / 1e3) / 1e9 / hbm, 4),
+                "clocks": clk2,
+                "us_x_median_sm_mhz": (round(sus_ms / sus_steps * 1e3 * clk2["sm_mhz"], 1)
+                                       if clk2.get("sm_mhz") else None),
+                "headline_us_x_median_sm_mhz": (round(total_ms / args.steps * 1e3 * clk["sm_mhz"], 1)
+                                                if clk.get("sm_mhz") else None)},
             "train_step": train,
             "l384_sweep": l384,
             "block_sweep": block,

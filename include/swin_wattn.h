@@ -152,9 +152,13 @@ int swin_wattn_bwd(swin_wattn_plan_t plan, const void* qkv, const void* dout, vo
  * SWIN_WATTN_ERR_UNSUPPORTED and the reason in swin_wattn_last_error().
  *
  * The first call on a device looks up the array's device address (cudaGetSymbolAddress)
- * with that device current; make that first call before any stream capture. Every call
- * on a device shares the one array and overwrites it completely, so two calls that
- * overlap on the GPU (different streams without ordering between them) race: order them.
+ * with that device current; make that first call before any stream capture. The address
+ * is kept for the life of the process, so do not call this entry point on a device after
+ * a cudaDeviceReset of that device (the reset unloads the array it points into). Every
+ * call on a device shares the one array and rewrites the parts it reads before reading
+ * them, so two calls that overlap on the GPU (different streams without ordering between
+ * them) race: order them. Three kernel launches on `stream` (fragments, backward,
+ * table-gradient sum), counted by swin_wattn_launch_count.
  */
 int swin_wattn_bwd_noalloc(const void* qkv, const void* dout, void* dqkv, float* dtable,
                            const float* bias_table, int B, int H, int W, int C, int num_heads,

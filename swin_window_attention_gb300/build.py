@@ -1,8 +1,11 @@
 """Builds libswin_wattn.so in-tree from csrc/*.cu with nvcc for sm_103a.
 
 Each translation unit compiles in its own nvcc process (in parallel), then one link
-step produces the shared library next to this file. Run ``python -m
-swin_window_attention_gb300.build [--force] [--verbose-ptxas]``.
+step produces the shared library next to this file. ``debug=True`` builds the
+fault-injection variant libswin_wattn_debug.so from the same sources with
+SWIN_WATTN_FAULT_INJECTION defined (include/swin_wattn_debug.h); it is used only by the
+tests of the bounded device waits. Run ``python -m swin_window_attention_gb300.build
+[--force] [--verbose-ptxas] [--debug]``.
 """
 from __future__ import annotations
 
@@ -19,6 +22,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libswin_wattn.so")
+BUILD_DEBUG = os.path.join(HERE, "_build_debug")
+LIB_DEBUG = os.path.join(HERE, "libswin_wattn_debug.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -38,25 +43,29 @@ def _deps():
         os.path.join(INCLUDE, "*.h")) + [os.path.abspath(__file__)]
 
 
-def is_stale() -> bool:
-    if not os.path.exists(LIB):
+def is_stale(debug: bool = False) -> bool:
+    lib = LIB_DEBUG if debug else LIB
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return any(os.path.getmtime(d) > t for d in _deps())
 
 
-def build(force: bool = False, verbose_ptxas: bool = False) -> str:
-    if not force and not is_stale():
-        return LIB
+def build(force: bool = False, verbose_ptxas: bool = False, debug: bool = False) -> str:
+    lib, bdir = (LIB_DEBUG, BUILD_DEBUG) if debug else (LIB, BUILD)
+    if not force and not is_stale(debug):
+        return lib
     nvcc = _nvcc()
-    os.makedirs(BUILD, exist_ok=True)
+    os.makedirs(bdir, exist_ok=True)
     common = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE,
                      "--use_fast_math"]
+    if debug:
+        common += ["-DSWIN_WATTN_FAULT_INJECTION"]
     if verbose_ptxas:
         common += ["-Xptxas", "-v"]
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(bdir, os.path.basename(src)[:-3] + ".o")
         cmd = [nvcc, "-c", src, "-o", obj] + common
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -68,19 +77,20 @@ def build(force: bool = False, verbose_ptxas: bool = False) -> str:
     if verbose_ptxas:
         for _, err in results:
             sys.stderr.write(err)
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [nvcc, "-shared", "-o", tmp] + [o for o, _ in results] + ARCH + [
         "-cudart", "shared", "-Xlinker", "-rpath", "-Xlinker", "/usr/local/cuda/lib64"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
     ap = argparse.ArgumentParser()
     ap.add_argument("--force", action="store_true")
     ap.add_argument("--verbose-ptxas", action="store_true")
+    ap.add_argument("--debug", action="store_true", help="the fault-injection variant")
     a = ap.parse_args()
-    print(build(force=a.force or a.verbose_ptxas, verbose_ptxas=a.verbose_ptxas))
+    print(build(force=a.force or a.verbose_ptxas, verbose_ptxas=a.verbose_ptxas, debug=a.debug))

@@ -54,7 +54,16 @@ SIGNATURES = {
     "swin_wattn_launch_count": ([_i], ctypes.c_uint64),
 }
 
+# The fault-injection library (include/swin_wattn_debug.h) adds one entry point.
+DEBUG_LIB_PATH = os.path.join(_HERE, "libswin_wattn_debug.so")
+DEBUG_SIGNATURES = {"swin_wattn_debug_set_fault": ([_i, ctypes.c_int64], _i)}
+FAULT_NONE = 0
+FAULT_FWD_MMA_SYNC = 1
+FAULT_FWD_TCGEN05 = 2
+FAULT_GEMM = 3
+
 _lib = None
+_debug_lib = None
 
 
 class SwinWAttnError(RuntimeError):
@@ -81,6 +90,24 @@ def load() -> ctypes.CDLL:
             fn.restype = res
         _lib = lib
     return _lib
+
+
+def load_debug() -> ctypes.CDLL:
+    """Load the fault-injection build (once), a separate library with the same entry
+    points plus swin_wattn_debug_set_fault. Raises if it has not been built
+    (``python -m swin_window_attention_gb300.build --debug``)."""
+    global _debug_lib
+    if _debug_lib is None:
+        if not os.path.exists(DEBUG_LIB_PATH):
+            raise RuntimeError(f"{DEBUG_LIB_PATH} is missing: build it with "
+                               "`python -m swin_window_attention_gb300.build --debug`")
+        lib = ctypes.CDLL(DEBUG_LIB_PATH)
+        for name, (args, res) in list(SIGNATURES.items()) + list(DEBUG_SIGNATURES.items()):
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = res
+        _debug_lib = lib
+    return _debug_lib
 
 
 # ---- same names as the C entry points --------------------------------------------------

@@ -623,34 +623,9 @@ cudaError_t bwd_launch(const Plan& pl, const BwdLaunch& L, const void* qkv, cons
 constexpr size_t kNoAllocScratchBytes = size_t(2) << 20;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-// Bias fragments straight from the table (no dense bias); the mask fragments come from
-// the region labels exactly as in the plan's fragment kernel.
-template <int M>
-__global__ void noalloc_fragments_kernel(const float* __restrict__ table, int nH, int H, int W,
-                                         int s, float4* __restrict__ bias_frag,
-                                         uint32_t* __restrict__ mask_frag) {
-  using G = Geo<M>;
-  constexpr int N = G::N, NT = G::NT;
-  const int per_head = G::WARPS * NT * 32;
-  const int nbias = nH * per_head;
-  const int nmask = mask_frag ? G::MASK_BYTES / 4 : 0;
-  for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < nbias + nmask; e += gridDim.x * blockDim.x) {
-    if (e < nbias) {
-      const int h = e / per_head, f = e % per_head;
-      const int ln = f & 31, nt = (f >> 5) % NT, wp = (f >> 5) / NT;
-      const int r0 = wp * 16 + (ln >> 2), c0 = nt * 8 + 2 * (ln & 3);
-      float v[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int r = r0 + 8 * (q >> 1), c = c0 + (q & 1);
-        v[q] = c >= N ? -INFINITY : (r >= N ? 0.0f : table[(int64_t)rel_index(r, c, M) * nH + h] * kInvScale);
-      }
-      bias_frag[e] = make_float4(v[0], v[1], v[2], v[3]);
-    } else {
-      mask_frag[e - nbias] = mask_frag_word<M>(e - nbias, H, W, s);
-    }
-  }
-}
+cudaError_t launch_bias_frags(int M, const float* table, int nH, int H, int W, int s, float4* bias_frag,
+                              uint32_t* mask_frag, float* dense, cudaStream_t st);
+void count_launches(int n);
 
 namespace {
 
@@ -692,12 +667,12 @@ cudaError_t noalloc_bwd_t(Plan& pl, const float* table, const void* qkv, const v
   pl.bias_frag = reinterpret_cast<float4*>(base);
   pl.mask_frag = pl.s > 0 ? reinterpret_cast<uint32_t*>(base + bias_bytes) : nullptr;
   pl.dt_partial = reinterpret_cast<float*>(base + bias_bytes + mask_bytes);
-  const int nfrag = pl.nH * Geo<M>::WARPS * Geo<M>::NT * 32 + (pl.s > 0 ? Geo<M>::MASK_BYTES / 4 : 0);
-  noalloc_fragments_kernel<M><<<(nfrag + 255) / 256, 256, 0, st>>>(table, pl.nH, pl.H, pl.W, pl.s,
-                                                                   pl.bias_frag, pl.mask_frag);
-  e = cudaGetLastError();
+  // the plan's own fragment kernel, without the dense bias (the kernels never read it)
+  e = launch_bias_frags(M, table, pl.nH, pl.H, pl.W, pl.s, pl.bias_frag, pl.mask_frag, nullptr, st);
   if (e != cudaSuccess) return e;
-  return blaunch_t<M, TIO, STAGES>(pl, L, qkv, dout, dqkv, dtable, st);
+  e = blaunch_t<M, TIO, STAGES>(pl, L, qkv, dout, dqkv, dtable, st);
+  if (e == cudaSuccess) count_launches(3);  // fragments, backward, table-gradient reduction
+  return e;
 }
 
 }  // namespace

@@ -1,5 +1,6 @@
 // C ABI of the swin_wattn library: argument validation, plan ownership, launches and
 // error surfacing. No exception, abort or trap crosses this boundary.
+#include <atomic>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -136,7 +137,28 @@ void free_plan_buffers(swin::Plan& p) {
 namespace swin {
 void set_last_error(const char* msg) { std::snprintf(g_last_error, sizeof(g_last_error), "%s", msg); }
 int check_device_ptr_abi(const void* ptr, size_t align) { return check_device_ptr(ptr, align); }
+// Kernel launches issued by the calling thread outside this file (swin_wattn_launch_count).
+void count_launches(int n) { g_launches += (uint64_t)n; }
+
+namespace {
+std::atomic<uint64_t> g_wait_ns{1000000000ull};
+std::atomic<int> g_fault{kFaultNone};
+}  // namespace
+uint64_t wait_limit_ns() { return g_wait_ns.load(std::memory_order_relaxed); }
+int fault_site() { return g_fault.load(std::memory_order_relaxed); }
 }  // namespace swin
+
+#ifdef SWIN_WATTN_FAULT_INJECTION
+#include "../../include/swin_wattn_debug.h"
+
+extern "C" int swin_wattn_debug_set_fault(int site, int64_t wait_limit_ns) {
+  if (site < swin::kFaultNone || site > swin::kFaultGemm) return SWIN_WATTN_ERR_INVALID_ARG;
+  if (wait_limit_ns < 1000 || wait_limit_ns > 10000000000ll) return SWIN_WATTN_ERR_INVALID_ARG;
+  swin::g_wait_ns.store((uint64_t)wait_limit_ns);
+  swin::g_fault.store(site);
+  return SWIN_WATTN_OK;
+}
+#endif
 
 extern "C" {
 

@@ -46,6 +46,18 @@ struct Plan {
   int fwd_kernel;
 };
 
+// ---- bounded waits and the fault-injection build ---------------------------------
+//
+// Every device-side wait on an mbarrier gives up after wait_limit_ns() (1 s) and the
+// kernel reports SWIN_WATTN_ERR_TIMEOUT through an error word. The fault-injection build
+// (compiled with SWIN_WATTN_FAULT_INJECTION, libswin_wattn_debug.so) can shorten that
+// limit and arm one site that withholds a single mbarrier arrival, so that one wait runs
+// out and the error path runs; the default build contains no injection code and its
+// fault site is always kFaultNone.
+enum FaultSite { kFaultNone = 0, kFaultFwdMmaSync = 1, kFaultFwdTcgen05 = 2, kFaultGemm = 3 };
+uint64_t wait_limit_ns();
+int fault_site();
+
 // ---- geometry shared by every kernel that touches a window -----------------------
 
 // Original-grid token index (b*H + y)*W + x read by slot i of window w in batch b.
@@ -88,6 +100,8 @@ template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
 }
+// Every cp.async of this thread, committed to a group or not, has landed.
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
                                         uint32_t& r3) {

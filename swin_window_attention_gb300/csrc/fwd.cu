@@ -34,6 +34,8 @@ struct FwdParams {
   int chunks;             // window ranges per head
   float qk_scale_log2;    // hd^-0.5 * log2(e)
   int* err;               // plan error word (bit 0: a bounded wait ran out)
+  uint64_t wait_ns;       // bound of each wait on a stage barrier
+  int fault;              // armed fault site (fault-injection build only)
 };
 
 // With TMA loads the tiles sit on 1024-byte boundaries (the copy engine's 64-byte swizzle
@@ -105,6 +107,9 @@ __global__ void __launch_bounds__(Geo<M>::THREADS, FwdMinBlocks<M>::value)
   }
   int cb = lb, cwy = lwy, cwx = lwx;  // cursor of the window being computed
   const uint32_t tiles_u32 = smem_u32(stiles);
+#ifdef SWIN_WATTN_FAULT_INJECTION
+  bool first_issue = true;  // the CTA's first window is being issued
+#endif
 
   auto issue = [&](uint32_t stage_off, int stage) {
     const uint32_t base = tiles_u32 + stage_off;
@@ -135,6 +140,9 @@ __global__ void __launch_bounds__(Geo<M>::THREADS, FwdMinBlocks<M>::value)
           }
         }
         tc::cp_async_arrive(full);
+#ifdef SWIN_WATTN_FAULT_INJECTION
+        first_issue = false;
+#endif
         if (++lwx == p.nWx) {
           lwx = 0;
           if (++lwy == p.nWy) {
@@ -160,7 +168,17 @@ __global__ void __launch_bounds__(Geo<M>::THREADS, FwdMinBlocks<M>::value)
           load_chunk<TIO>(base + tt * G::TILE_BYTES + ld_soff[j], src + tt * p.C);
       }
     }
-    if constexpr (TMA) tc::cp_async_arrive(bar0 + 8 * stage);
+    if constexpr (TMA) {
+#ifdef SWIN_WATTN_FAULT_INJECTION
+      // armed: thread 0 withholds its arrival on the CTA's first window, so that window's
+      // bounded wait runs out (a cp.async window: no copy-engine bytes land after it)
+      if (!(p.fault == kFaultFwdMmaSync && tid == 0 && first_issue))
+#endif
+        tc::cp_async_arrive(bar0 + 8 * stage);
+    }
+#ifdef SWIN_WATTN_FAULT_INJECTION
+    first_issue = false;
+#endif
     if (++lwx == p.nWx) {
       lwx = 0;
       if (++lwy == p.nWy) {
@@ -226,13 +244,14 @@ __global__ void __launch_bounds__(Geo<M>::THREADS, FwdMinBlocks<M>::value)
   const uint32_t st_off1 = tile_off(warp * 16 + r8 + ((mi & 1) << 3), 2 + (mi >> 1));
 
   uint32_t cur_off = 0, nxt_off = (STAGES - 1) * G::STAGE_BYTES;
-  int cur_st = 0, nxt_st = STAGES - 1, bad = 0;
+  int cur_st = 0, nxt_st = STAGES - 1, bad = 0, bad_it = 0;
   for (int it = 0; it < nwin; ++it) {
     if constexpr (TMA) {
       // the window's tiles: every thread's cp.async and the copy engine's bytes (bounded)
-      const bool ok = tc::mbar_wait(bar0 + 8 * cur_st, (it / STAGES) & 1, 1000000000ull);
+      const bool ok = tc::mbar_wait(bar0 + 8 * cur_st, (it / STAGES) & 1, p.wait_ns);
       if (__syncthreads_or(ok ? 0 : 1)) {
         bad = 1;
+        bad_it = it;
         break;
       }
       if (it + STAGES - 1 < nwin) issue(nxt_off, nxt_st);
@@ -393,7 +412,15 @@ __global__ void __launch_bounds__(Geo<M>::THREADS, FwdMinBlocks<M>::value)
       }
     }
   }
-  cp_async_wait<0>();
+  if constexpr (TMA) {
+    if (bad) {
+      // after a timeout: the windows already issued behind the one whose wait ran out
+      // land before the CTA leaves (their barriers complete with their last bytes)
+      for (int k = bad_it + 1; k < nwin && k < bad_it + STAGES - 1; ++k)
+        tc::mbar_wait(bar0 + 8 * (k % STAGES), (k / STAGES) & 1, p.wait_ns);
+    }
+  }
+  cp_async_wait_all();
   if (bad && tid == 0) atomicOr(p.err, 1);
 }
 
@@ -465,6 +492,8 @@ static cudaError_t launch_t(const Plan& pl, const FwdLaunch& L0, const void* qkv
   p.chunks = L.chunks;
   p.qk_scale_log2 = kLog2e / kInvScale;
   p.err = pl.err;
+  p.wait_ns = wait_limit_ns();
+  p.fault = fault_site();
   return launch_pdl(fwd_kernel<M, TIO, STAGES, TMA>, dim3(L.grid), dim3(L.threads), L.smem, st, box_map, top_map,
                     bot_map, p);
 }

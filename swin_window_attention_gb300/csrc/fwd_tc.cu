@@ -66,7 +66,7 @@ constexpr int kOFF_U = kSTAGES * kSTAGE;
 constexpr int kOFF_VC = kOFF_U + kU_BYTES;
 constexpr int kOFF_BIAS = kOFF_U + kMASK_BYTES;
 constexpr int kOFF_BAR = kOFF_BIAS + kBIAS_BYTES;
-constexpr int kNBAR = 2 * kSTAGES + 6;
+constexpr int kNBAR = 2 * kSTAGES + 7;
 constexpr int kSMEM = kOFF_BAR + 8 * kNBAR + 8 + 1024;  // + alignment slack
 constexpr uint32_t kG4_TX = 3 * kGROUPS * 4 * kROW_BYTES;  // bytes of one window's gather4 loads
 constexpr uint32_t kBOX_TX = 3 * kTN * kROW_BYTES;           // bytes of one window's box loads
@@ -74,7 +74,6 @@ constexpr uint32_t kBOX_TX = 3 * kTN * kROW_BYTES;           // bytes of one win
 // pairs over the row's own 64 keys), O [160, 240) (window a, window b, row sums).
 constexpr int kTMEM_COLS = 256;
 constexpr int kS_COL = 0, kP_COL = 128, kO_COL = 160;
-constexpr uint64_t kWaitLimitNs = 1000000000ull;
 constexpr uint32_t kSW64 = 4;                  // descriptor layout: 64-byte swizzle
 
 static_assert(kSMEM * 3 > 233472, "at most two CTAs per SM: each holds half the tensor memory");
@@ -86,8 +85,8 @@ __device__ __forceinline__ uint32_t k16_off(int r, int k) {
 }
 
 // A bounded wait whose outcome is the same for the whole warp.
-__device__ __forceinline__ bool warp_wait(uint32_t mbar, uint32_t parity) {
-  return __all_sync(0xffffffffu, tc::mbar_wait(mbar, parity, kWaitLimitNs)) != 0;
+__device__ __forceinline__ bool warp_wait(uint32_t mbar, uint32_t parity, uint64_t limit_ns) {
+  return __all_sync(0xffffffffu, tc::mbar_wait(mbar, parity, limit_ns)) != 0;
 }
 
 struct TcParams {
@@ -98,6 +97,8 @@ struct TcParams {
   int64_t total_windows;
   int chunks;
   float qk_scale_log2;  // hd^-0.5 * log2(e)
+  uint64_t wait_ns;     // bound of each wait
+  int fault;            // armed fault site (fault-injection build only)
 };
 
 // Window cursor: (b, wy, wx) advanced one window at a time.
@@ -136,6 +137,8 @@ __global__ void __launch_bounds__(kTHREADS, 1) fwd_tc_kernel(const __grid_consta
   auto empty_bar = [&](int st) { return bar0 + 8 * (kSTAGES + st); };
   const uint32_t s_full = bar0 + 8 * (2 * kSTAGES), s_free = s_full + 8, p_full = s_full + 16;
   const uint32_t o_full = s_full + 24, o_free = s_full + 32, const_bar = s_full + 40;
+  const uint32_t drain_bar = s_full + 48;  // the MMA thread's last commit before it leaves
+  auto wwait = [&](uint32_t mbar, uint32_t parity) { return warp_wait(mbar, parity, p.wait_ns); };
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int h = blockIdx.x % p.nH;
@@ -165,6 +168,7 @@ __global__ void __launch_bounds__(kTHREADS, 1) fwd_tc_kernel(const __grid_consta
     tc::mbar_init(o_full, 1);
     tc::mbar_init(o_free, 4);
     tc::mbar_init(const_bar, 1);
+    tc::mbar_init(drain_bar, 1);
     tc::mbar_init_fence();
   }
   // Stage tiles start zeroed: slot rows 52..63 are never written by the gathers. The
@@ -211,11 +215,13 @@ __global__ void __launch_bounds__(kTHREADS, 1) fwd_tc_kernel(const __grid_consta
       const bool wrap_x = c.wx * kTM + s + kTM > W, wrap_y = c.wy * kTM + s + kTM > H;
       return !wrap_x && !wrap_y ? 0 : (!wrap_x && split_ok ? 1 : 2);
     };
+    int issued = 0;  // pairs whose loads were issued
     for (int n = 0, st = 0; n < npair; ++n) {
-      if (n >= kSTAGES && !warp_wait(empty_bar(st), ((n / kSTAGES) - 1) & 1)) {
+      if (n >= kSTAGES && !wwait(empty_bar(st), ((n / kSTAGES) - 1) & 1)) {
         bad = 1;
         break;
       }
+      issued = n + 1;
       const bool has_b = 2 * n + 1 < nwin;
       Cursor wa = cur, wb = cur;
       wb.next(p.nWy, p.nWx);
@@ -264,6 +270,12 @@ __global__ void __launch_bounds__(kTHREADS, 1) fwd_tc_kernel(const __grid_consta
       cur.next(p.nWy, p.nWx);
       st = st + 1 == kSTAGES ? 0 : st + 1;
     }
+    // every load issued has landed before the CTA leaves, also when another role's wait
+    // ran out before it consumed them (the latest phase of each stage completes with its
+    // bytes; older phases have completed)
+    for (int m = issued > kSTAGES ? issued - kSTAGES : 0; m < issued; ++m)
+      tc::mbar_wait(full_bar(m % kSTAGES), (m / kSTAGES) & 1, p.wait_ns);
+    tc::mbar_wait(const_bar, 0, p.wait_ns);  // and the constant operands
   } else if (warp == kMMA_WARP) {
     // ==== MMA issue: one thread; the warp waits together ==============================
     const uint32_t idesc_qk = tc::idesc_bf16(128, 128, false);
@@ -298,7 +310,7 @@ __global__ void __launch_bounds__(kTHREADS, 1) fwd_tc_kernel(const __grid_consta
       __syncwarp();
     };
     if (npair > 0) {
-      if (warp_wait(const_bar, 0) && warp_wait(full_bar(0), 0))
+      if (wwait(const_bar, 0) && wwait(full_bar(0), 0))
         issue_qk(0);
       else
         bad = 1;
@@ -306,7 +318,7 @@ __global__ void __launch_bounds__(kTHREADS, 1) fwd_tc_kernel(const __grid_consta
     // P V of pair n as soon as its P is written, then Q K^T of pair n + 1 as soon as its
     // tiles have landed and S has been read out (usually long before).
     for (int n = 0; n < npair && !bad; ++n) {
-      if (!warp_wait(p_full, n & 1) || (n > 0 && !warp_wait(o_free, (n - 1) & 1))) {
+      if (!wwait(p_full, n & 1) || (n > 0 && !wwait(o_free, (n - 1) & 1))) {
         bad = 1;
         break;
       }
@@ -323,13 +335,17 @@ __global__ void __launch_bounds__(kTHREADS, 1) fwd_tc_kernel(const __grid_consta
       __syncwarp();
       if (n + 1 < npair) {
         const int st1 = (n + 1) % kSTAGES;
-        if (!warp_wait(full_bar(st1), ((n + 1) / kSTAGES) & 1) || !warp_wait(s_free, n & 1)) {
+        if (!wwait(full_bar(st1), ((n + 1) / kSTAGES) & 1) || !wwait(s_free, n & 1)) {
           bad = 1;
           break;
         }
         issue_qk(n + 1);
       }
     }
+    // every MMA this thread issued has completed before the tensor memory is released
+    if (lane == 0) tc::commit(drain_bar);
+    __syncwarp();
+    if (!wwait(drain_bar, 0)) bad = 1;
   } else {
     // ==== row warps: softmax of row r, then its output ================================
     const int win = tid >> 6, i = tid & 63;  // window of the pair (warp-uniform) and slot
@@ -338,13 +354,13 @@ __global__ void __launch_bounds__(kTHREADS, 1) fwd_tc_kernel(const __grid_consta
     const float* brow = sbias + i * kBIAS_STRIDE;
     const uint32_t trow = tmem + ((uint32_t)(32 * warp) << 16);
     Cursor cur = first;
-    if (npair > 0 && !warp_wait(const_bar, 0)) bad = 1;
+    if (npair > 0 && !wwait(const_bar, 0)) bad = 1;
     for (int n = 0; n < npair && !bad; ++n) {
       Cursor me = cur;
       if (win) me.next(p.nWy, p.nWx);
       const bool active = i < kTN && (win == 0 || 2 * n + 1 < nwin);
 
-      if (!warp_wait(s_full, n & 1)) {
+      if (!wwait(s_full, n & 1)) {
         bad = 1;
         break;
       }
@@ -398,9 +414,14 @@ __global__ void __launch_bounds__(kTHREADS, 1) fwd_tc_kernel(const __grid_consta
       tc::wait_st();
       tc::fence_before_sync();
       __syncwarp();
-      if (lane == 0) tc::mbar_arrive(p_full);
+#ifdef SWIN_WATTN_FAULT_INJECTION
+      // armed: row warp 0 withholds its arrival for the first pair, so the MMA thread's
+      // bounded wait for P runs out
+      if (!(p.fault == kFaultFwdTcgen05 && warp == 0 && n == 0))
+#endif
+        if (lane == 0) tc::mbar_arrive(p_full);
 
-      if (!warp_wait(o_full, n & 1)) {
+      if (!wwait(o_full, n & 1)) {
         bad = 1;
         break;
       }
@@ -602,6 +623,8 @@ cudaError_t fwd_tc_launch(const Plan& pl, const FwdLaunch& L0, const void* qkv, 
   p.total_windows = total;
   p.chunks = L.chunks;
   p.qk_scale_log2 = kLog2e / kInvScale;
+  p.wait_ns = wait_limit_ns();
+  p.fault = fault_site();
   return launch_pdl(fwd_tc_kernel, dim3(L.grid), dim3(L.threads), L.smem, st, map, box_map, top_map, bot_map, p);
 }
 

@@ -100,14 +100,14 @@ __host__ __device__ constexpr int uv_warp_bytes() { return MODE == 0 ? 0 : 4 * 6
 template <int MODE>
 __host__ __device__ constexpr int out_bytes() { return 8 * (out_bufs<MODE>() * 32 * 64 + uv_warp_bytes<MODE>()); }
 constexpr int kRBAR0 = 2 * kMaxSTAGES + 8;  // consumer: residual-load barriers, 3 per epilogue warp
-constexpr int kNBAR = kRBAR0 + 8 * 3;
+constexpr int kDRAIN = kRBAR0 + 8 * 3;      // the MMA thread's last commit before it leaves
+constexpr int kNBAR = kDRAIN + 1;
 template <int MODE>
 __host__ __device__ constexpr int tail_bytes() { return out_bytes<MODE>() + 8 * kNBAR + 8 + 1024; }  // + alignment slack
 // More than half of an SM's shared memory: one CTA per SM, so the 512-column tensor
 // memory allocation never waits for another CTA of this kernel.
 constexpr int kMinSMEM = 120 * 1024;
 constexpr int kTMEM_COLS = 512;                // two accumulators of up to 256 columns
-constexpr uint64_t kWaitLimitNs = 1000000000ull;
 constexpr uint32_t kSW128 = 2;  // descriptor layout: 128-byte swizzle
 
 struct GemmParams {
@@ -116,14 +116,16 @@ struct GemmParams {
   const float* v;                  // [N] producer: beta W^T + b; consumer: bp
   const float2* stats;             // [T] (mean, rstd), producer with the prep pass
   int* status;                     // optional: bit 0 set when a bounded wait ran out
+  uint64_t wait_ns;                // bound of each wait
+  int fault;                       // armed fault site (fault-injection build only)
   int T, K, N, NT, tiles_per_item, n_tt, n_items;
   int stages, stage_bytes;  // the ring: stages x (x chunk + NT x 128 bytes), 1024-byte multiples
   int off_stats, off_out, off_bar;
   float eps;
 };
 
-__device__ __forceinline__ bool warp_wait(uint32_t mbar, uint32_t parity) {
-  return __all_sync(0xffffffffu, tc::mbar_wait(mbar, parity, kWaitLimitNs)) != 0;
+__device__ __forceinline__ bool warp_wait(uint32_t mbar, uint32_t parity, uint64_t limit_ns) {
+  return __all_sync(0xffffffffu, tc::mbar_wait(mbar, parity, limit_ns)) != 0;
 }
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -174,6 +176,7 @@ __global__ void __launch_bounds__(Roles<MODE>::kTHREADS, 1)
       tc::mbar_init(sfull_bar(b), 4);
       tc::mbar_init(sfree_bar(b), 8);
     }
+    tc::mbar_init(bar0 + 8 * kDRAIN, 1);
     tc::mbar_init_fence();
   }
   tc::fence_before_sync();
@@ -194,7 +197,7 @@ __global__ void __launch_bounds__(Roles<MODE>::kTHREADS, 1)
         int t0, j0, ntile;
         item_tiles(it, t0, j0, ntile);
         for (int s_ = 0; s_ < ntile * kcn; ++s_) {
-          if (!first && !tc::mbar_wait(empty_bar(st), ph ^ 1, kWaitLimitNs)) {
+          if (!first && !tc::mbar_wait(empty_bar(st), ph ^ 1, p.wait_ns)) {
             bad = 1;
             break;
           }
@@ -210,12 +213,11 @@ __global__ void __launch_bounds__(Roles<MODE>::kTHREADS, 1)
           }
         }
       }
-      if (bad) {
-        // after a timeout: let the loads still in flight land before the CTA leaves (a
-        // stage's last phase has completed already unless its bytes are still coming)
-        for (int s2 = 0; s2 < (first ? st : stages); ++s2)
-          tc::mbar_wait(full_bar(s2), s2 < st ? ph : ph ^ 1, kWaitLimitNs);
-      }
+      // every load issued has landed before the CTA leaves, also when another role's wait
+      // ran out before it consumed them (a stage's last phase has completed already unless
+      // its bytes are still coming)
+      for (int s2 = 0; s2 < (first ? st : stages); ++s2)
+        tc::mbar_wait(full_bar(s2), s2 < st ? ph : ph ^ 1, p.wait_ns);
     }
     __syncwarp();
   } else if (warp == R::kMMA) {
@@ -228,12 +230,12 @@ __global__ void __launch_bounds__(Roles<MODE>::kTHREADS, 1)
       item_tiles(it, t0, j0, ntile);
       for (int jj = 0; jj < ntile && !bad; ++jj, ++g) {
         const int buf = g & 1;
-        if (g >= 2 && !warp_wait(dfree_bar(buf), ((g >> 1) - 1) & 1)) {
+        if (g >= 2 && !warp_wait(dfree_bar(buf), ((g >> 1) - 1) & 1, p.wait_ns)) {
           bad = 1;
           break;
         }
         for (int kc = 0; kc < kcn; ++kc) {
-          if (!warp_wait(full_bar(st), ph)) {
+          if (!warp_wait(full_bar(st), ph, p.wait_ns)) {
             bad = 1;
             break;
           }
@@ -245,7 +247,12 @@ __global__ void __launch_bounds__(Roles<MODE>::kTHREADS, 1)
               tc::mma_ss(tmem + buf * kMaxNT, tc::sdesc(a + kk * 32, 16, 1024, kSW128),
                          tc::sdesc(w + kk * 32, 16, 1024, kSW128), idesc, kc > 0 || kk > 0);
             tc::commit(empty_bar(st));
-            if (kc == kcn - 1) tc::commit(dfull_bar(buf));
+#ifdef SWIN_WATTN_FAULT_INJECTION
+            // armed: the first output tile's accumulator is never announced, so the
+            // epilogue's bounded wait for it runs out
+            if (!(p.fault == kFaultGemm && g == 0))
+#endif
+              if (kc == kcn - 1) tc::commit(dfull_bar(buf));
           }
           __syncwarp();
           if (++st == stages) {
@@ -255,6 +262,10 @@ __global__ void __launch_bounds__(Roles<MODE>::kTHREADS, 1)
         }
       }
     }
+    // every MMA this thread issued has completed before the tensor memory is released
+    if (lane == 0) tc::commit(bar0 + 8 * kDRAIN);
+    __syncwarp();
+    if (!warp_wait(bar0 + 8 * kDRAIN, 0, p.wait_ns)) bad = 1;
   } else if (warp < R::kEPI0) {
     // ==== statistics warps: shifted sums of row r over the item's first output tile =====
     const int r = tid;
@@ -266,7 +277,7 @@ __global__ void __launch_bounds__(Roles<MODE>::kTHREADS, 1)
       float shift = 0.0f;
       float2 sh2 = make_float2(0.0f, 0.0f), s1v = make_float2(0.0f, 0.0f), s2v = make_float2(0.0f, 0.0f);
       for (int s_ = 0; s_ < ntile * kcn; ++s_) {
-        if (!warp_wait(full_bar(st), ph)) {
+        if (!warp_wait(full_bar(st), ph, p.wait_ns)) {
           bad = 1;
           break;
         }
@@ -300,7 +311,7 @@ __global__ void __launch_bounds__(Roles<MODE>::kTHREADS, 1)
           const float m1 = (s1v.x + s1v.y) / p.K;
           const float var = fmaxf((s2v.x + s2v.y) / p.K - m1 * m1, 0.0f);
           const int sb = k & 1;
-          if (k >= 2 && !warp_wait(sfree_bar(sb), ((k >> 1) - 1) & 1)) {
+          if (k >= 2 && !warp_wait(sfree_bar(sb), ((k >> 1) - 1) & 1, p.wait_ns)) {
             bad = 1;
             break;
           }
@@ -354,7 +365,7 @@ __global__ void __launch_bounds__(Roles<MODE>::kTHREADS, 1)
       float2 ms = make_float2(0.0f, 1.0f);
       if constexpr (MODE == kLnChipStats) {
         const int sb = k & 1;
-        if (!warp_wait(sfull_bar(sb), (k >> 1) & 1)) {
+        if (!warp_wait(sfull_bar(sb), (k >> 1) & 1, p.wait_ns)) {
           bad = 1;
           break;
         }
@@ -392,7 +403,7 @@ __global__ void __launch_bounds__(Roles<MODE>::kTHREADS, 1)
           }
           __syncwarp();
         }
-        if (!warp_wait(dfull_bar(buf), (g >> 1) & 1)) {
+        if (!warp_wait(dfull_bar(buf), (g >> 1) & 1, p.wait_ns)) {
           bad = 1;
           break;
         }
@@ -416,7 +427,7 @@ __global__ void __launch_bounds__(Roles<MODE>::kTHREADS, 1)
           uint32_t a[32];
           tc::ld32_wait(trow + buf * kMaxNT + c0, a);
           if constexpr (MODE == kBiasResidual) {
-            if (!warp_wait(rbar0 + 8 * (m % 3), (m / 3) & 1)) {
+            if (!warp_wait(rbar0 + 8 * (m % 3), (m / 3) & 1, p.wait_ns)) {
               bad = 1;
               break;
             }
@@ -467,7 +478,7 @@ __global__ void __launch_bounds__(Roles<MODE>::kTHREADS, 1)
     }
     if constexpr (MODE == kBiasResidual) {
       // after a timeout: let the residual loads still in flight land before the CTA leaves
-      for (int q = m; q < issued; ++q) warp_wait(rbar0 + 8 * (q % 3), (q / 3) & 1);
+      for (int q = m; q < issued; ++q) warp_wait(rbar0 + 8 * (q % 3), (q / 3) & 1, p.wait_ns);
     }
     if (lane == 0) tc::bulk_wait_all();
   }
@@ -691,6 +702,8 @@ GemmParams base_params(void* out, int T, int K, int N, int* status) {
   GemmParams p{};
   p.out = reinterpret_cast<__nv_bfloat16*>(out);
   p.status = status;
+  p.wait_ns = wait_limit_ns();
+  p.fault = fault_site();
   p.T = T;
   p.K = K;
   p.N = N;

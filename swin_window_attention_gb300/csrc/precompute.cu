@@ -110,27 +110,34 @@ size_t mask_frag_bytes(int M) {
   }
 }
 
-// The plan's bias fragments and dense bias from `table` [and its mask fragments], one
-// launch.
-cudaError_t launch_bias_tables(const Plan& p, const float* table, bool with_mask, cudaStream_t st) {
-  uint32_t* mask = with_mask && p.s > 0 ? p.mask_frag : nullptr;
-  const int64_t n = (int64_t)bias_frag_bytes(p.M, p.nH) / 16 + (mask ? mask_frag_bytes(p.M) / 4 : 0) +
-                    (int64_t)p.nH * p.N * p.N;
+// Bias fragments from `table` for window size M, with the class mask fragments when
+// `mask_frag` is given and the dense bias when `dense` is given: one launch.
+cudaError_t launch_bias_frags(int M, const float* table, int nH, int H, int W, int s, float4* bias_frag,
+                              uint32_t* mask_frag, float* dense, cudaStream_t st) {
+  const int64_t n = (int64_t)bias_frag_bytes(M, nH) / 16 + (mask_frag ? mask_frag_bytes(M) / 4 : 0) +
+                    (dense ? (int64_t)nH * M * M * M * M : 0);
   const int grid = grid_for(n, 256);
-  switch (p.M) {
+  switch (M) {
     case 4:
-      bias_tables_kernel<4><<<grid, 256, 0, st>>>(table, p.nH, p.H, p.W, p.s, p.bias_frag, mask, p.dense_bias);
+      bias_tables_kernel<4><<<grid, 256, 0, st>>>(table, nH, H, W, s, bias_frag, mask_frag, dense);
       break;
     case 7:
-      bias_tables_kernel<7><<<grid, 256, 0, st>>>(table, p.nH, p.H, p.W, p.s, p.bias_frag, mask, p.dense_bias);
+      bias_tables_kernel<7><<<grid, 256, 0, st>>>(table, nH, H, W, s, bias_frag, mask_frag, dense);
       break;
     case 12:
-      bias_tables_kernel<12><<<grid, 256, 0, st>>>(table, p.nH, p.H, p.W, p.s, p.bias_frag, mask, p.dense_bias);
+      bias_tables_kernel<12><<<grid, 256, 0, st>>>(table, nH, H, W, s, bias_frag, mask_frag, dense);
       break;
     default:
       return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
+}
+
+// The plan's bias fragments and dense bias from `table` [and its mask fragments], one
+// launch.
+cudaError_t launch_bias_tables(const Plan& p, const float* table, bool with_mask, cudaStream_t st) {
+  uint32_t* mask = with_mask && p.s > 0 ? p.mask_frag : nullptr;
+  return launch_bias_frags(p.M, table, p.nH, p.H, p.W, p.s, p.bias_frag, mask, p.dense_bias, st);
 }
 
 cudaError_t launch_gather_map(int H, int W, int M, int s, int32_t* out, cudaStream_t st) {

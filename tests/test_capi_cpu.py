@@ -36,6 +36,27 @@ def test_library_exports_every_declared_symbol(lib):
     assert set(_declared()) == set(lib.SIGNATURES)
 
 
+def test_debug_library_exports_its_header_and_the_library_does_not():
+    """The fault-injection build exports every entry point of both headers; the default
+    library exports nothing of include/swin_wattn_debug.h."""
+    from swin_window_attention_gb300 import build, capi
+    build.build(debug=True)
+    txt = open(os.path.join(ROOT, "include", "swin_wattn_debug.h")).read()
+    txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+    names = sorted(set(re.findall(r"\b(swin_wattn_[a-z0-9_]+)\s*\(", txt)))
+    assert names == sorted(capi.DEBUG_SIGNATURES)
+    dbg = capi.load_debug()
+    for n in _declared() + names:
+        assert hasattr(dbg, n), n
+    so = capi.load()
+    for n in names:
+        assert not hasattr(so, n), n
+    # argument checks, host-side only
+    assert dbg.swin_wattn_debug_set_fault(9, 1000000) == capi.ERR_INVALID_ARG
+    assert dbg.swin_wattn_debug_set_fault(capi.FAULT_NONE, 10) == capi.ERR_INVALID_ARG
+    assert dbg.swin_wattn_debug_set_fault(capi.FAULT_NONE, 1000000000) == capi.OK
+
+
 def test_status_strings(lib):
     for code in range(7):
         assert lib.swin_wattn_status_string(code)
