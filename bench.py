@@ -350,7 +350,7 @@ def run_gpu(args):
     # time is also known at the clock the GPU settles to under sustained load (the kernels
     # are paced by instruction issue, so their speed follows the SM clock).
     step_s = total_ms / args.steps / 1e3
-    sus_steps = max(args.steps, int(math.ceil(1.0 / max(step_s, 1e-9))))
+    sus_steps = args.steps if args.skip_sustained else max(args.steps, int(math.ceil(1.0 / max(step_s, 1e-9))))
     clocks2 = ClockSampler(local)
     clocks2.start()
     time.sleep(0.3)
@@ -933,6 +933,8 @@ def main():
                     help="forward kernel of every plan (auto: the library's default)")
     ap.add_argument("--skip-train", action="store_true")
     ap.add_argument("--skip-cpu-baseline", action="store_true")
+    ap.add_argument("--skip-sustained", action="store_true",
+                    help="no seconds-long timed region (kernel profiling runs)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
