@@ -435,6 +435,8 @@ def run_gpu(args):
     l384 = run_fwd_sweep(L384, args, dev, stream, lib, capi, hbm, ws) if not args.skip_train else None
     block = run_block_sweep(SWEEP, args, dev, stream, lib, capi, peaks, ws) if not args.skip_train else None
     fp8 = run_fp8_sweep(SWEEP, args, dev, stream, lib, capi, hbm, ws) if not args.skip_train else None
+    block8 = (run_block_sweep(SWEEP, args, dev, stream, lib, capi, peaks, ws, fp8=True)
+              if not args.skip_train else None)
 
     if rank == 0:
         line = {
@@ -481,6 +483,7 @@ def run_gpu(args):
             "l384_sweep": l384,
             "block_sweep": block,
             "fp8_sweep": fp8,
+            "fp8_block_sweep": block8,
         }
         if ws == 1 and not args.skip_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(sweep)
@@ -600,13 +603,15 @@ def run_fp8_sweep(names, args, dev, stream, lib, capi, hbm, ws):
             "stages": stages}
 
 
-def run_block_sweep(names, args, dev, stream, lib, capi, peaks, ws):
+def run_block_sweep(names, args, dev, stream, lib, capi, peaks, ws, fp8=False):
     """The attention sub-block of each stage, x -> LayerNorm + qkv projection -> shifted-
     window attention -> output projection + bias + residual x, captured as one CUDA graph
     and replayed; per-call times from a second, eager region with CUDA events around every
     call. The qkv weights are prepared once per stage (the fold of gamma into W and the
     bias vectors), as an inference deployment does with fixed weights; the dense bias and
-    mask of each attention plan are likewise built once."""
+    mask of each attention plan are likewise built once. With fp8, the producer writes
+    OCP FP8 E4M3 qkv (per-tensor scales from the max |qkv| of one earlier pass: delayed
+    scaling) and the attention runs on those 8-bit operands."""
     sh = stream.cuda_stream
     st = []
     with torch.cuda.stream(stream):
@@ -618,9 +623,16 @@ def run_block_sweep(names, args, dev, stream, lib, capi, peaks, ws):
             T = wl.tokens
             proj = capi.QkvProjection(g, be, w, b, stream=stream)
             nws = capi.swin_wattn_qkv_stats_bytes(T)
-            st.append(dict(wl=wl, x=x, wp=wp, bp=bp, h=h, T=T, nws=nws, prep=proj.prepared,
+            sc = (1.0, 1.0, 1.0)
+            if fp8:
+                amax = torch.zeros(3, dtype=torch.float32, device=dev)
+                proj.fp8(x, sc, amax=amax, stream=stream)
+                torch.cuda.synchronize()
+                sc = tuple(float(a) / 448.0 for a in amax.cpu())
+            st.append(dict(wl=wl, x=x, wp=wp, bp=bp, h=h, T=T, nws=nws, prep=proj.prepared, sc=sc,
                            ws=torch.empty(nws, dtype=torch.uint8, device=dev),
-                           qkv=torch.empty(wl.B, wl.H, wl.W, 3 * wl.C, dtype=torch.bfloat16, device=dev),
+                           qkv=torch.empty(wl.B, wl.H, wl.W, 3 * wl.C, dtype=torch.uint8 if fp8 else torch.bfloat16,
+                                           device=dev),
                            o=torch.empty_like(x), y=torch.empty_like(x)))
     torch.cuda.synchronize()
 
@@ -629,12 +641,22 @@ def run_block_sweep(names, args, dev, stream, lib, capi, peaks, ws):
             wl = z["wl"]
             if events is not None:
                 events[k][0].record(stream)
-            ok = lib.swin_wattn_qkv_proj_prepared(z["x"].data_ptr(), z["prep"].data_ptr(), z["qkv"].data_ptr(),
-                                                  z["T"], wl.C, 1e-5, z["ws"].data_ptr(), z["nws"], None,
-                                                  sh) == capi.OK
+            if fp8:
+                sq, sk, sv = z["sc"]
+                ok = lib.swin_wattn_qkv_proj_prepared_fp8(z["x"].data_ptr(), z["prep"].data_ptr(),
+                                                          z["qkv"].data_ptr(), z["T"], wl.C, 1e-5, sq, sk, sv, None,
+                                                          z["ws"].data_ptr(), z["nws"], None, sh) == capi.OK
+            else:
+                ok = lib.swin_wattn_qkv_proj_prepared(z["x"].data_ptr(), z["prep"].data_ptr(), z["qkv"].data_ptr(),
+                                                      z["T"], wl.C, 1e-5, z["ws"].data_ptr(), z["nws"], None,
+                                                      sh) == capi.OK
             if events is not None:
                 events[k][1].record(stream)
-            ok &= lib.swin_wattn_fwd(z["h"], z["qkv"].data_ptr(), z["o"].data_ptr(), sh) == capi.OK
+            if fp8:
+                ok &= lib.swin_wattn_fwd_fp8(z["h"], z["qkv"].data_ptr(), sq, sk, sv, z["o"].data_ptr(),
+                                             sh) == capi.OK
+            else:
+                ok &= lib.swin_wattn_fwd(z["h"], z["qkv"].data_ptr(), z["o"].data_ptr(), sh) == capi.OK
             if events is not None:
                 events[k][2].record(stream)
             ok &= lib.swin_wattn_proj_residual(z["o"].data_ptr(), z["wp"].data_ptr(), z["bp"].data_ptr(),
@@ -682,16 +704,19 @@ def run_block_sweep(names, args, dev, stream, lib, capi, peaks, ws):
         wl = z["wl"]
         q_ms, f_ms, p_ms = (statistics.mean(ev[i][k][j].elapsed_time(ev[i][k][j + 1]) for i in range(steps))
                             for j in range(3))
+        qb = qkv_bytes(wl) - (3 * wl.C * wl.tokens if fp8 else 0)  # 8-bit qkv written
+        fb = fwd_fp8_bytes(wl) if fp8 else fwd_bytes(wl)
         stages.append({"workload": wl.name,
-                       "producer": gemm_roofline(qkv_bytes(wl), qkv_flops(wl), q_ms, peaks),
+                       "producer": gemm_roofline(qb, qkv_flops(wl), q_ms, peaks),
                        "attention": {"us": round(f_ms * 1e3, 2),
-                                     "frac_of_measured_hbm": round(fwd_bytes(wl) / (f_ms / 1e3) / 1e9 / hbm, 4)},
+                                     "frac_of_measured_hbm": round(fb / (f_ms / 1e3) / 1e9 / hbm, 4)},
                        "consumer": gemm_roofline(proj_bytes(wl), proj_flops(wl), p_ms, peaks)})
     for z in st:
         capi.swin_wattn_destroy(z["h"])
     tokens = sum(z["T"] for z in st)
     return {"workload": "swin_l224 attention sub-block sweep (B=64 per GPU; per stage LayerNorm + qkv "
-                        "projection, SW-MSA, output projection + bias + residual)",
+                        "projection, SW-MSA, output projection + bias + residual)"
+                        + (" with qkv as OCP FP8 E4M3 between the producer and the attention" if fp8 else ""),
             "steps": steps, "graph_us_per_step": round(graph_ms * 1e3, 2),
             "eager_us_per_step": round(eager_ms * 1e3, 2), "tokens_per_s": ws * tokens / (graph_ms / 1e3),
             "launches_per_step": int(launches_per_step),

@@ -228,6 +228,25 @@ int swin_wattn_qkv_proj_prepared(const void* x, const void* prepared, void* qkv,
                                  struct CUstream_st* stream);
 
 /*
+ * The producer step on prepared weights with OCP FP8 E4M3 output, the input of
+ * swin_wattn_fwd_fp8 (NVIDIA Swin talk, section 3: the inference path takes its GEMMs to 8
+ * bits with scales calibrated ahead of time; here the qkv the attention reads): the same
+ * qkv as swin_wattn_qkv_proj_prepared, in fp32, then for each channel of tensor t (q, k, v)
+ *   qkv8 = E4M3(qkv / scale_t), rounded to nearest even, saturated to +-448;
+ *   qkv8   device, 16-byte aligned: [tokens, 3C] bytes, written (the token layout of qkv);
+ *   scale_q, scale_k, scale_v  one fp32 scale per tensor, finite and positive (static
+ *          scaling: e.g. the calibrated max |qkv_t| / 448);
+ *   amax   optional device float[3] (may be NULL): max |qkv_t| of this call's fp32 values is
+ *          max-ed into amax[t] atomically (the caller zeroes it; a later call can take its
+ *          scales from it: delayed scaling).
+ * Other arguments and errors as for swin_wattn_qkv_proj_prepared (INVALID_ARG also for a bad
+ * scale). One or two launches; nothing is allocated.
+ */
+int swin_wattn_qkv_proj_prepared_fp8(const void* x, const void* prepared, void* qkv8, int tokens, int C, float eps,
+                                     float scale_q, float scale_k, float scale_v, float* amax, void* stats_workspace,
+                                     size_t stats_bytes, int* status, struct CUstream_st* stream);
+
+/*
  * The consumer step after the attention: the output projection, then its bias and the
  * residual added, fused into the product's epilogue (NVIDIA Swin talk, uticex.com article
  * 1598, section 3 "inference optimisation": the bias-plus-residual pass in its half2

@@ -43,6 +43,8 @@ SIGNATURES = {
     "swin_wattn_qkv_stats_bytes": ([_i], ctypes.c_size_t),
     "swin_wattn_qkv_prepare": ([_vp] * 4 + [_i, _vp, ctypes.c_size_t, _vp], _i),
     "swin_wattn_qkv_proj_prepared": ([_vp] * 3 + [_i, _i, ctypes.c_float, _vp, ctypes.c_size_t, _vp, _vp], _i),
+    "swin_wattn_qkv_proj_prepared_fp8": ([_vp] * 3 + [_i, _i] + [ctypes.c_float] * 4 +
+                                         [_vp, _vp, ctypes.c_size_t, _vp, _vp], _i),
     "swin_wattn_proj_residual": ([_vp] * 5 + [_i, _i, _vp, _vp], _i),
     "swin_wattn_fwd_fp8": ([_vp, _vp, ctypes.c_float, ctypes.c_float, ctypes.c_float, _vp, _vp], _i),
     "swin_wattn_set_fwd_kernel": ([_vp, _i], _i),
@@ -227,6 +229,33 @@ class QkvProjection:
         if rc != OK:
             raise SwinWAttnError("swin_wattn_qkv_proj_prepared", rc)
         return qkv
+
+    def fp8(self, x, scales, qkv8=None, amax=None, eps=1e-5, status=None, stream=None):
+        """The same projection with OCP FP8 E4M3 output, qkv8 = E4M3(qkv / scale_t) for the
+        tensor t (q, k, v) of each channel, as a uint8 [..., 3C] tensor (allocated here when
+        not given); amax, an optional CUDA float tensor [3], receives max |qkv_t| (max-ed)."""
+        import torch
+        C = self.C
+        tokens = x.numel() // C
+        if qkv8 is None:
+            qkv8 = torch.empty(x.shape[:-1] + (3 * C,), dtype=torch.uint8, device=x.device)
+        need = max(swin_wattn_qkv_stats_bytes(tokens), 16)
+        if self.stats is None or self.stats.numel() < need:
+            self.stats = torch.empty(need, dtype=torch.uint8, device=x.device)
+        sq, sk, sv = (float(v) for v in scales)
+        rc = swin_wattn_qkv_proj_prepared_fp8(x.data_ptr(), self.prepared.data_ptr(), qkv8.data_ptr(), tokens, C,
+                                              eps, sq, sk, sv, None if amax is None else amax.data_ptr(),
+                                              self.stats.data_ptr(), self.stats.numel(),
+                                              None if status is None else status.data_ptr(), _stream_handle(stream))
+        if rc != OK:
+            raise SwinWAttnError("swin_wattn_qkv_proj_prepared_fp8", rc)
+        return qkv8
+
+
+def swin_wattn_qkv_proj_prepared_fp8(x_ptr, prepared_ptr, qkv8_ptr, tokens, C, eps, scale_q, scale_k, scale_v,
+                                     amax_ptr, stats_ptr, stats_bytes, status_ptr, stream):
+    return load().swin_wattn_qkv_proj_prepared_fp8(x_ptr, prepared_ptr, qkv8_ptr, tokens, C, eps, scale_q, scale_k,
+                                                   scale_v, amax_ptr, stats_ptr, stats_bytes, status_ptr, stream)
 
 
 def swin_wattn_proj_residual(o_ptr, wp_ptr, bp_ptr, residual_ptr, y_ptr, tokens, C, status_ptr, stream):

@@ -38,6 +38,9 @@ cudaError_t qkv_prepare_launch(const float* gamma, const float* beta, const void
 cudaError_t qkv_proj_prepared_launch(const void* x, const void* prepared, void* out, int T, int C, float eps,
                                      void* stats_workspace, int* status, cudaStream_t st);
 int qkv_launches(int T, int C, bool fold);
+cudaError_t qkv_proj_fp8_launch(const void* x, const void* prepared, void* out8, int T, int C, float eps,
+                                const float scales[3], unsigned int* amax, void* stats_workspace, int* status,
+                                cudaStream_t st);
 cudaError_t proj_residual_launch(const void* o, const void* wp, const float* bp, const void* residual, void* y,
                                  int T, int C, int* status, cudaStream_t st);
 cudaError_t bwd_launch(const Plan& pl, const BwdLaunch& L, const void* qkv, const void* dout,
@@ -502,6 +505,35 @@ int swin_wattn_qkv_proj_prepared(const void* x, const void* prepared, void* qkv,
                                                  reinterpret_cast<cudaStream_t>(stream));
   g_launches += swin::qkv_launches(tokens, C, false);
   return e == cudaSuccess ? SWIN_WATTN_OK : cuda_fail(e, "swin_wattn_qkv_proj_prepared");
+}
+
+int swin_wattn_qkv_proj_prepared_fp8(const void* x, const void* prepared, void* qkv8, int tokens, int C, float eps,
+                                     float scale_q, float scale_k, float scale_v, float* amax, void* stats_workspace,
+                                     size_t stats_bytes, int* status, struct CUstream_st* stream) {
+  if (tokens < 0 || !(eps >= 0.0f) || !std::isfinite(eps)) return SWIN_WATTN_ERR_INVALID_ARG;
+  for (const float sc : {scale_q, scale_k, scale_v})
+    if (!(sc > 0.0f) || !std::isfinite(sc) || !std::isfinite(1.0f / sc)) return SWIN_WATTN_ERR_INVALID_ARG;
+  if (C < 32 || C > 1536 || C % 32 != 0) return SWIN_WATTN_ERR_UNSUPPORTED;
+  if ((int64_t)tokens >= ((int64_t)1 << 31)) return SWIN_WATTN_ERR_UNSUPPORTED;
+  if (tokens == 0) return SWIN_WATTN_OK;
+  if (stats_bytes < swin::qkv_stats_bytes(tokens)) {
+    swin::set_last_error("swin_wattn_qkv_proj_prepared_fp8: statistics workspace smaller than "
+                         "swin_wattn_qkv_stats_bytes(tokens)");
+    return SWIN_WATTN_ERR_INVALID_ARG;
+  }
+  int rc;
+  if ((rc = check_device_ptr(x, 16)) != SWIN_WATTN_OK) return rc;
+  if ((rc = check_device_ptr(prepared, 256)) != SWIN_WATTN_OK) return rc;
+  if ((rc = check_device_ptr(qkv8, 16)) != SWIN_WATTN_OK) return rc;
+  if ((rc = check_device_ptr(stats_workspace, 16)) != SWIN_WATTN_OK) return rc;
+  if (amax != nullptr && (rc = check_device_ptr(amax, 4)) != SWIN_WATTN_OK) return rc;
+  if (status != nullptr && (rc = check_device_ptr(status, 4)) != SWIN_WATTN_OK) return rc;
+  const float scales[3] = {scale_q, scale_k, scale_v};
+  cudaError_t e = swin::qkv_proj_fp8_launch(x, prepared, qkv8, tokens, C, eps, scales,
+                                            reinterpret_cast<unsigned int*>(amax), stats_workspace, status,
+                                            reinterpret_cast<cudaStream_t>(stream));
+  g_launches += swin::qkv_launches(tokens, C, false);
+  return e == cudaSuccess ? SWIN_WATTN_OK : cuda_fail(e, "swin_wattn_qkv_proj_prepared_fp8");
 }
 
 int swin_wattn_proj_residual(const void* o, const void* w_proj, const float* b_proj, const void* residual,

@@ -118,6 +118,10 @@ struct GemmParams {
   int* status;                     // optional: bit 0 set when a bounded wait ran out
   uint64_t wait_ns;                // bound of each wait
   int fault;                       // armed fault site (fault-injection build only)
+  // producer with 8-bit output: 1 / scale of q, k and v (output channel n belongs to
+  // tensor n / K), and the optional per-tensor max |value| (float bits, atomically max-ed)
+  float f8_inv[3];
+  unsigned int* f8_amax;
   int T, K, N, NT, tiles_per_item, n_tt, n_items;
   int stages, stage_bytes;  // the ring: stages x (x chunk + NT x 128 bytes), 1024-byte multiples
   int off_stats, off_out, off_bar;
@@ -128,10 +132,18 @@ __device__ __forceinline__ bool warp_wait(uint32_t mbar, uint32_t parity, uint64
   return __all_sync(0xffffffffu, tc::mbar_wait(mbar, parity, limit_ns)) != 0;
 }
 
+// Two fp32 values rounded to OCP FP8 E4M3 (nearest even, saturated to +-448): `lo` in the
+// low byte.
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;\n" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
-template <int MODE>
+template <int MODE, bool F8>
 __global__ void __launch_bounds__(Roles<MODE>::kTHREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_constant__ CUtensorMap w_map,
                 const __grid_constant__ CUtensorMap out_map, const __grid_constant__ CUtensorMap res_map,
@@ -421,6 +433,11 @@ __global__ void __launch_bounds__(Roles<MODE>::kTHREADS, 1)
             if (lane == 0) tc::bulk_wait_read<NB - 1>();  // the store of slice m - NB has read its tile
             __syncwarp();
           }
+          // 8-bit output: this slice's tensor scale, the row's max |value|, packed words
+          [[maybe_unused]] const int f8t = (n0 + c0) / p.K;
+          [[maybe_unused]] const float f8inv = f8t == 0 ? p.f8_inv[0] : (f8t == 1 ? p.f8_inv[1] : p.f8_inv[2]);
+          [[maybe_unused]] float f8max = 0.0f;
+          [[maybe_unused]] uint32_t f8w[4];
           const float4* u4s = MODE == kLnPrepStats ? reinterpret_cast<const float4*>(p.u + n0 + c0)
                                                    : reinterpret_cast<const float4*>(wuv + 64 * si);
           const float4* v4s = MODE == kLnPrepStats ? reinterpret_cast<const float4*>(p.v + n0 + c0) : u4s + 8;
@@ -459,9 +476,31 @@ __global__ void __launch_bounds__(Roles<MODE>::kTHREADS, 1)
               } else {
                 y = __ffma2_rn(a0, r2, __ffma2_rn(nm2, make_float2(uu[2 * q], uu[2 * q + 1]), v2));
               }
-              o[q] = pack_bf16(y.x, y.y);
+              if constexpr (F8) {
+                f8max = fmax3(f8max, fabsf(y.x), fabsf(y.y));
+                const float2 z = __fmul2_rn(y, make_float2(f8inv, f8inv));
+                o[q] = e4m3x2(z.x, z.y);  // channels 8c + 2q, +1 as two bytes
+              } else {
+                o[q] = pack_bf16(y.x, y.y);
+              }
             }
-            *sp = make_uint4(o[0], o[1], o[2], o[3]);
+            if constexpr (F8) {
+              // 8 bytes of this row: its 32-byte row holds 16-byte chunk c >> 1 at position
+              // (c >> 1) ^ ((row >> 2) & 1) (the copy engine's 32-byte swizzle)
+              f8w[2 * (c & 1)] = o[0] | (o[1] << 16);
+              f8w[2 * (c & 1) + 1] = o[2] | (o[3] << 16);
+              if (c & 1)
+                *reinterpret_cast<uint4*>(so + lane * 32 + (((c >> 1) ^ ((lane >> 2) & 1)) << 4)) =
+                    make_uint4(f8w[0], f8w[1], f8w[2], f8w[3]);
+            } else {
+              *sp = make_uint4(o[0], o[1], o[2], o[3]);
+            }
+          }
+          if constexpr (F8) {
+            if (p.f8_amax != nullptr) {
+              const unsigned int mx = __reduce_max_sync(0xffffffffu, __float_as_uint(f8max));
+              if (lane == 0) atomicMax(p.f8_amax + f8t, mx);
+            }
           }
           tc::fence_proxy_async();  // the staging tile to the copy engine
           __syncwarp();
@@ -648,19 +687,24 @@ cudaError_t plan_items(int T, int N, ItemPlan* ip) {
   return cudaSuccess;
 }
 
+// A row-major [outer, inner] tensor of bf16 (or of bytes with `bytes`) for the copy engine.
 cudaError_t encode_2d(PFN_cuTensorMapEncodeTiled_v12000 encode, CUtensorMap* map, const void* base, int inner,
-                      int outer, int box_inner, int box_outer, CUtensorMapSwizzle swz, CUtensorMapL2promotion l2) {
+                      int outer, int box_inner, int box_outer, CUtensorMapSwizzle swz, CUtensorMapL2promotion l2,
+                      bool bytes = false) {
   const cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
-  const cuuint64_t strides[1] = {(cuuint64_t)inner * 2};
+  const cuuint64_t strides[1] = {(cuuint64_t)inner * (bytes ? 1 : 2)};
   const cuuint32_t box[2] = {(cuuint32_t)box_inner, (cuuint32_t)box_outer};
   const cuuint32_t es[2] = {1, 1};
-  return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
-                CU_TENSOR_MAP_INTERLEAVE_NONE, swz, l2, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS
+  return encode(map, bytes ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, l2,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS
              ? cudaSuccess
              : cudaErrorInvalidValue;
 }
 
-template <int MODE>
+// F8: the producer's output is OCP FP8 E4M3 bytes [T, N] (32-byte-swizzled staging tiles of
+// 32 rows x 32 channels, stored by the copy engine).
+template <int MODE, bool F8 = false>
 cudaError_t launch_gemm(const ItemPlan& ip, GemmParams p, const void* a, const void* w, cudaStream_t st,
                         const void* residual = nullptr) {
   PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder_fn();
@@ -672,8 +716,8 @@ cudaError_t launch_gemm(const ItemPlan& ip, GemmParams p, const void* a, const v
     e = encode_2d(encode, &w_map, w, p.K, p.N, kKC, ip.NT, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
   if (e == cudaSuccess)
-    e = encode_2d(encode, &out_map, p.out, p.N, p.T, kSC, 32, CU_TENSOR_MAP_SWIZZLE_64B,
-                  CU_TENSOR_MAP_L2_PROMOTION_NONE);
+    e = encode_2d(encode, &out_map, p.out, p.N, p.T, kSC, 32, F8 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_64B,
+                  CU_TENSOR_MAP_L2_PROMOTION_NONE, F8);
   CUtensorMap res_map = out_map;  // read only by the consumer
   if (e == cudaSuccess && residual != nullptr)
     e = encode_2d(encode, &res_map, residual, p.N, p.T, kSC, 32, CU_TENSOR_MAP_SWIZZLE_64B,
@@ -692,10 +736,10 @@ cudaError_t launch_gemm(const ItemPlan& ip, GemmParams p, const void* a, const v
   p.off_out = p.off_stats + kStatsBytes;
   p.off_bar = p.off_out + out_bytes<MODE>();
   const int smem = std::max(kMinSMEM, p.stages * p.stage_bytes + fixed);
-  e = cudaFuncSetAttribute(gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  e = cudaFuncSetAttribute(gemm_kernel<MODE, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(gemm_kernel<MODE>, dim3(std::min(ip.n_items, ip.sms)), dim3(Roles<MODE>::kTHREADS), smem, st,
-                    a_map, w_map, out_map, res_map, p);
+  return launch_pdl(gemm_kernel<MODE, F8>, dim3(std::min(ip.n_items, ip.sms)), dim3(Roles<MODE>::kTHREADS), smem,
+                    st, a_map, w_map, out_map, res_map, p);
 }
 
 GemmParams base_params(void* out, int T, int K, int N, int* status) {
@@ -734,7 +778,7 @@ Prepared prepared_parts(void* prepared, int C) {
 // on chip) in one launch, then the product.
 cudaError_t qkv_run(const void* x, const float* gamma, const float* beta, const void* w, const float* b,
                     const Prepared& pw, float2* stats, void* out, int T, int C, float eps, int* status,
-                    cudaStream_t st) {
+                    cudaStream_t st, const float* f8_scales = nullptr, unsigned int* f8_amax = nullptr) {
   const int N = 3 * C;
   ItemPlan ip;
   cudaError_t e = plan_items(T, N, &ip);
@@ -752,6 +796,13 @@ cudaError_t qkv_run(const void* x, const float* gamma, const float* beta, const 
   p.u = pw.u;
   p.v = pw.v;
   p.eps = eps;
+  if (f8_scales != nullptr) {
+    for (int t = 0; t < 3; ++t) p.f8_inv[t] = 1.0f / f8_scales[t];
+    p.f8_amax = f8_amax;
+    if (chip_stats) return launch_gemm<kLnChipStats, true>(ip, p, x, pw.wf, st);
+    p.stats = stats;
+    return launch_gemm<kLnPrepStats, true>(ip, p, x, pw.wf, st);
+  }
   if (chip_stats) return launch_gemm<kLnChipStats>(ip, p, x, pw.wf, st);
   p.stats = stats;
   return launch_gemm<kLnPrepStats>(ip, p, x, pw.wf, st);
@@ -787,6 +838,17 @@ cudaError_t qkv_proj_prepared_launch(const void* x, const void* prepared, void* 
   if (C % 32 != 0 || C < 32 || C > kMaxC) return cudaErrorInvalidValue;
   return qkv_run(x, nullptr, nullptr, nullptr, nullptr, prepared_parts(const_cast<void*>(prepared), C),
                  static_cast<float2*>(stats_workspace), out, T, C, eps, status, st);
+}
+
+// Producer on prepared weights with OCP FP8 E4M3 output: qkv8 = satfinite(qkv / scale_t)
+// for the tensor t (q, k, v) of each channel, and optionally max |qkv_t| into amax[t].
+cudaError_t qkv_proj_fp8_launch(const void* x, const void* prepared, void* out8, int T, int C, float eps,
+                                const float scales[3], unsigned int* amax, void* stats_workspace, int* status,
+                                cudaStream_t st) {
+  if (T <= 0) return cudaSuccess;
+  if (C % 32 != 0 || C < 32 || C > kMaxC) return cudaErrorInvalidValue;
+  return qkv_run(x, nullptr, nullptr, nullptr, nullptr, prepared_parts(const_cast<void*>(prepared), C),
+                 static_cast<float2*>(stats_workspace), out8, T, C, eps, status, st, scales, amax);
 }
 
 // Launches of one producer call for T tokens of C channels with or without the fold.
