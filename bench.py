@@ -806,7 +806,8 @@ def kernel_name(capi, h):
 
 
 def make_plan(capi, wl, tab, sh, args):
-    """A bf16 plan for the workload, with the forward kernel --fwd-kernel asks for."""
+    """A bf16 plan for the workload, with the forward (and, for a training workload, the
+    backward) kernel that --fwd-kernel / --bwd-kernel ask for."""
     rc, h = capi.swin_wattn_plan(wl.B, wl.H, wl.W, wl.C, wl.nH, wl.M, wl.s, capi.BF16,
                                  tab.data_ptr(), sh)
     if rc != capi.OK:
@@ -816,6 +817,11 @@ def make_plan(capi, wl, tab, sh, args):
         rc = capi.swin_wattn_set_fwd_kernel(h, kernel)
         if rc != capi.OK:
             raise capi.SwinWAttnError("swin_wattn_set_fwd_kernel", rc)
+    kernel = FWD_KERNELS[getattr(args, "bwd_kernel", "auto")]
+    if kernel != 0 and wl.bwd:
+        rc = capi.swin_wattn_set_bwd_kernel(h, kernel)
+        if rc != capi.OK:
+            raise capi.SwinWAttnError("swin_wattn_set_bwd_kernel", rc)
     return h
 
 
@@ -881,6 +887,7 @@ def run_bwd_only(args):
     dev = torch.device("cuda", 0)
     att = capi.WindowAttention(wl.B, wl.H, wl.W, wl.C, wl.nH, wl.M, wl.s,
                                inputs.make_table(wl).to(dev))
+    att.set_bwd_kernel(FWD_KERNELS[args.bwd_kernel])
     q, d = inputs.make_qkv(wl).to(dev), inputs.make_dout(wl).to(dev)
     dq, dt = torch.empty_like(q), torch.empty((2 * wl.M - 1) ** 2, wl.nH, device=dev)
     for _ in range(args.warmup):
@@ -893,7 +900,7 @@ def run_bwd_only(args):
     b.record()
     torch.cuda.synchronize()
     ms = a.elapsed_time(b) / args.steps
-    print(json.dumps({"workload": wl.name, "bwd_us": ms * 1e3,
+    print(json.dumps({"workload": wl.name, "bwd_us": ms * 1e3, "bwd_kernel": att.bwd_kernel,
                       "frac_of_measured_hbm": bwd_bytes(wl) / (ms / 1e3) / 1e9 / load_peaks()[0]["hbm_gbs"]}))
     att.close()
 
@@ -954,6 +961,8 @@ def main():
                     help="profiling run: only the forward on FP8 operands of this workload, a few launches")
     ap.add_argument("--gemm-workload", choices=sorted(inputs.BY_NAME),
                     help="profiling run: only the producer and consumer of this workload, a few launches")
+    ap.add_argument("--bwd-kernel", default="auto", choices=sorted(FWD_KERNELS),
+                    help="backward kernel of the plans (training step and --bwd-workload runs)")
     ap.add_argument("--fwd-kernel", default="auto", choices=sorted(FWD_KERNELS),
                     help="forward kernel of every plan (auto: the library's default)")
     ap.add_argument("--skip-train", action="store_true")

@@ -300,6 +300,18 @@ int swin_wattn_set_fwd_kernel(swin_wattn_plan_t plan, int kernel);
 int swin_wattn_fwd_kernel(swin_wattn_plan_t plan);
 
 /*
+ * Choose the plan's backward kernel (SWIN_WATTN_KERNEL_*): MMA_SYNC (window 4 or 7, both
+ * dtypes) or TCGEN05 (the tensor-memory kernel: window 7, bf16). Both compute the same
+ * gradients to the same tolerance and are deterministic; AUTO is the default (MMA_SYNC).
+ * UNSUPPORTED where the choice does not apply (the plan is then unchanged). Host-side only;
+ * call it between launches.
+ */
+int swin_wattn_set_bwd_kernel(swin_wattn_plan_t plan, int kernel);
+
+/* The backward kernel the plan launches (MMA_SYNC or TCGEN05), or -1 for a bad handle. */
+int swin_wattn_bwd_kernel(swin_wattn_plan_t plan);
+
+/*
  * Synchronise `stream` and report the plan's device error word: SWIN_WATTN_ERR_TIMEOUT
  * if a kernel's bounded wait on the tensor core (1 s) ran out since the last call, in
  * which case that launch's output is not valid; the word is cleared. Otherwise OK.

@@ -49,6 +49,8 @@ SIGNATURES = {
     "swin_wattn_fwd_fp8": ([_vp, _vp, ctypes.c_float, ctypes.c_float, ctypes.c_float, _vp, _vp], _i),
     "swin_wattn_set_fwd_kernel": ([_vp, _i], _i),
     "swin_wattn_fwd_kernel": ([_vp], _i),
+    "swin_wattn_set_bwd_kernel": ([_vp, _i], _i),
+    "swin_wattn_bwd_kernel": ([_vp], _i),
     "swin_wattn_device_status": ([_vp, _vp], _i),
     "swin_wattn_destroy": ([_vp], _i),
     "swin_wattn_status_string": ([_i], _cp),
@@ -291,6 +293,14 @@ def swin_wattn_fwd_kernel(plan):
     return load().swin_wattn_fwd_kernel(plan)
 
 
+def swin_wattn_set_bwd_kernel(plan, kernel):
+    return load().swin_wattn_set_bwd_kernel(plan, kernel)
+
+
+def swin_wattn_bwd_kernel(plan):
+    return load().swin_wattn_bwd_kernel(plan)
+
+
 def swin_wattn_device_status(plan, stream):
     return load().swin_wattn_device_status(plan, stream)
 
@@ -347,6 +357,16 @@ class WindowAttention:
     @property
     def fwd_kernel(self):
         return swin_wattn_fwd_kernel(self.handle)
+
+    def set_bwd_kernel(self, kernel):
+        """KERNEL_AUTO, KERNEL_MMA_SYNC or KERNEL_TCGEN05 for later backwards."""
+        rc = swin_wattn_set_bwd_kernel(self.handle, kernel)
+        if rc != OK:
+            raise SwinWAttnError("swin_wattn_set_bwd_kernel", rc)
+
+    @property
+    def bwd_kernel(self):
+        return swin_wattn_bwd_kernel(self.handle)
 
     def device_status(self, stream=None):
         """Synchronise and raise if a bounded device wait ran out since the last check."""

@@ -523,6 +523,16 @@ __global__ void dtable_reduce_kernel(const float* __restrict__ partial, int R, i
 
 // ---- host side ---------------------------------------------------------------------
 
+cudaError_t launch_dtable_reduce(const float* partial, int R, int nH, int chunks, float* dtable, cudaStream_t st) {
+  dtable_reduce_kernel<<<(R * nH + 255) / 256, 256, 0, st>>>(partial, R, nH, chunks, dtable);
+  return cudaGetLastError();
+}
+
+bool bwd_tc_applies(const Plan& pl);
+cudaError_t bwd_tc_config(const Plan& pl, BwdLaunch* L);
+cudaError_t bwd_tc_launch(const Plan& pl, const BwdLaunch& L, const void* qkv, const void* dout, void* dqkv,
+                          float* dtable, cudaStream_t st);
+
 template <int M> struct BwdStages { static constexpr int value = 2; };
 
 template <int M, typename TIO, int STAGES>
@@ -579,7 +589,11 @@ static cudaError_t blaunch_t(const Plan& pl, const BwdLaunch& L, const void* qkv
   return cudaGetLastError();
 }
 
+// Kernel choice: the tcgen05 kernel when the plan asks for it (7x7 windows, bf16), else
+// the mma.sync kernel.
 cudaError_t bwd_config(const Plan& pl, BwdLaunch* L) {
+  *L = BwdLaunch();
+  if (pl.bwd_kernel == SWIN_WATTN_KERNEL_TCGEN05) return bwd_tc_applies(pl) ? bwd_tc_config(pl, L) : cudaErrorNotSupported;
   const bool f32 = pl.dtype == SWIN_WATTN_FP32;
   switch (pl.M) {
     case 4:
@@ -596,6 +610,7 @@ cudaError_t bwd_config(const Plan& pl, BwdLaunch* L) {
 
 cudaError_t bwd_launch(const Plan& pl, const BwdLaunch& L, const void* qkv, const void* dout,
                        void* dqkv, float* dtable, cudaStream_t st) {
+  if (L.tc) return bwd_tc_launch(pl, L, qkv, dout, dqkv, dtable, st);
   const bool f32 = pl.dtype == SWIN_WATTN_FP32;
   switch (pl.M) {
     case 4:

@@ -28,6 +28,8 @@ cudaError_t fwd_launch(const Plan& pl, const FwdLaunch& L, const void* qkv, void
 cudaError_t fwd_launch_batch(const Plan& pl, const FwdLaunch& L, const void* qkv, void* out,
                              int batch, cudaStream_t st);
 cudaError_t bwd_config(const Plan& pl, BwdLaunch* L);
+bool bwd_tc_applies(const Plan& pl);
+cudaError_t bwd_tc_config(const Plan& pl, BwdLaunch* L);
 cudaError_t qkv_proj_launch(const void* x, const float* gamma, const float* beta, const void* w, const float* b,
                             void* out, int T, int C, float eps, void* workspace, int* status, cudaStream_t st);
 size_t qkv_workspace_bytes(int C, int64_t T);
@@ -232,8 +234,15 @@ int swin_wattn_plan(swin_wattn_plan_t* out, int B, int H, int W, int C, int num_
 
   if (e == cudaSuccess) e = swin::fwd_config(p, &pl->fwd);
   if (e == cudaSuccess) e = swin::bwd_config(p, &pl->bwd);
-  if (e == cudaSuccess && pl->bwd.partial_rows > 0) {
-    p.dt_partial_rows = pl->bwd.partial_rows;
+  // the table-gradient partials, sized for either backward kernel (the choice may change)
+  int partial_rows = pl->bwd.partial_rows;
+  if (e == cudaSuccess && swin::bwd_tc_applies(p)) {
+    swin::BwdLaunch Lt;
+    e = swin::bwd_tc_config(p, &Lt);
+    if (e == cudaSuccess && Lt.partial_rows > partial_rows) partial_rows = Lt.partial_rows;
+  }
+  if (e == cudaSuccess && partial_rows > 0) {
+    p.dt_partial_rows = partial_rows;
     e = cudaMalloc(&p.dt_partial, sizeof(float) * (size_t)p.dt_partial_rows * (2 * p.M - 1) *
                                       (2 * p.M - 1));
   }
@@ -280,9 +289,9 @@ int swin_wattn_set_bias(swin_wattn_plan_t plan, const float* bias_table,
 
 // The tcgen05 forward's constant tables, rebuilt from the dense bias on `st` when the bias
 // changed since they were last built.
-static cudaError_t ensure_tc_tables(swin_wattn_plan_s* plan, cudaStream_t st) {
+static cudaError_t ensure_tc_tables(swin_wattn_plan_s* plan, cudaStream_t st, bool for_bwd = false) {
   swin::Plan& p = plan->p;
-  if (!plan->fwd.tc || !p.tc_stale) return cudaSuccess;
+  if (!(for_bwd ? plan->bwd.tc : plan->fwd.tc) || !p.tc_stale) return cudaSuccess;
   const cudaError_t e = swin::launch_tc_tables(p, st);
   ++g_launches;
   if (e == cudaSuccess) p.tc_stale = false;
@@ -394,7 +403,8 @@ int swin_wattn_bwd(swin_wattn_plan_t plan, const void* qkv, const void* dout, vo
   if ((rc = check_device_ptr(qkv, 16)) != SWIN_WATTN_OK) return rc;
   if ((rc = check_device_ptr(dout, 16)) != SWIN_WATTN_OK) return rc;
   if ((rc = check_device_ptr(dqkv, 16)) != SWIN_WATTN_OK) return rc;
-  cudaError_t e = swin::bwd_launch(p, plan->bwd, qkv, dout, dqkv, dtable, st);
+  cudaError_t e = ensure_tc_tables(plan, st, true);
+  if (e == cudaSuccess) e = swin::bwd_launch(p, plan->bwd, qkv, dout, dqkv, dtable, st);
   g_launches += 2;
   return e == cudaSuccess ? SWIN_WATTN_OK : cuda_fail(e, "swin_wattn_bwd");
 }
@@ -587,6 +597,34 @@ int swin_wattn_set_fwd_kernel(swin_wattn_plan_t plan, int kernel) {
 int swin_wattn_fwd_kernel(swin_wattn_plan_t plan) {
   if (check_plan(plan) != SWIN_WATTN_OK) return -1;
   return plan->fwd.tc ? SWIN_WATTN_KERNEL_TCGEN05 : SWIN_WATTN_KERNEL_MMA_SYNC;
+}
+
+int swin_wattn_set_bwd_kernel(swin_wattn_plan_t plan, int kernel) {
+  int rc = check_plan(plan);
+  if (rc != SWIN_WATTN_OK) return rc;
+  if (kernel != SWIN_WATTN_KERNEL_AUTO && kernel != SWIN_WATTN_KERNEL_MMA_SYNC &&
+      kernel != SWIN_WATTN_KERNEL_TCGEN05)
+    return SWIN_WATTN_ERR_INVALID_ARG;
+  swin::Plan& p = plan->p;
+  const int old = p.bwd_kernel;
+  p.bwd_kernel = kernel;
+  swin::BwdLaunch L;
+  cudaError_t e = swin::bwd_config(p, &L);
+  if (e == cudaErrorNotSupported || (e == cudaSuccess && L.grid == 0 && p.B > 0)) {
+    p.bwd_kernel = old;
+    return SWIN_WATTN_ERR_UNSUPPORTED;
+  }
+  if (e != cudaSuccess) {
+    p.bwd_kernel = old;
+    return cuda_fail(e, "swin_wattn_set_bwd_kernel");
+  }
+  plan->bwd = L;
+  return SWIN_WATTN_OK;
+}
+
+int swin_wattn_bwd_kernel(swin_wattn_plan_t plan) {
+  if (check_plan(plan) != SWIN_WATTN_OK) return -1;
+  return plan->bwd.tc ? SWIN_WATTN_KERNEL_TCGEN05 : SWIN_WATTN_KERNEL_MMA_SYNC;
 }
 
 int swin_wattn_device_status(swin_wattn_plan_t plan, struct CUstream_st* stream) {

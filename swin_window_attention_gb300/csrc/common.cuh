@@ -42,8 +42,9 @@ struct Plan {
   // Device error word written by kernels with bounded waits (bit 0: a wait ran out).
   // Owned.
   int* err;
-  // Forward kernel request: SWIN_WATTN_KERNEL_AUTO, _MMA_SYNC or _TCGEN05.
+  // Forward and backward kernel requests: SWIN_WATTN_KERNEL_AUTO, _MMA_SYNC or _TCGEN05.
   int fwd_kernel;
+  int bwd_kernel;
 };
 
 // ---- bounded waits and the fault-injection build ---------------------------------
@@ -324,6 +325,7 @@ struct FwdLaunch {
 };
 struct BwdLaunch {
   int grid = 0, threads = 0, smem = 0, chunks = 0, partial_rows = 0;
+  bool tc = false;  // the tcgen05 kernel (bwd_tc.cu) rather than the mma.sync one
 };
 
 }  // namespace swin

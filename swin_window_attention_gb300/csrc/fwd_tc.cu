@@ -533,11 +533,18 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder_fn() {
 //           wraps at the bottom border only.
 cudaError_t make_qkv_maps(const Plan& pl, const void* qkv, int batch, CUtensorMap* gather, CUtensorMap* box,
                           CUtensorMap* top, CUtensorMap* bot) {
+  return make_act_maps(pl, qkv, batch, 3 * pl.C, gather, box, top, bot);
+}
+
+// The same maps for any [batch, H, W, channels] bf16 activation (qkv: 3C; dO: C).
+cudaError_t make_act_maps(const Plan& pl, const void* act, int batch, int channels, CUtensorMap* gather,
+                          CUtensorMap* box, CUtensorMap* top, CUtensorMap* bot) {
   PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder_fn();
   if (encode == nullptr) return cudaErrorNotSupported;
+  const void* qkv = act;
   const int64_t tokens = (int64_t)batch * pl.H * pl.W;
-  const cuuint64_t row = (cuuint64_t)(3 * pl.C) * 2;
-  const cuuint64_t dims[2] = {(cuuint64_t)(3 * pl.C), (cuuint64_t)tokens};
+  const cuuint64_t row = (cuuint64_t)channels * 2;
+  const cuuint64_t dims[2] = {(cuuint64_t)channels, (cuuint64_t)tokens};
   const cuuint64_t strides[1] = {row};
   const cuuint32_t gbox[2] = {kHeadDim, 1};
   const cuuint32_t estride[4] = {1, 1, 1, 1};
@@ -545,7 +552,7 @@ cudaError_t make_qkv_maps(const Plan& pl, const void* qkv, int batch, CUtensorMa
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
-  const cuuint64_t bdims[4] = {(cuuint64_t)(3 * pl.C), (cuuint64_t)pl.W, (cuuint64_t)pl.H, (cuuint64_t)batch};
+  const cuuint64_t bdims[4] = {(cuuint64_t)channels, (cuuint64_t)pl.W, (cuuint64_t)pl.H, (cuuint64_t)batch};
   const cuuint64_t bstrides[3] = {row, row * pl.W, row * pl.W * pl.H};
   const cuuint32_t heights[3] = {kTM, (cuuint32_t)(pl.s > 0 ? kTM - pl.s : kTM), (cuuint32_t)(pl.s > 0 ? pl.s : kTM)};
   CUtensorMap* maps[3] = {box, top, bot};

@@ -27,11 +27,15 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t 
          ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | ((uint64_t)1 << 46) | ((uint64_t)layout << 61);
 }
 
+// The descriptor of the same layout `bytes` further on (a multiple of 16): the start address
+// field is added to in place, so the address must stay below 2^18 (all of shared memory).
+__device__ __forceinline__ uint64_t desc_add(uint64_t desc, uint32_t bytes) { return desc + (bytes >> 4); }
+
 // Instruction descriptor of kind::f16 with bf16 A and B and an fp32 accumulator:
 // [4,6) D format (1 = f32), [7,10) A format (1 = bf16), [10,13) B format, bit 15 A
 // MN-major, bit 16 B MN-major, [17,23) N >> 3, [24,29) M >> 4.
-__host__ __device__ constexpr uint32_t idesc_bf16(int m, int n, bool b_mn_major) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
+__host__ __device__ constexpr uint32_t idesc_bf16(int m, int n, bool b_mn_major, bool a_mn_major = false) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
          ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
 
@@ -261,6 +265,61 @@ __device__ __forceinline__ void ld32_1_wait(uint32_t a_addr, uint32_t c_addr, ui
       : "memory");
 }
 
+// Loads without the wait, for several loads in flight at once: each must be followed by
+// wait_ld_then() (once) and a dep32 / dep16 / dep1 on every destination array, in that
+// order (volatile statements keep their order; the dependencies keep every use of the
+// registers after the wait).
+__device__ __forceinline__ void ld32_nowait(uint32_t taddr, uint32_t (&a)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
+      : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3]), "=r"(a[4]), "=r"(a[5]), "=r"(a[6]), "=r"(a[7]),
+        "=r"(a[8]), "=r"(a[9]), "=r"(a[10]), "=r"(a[11]), "=r"(a[12]), "=r"(a[13]), "=r"(a[14]), "=r"(a[15]),
+        "=r"(a[16]), "=r"(a[17]), "=r"(a[18]), "=r"(a[19]), "=r"(a[20]), "=r"(a[21]), "=r"(a[22]), "=r"(a[23]),
+        "=r"(a[24]), "=r"(a[25]), "=r"(a[26]), "=r"(a[27]), "=r"(a[28]), "=r"(a[29]), "=r"(a[30]), "=r"(a[31])
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void ld16_nowait(uint32_t taddr, uint32_t (&a)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n"
+      : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3]), "=r"(a[4]), "=r"(a[5]), "=r"(a[6]), "=r"(a[7]),
+        "=r"(a[8]), "=r"(a[9]), "=r"(a[10]), "=r"(a[11]), "=r"(a[12]), "=r"(a[13]), "=r"(a[14]), "=r"(a[15])
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void ld1_nowait(uint32_t taddr, uint32_t& a) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];\n" : "=r"(a) : "r"(taddr) : "memory");
+}
+__device__ __forceinline__ void wait_ld_then() { asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory"); }
+__device__ __forceinline__ void dep32(uint32_t (&a)[32]) {
+  asm volatile(""
+               : "+r"(a[0]), "+r"(a[1]), "+r"(a[2]), "+r"(a[3]), "+r"(a[4]), "+r"(a[5]), "+r"(a[6]), "+r"(a[7]),
+                 "+r"(a[8]), "+r"(a[9]), "+r"(a[10]), "+r"(a[11]), "+r"(a[12]), "+r"(a[13]), "+r"(a[14]),
+                 "+r"(a[15]), "+r"(a[16]), "+r"(a[17]), "+r"(a[18]), "+r"(a[19]), "+r"(a[20]), "+r"(a[21]),
+                 "+r"(a[22]), "+r"(a[23]), "+r"(a[24]), "+r"(a[25]), "+r"(a[26]), "+r"(a[27]), "+r"(a[28]),
+                 "+r"(a[29]), "+r"(a[30]), "+r"(a[31])::"memory");
+}
+__device__ __forceinline__ void dep16(uint32_t (&a)[16]) {
+  asm volatile(""
+               : "+r"(a[0]), "+r"(a[1]), "+r"(a[2]), "+r"(a[3]), "+r"(a[4]), "+r"(a[5]), "+r"(a[6]), "+r"(a[7]),
+                 "+r"(a[8]), "+r"(a[9]), "+r"(a[10]), "+r"(a[11]), "+r"(a[12]), "+r"(a[13]), "+r"(a[14]),
+                 "+r"(a[15])::"memory");
+}
+__device__ __forceinline__ void dep1(uint32_t& a) { asm volatile("" : "+r"(a)::"memory"); }
+
+// Warpgroup register reallocation (all four warps of the warpgroup execute it): the
+// warps' per-thread register limit becomes N (a multiple of 8 in [24, 256]). The sum over
+// the CTA must stay within the registers the CTA was launched with.
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(N));
+}
+
 // ---- registers -> tensor memory ---------------------------------------------------
 
 __device__ __forceinline__ void st_x32(uint32_t taddr, const uint32_t (&r)[32]) {
@@ -283,5 +342,7 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder_fn();
 // Tensor maps of a q/k/v tensor for the copy engine (fwd_tc.cu).
 cudaError_t make_qkv_maps(const Plan& pl, const void* qkv, int batch, CUtensorMap* gather, CUtensorMap* box,
                           CUtensorMap* top, CUtensorMap* bot);
+cudaError_t make_act_maps(const Plan& pl, const void* act, int batch, int channels, CUtensorMap* gather,
+                          CUtensorMap* box, CUtensorMap* top, CUtensorMap* bot);
 
 }  // namespace swin
