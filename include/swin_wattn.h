@@ -69,9 +69,9 @@ enum swin_wattn_status {
 
 enum swin_wattn_dtype { SWIN_WATTN_BF16 = 0, SWIN_WATTN_FP32 = 1 };
 
-/* Forward kernels (swin_wattn_set_fwd_kernel). */
+/* Forward and backward kernels (swin_wattn_set_fwd_kernel, swin_wattn_set_bwd_kernel). */
 enum swin_wattn_kernel {
-  SWIN_WATTN_KERNEL_AUTO = 0,      /* the faster kernel as measured: mma.sync (default) */
+  SWIN_WATTN_KERNEL_AUTO = 0,      /* the faster kernel as measured (see the setters below) */
   SWIN_WATTN_KERNEL_MMA_SYNC = 1,  /* warp-level mma.sync kernel: every M, both dtypes */
   SWIN_WATTN_KERNEL_TCGEN05 = 2    /* tensor-memory kernel: M = 7 with bf16 only */
 };
@@ -143,9 +143,10 @@ int swin_wattn_bwd(swin_wattn_plan_t plan, const void* qkv, const void* dout, vo
  * later cudaMalloc, or frameworks whose own allocator must own every device byte; such
  * callers cannot create a plan, because a plan allocates).
  *
- * Same arguments and results as swin_wattn_plan followed by swin_wattn_bwd (qkv, dout,
- * dqkv, dtable and the bias table are the caller's device buffers; window must be 4 or
- * 7), but no plan is made and nothing is allocated or freed: the working memory (bias
+ * Same arguments and results as swin_wattn_plan followed by swin_wattn_bwd with the
+ * MMA_SYNC backward kernel (qkv, dout, dqkv, dtable and the bias table are the caller's
+ * device buffers; window must be 4 or 7), but no plan is made and nothing is allocated or
+ * freed: the working memory (bias
  * fragments, mask bits, per-CTA table-gradient partials) lives in one fixed 2 MiB
  * device array inside the library, which every GPU that loads the library holds until
  * the process exits. A shape whose working memory exceeds 2 MiB is refused with
@@ -291,7 +292,8 @@ int swin_wattn_fwd_fp8(swin_wattn_plan_t plan, const void* qkv8, float scale_q, 
 
 /*
  * Choose the plan's forward kernel (SWIN_WATTN_KERNEL_*). Both kernels compute the same
- * function to the same tolerance; AUTO is the default. Asking for TCGEN05 where it does not apply returns SWIN_WATTN_ERR_UNSUPPORTED
+ * function to the same tolerance; AUTO, the default, is MMA_SYNC (measured faster for the
+ * forward). Asking for TCGEN05 where it does not apply returns SWIN_WATTN_ERR_UNSUPPORTED
  * and leaves the plan unchanged. Host-side only; call it between launches.
  */
 int swin_wattn_set_fwd_kernel(swin_wattn_plan_t plan, int kernel);
@@ -302,9 +304,11 @@ int swin_wattn_fwd_kernel(swin_wattn_plan_t plan);
 /*
  * Choose the plan's backward kernel (SWIN_WATTN_KERNEL_*): MMA_SYNC (window 4 or 7, both
  * dtypes) or TCGEN05 (the tensor-memory kernel: window 7, bf16). Both compute the same
- * gradients to the same tolerance and are deterministic; AUTO is the default (MMA_SYNC).
- * UNSUPPORTED where the choice does not apply (the plan is then unchanged). Host-side only;
- * call it between launches.
+ * gradients to the same tolerance and are deterministic. AUTO, the default, takes the
+ * faster as measured: TCGEN05 where it applies, except at shifted layers whose window grid
+ * is at most two windows wide (there half or more of the windows wrap at the right edge
+ * and are gathered four rows at a time), else MMA_SYNC. UNSUPPORTED where the choice does
+ * not apply (the plan is then unchanged). Host-side only; call it between launches.
  */
 int swin_wattn_set_bwd_kernel(swin_wattn_plan_t plan, int kernel);
 

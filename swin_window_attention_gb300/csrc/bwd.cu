@@ -513,6 +513,7 @@ __global__ void __launch_bounds__(Geo<M>::THREADS, BwdMinBlocks<M>::value) bwd_k
 // dtable[r, h] = sum over chunks c (in order) of partial[c*nH + h, r].
 __global__ void dtable_reduce_kernel(const float* __restrict__ partial, int R, int nH, int chunks,
                                      float* __restrict__ dtable) {
+  pdl_wait();  // launched early; the partials are complete once the backward grid is
   const int e = blockIdx.x * blockDim.x + threadIdx.x;
   if (e >= R * nH) return;
   const int r = e / nH, h = e % nH;
@@ -524,8 +525,8 @@ __global__ void dtable_reduce_kernel(const float* __restrict__ partial, int R, i
 // ---- host side ---------------------------------------------------------------------
 
 cudaError_t launch_dtable_reduce(const float* partial, int R, int nH, int chunks, float* dtable, cudaStream_t st) {
-  dtable_reduce_kernel<<<(R * nH + 255) / 256, 256, 0, st>>>(partial, R, nH, chunks, dtable);
-  return cudaGetLastError();
+  return launch_pdl(dtable_reduce_kernel, dim3((R * nH + 255) / 256), dim3(256), 0, st, partial, R, nH, chunks,
+                    dtable);
 }
 
 bool bwd_tc_applies(const Plan& pl);
@@ -584,16 +585,17 @@ static cudaError_t blaunch_t(const Plan& pl, const BwdLaunch& L, const void* qkv
   cudaError_t e = launch_pdl(bwd_kernel<M, TIO, STAGES>, dim3(L.grid), dim3(L.threads), L.smem, st, p);
   if (e != cudaSuccess) return e;
   const int R = BGeo<M>::R;
-  dtable_reduce_kernel<<<(R * pl.nH + 255) / 256, 256, 0, st>>>(pl.dt_partial, R, pl.nH, L.chunks,
-                                                                dtable);
-  return cudaGetLastError();
+  return launch_dtable_reduce(pl.dt_partial, R, pl.nH, L.chunks, dtable, st);
 }
 
-// Kernel choice: the tcgen05 kernel when the plan asks for it (7x7 windows, bf16), else
-// the mma.sync kernel.
+// Kernel choice: the tcgen05 kernel when the plan asks for it (7x7 windows, bf16), or
+// by default where it applies and was measured faster (all but shifted layers at most two
+// windows wide, where its right-edge gathers dominate); else the mma.sync kernel.
 cudaError_t bwd_config(const Plan& pl, BwdLaunch* L) {
   *L = BwdLaunch();
   if (pl.bwd_kernel == SWIN_WATTN_KERNEL_TCGEN05) return bwd_tc_applies(pl) ? bwd_tc_config(pl, L) : cudaErrorNotSupported;
+  if (pl.bwd_kernel == SWIN_WATTN_KERNEL_AUTO && bwd_tc_applies(pl) && !(pl.s > 0 && pl.nWx <= 2))
+    return bwd_tc_config(pl, L);
   const bool f32 = pl.dtype == SWIN_WATTN_FP32;
   switch (pl.M) {
     case 4:

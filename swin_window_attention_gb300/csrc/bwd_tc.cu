@@ -22,8 +22,9 @@
 //   lane's partial sums (below) and stores its row at the token it was loaded from;
 // * control (warps 8-11): S = Q K^T (+ the shift mask as a rank-4 product) and
 //   dP = dO V^T as M128 N128 products; the TMA producer (7 x 7-token boxes, two row bands
-//   at a bottom wrap, tile::gather4 at a right wrap), three stages deep; two warps that
-//   issue the gradient products, one thread per accumulator.
+//   at a bottom wrap, tile::gather4 at a right wrap), three stages deep; one thread that
+//   issues the gradient products, dV, dK, dQ in that order with a commit after each kind,
+//   so that the softmax warps write the next pair's P and dS as soon as each is free.
 // The gradient products run per window with the hi and lo halves stacked in M: for
 // dV = P^T dO the A operand is [P_hi^T ; P_lo^T] (64 keys twice, K = the window's 64
 // queries), so D rows m and m + 64 are two partial sums of key m's gradient row and one
@@ -50,8 +51,8 @@ constexpr int kTM = 7, kTN = 49;
 constexpr int kR = (2 * kTM - 1) * (2 * kTM - 1);  // 169 table rows
 constexpr int kGROUPS = (kTN + 3) / 4;              // gather4 row groups per window tile
 // warps 0-3: softmax (one warpgroup), 4-7: epilogue, 8: MMA (S, dP), 9: producer,
-// 10: MMA (dV, dK), 11: MMA (dQ)
-constexpr int kA_WARP = 8, kPROD_WARP = 9, kDKV_WARP = 10, kDQ_WARP = 11;
+// 10: MMA (dV, dK, dQ), 11: idle
+constexpr int kA_WARP = 8, kPROD_WARP = 9, kGRAD_WARP = 10;
 constexpr int kTHREADS = 12 * 32;
 constexpr int kROW = 64;                     // one token's 32 bf16 head channels
 constexpr int kWIN = 64 * kROW;              // 64 slot rows of one window (4 KB)
@@ -76,7 +77,7 @@ constexpr int kOFF_BIAS = kOFF_U + kMASK_BYTES;
 constexpr int kXCH = 128 * kROW;
 constexpr int kOFF_XCH = kOFF_BIAS + kBIAS_BYTES;
 constexpr int kOFF_BAR = kOFF_XCH + 3 * kXCH;
-constexpr int kNBAR = 2 * kSTAGES + 7;
+constexpr int kNBAR = 2 * kSTAGES + 9;
 constexpr int kSMEM = kOFF_BAR + 8 * kNBAR + 8 + 1024;  // + alignment slack
 constexpr uint32_t kG4_TX = 4 * kGROUPS * 4 * kROW;     // one window's gather4 bytes, 4 tensors
 constexpr uint32_t kBOX_TX = 4 * kTN * kROW;            // one window's box bytes, 4 tensors
@@ -164,7 +165,7 @@ __global__ void __launch_bounds__(kTHREADS, 1)
   auto empty_bar = [&](int st) { return bar0 + 8 * (kSTAGES + st); };
   const uint32_t sdp_full = bar0 + 8 * (2 * kSTAGES), sdp_free = sdp_full + 8, pds_full = sdp_full + 16;
   const uint32_t b_done = sdp_full + 24, acc_free = sdp_full + 32, const_bar = sdp_full + 40;
-  const uint32_t drain_bar = sdp_full + 48;
+  const uint32_t drain_bar = sdp_full + 48, p_free = sdp_full + 56, ds_free = sdp_full + 64;
   auto wwait = [&](uint32_t mbar, uint32_t parity) { return warp_wait(mbar, parity, p.wait_ns); };
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -187,20 +188,22 @@ __global__ void __launch_bounds__(kTHREADS, 1)
   if (tid == 0) {
     for (int st = 0; st < kSTAGES; ++st) {
       tc::mbar_init(full_bar(st), 1);
-      tc::mbar_init(empty_bar(st), 2);  // the gradient products' two issuing warps
+      tc::mbar_init(empty_bar(st), 1);  // the gradient products' issuing thread
     }
     tc::mbar_init(sdp_full, 1);
     tc::mbar_init(sdp_free, 4);
     tc::mbar_init(pds_full, 4);
-    tc::mbar_init(b_done, 2);
+    tc::mbar_init(b_done, 1);
+    tc::mbar_init(p_free, 1);
+    tc::mbar_init(ds_free, 1);
     tc::mbar_init(acc_free, 4);
     tc::mbar_init(const_bar, 1);
     tc::mbar_init(drain_bar, 3);
     tc::mbar_init_fence();
   }
-  // The stage tiles (rows past the loaded slots must hold finite values: they meet zero
-  // weights) and the P / dS operand blocks (the zero blocks and the padded rows and keys
-  // stay zero) start zeroed.
+  // The stage tiles (rows past the loaded slots, and a pair's second window when it has
+  // none, meet zero weights, so they must hold finite values) and the P / dS operand
+  // blocks (the padded rows and keys stay zero) start zeroed.
   for (int e = tid; e < (kOFF_OPS + 2 * kOP) / 16; e += kTHREADS)
     reinterpret_cast<uint4*>(smem)[e] = make_uint4(0u, 0u, 0u, 0u);
   tc::fence_proxy_async();
@@ -342,13 +345,14 @@ __global__ void __launch_bounds__(kTHREADS, 1)
         }
         __syncwarp();
       }
-    } else {
+    } else if (warp == kGRAD_WARP) {
       // Per window: dV = P^T dO and dK = dS^T Q (A transposed from the shared operand
       // blocks), dQ = dS K (A from tensor memory), once the pair's P and dS are written and
       // the last pair's gradients have been read out. The A rows are the window's 64 rows
       // twice, hi halves and lo halves, so D row m and row m + 64 are two partial sums of
-      // one gradient row. kDKV_WARP issues dV and window a's dK, kDQ_WARP window b's dK
-      // and dQ: one thread per accumulator, twelve products each.
+      // one gradient row. Issued in that order, with a commit after each kind, so that the
+      // softmax warps may write the next pair's P once the dV products are done, its dS
+      // once the dK products are.
       const uint64_t dops = tc::sdesc(ops, kBLK, 512, kSW64);
       for (int n = 0, st = 0; n < npair && !bad; ++n, st = st + 1 == kSTAGES ? 0 : st + 1) {
         if (!wwait(pds_full, n & 1) || (n > 0 && !wwait(acc_free, (n - 1) & 1))) {
@@ -360,24 +364,25 @@ __global__ void __launch_bounds__(kTHREADS, 1)
           // descriptors as offsets from the stage's MN-major one (addresses below 256 KB)
           const uint64_t d = tc::sdesc(smem0 + st * kSTAGE, kWIN, 512, kSW64);
 #pragma unroll
-          for (int w = 0; w < 2; ++w) {
+          for (int w = 0; w < 2; ++w)
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {  // the window's queries (dV, dK) or keys (dQ)
-              const uint32_t a_off = w * 4 * kBLK + kk * 1024, b_off = (4 * w + kk) * 1024;
-              const bool acc = kk > 0;
-              if (warp == kDKV_WARP) {
-                tc::mma_ss(tmem + kDV_COL + 32 * w, tc::desc_add(dops, a_off), tc::desc_add(d, kOFF_O + b_off), id_t,
-                           acc);
-                if (w == 0)
-                  tc::mma_ss(tmem + kDK_COL, tc::desc_add(dops, kOP + a_off), tc::desc_add(d, b_off), id_t, acc);
-              } else if (warp == kDQ_WARP) {
-                if (w == 1)
-                  tc::mma_ss(tmem + kDK_COL + 32, tc::desc_add(dops, kOP + a_off), tc::desc_add(d, b_off), id_t, acc);
-                tc::mma_ts(tmem + kDQ_COL + 32 * w, tmem + kDSA_COL + 32 * w + kk * 8,
-                           tc::desc_add(d, kOFF_K + b_off), id_q, acc);
-              }
-            }
-          }
+            for (int kk = 0; kk < 4; ++kk)  // the window's queries
+              tc::mma_ss(tmem + kDV_COL + 32 * w, tc::desc_add(dops, w * 4 * kBLK + kk * 1024),
+                         tc::desc_add(d, kOFF_O + (4 * w + kk) * 1024), id_t, kk > 0);
+          tc::commit(p_free);
+#pragma unroll
+          for (int w = 0; w < 2; ++w)
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)  // the window's queries
+              tc::mma_ss(tmem + kDK_COL + 32 * w, tc::desc_add(dops, kOP + w * 4 * kBLK + kk * 1024),
+                         tc::desc_add(d, (4 * w + kk) * 1024), id_t, kk > 0);
+          tc::commit(ds_free);
+#pragma unroll
+          for (int w = 0; w < 2; ++w)
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)  // the window's keys
+              tc::mma_ts(tmem + kDQ_COL + 32 * w, tmem + kDSA_COL + 32 * w + kk * 8,
+                         tc::desc_add(d, kOFF_K + (4 * w + kk) * 1024), id_q, kk > 0);
           tc::commit(b_done);
           tc::commit(empty_bar(st));
         }
@@ -516,13 +521,15 @@ __global__ void __launch_bounds__(kTHREADS, 1)
       for (int q = 25; q < 32; ++q) sh[q] = sl[q] = 0u;
 
       // ---- the last pair's gradient products are done: write this pair's operands -----
-      if (!bad && n > 0 && !wwait(b_done, (n - 1) & 1)) bad = 1;
       // (rows past the window's 49 slots and keys 56-63 are never written: they keep the
-      // zeros of the set-up)
-      if (i < kTN) {
-        const uint32_t* mats[4] = {ph, pl, sh, sl};
+      // zeros of the set-up); P once the last pair's dV products are done, dS once its dK
+      // products are, the tensor-memory rows once all its products are
+      const uint32_t* mats[4] = {ph, pl, sh, sl};
 #pragma unroll
-        for (int m = 0; m < 4; ++m) {
+      for (int m = 0; m < 4; ++m) {
+        if (m == 0 && !bad && n > 0 && !wwait(p_free, (n - 1) & 1)) bad = 1;
+        if (m == 2 && !bad && n > 0 && !wwait(ds_free, (n - 1) & 1)) bad = 1;
+        if (i < kTN) {
           unsigned char* dst = ops + (m >> 1) * kOP + ((m & 1) ? lo_blk : hi_blk);
 #pragma unroll
           for (int a = 0; a < 2; ++a) {
@@ -537,6 +544,7 @@ __global__ void __launch_bounds__(kTHREADS, 1)
       }
       // dQ's A operand: lane r holds its own window's dS hi row and the other window's dS lo
       // row of the same slot (written by the thread 64 lanes away)
+      if (!bad && n > 0 && !wwait(b_done, (n - 1) & 1)) bad = 1;
       tc::st_x32(trow + kDSA_COL + 32 * w, sh);
       if (bar_or(1, 128, bad)) {
         bad = 1;
@@ -564,24 +572,35 @@ __global__ void __launch_bounds__(kTHREADS, 1)
     if (!bad && npair > 0 && !wwait(b_done, (npair - 1) & 1)) bad = 1;
 
     // ---- fold the per-(i, j) dS sums into this CTA's table-gradient partial ----------
-    // (both windows' rows of slot i)
-    float* sdt = reinterpret_cast<float*>(ops);  // [128][49]
+    // Window a's threads store their rows, window b's add theirs to the same slot's row;
+    // then table entry (dy, dx) sums row si, column si - (7 dy + dx) over the slots si
+    // whose partner lies in the window.
+    float* sdt = reinterpret_cast<float*>(ops);  // [64][49]
+    if (w == 0) {
 #pragma unroll
-    for (int j = 0; j < kTN; ++j) sdt[tid * kTN + j] = i < kTN ? dt[j] : 0.0f;
+      for (int j = 0; j < kTN; ++j) sdt[i * kTN + j] = i < kTN ? dt[j] : 0.0f;
+    }
+    asm volatile("bar.sync 1, 128;\n" ::: "memory");
+    if (w == 1 && i < kTN) {
+#pragma unroll
+      for (int j = 0; j < kTN; ++j) sdt[i * kTN + j] += dt[j];
+    }
     asm volatile("bar.sync 1, 128;\n" ::: "memory");
     for (int rr = tid; rr < kR; rr += 128) {
       const int dy = rr / (2 * kTM - 1) - (kTM - 1), dx = rr % (2 * kTM - 1) - (kTM - 1);
-      float acc = 0.0f;
-      for (int yi = 0; yi < kTM; ++yi) {
-        const int yj = yi - dy;
-        if (yj < 0 || yj >= kTM) continue;
-        for (int xi = 0; xi < kTM; ++xi) {
-          const int xj = xi - dx;
-          if (xj < 0 || xj >= kTM) continue;
-          const int si = yi * kTM + xi, sj = yj * kTM + xj;
-          acc += sdt[si * kTN + sj] + sdt[(64 + si) * kTN + sj];
+      const int y0 = max(0, dy), y1 = min(kTM, kTM + dy), x0 = max(0, dx), x1 = min(kTM, kTM + dx);
+      const int off = dy * kTM + dx;
+      float acc0 = 0.0f, acc1 = 0.0f;
+      for (int yi = y0; yi < y1; ++yi) {
+        const float* rowp = sdt + (yi * kTM) * (kTN + 1) - off;  // element (si, si - off) at si * 50 - off
+        int xi = x0;
+        for (; xi + 1 < x1; xi += 2) {
+          acc0 += rowp[xi * (kTN + 1)];
+          acc1 += rowp[(xi + 1) * (kTN + 1)];
         }
+        if (xi < x1) acc0 += rowp[xi * (kTN + 1)];
       }
+      const float acc = acc0 + acc1;
       p.partial[(int64_t)blockIdx.x * kR + rr] = acc;
     }
   } else {

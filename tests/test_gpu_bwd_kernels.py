@@ -112,3 +112,21 @@ def test_tcgen05_bwd_refused_where_it_does_not_apply(M, dt):
     assert att.bwd_kernel == kern
     assert capi.swin_wattn_set_bwd_kernel(att.handle, 9) == capi.ERR_INVALID_ARG
     att.close()
+
+
+def test_tcgen05_bwd_output_16_byte_aligned():
+    """dqkv on a 16-byte (not 32-byte) boundary: the kernel stores in 16-byte pieces."""
+    wl = workload(2, 14, 14, 64, 2, 7, 3, "bf16", seed=77)
+    qkv, table, dout = inputs.make_qkv(wl), inputs.make_table(wl), inputs.make_dout(wl)
+    att = plan(wl, table.to(DEV))
+    att.set_bwd_kernel(capi.KERNEL_TCGEN05)
+    buf = torch.full((qkv.numel() + 16,), float("nan"), dtype=qkv.dtype, device=DEV)
+    dq = buf[8:8 + qkv.numel()].view(qkv.shape)
+    assert dq.data_ptr() % 32 == 16
+    _, dt = att.bwd(qkv.to(DEV), dout.to(DEV), dqkv=dq)
+    att.device_status()
+    ref_dq, ref_dt = oracle_bwd(qkv, dout, table, wl)
+    assert_close("dqkv 16-byte aligned", dq, ref_dq)
+    assert_close("dtable", dt, ref_dt)
+    assert torch.isnan(buf[:8]).all() and torch.isnan(buf[8 + qkv.numel():]).all()
+    att.close()

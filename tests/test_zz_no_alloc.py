@@ -2,10 +2,10 @@
 when they run it (a runtime with a device memory plan fixed at start-up, or a framework
 whose allocator must own every device byte), so they cannot create a plan.
 
-It runs the plan backward's kernels on fragments built by the plan's own fragment kernel
-into a fixed array inside the library, so its dqkv and bias-table gradient must equal the
-plan-based swin_wattn_bwd bit for bit, call after call, whatever ran before it on the
-shared array. One case is also compared with the fp64 oracle directly.
+It runs the plan backward's mma.sync kernels on fragments built by the plan's own
+fragment kernel into a fixed array inside the library, so its dqkv and bias-table gradient
+must equal the plan-based swin_wattn_bwd with that kernel bit for bit, call after call,
+whatever ran before it on the shared array. One case is also compared with the fp64 oracle directly.
 
 Kept in a file of its own that pytest collects last; it passes alone in a fresh process
 and after the other tests."""
@@ -43,6 +43,7 @@ def noalloc(wl, q, d, t):
 
 def plan_bwd(wl, q, d, t):
     att = plan(wl, t)
+    att.set_bwd_kernel(capi.KERNEL_MMA_SYNC)
     dq, dt = att.bwd(q, d)
     torch.cuda.synchronize()
     att.close()
