@@ -23,8 +23,8 @@ extern "C" {
 
 enum swin_wattn_fault_site {
   SWIN_WATTN_FAULT_NONE = 0,
-  /* mma.sync forward with copy-engine tiles (7x7 windows, bf16): in every CTA whose first
-     window is gathered by cp.async (a window of the last window column of a shifted layer),
+  /* mma.sync forward with copy-engine tiles (7x7 windows, bf16): in every CTA, on the first
+     window it gathers by cp.async (a window of the last window column of a shifted layer),
      thread 0 does not arrive on that window's stage barrier. */
   SWIN_WATTN_FAULT_FWD_MMA_SYNC = 1,
   /* tcgen05 forward: row warp 0 does not arrive on the "P written" barrier of the first

@@ -67,7 +67,6 @@ __global__ void __launch_bounds__(Geo<M>::THREADS, FwdMinBlocks<M>::value)
   // plan's fragments, which the previous kernel may just have rebuilt) waits for the
   // previous kernel to complete.
   pdl_launch_dependents();
-  pdl_wait();
   const uint32_t bar0 = smem_u32(smem) + G::BIAS_BYTES + G::MASK_BYTES + STAGES * G::STAGE_BYTES;
   float4* sbias = reinterpret_cast<float4*>(smem);
   uint32_t* smask = reinterpret_cast<uint32_t*>(smem + G::BIAS_BYTES);
@@ -108,7 +107,7 @@ __global__ void __launch_bounds__(Geo<M>::THREADS, FwdMinBlocks<M>::value)
   int cb = lb, cwy = lwy, cwx = lwx;  // cursor of the window being computed
   const uint32_t tiles_u32 = smem_u32(stiles);
 #ifdef SWIN_WATTN_FAULT_INJECTION
-  bool first_issue = true;  // the CTA's first window is being issued
+  bool first_gather = true;  // the CTA's first cp.async-gathered window is being issued
 #endif
 
   auto issue = [&](uint32_t stage_off, int stage) {
@@ -140,9 +139,6 @@ __global__ void __launch_bounds__(Geo<M>::THREADS, FwdMinBlocks<M>::value)
           }
         }
         tc::cp_async_arrive(full);
-#ifdef SWIN_WATTN_FAULT_INJECTION
-        first_issue = false;
-#endif
         if (++lwx == p.nWx) {
           lwx = 0;
           if (++lwy == p.nWy) {
@@ -170,14 +166,14 @@ __global__ void __launch_bounds__(Geo<M>::THREADS, FwdMinBlocks<M>::value)
     }
     if constexpr (TMA) {
 #ifdef SWIN_WATTN_FAULT_INJECTION
-      // armed: thread 0 withholds its arrival on the CTA's first window, so that window's
-      // bounded wait runs out (a cp.async window: no copy-engine bytes land after it)
-      if (!(p.fault == kFaultFwdMmaSync && tid == 0 && first_issue))
+      // armed: thread 0 withholds its arrival on the CTA's first cp.async-gathered window
+      // (no copy-engine bytes land after it), so that window's bounded wait runs out
+      if (!(p.fault == kFaultFwdMmaSync && tid == 0 && first_gather))
 #endif
         tc::cp_async_arrive(bar0 + 8 * stage);
     }
 #ifdef SWIN_WATTN_FAULT_INJECTION
-    first_issue = false;
+    first_gather = false;
 #endif
     if (++lwx == p.nWx) {
       lwx = 0;
@@ -188,6 +184,23 @@ __global__ void __launch_bounds__(Geo<M>::THREADS, FwdMinBlocks<M>::value)
     }
   };
 
+  if constexpr (TMA) {
+    if (tid == 0) {
+      for (int st = 0; st < STAGES; ++st) tc::mbar_init(bar0 + 8 * st, THREADS + 1);
+      tc::mbar_init_fence();
+    }
+    __syncthreads();
+  }
+  // Padded rows N..NPAD-1 of every q/k/v tile are zero (loads never touch them).
+  if constexpr (G::NPAD > N) {
+    constexpr int PADROWS = G::NPAD - N;
+    for (int e = tid; e < STAGES * 3 * PADROWS * 4; e += THREADS) {
+      const int c = e & 3, r = (e >> 2) % PADROWS, tile = (e >> 2) / PADROWS;
+      *reinterpret_cast<uint4*>(stiles + tile * G::TILE_BYTES + tile_off(N + r, c)) =
+          make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+  pdl_wait();
   // This head's bias fragments and the class mask fragments (built by the plan in this
   // kernel's fragment order) travel in the first copy group, with window 0.
   {
@@ -199,28 +212,12 @@ __global__ void __launch_bounds__(Geo<M>::THREADS, FwdMinBlocks<M>::value)
         cp_async_16(smem_u32(smem + G::BIAS_BYTES + e * 16), msrc + e * 16);
     }
   }
-  if constexpr (TMA) {
-    if (tid == 0) {
-      for (int st = 0; st < STAGES; ++st) tc::mbar_init(bar0 + 8 * st, THREADS + 1);
-      tc::mbar_init_fence();
-    }
-    __syncthreads();
-  }
 #pragma unroll
   for (int st = 0; st < STAGES - 1; ++st) {
     if (st < nwin) issue(st * G::STAGE_BYTES, st);
     if constexpr (!TMA) cp_async_commit();
   }
 
-  // Padded rows N..NPAD-1 of every q/k/v tile are zero (loads never touch them).
-  if constexpr (G::NPAD > N) {
-    constexpr int PADROWS = G::NPAD - N;
-    for (int e = tid; e < STAGES * 3 * PADROWS * 4; e += THREADS) {
-      const int c = e & 3, r = (e >> 2) % PADROWS, tile = (e >> 2) / PADROWS;
-      *reinterpret_cast<uint4*>(stiles + tile * G::TILE_BYTES + tile_off(N + r, c)) =
-          make_uint4(0u, 0u, 0u, 0u);
-    }
-  }
   const float4* bfrag = sbias + warp * NT * 32 + lane;
   const float c_l2 = p.qk_scale_log2;            // scale * log2(e)
   // Output slots of this lane: rows warp*16 + g + {0, 8}, 16-byte chunk t.

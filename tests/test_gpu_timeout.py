@@ -48,8 +48,8 @@ def _plan(lib, wl, table):
 
 
 def _armed_then_clean_forward(lib, kernel, site):
-    # 228 images of 2 x 2 shifted windows, three windows per CTA range: ranges that start
-    # in the last window column (gathered by cp.async) are followed by copy-engine windows
+    # 228 images of 2 x 2 shifted windows: half of them lie in the last window column
+    # (gathered by cp.async), the others come through the copy engine
     wl = workload(228, 14, 14, 64, 2, 7, 3, seed=61)
     qkv, table = inputs.make_qkv(wl), inputs.make_table(wl)
     q, t = qkv.to(DEV), table.to(DEV)
