@@ -130,3 +130,23 @@ def test_tcgen05_bwd_output_16_byte_aligned():
     assert_close("dtable", dt, ref_dt)
     assert torch.isnan(buf[:8]).all() and torch.isnan(buf[8 + qkv.numel():]).all()
     att.close()
+
+
+@pytest.mark.parametrize("B,H,W,C,nH,M,s,dt,expect", [
+    (2, 56, 56, 128, 4, 7, 3, "bf16", capi.KERNEL_TCGEN05),   # 8 windows wide, shifted
+    (2, 28, 28, 256, 8, 7, 3, "bf16", capi.KERNEL_TCGEN05),
+    (2, 14, 14, 512, 16, 7, 3, "bf16", capi.KERNEL_MMA_SYNC),  # 2 windows wide, shifted
+    (2, 14, 14, 512, 16, 7, 0, "bf16", capi.KERNEL_TCGEN05),   # not shifted
+    (2, 7, 7, 1024, 32, 7, 0, "bf16", capi.KERNEL_TCGEN05),
+    (2, 56, 56, 128, 4, 7, 3, "fp32", capi.KERNEL_MMA_SYNC),   # tcgen05 is bf16 only
+    (2, 16, 16, 64, 2, 4, 2, "bf16", capi.KERNEL_MMA_SYNC),    # window 4
+])
+def test_auto_backward_kernel_choice(B, H, W, C, nH, M, s, dt, expect):
+    wl = workload(B, H, W, C, nH, M, s, dt)
+    att = plan(wl, inputs.make_table(wl).to(DEV))
+    assert att.bwd_kernel == expect
+    att.set_bwd_kernel(capi.KERNEL_MMA_SYNC)
+    assert att.bwd_kernel == capi.KERNEL_MMA_SYNC
+    att.set_bwd_kernel(capi.KERNEL_AUTO)
+    assert att.bwd_kernel == expect
+    att.close()
