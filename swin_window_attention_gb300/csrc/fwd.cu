@@ -538,6 +538,10 @@ static cudaError_t mma_launch(const Plan& pl, const FwdLaunch& L, const void* qk
 
 bool fwd_tc_applies(const Plan& pl);
 cudaError_t fwd_tc_config(const Plan& pl, FwdLaunch* L);
+bool fwd12_tc_applies(const Plan& pl);
+cudaError_t fwd12_tc_config(const Plan& pl, FwdLaunch* L);
+cudaError_t fwd12_tc_launch(const Plan& pl, const FwdLaunch& L, const void* qkv, void* out, int batch,
+                            cudaStream_t st);
 cudaError_t fwd_tc_launch(const Plan& pl, const FwdLaunch& L, const void* qkv, void* out, int batch,
                           cudaStream_t st);
 
@@ -545,22 +549,26 @@ cudaError_t fwd_tc_launch(const Plan& pl, const FwdLaunch& L, const void* qkv, v
 // the mma.sync kernel (the default: the faster of the two as measured).
 cudaError_t fwd_config(const Plan& pl, FwdLaunch* L) {
   *L = FwdLaunch();
-  if (pl.fwd_kernel == SWIN_WATTN_KERNEL_TCGEN05 && !fwd_tc_applies(pl)) return cudaErrorNotSupported;
   if (pl.fwd_kernel == SWIN_WATTN_KERNEL_TCGEN05) {
     L->tc = true;
-    return fwd_tc_config(pl, L);
+    if (fwd_tc_applies(pl)) return fwd_tc_config(pl, L);
+    if (fwd12_tc_applies(pl)) return fwd12_tc_config(pl, L);
+    *L = FwdLaunch();
+    return cudaErrorNotSupported;
   }
   return mma_config(pl, L);
 }
 
 cudaError_t fwd_launch(const Plan& pl, const FwdLaunch& L, const void* qkv, void* out,
                        cudaStream_t st) {
-  return L.tc ? fwd_tc_launch(pl, L, qkv, out, pl.B, st) : mma_launch(pl, L, qkv, out, pl.B, st);
+  if (L.tc) return pl.M == 12 ? fwd12_tc_launch(pl, L, qkv, out, pl.B, st) : fwd_tc_launch(pl, L, qkv, out, pl.B, st);
+  return mma_launch(pl, L, qkv, out, pl.B, st);
 }
 
 cudaError_t fwd_launch_batch(const Plan& pl, const FwdLaunch& L, const void* qkv, void* out,
                              int batch, cudaStream_t st) {
-  return L.tc ? fwd_tc_launch(pl, L, qkv, out, batch, st) : mma_launch(pl, L, qkv, out, batch, st);
+  if (L.tc) return pl.M == 12 ? fwd12_tc_launch(pl, L, qkv, out, batch, st) : fwd_tc_launch(pl, L, qkv, out, batch, st);
+  return mma_launch(pl, L, qkv, out, batch, st);
 }
 
 }  // namespace swin
