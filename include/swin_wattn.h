@@ -73,7 +73,7 @@ enum swin_wattn_dtype { SWIN_WATTN_BF16 = 0, SWIN_WATTN_FP32 = 1 };
 enum swin_wattn_kernel {
   SWIN_WATTN_KERNEL_AUTO = 0,      /* the faster kernel as measured (see the setters below) */
   SWIN_WATTN_KERNEL_MMA_SYNC = 1,  /* warp-level mma.sync kernel: every M, both dtypes */
-  SWIN_WATTN_KERNEL_TCGEN05 = 2    /* tensor-memory kernel: M = 7 with bf16 only */
+  SWIN_WATTN_KERNEL_TCGEN05 = 2    /* tensor-memory kernels: M = 7 or 12 with bf16 */
 };
 
 /*
@@ -291,10 +291,13 @@ int swin_wattn_fwd_fp8(swin_wattn_plan_t plan, const void* qkv8, float scale_q, 
                        void* out, struct CUstream_st* stream);
 
 /*
- * Choose the plan's forward kernel (SWIN_WATTN_KERNEL_*). Both kernels compute the same
- * function to the same tolerance; AUTO, the default, is MMA_SYNC (measured faster for the
- * forward). Asking for TCGEN05 where it does not apply returns SWIN_WATTN_ERR_UNSUPPORTED
- * and leaves the plan unchanged. Host-side only; call it between launches.
+ * Choose the plan's forward kernel (SWIN_WATTN_KERNEL_*): MMA_SYNC (every window size and
+ * dtype) or TCGEN05 (the tensor-memory kernels: window 7 or 12, bf16). Both compute the
+ * same function to the same tolerance. AUTO, the default, takes the faster as measured:
+ * TCGEN05 for 12 x 12 windows when the plan has at least 16 window-heads per SM
+ * (B * windows * heads >= 16 * SMs), else MMA_SYNC. Asking for TCGEN05 where it does not
+ * apply returns SWIN_WATTN_ERR_UNSUPPORTED and leaves the plan unchanged. Host-side only;
+ * call it between launches.
  */
 int swin_wattn_set_fwd_kernel(swin_wattn_plan_t plan, int kernel);
 

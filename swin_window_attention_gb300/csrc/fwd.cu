@@ -545,11 +545,18 @@ cudaError_t fwd12_tc_launch(const Plan& pl, const FwdLaunch& L, const void* qkv,
 cudaError_t fwd_tc_launch(const Plan& pl, const FwdLaunch& L, const void* qkv, void* out, int batch,
                           cudaStream_t st);
 
-// Kernel choice: the tcgen05 kernel when the plan asks for it (7x7 windows, bf16), else
-// the mma.sync kernel (the default: the faster of the two as measured).
+// Kernel choice: the tcgen05 kernel when the plan asks for it (7x7 or 12x12 windows,
+// bf16); with AUTO, the tcgen05 kernel for 12x12 windows when there are at least 16
+// window-heads per SM (its per-CTA start-up then amortises: measured faster on the Swin-L
+// 384 96x96 and 48x48 stages, slower on the 24x24 one), else the mma.sync kernel.
+static bool fwd12_auto(const Plan& pl) {
+  return pl.fwd_kernel == SWIN_WATTN_KERNEL_AUTO && fwd12_tc_applies(pl) &&
+         (int64_t)pl.B * pl.nW * pl.nH >= 16 * (int64_t)pl.num_sms;
+}
+
 cudaError_t fwd_config(const Plan& pl, FwdLaunch* L) {
   *L = FwdLaunch();
-  if (pl.fwd_kernel == SWIN_WATTN_KERNEL_TCGEN05) {
+  if (pl.fwd_kernel == SWIN_WATTN_KERNEL_TCGEN05 || fwd12_auto(pl)) {
     L->tc = true;
     if (fwd_tc_applies(pl)) return fwd_tc_config(pl, L);
     if (fwd12_tc_applies(pl)) return fwd12_tc_config(pl, L);

@@ -124,6 +124,31 @@ def test_fwd12_tcgen05_workload_every_image(name):
     acc.check(f"{name} Y tcgen05")
 
 
+@pytest.mark.parametrize("name,expect", [
+    ("swin_l384_s1", capi.KERNEL_TCGEN05),
+    ("swin_l384_s2", capi.KERNEL_TCGEN05),
+    ("swin_l384_s3", capi.KERNEL_MMA_SYNC),
+    ("swin_l384_s4", capi.KERNEL_MMA_SYNC),
+    ("swin_l224_s1", capi.KERNEL_MMA_SYNC),
+])
+def test_auto_forward_kernel_choice(name, expect):
+    """AUTO takes the tcgen05 kernel for 12x12 windows with at least 16 window-heads per SM
+    (on this GPU's SM count), else the mma.sync kernel; choosing a kernel and going back to
+    AUTO restores the choice."""
+    wl = inputs.BY_NAME[name]
+    nsm = torch.cuda.get_device_properties(0).multi_processor_count
+    wh = wl.B * (wl.H // wl.M) * (wl.W // wl.M) * wl.nH
+    if wl.M == 12 and (wh >= 16 * nsm) != (expect == capi.KERNEL_TCGEN05):
+        pytest.skip(f"{nsm} SMs: the window-head count {wh} falls on the other side of the rule")
+    att = plan(wl, inputs.make_table(wl).to(DEV))
+    assert att.fwd_kernel == expect
+    att.set_fwd_kernel(capi.KERNEL_MMA_SYNC)
+    assert att.fwd_kernel == capi.KERNEL_MMA_SYNC
+    att.set_fwd_kernel(capi.KERNEL_AUTO)
+    assert att.fwd_kernel == expect
+    att.close()
+
+
 def test_tcgen05_kernel_is_deterministic():
     wl = inputs.BY_NAME["swin_l224_s2"]
     qkv, table = inputs.make_qkv(wl), inputs.make_table(wl)

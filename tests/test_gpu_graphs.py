@@ -19,6 +19,7 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda"
 L224 = ["swin_l224_s1", "swin_l224_s2", "swin_l224_s3", "swin_l224_s4"]
 B224 = ["swin_b224_s1", "swin_b224_s2", "swin_b224_s3", "swin_b224_s4"]
+L384 = ["swin_l384_s1", "swin_l384_s2", "swin_l384_s3", "swin_l384_s4"]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -53,11 +54,16 @@ def _replay(g, stream, outs):
     stream.synchronize()
 
 
-@pytest.mark.parametrize("kernel", [capi.KERNEL_MMA_SYNC, capi.KERNEL_TCGEN05])
-def test_l224_sweep_graph_replays_match_the_oracle(kernel):
-    """The headline step: the four Swin-L 224 stage forwards (B = 64) as one graph."""
+@pytest.mark.parametrize("names,kernel", [
+    (L224, capi.KERNEL_MMA_SYNC),
+    (L224, capi.KERNEL_TCGEN05),
+    (L384, capi.KERNEL_AUTO),
+], ids=["l224-mma_sync", "l224-tcgen05", "l384-auto"])
+def test_sweep_graph_replays_match_the_oracle(names, kernel):
+    """The headline step: the four Swin-L 224 stage forwards (B = 64) as one graph; and the
+    four Swin-L 384 ones (12x12 windows, B = 16) with the kernels AUTO picks per stage."""
     stream = torch.cuda.Stream()
-    wls = [inputs.BY_NAME[n] for n in L224]
+    wls = [inputs.BY_NAME[n] for n in names]
     tabs = [inputs.make_table(wl) for wl in wls]
     atts = [plan(wl, t.to(DEV)) for wl, t in zip(wls, tabs)]
     for a in atts:
