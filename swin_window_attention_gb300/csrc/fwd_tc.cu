@@ -25,8 +25,9 @@
 //   V) in column 64.
 // * Row warps (0..3): thread r loads its 49 logits from tensor memory, adds the relative
 //   position bias, takes max and exp2, writes the bf16 row of P to tensor memory (the A
-//   operand of P V), and finally normalises its row of O and stores it at the token the
-//   row was read from.
+//   operand of P V); one pair later (its P V ran meanwhile) it normalises its row of O and
+//   stores it at the token the row was read from. The MMA thread issues the next pair's
+//   Q K^T as soon as S has been read out, ahead of the current pair's P V.
 //
 // The bias image of the CTA's head and the mask operands are built once per plan and
 // arrive with one bulk copy. Hand-offs go through mbarriers (stage full / empty, S full /
@@ -315,9 +316,19 @@ __global__ void __launch_bounds__(kTHREADS, 1) fwd_tc_kernel(const __grid_consta
       else
         bad = 1;
     }
-    // P V of pair n as soon as its P is written, then Q K^T of pair n + 1 as soon as its
-    // tiles have landed and S has been read out (usually long before).
+    // Q K^T of pair n + 1 as soon as its tiles have landed and the row warps have read S
+    // of pair n out (early in their softmax of pair n), then P V of pair n once its P is
+    // written and O of pair n - 1 has been read out: the row warps find S of the next pair
+    // ready, and P V runs while they work on the next pair.
     for (int n = 0; n < npair && !bad; ++n) {
+      if (n + 1 < npair) {
+        const int st1 = (n + 1) % kSTAGES;
+        if (!wwait(full_bar(st1), ((n + 1) / kSTAGES) & 1) || !wwait(s_free, n & 1)) {
+          bad = 1;
+          break;
+        }
+        issue_qk(n + 1);
+      }
       if (!wwait(p_full, n & 1) || (n > 0 && !wwait(o_free, (n - 1) & 1))) {
         bad = 1;
         break;
@@ -333,14 +344,6 @@ __global__ void __launch_bounds__(kTHREADS, 1) fwd_tc_kernel(const __grid_consta
         tc::commit(empty_bar(n % kSTAGES));
       }
       __syncwarp();
-      if (n + 1 < npair) {
-        const int st1 = (n + 1) % kSTAGES;
-        if (!wwait(full_bar(st1), ((n + 1) / kSTAGES) & 1) || !wwait(s_free, n & 1)) {
-          bad = 1;
-          break;
-        }
-        issue_qk(n + 1);
-      }
     }
     // every MMA this thread issued has completed before the tensor memory is released
     if (lane == 0) tc::commit(drain_bar);
@@ -353,52 +356,53 @@ __global__ void __launch_bounds__(kTHREADS, 1) fwd_tc_kernel(const __grid_consta
     const float c_l2 = p.qk_scale_log2;
     const float* brow = sbias + i * kBIAS_STRIDE;
     const uint32_t trow = tmem + ((uint32_t)(32 * warp) << 16);
-    Cursor cur = first;
+    Cursor cur = first, prev = first;  // the pair being computed; the pair whose O is stored
+    bool prev_active = false;
     if (npair > 0 && !wwait(const_bar, 0)) bad = 1;
-    for (int n = 0; n < npair && !bad; ++n) {
+    // Pair n's softmax, then pair n - 1's output (its P V ran meanwhile), then pair n's P.
+    for (int n = 0; n <= npair && !bad; ++n) {
       Cursor me = cur;
       if (win) me.next(p.nWy, p.nWx);
-      const bool active = i < kTN && (win == 0 || 2 * n + 1 < nwin);
-
-      if (!wwait(s_full, n & 1)) {
-        bad = 1;
-        break;
-      }
-      tc::fence_after_sync();
-      uint32_t sa[32], sb[16], sc;
-      tc::ld49_wait(trow + kS_COL + 64 * win, sa, sb, sc);
-      tc::fence_before_sync();
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(s_free);
-
-      float y[kTN];
-      {
-        const float2 c2 = make_float2(c_l2, c_l2);
-        const float4* b4 = reinterpret_cast<const float4*>(brow);
-#pragma unroll
-        for (int q = 0; q < 12; ++q) {
-          const float4 bb = b4[q];
-          const uint32_t* src = q < 8 ? &sa[4 * q] : &sb[4 * (q - 8)];
-          const float2 e0 = __ffma2_rn(make_float2(__uint_as_float(src[0]), __uint_as_float(src[1])), c2,
-                                       make_float2(bb.x, bb.y));
-          const float2 e1 = __ffma2_rn(make_float2(__uint_as_float(src[2]), __uint_as_float(src[3])), c2,
-                                       make_float2(bb.z, bb.w));
-          y[4 * q] = e0.x;
-          y[4 * q + 1] = e0.y;
-          y[4 * q + 2] = e1.x;
-          y[4 * q + 3] = e1.y;
-        }
-        y[48] = fmaf(__uint_as_float(sc), c_l2, brow[48]);
-      }
-      float ma = y[48], mb = y[47];
-#pragma unroll
-      for (int q = 0; q < 46; q += 4) {
-        ma = fmax3(ma, y[q], y[q + 1]);
-        mb = fmax3(mb, y[q + 2], y[q + 3]);
-      }
-      ma = fmax3(ma, mb, y[46]);
+      const bool active = n < npair && i < kTN && (win == 0 || 2 * n + 1 < nwin);
       uint32_t pw[32];
-      {
+      if (n < npair) {
+        if (!wwait(s_full, n & 1)) {
+          bad = 1;
+          break;
+        }
+        tc::fence_after_sync();
+        uint32_t sa[32], sb[16], sc;
+        tc::ld49_wait(trow + kS_COL + 64 * win, sa, sb, sc);
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(s_free);
+
+        float y[kTN];
+        {
+          const float2 c2 = make_float2(c_l2, c_l2);
+          const float4* b4 = reinterpret_cast<const float4*>(brow);
+#pragma unroll
+          for (int q = 0; q < 12; ++q) {
+            const float4 bb = b4[q];
+            const uint32_t* src = q < 8 ? &sa[4 * q] : &sb[4 * (q - 8)];
+            const float2 e0 = __ffma2_rn(make_float2(__uint_as_float(src[0]), __uint_as_float(src[1])), c2,
+                                         make_float2(bb.x, bb.y));
+            const float2 e1 = __ffma2_rn(make_float2(__uint_as_float(src[2]), __uint_as_float(src[3])), c2,
+                                         make_float2(bb.z, bb.w));
+            y[4 * q] = e0.x;
+            y[4 * q + 1] = e0.y;
+            y[4 * q + 2] = e1.x;
+            y[4 * q + 3] = e1.y;
+          }
+          y[48] = fmaf(__uint_as_float(sc), c_l2, brow[48]);
+        }
+        float ma = y[48], mb = y[47];
+#pragma unroll
+        for (int q = 0; q < 46; q += 4) {
+          ma = fmax3(ma, y[q], y[q + 1]);
+          mb = fmax3(mb, y[q + 2], y[q + 3]);
+        }
+        ma = fmax3(ma, mb, y[46]);
         const float2 nm = make_float2(-ma, -ma);
 #pragma unroll
         for (int q = 0; q < 24; ++q) {
@@ -409,50 +413,56 @@ __global__ void __launch_bounds__(kTHREADS, 1) fwd_tc_kernel(const __grid_consta
 #pragma unroll
         for (int q = 25; q < 32; ++q) pw[q] = 0u;
       }
-      // P's previous contents were consumed: this thread waited for O of pair n - 1
-      tc::st_x32(trow + kP_COL, pw);
-      tc::wait_st();
-      tc::fence_before_sync();
-      __syncwarp();
-#ifdef SWIN_WATTN_FAULT_INJECTION
-      // armed: row warp 0 withholds its arrival for the first pair, so the MMA thread's
-      // bounded wait for P runs out
-      if (!(p.fault == kFaultFwdTcgen05 && warp == 0 && n == 0))
-#endif
-        if (lane == 0) tc::mbar_arrive(p_full);
-
-      if (!wwait(o_full, n & 1)) {
-        bad = 1;
-        break;
-      }
-      tc::fence_after_sync();
-      uint32_t o[32], osum;
-      tc::ld32_1_wait(trow + kO_COL + 32 * win, trow + kO_COL + 64, o, osum);
-      tc::fence_before_sync();
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(o_free);
-      if (active) {
-        const float inv = 1.0f / __uint_as_float(osum);
-        const float2 i2 = make_float2(inv, inv);
-        int yy = me.wy * kTM + ly + s, xx = me.wx * kTM + lx + s;
-        yy = yy >= H ? yy - H : yy;
-        xx = xx >= W ? xx - W : xx;
-        const int64_t tok = ((int64_t)me.b * H + yy) * W + xx;
-        uint4* dst = reinterpret_cast<uint4*>(p.out + tok * p.C + h * kHeadDim);
+      if (n > 0) {
+        // ---- pair n - 1: its row of O / the row sum, at the token the row was read from
+        if (!wwait(o_full, (n - 1) & 1)) {
+          bad = 1;
+          break;
+        }
+        tc::fence_after_sync();
+        uint32_t o[32], osum;
+        tc::ld32_1_wait(trow + kO_COL + 32 * win, trow + kO_COL + 64, o, osum);
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(o_free);
+        if (prev_active) {
+          const float inv = 1.0f / __uint_as_float(osum);
+          const float2 i2 = make_float2(inv, inv);
+          int yy = prev.wy * kTM + ly + s, xx = prev.wx * kTM + lx + s;
+          yy = yy >= H ? yy - H : yy;
+          xx = xx >= W ? xx - W : xx;
+          const int64_t tok = ((int64_t)prev.b * H + yy) * W + xx;
+          uint4* dst = reinterpret_cast<uint4*>(p.out + tok * p.C + h * kHeadDim);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint32_t w4[4];
+          for (int q = 0; q < 4; ++q) {
+            uint32_t w4[4];
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const float2 v = __fmul2_rn(
-                make_float2(__uint_as_float(o[8 * q + 2 * u]), __uint_as_float(o[8 * q + 2 * u + 1])), i2);
-            w4[u] = pack_bf16(v.x, v.y);
+            for (int u = 0; u < 4; ++u) {
+              const float2 v = __fmul2_rn(
+                  make_float2(__uint_as_float(o[8 * q + 2 * u]), __uint_as_float(o[8 * q + 2 * u + 1])), i2);
+              w4[u] = pack_bf16(v.x, v.y);
+            }
+            dst[q] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
           }
-          dst[q] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
         }
       }
-      cur.next(p.nWy, p.nWx);
-      cur.next(p.nWy, p.nWx);
+      if (n < npair) {
+        // P's previous contents were consumed: this thread waited for O of pair n - 1
+        tc::st_x32(trow + kP_COL, pw);
+        tc::wait_st();
+        tc::fence_before_sync();
+        __syncwarp();
+#ifdef SWIN_WATTN_FAULT_INJECTION
+        // armed: row warp 0 withholds its arrival for the first pair, so the MMA thread's
+        // bounded wait for P runs out
+        if (!(p.fault == kFaultFwdTcgen05 && warp == 0 && n == 0))
+#endif
+          if (lane == 0) tc::mbar_arrive(p_full);
+        prev = me;
+        prev_active = active;
+        cur.next(p.nWy, p.nWx);
+        cur.next(p.nWy, p.nWx);
+      }
     }
   }
   if (bad) atomicOr(p.err, 1);
