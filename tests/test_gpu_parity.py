@@ -219,13 +219,27 @@ def test_batch_shards_concatenate_exactly():
     full.close()
 
 
-@pytest.mark.parametrize("name,batch", [("swin_t_s1_swmsa", 32), ("tiny", 1), ("swin_l224_s3", 3)])
-def test_fwd_host_buffers_match_device_path(name, batch):
+@pytest.mark.parametrize("name,batch,kernel", [
+    ("swin_t_s1_swmsa", 32, capi.KERNEL_AUTO),
+    ("tiny", 1, capi.KERNEL_AUTO),
+    ("swin_l224_s3", 3, capi.KERNEL_AUTO),
+    ("swin_l224_s2", 5, capi.KERNEL_TCGEN05),
+    ("swin_l384_s1", 16, capi.KERNEL_AUTO),
+    ("swin_l384_s3", 3, capi.KERNEL_TCGEN05),
+])
+def test_fwd_host_buffers_match_device_path(name, batch, kernel):
     """swin_wattn_fwd_host (pinned host in/out, chunked copy/compute pipeline) gives the
-    device path's output bit for bit."""
+    device path's output bit for bit, for each forward kernel (the batch chunks of the host
+    path launch with their own window ranges)."""
     wl = inputs.BY_NAME[name].with_batch(batch)
     qkv, table = inputs.make_qkv(wl), inputs.make_table(wl)
     att = plan(wl, table.to(DEV))
+    att.set_fwd_kernel(kernel)
+    if kernel == capi.KERNEL_AUTO and wl.M == 12:
+        # AUTO's rule for 12x12 windows: tcgen05 from 16 window-heads per SM
+        nsm = torch.cuda.get_device_properties(0).multi_processor_count
+        wh = wl.B * (wl.H // wl.M) * (wl.W // wl.M) * wl.nH
+        assert att.fwd_kernel == (capi.KERNEL_TCGEN05 if wh >= 16 * nsm else capi.KERNEL_MMA_SYNC)
     ref = att.fwd(qkv.to(DEV)).cpu()
     qh = qkv.pin_memory()
     oh = torch.empty(ref.shape, dtype=ref.dtype).pin_memory()
