@@ -524,7 +524,9 @@ def run_fwd_sweep(names, args, dev, stream, lib, capi, hbm, ws):
         tot_ms += ms
         out.append({"workload": wl.name, "us": round(ms * 1e3, 2),
                     "frac_of_measured_hbm": round(fwd_bytes(wl) / (ms / 1e3) / 1e9 / hbm, 4),
-                    "tflops": round(fwd_flops(wl) / (ms / 1e3) / 1e12, 1)})
+                    "tflops": round(fwd_flops(wl) / (ms / 1e3) / 1e12, 1),
+                    "fwd_kernel": "tcgen05" if capi.swin_wattn_fwd_kernel(x["h"]) == capi.KERNEL_TCGEN05
+                    else "mma.sync"})
         capi.swin_wattn_destroy(x["h"])
     return {"workload": "swin_l384_sweep_fwd (B=16, 12x12 windows)", "us": round(tot_ms * 1e3, 2),
             "tokens_per_s": sum(x["wl"].tokens for x in st) / (tot_ms / 1e3),
