@@ -27,8 +27,9 @@ enum swin_wattn_fault_site {
      window it gathers by cp.async (a window of the last window column of a shifted layer),
      thread 0 does not arrive on that window's stage barrier. */
   SWIN_WATTN_FAULT_FWD_MMA_SYNC = 1,
-  /* tcgen05 forward: row warp 0 does not arrive on the "P written" barrier of the first
-     pair of windows, so the MMA warp's wait runs out, then the other roles' waits. */
+  /* tcgen05 forwards: row warp 0 does not arrive on the "P written" barrier of the first
+     pair of windows (7x7) or of the first window (12x12), so the MMA warp's wait runs out,
+     then the other roles' waits. */
   SWIN_WATTN_FAULT_FWD_TCGEN05 = 2,
   /* GEMM steps (qkv projection, output projection): the MMA thread does not commit the
      "accumulator full" barrier of its first output tile, so the epilogue warps' wait runs

@@ -75,6 +75,7 @@ struct Fwd12Params {
   int H, W, C, nH, s, nWy, nWx, nW;
   int64_t total_windows;
   int chunks;
+  int fault;    // armed fault site (fault-injection build only)
   float scale;  // hd^-0.5
   // key j lies in the wrapped row band when j / 12 >= 12 - s (bit j % 32 of ky[j / 32]), in
   // the wrapped column band when j % 12 >= 12 - s (kx)
@@ -414,7 +415,12 @@ __global__ void __launch_bounds__(kTHREADS, 1)
         tc::wait_st();
         tc::fence_before_sync();
         __syncwarp();
-        if (lane == 0) tc::mbar_arrive(p_full);
+#ifdef SWIN_WATTN_FAULT_INJECTION
+        // armed: softmax warp 0 withholds its arrival for the first window, so the O
+        // issuer's bounded wait for P runs out
+        if (!(p.fault == kFaultFwdTcgen05 && warp == 0 && n == 0))
+#endif
+          if (lane == 0) tc::mbar_arrive(p_full);
         inv_prev = inv;
         prev = cur;
         cur.next(p.nWy, p.nWx);
@@ -669,6 +675,7 @@ cudaError_t fwd12_tc_launch(const Plan& pl, const FwdLaunch& L0, const void* qkv
   p.total_windows = total;
   p.chunks = L.chunks;
   p.scale = 1.0f / kInvScale;
+  p.fault = fault_site();
   for (int w = 0; w < 5; ++w) {
     p.ky[w] = p.kx[w] = 0;
     for (int b = 0; b < 32; ++b) {

@@ -47,10 +47,11 @@ def _plan(lib, wl, table):
     return h.value
 
 
-def _armed_then_clean_forward(lib, kernel, site):
-    # 228 images of 2 x 2 shifted windows: half of them lie in the last window column
-    # (gathered by cp.async), the others come through the copy engine
-    wl = workload(228, 14, 14, 64, 2, 7, 3, seed=61)
+def _armed_then_clean_forward(lib, kernel, site, M=7):
+    # 2 x 2 shifted windows per image, half of them in the last window column (gathered
+    # four rows at a time or by cp.async), the others through the copy engine: 228 images
+    # of 7x7 windows, or 40 of 12x12 windows
+    wl = workload(228, 14, 14, 64, 2, 7, 3, seed=61) if M == 7 else workload(40, 24, 24, 64, 2, 12, 5, seed=62)
     qkv, table = inputs.make_qkv(wl), inputs.make_table(wl)
     q, t = qkv.to(DEV), table.to(DEV)
     y = torch.empty(wl.B, wl.H, wl.W, wl.C, dtype=torch.bfloat16, device=DEV)
@@ -81,8 +82,9 @@ def test_mma_sync_forward_stage_wait_runs_out(dbg):
     _armed_then_clean_forward(dbg, capi.KERNEL_MMA_SYNC, capi.FAULT_FWD_MMA_SYNC)
 
 
-def test_tcgen05_forward_wait_runs_out_and_tensor_memory_is_released(dbg):
-    _armed_then_clean_forward(dbg, capi.KERNEL_TCGEN05, capi.FAULT_FWD_TCGEN05)
+@pytest.mark.parametrize("M", [7, 12])
+def test_tcgen05_forward_wait_runs_out_and_tensor_memory_is_released(dbg, M):
+    _armed_then_clean_forward(dbg, capi.KERNEL_TCGEN05, capi.FAULT_FWD_TCGEN05, M)
 
 
 def _f64(t):
